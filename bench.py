@@ -1,0 +1,614 @@
+"""Benchmark of the 8-bit rollout linear-layer hot path on GB300.
+
+Headline (one JSON line on rank 0): the Qwen2.5-7B-shaped layer set (qkv
+3584->4608, o_proj 3584->3584, gate_up 3584->37888, down 18944->3584) at decode
+batch M=64 with a per-step FP8 weight requant.  One step is one pass of the
+FP8 path over that layer set:
+  A1  requant all four bf16 weights to 128x128-block E4M3 + fp32 scales
+      (one grouped launch),
+  A2  quantize the four layer inputs X [64, K] to 1x128-group E4M3,
+  A4  run the four block-scaled FP8 GEMMs -> bf16 Y [64, N].
+value = algorithmic HBM bytes of the step / step time (GB/s).  Four copies of
+the layer set rotate: step s requants copy s%4 and runs the GEMMs on copy
+(s+2)%4, whose E4M3 weights were written two steps (1.4 GB of traffic)
+earlier, so every weight byte comes from HBM, not from L2.
+
+Other rows are measured as sub-benchmarks under "extras" (not in `value`):
+prefill FP8 GEMM TFLOP/s at M=8192 (Qwen2.5-32B shapes), the 32B decode sweep
+M in {1,8,32,128,256}, the 64-layer 32B requant, and the INT8 W8A8 path.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--extras all|none]
+    python bench.py --impl reference ...     # the CPU oracle on a bounded sample
+Under torchrun each rank is an independent replica (the path does not shard).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from precision_rl_rollout_gb300 import synth  # noqa: E402
+
+METRIC = "FP8 W8A8 GEMM TFLOP/s (prefill), HBM GB/s (decode M<=256), requant GB/s"
+UNIT = "GB/s"
+DECODE_M = 64
+COPIES = 4
+L2_BYTES = 129 * 2 ** 20
+
+# ncu-measured DRAM traffic of the dominant kernel, valid only for the source it
+# was taken on (checked by hash; null otherwise).  Filled from the committed
+# profile summary of the same workload.
+NCU_TRAFFIC = {"kernel": "quant_weight_block_kernel", "source_sha1": None, "bytes_per_launch": None,
+               "profile": "profiles/requant_weight_block_qwen7b.md"}
+
+
+# ------------------------------------------------------------------ algorithmic bytes
+
+def requant_bytes(N, K):
+    """bf16 read + e4m3 write + one fp32 scale per 128x128 block."""
+    return 2 * N * K + N * K + 4 * (N // 128) * (K // 128)
+
+
+def act_quant_bytes(M, K):
+    return 2 * M * K + M * K + 4 * M * (K // 128)
+
+
+def gemm_bytes(M, N, K):
+    """e4m3 W + its scales + e4m3 X + its scales + bf16 Y."""
+    return N * K + 4 * (N // 128) * (K // 128) + M * K + 4 * M * (K // 128) + 2 * M * N
+
+
+def int8_gemm_bytes(M, N, K):
+    return N * K + 4 * N + M * K + 4 * M + 2 * M * N
+
+
+def step_bytes(shapes, M):
+    return sum(requant_bytes(s.N, s.K) + act_quant_bytes(M, s.K) + gemm_bytes(M, s.N, s.K)
+               for s in shapes)
+
+
+# ------------------------------------------------------------------ environment
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d.get("hbm_gbs"), "bf16_tflops": d.get("bf16_tflops"),
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def _smi_id(device: int) -> str:
+    """nvidia-smi addresses GPUs by PCI bus id; torch's index is relative to
+    CUDA_VISIBLE_DEVICES, so translate through the PCI location."""
+    try:
+        p = torch.cuda.get_device_properties(device)
+        return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+    except Exception:
+        return str(device)
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Largest value over all ranks (the slowest replica sets the time)."""
+    if world <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int, rank: int = 0):
+        self.smi_id = _smi_id(device)
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.smi_id}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ device step
+
+class LayerSet:
+    """One copy of the FP8 layer set: bf16 weights, their E4M3 codes and scales,
+    the four layer inputs and their quantized forms, and the outputs."""
+
+    def __init__(self, shapes, M, seed_base, dev):
+        self.shapes = shapes
+        self.W, self.Wq, self.Ws, self.X, self.Xq, self.Xs, self.Y = [], [], [], [], [], [], []
+        for i, s in enumerate(shapes):
+            W = synth.weight_bf16_direct(s.N, s.K, seed_base + 10 * i, device=dev)
+            synth.policy_update_(W, seed_base + 10 * i + 5)           # A0, untimed
+            self.W.append(W)
+            self.Wq.append(torch.empty(s.N, s.K, dtype=torch.uint8, device=dev))
+            self.Ws.append(torch.empty(s.N // 128, s.K // 128, dtype=torch.float32, device=dev))
+            self.X.append(synth.activation(M, s.K, seed_base + 10 * i + 1, device=dev))
+            self.Xq.append(torch.empty(M, s.K, dtype=torch.uint8, device=dev))
+            self.Xs.append(torch.empty(s.K // 128, M, dtype=torch.float32, device=dev))
+            self.Y.append(torch.empty(M, s.N, dtype=torch.bfloat16, device=dev))
+        self.group = list(zip(self.W, self.Wq, self.Ws))
+
+
+def run_requant(fb, ls):
+    fb.fp8rl_quant_weight_block_grouped(ls.group)
+
+
+def run_decode(fb, ls, ws):
+    for i in range(len(ls.shapes)):
+        fb.fp8rl_quant_act_group(ls.X[i], ls.Xq[i], ls.Xs[i])
+        fb.fp8rl_gemm_w8a8_block(ls.Xq[i], ls.Xs[i], ls.Wq[i], ls.Ws[i], Y=ls.Y[i], workspace=ws)
+
+
+def time_headline(fb, args, dev, world, rank):
+    shapes = synth.QWEN25_7B
+    M = DECODE_M
+    sets = [LayerSet(shapes, M, synth.seed_for(2, 0) + 1000 * c, dev) for c in range(COPIES)]
+    ws_bytes = max(fb.fp8rl_gemm_workspace_bytes(M, s.N, s.K) for s in shapes)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    for c in range(COPIES):                          # every copy has valid codes before step 0
+        run_requant(fb, sets[c])
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream()
+    n_ev = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_ev)]
+
+    def step(s, record=None):
+        req, gem = sets[s % COPIES], sets[(s + COPIES // 2) % COPIES]
+        if record: record[0].record(stream)
+        run_requant(fb, req)
+        if record: record[1].record(stream)
+        for i in range(len(shapes)):
+            fb.fp8rl_quant_act_group(gem.X[i], gem.Xq[i], gem.Xs[i])
+        if record: record[2].record(stream)
+        for i in range(len(shapes)):
+            fb.fp8rl_gemm_w8a8_block(gem.Xq[i], gem.Xs[i], gem.Wq[i], gem.Ws[i], Y=gem.Y[i], workspace=ws)
+        if record: record[3].record(stream)
+
+    for s in range(args.warmup):
+        step(s)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device(), rank) as clk:
+        t0.record(stream)
+        for s in range(args.steps):
+            step(args.warmup + s, ev[s])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    req_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    aq_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    gm_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
+    assert fb.fp8rl_check_device_error() == 0
+    res = {"total_ms": total_ms, "req_ms": req_ms, "aq_ms": aq_ms, "gemm_ms": gm_ms,
+           "clocks": clk.summary(), "launches_per_step": 1 + 2 * len(shapes)}
+    del sets
+    torch.cuda.empty_cache()
+    return res
+
+
+def time_e2e(fb, args, dev):
+    """Same step through the public API with pinned host buffers: H2D of the
+    bf16 weights and inputs, requant, act quant, GEMM on the fresh codes, D2H of Y."""
+    shapes = synth.QWEN25_7B
+    M = DECODE_M
+    ls = LayerSet(shapes, M, synth.seed_for(2, 0) + 7000, dev)
+    hW = [w.cpu().pin_memory() for w in ls.W]
+    hX = [x.cpu().pin_memory() for x in ls.X]
+    hY = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in ls.Y]
+    ws_bytes = max(fb.fp8rl_gemm_workspace_bytes(M, s.N, s.K) for s in shapes)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in hW + hX)
+    d2h = sum(t.numel() * t.element_size() for t in hY)
+
+    def step():
+        for i in range(len(shapes)):
+            ls.W[i].copy_(hW[i], non_blocking=True)
+            ls.X[i].copy_(hX[i], non_blocking=True)
+        run_requant(fb, ls)
+        run_decode(fb, ls, ws)
+        for i in range(len(shapes)):
+            hY[i].copy_(ls.Y[i], non_blocking=True)
+
+    steps = max(3, min(args.steps, 20))
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    del ls
+    torch.cuda.empty_cache()
+    return {"value": step_bytes(shapes, M) / (ms * 1e-3) / 1e9, "unit": UNIT,
+            "ms_per_step": ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+# ------------------------------------------------------------------ extras
+
+def _flush_l2(buf):
+    buf.add_(1)
+
+
+def _time_op(fn, reps, flush=None, warm=3):
+    for _ in range(warm):
+        fn()
+    ts = []
+    for _ in range(reps):
+        if flush is not None:
+            flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def extras(fb, dev, reps=5):
+    out = {}
+    flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = lambda: _flush_l2(flush_buf)  # noqa: E731
+
+    # A3: prefill FP8 GEMM at M=8192 on the 32B shapes
+    pre = {}
+    for s in synth.QWEN25_32B:
+        W = synth.weight_bf16_direct(s.N, s.K, synth.seed_for(4, 0), device=dev)
+        Wq, Ws = fb.fp8rl_quant_weight_block(W)
+        del W
+        X = synth.activation(synth.PREFILL_M, s.K, synth.seed_for(4, 1), device=dev)
+        Xq, Xs = fb.fp8rl_quant_act_group(X)
+        del X
+        Y = torch.empty(synth.PREFILL_M, s.N, dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(max(1, fb.fp8rl_gemm_workspace_bytes(synth.PREFILL_M, s.N, s.K)),
+                         dtype=torch.uint8, device=dev)
+        ms = _time_op(lambda: fb.fp8rl_gemm_w8a8_block(Xq, Xs, Wq, Ws, Y=Y, workspace=ws), reps, flush)
+        pre[s.name] = {"ms": ms, "tflops": 2 * synth.PREFILL_M * s.N * s.K / (ms * 1e-3) / 1e12}
+        del Wq, Ws, Xq, Xs, Y
+    out["prefill_fp8_gemm_m8192"] = pre
+
+    # A2 + A4: 32B decode sweep; the GEMM is timed alone after an L2 flush
+    dec = {}
+    for s in synth.QWEN25_32B:
+        W = synth.weight_bf16_direct(s.N, s.K, synth.seed_for(3, 0), device=dev)
+        Wq, Ws = fb.fp8rl_quant_weight_block(W)
+        del W
+        for M in synth.DECODE_M_SWEEP:
+            X = synth.activation(M, s.K, synth.seed_for(3, 1), device=dev)
+            Xq, Xs = fb.fp8rl_quant_act_group(X)
+            Y = torch.empty(M, s.N, dtype=torch.bfloat16, device=dev)
+            ws = torch.empty(max(1, fb.fp8rl_gemm_workspace_bytes(M, s.N, s.K)), dtype=torch.uint8, device=dev)
+            ms = _time_op(lambda: fb.fp8rl_gemm_w8a8_block(Xq, Xs, Wq, Ws, Y=Y, workspace=ws), reps, flush)
+            aq = _time_op(lambda: fb.fp8rl_quant_act_group(X, Xq, Xs), reps, flush)
+            dec[f"{s.name}_M{M}"] = {"gemm_ms": ms, "gemm_gbs": gemm_bytes(M, s.N, s.K) / (ms * 1e-3) / 1e9,
+                                     "act_quant_ms": aq}
+        del Wq, Ws
+    out["decode_fp8_gemm_32b"] = dec
+
+    # A1 at full-model scale: 64 layers x 4 shapes in grouped launches
+    items = []
+    for layer in range(synth.QWEN25_32B_LAYERS):
+        for i, s in enumerate(synth.QWEN25_32B):
+            W = synth.weight_bf16_direct(s.N, s.K, synth.seed_for(4, 0) + 1000 * layer + i, device=dev)
+            items.append((W, torch.empty(s.N, s.K, dtype=torch.uint8, device=dev),
+                          torch.empty(s.N // 128, s.K // 128, dtype=torch.float32, device=dev)))
+    nbytes = sum(requant_bytes(s.N, s.K) for s in synth.QWEN25_32B) * synth.QWEN25_32B_LAYERS
+    ms = _time_op(lambda: fb.fp8rl_quant_weight_block_grouped(items), max(3, reps // 2))
+    out["requant_fp8_32b_64layers"] = {"ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9,
+                                       "bytes": nbytes, "tensors": len(items)}
+    del items
+    torch.cuda.empty_cache()
+
+    # A5-A7: INT8 on the 32B shapes
+    i8 = {}
+    for s in synth.QWEN25_32B:
+        W = synth.weight_bf16_direct(s.N, s.K, synth.seed_for(5, 0), device=dev)
+        Wq = torch.empty(s.N, s.K, dtype=torch.int8, device=dev)
+        Ws = torch.empty(s.N, dtype=torch.float32, device=dev)
+        wq_ms = _time_op(lambda: fb.int8rl_quant_weight_channel(W, Wq, Ws), reps, flush)
+        i8[f"{s.name}_wquant"] = {"ms": wq_ms, "gbs": (3 * s.N * s.K + 4 * s.N) / (wq_ms * 1e-3) / 1e9}
+        del W
+        for M in synth.INT8_M_SWEEP:
+            X = synth.activation(M, s.K, synth.seed_for(5, 1), device=dev)
+            Xq, Xs = fb.int8rl_quant_act_token(X)
+            Y = torch.empty(M, s.N, dtype=torch.bfloat16, device=dev)
+            ms = _time_op(lambda: fb.int8rl_gemm_w8a8(Xq, Xs, Wq, Ws, Y=Y), reps, flush)
+            i8[f"{s.name}_M{M}"] = {"gemm_ms": ms,
+                                    "gemm_gbs": int8_gemm_bytes(M, s.N, s.K) / (ms * 1e-3) / 1e9,
+                                    "gemm_tops": 2 * M * s.N * s.K / (ms * 1e-3) / 1e12}
+        del Wq, Ws
+    out["int8_32b"] = i8
+    torch.cuda.empty_cache()
+    return out
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+class OracleSample:
+    """The CPU oracle on a bounded sample of the headline step.  Set-up (untimed)
+    draws the same seeded inputs as the GPU and quantizes the full weights once
+    (the GEMM sample needs every weight row).  Each sample step times the
+    oracle's requant of `req_rows` rows of every weight, its act quant of all
+    four X [64, K] and its GEMM for `gemm_rows` tokens against the full weights,
+    then extrapolates each part linearly to the full step."""
+
+    def __init__(self, req_rows=128, gemm_rows=1):
+        import numpy as np
+
+        import oracle
+        oracle.build()
+        self.np, self.oracle = np, oracle
+        self.req_rows, self.gemm_rows = req_rows, gemm_rows
+        self.shapes = synth.QWEN25_7B
+        self.data = []
+        for i, s in enumerate(self.shapes):
+            W = synth.bf16_bits(synth.weight(s.N, s.K, synth.seed_for(2, 0) + 10 * i))
+            X = synth.bf16_bits(synth.activation(DECODE_M, s.K, synth.seed_for(2, 0) + 10 * i + 1))
+            wq, ws = oracle.fp8_quant_weight_block(W)
+            xq, xs = oracle.fp8_quant_act_group(X)
+            self.data.append((W, X, wq, ws, xq, xs))
+        self.step_idx = 0
+
+    def step(self):
+        np, oracle = self.np, self.oracle
+        t = {"requant": 0.0, "act_quant": 0.0, "gemm": 0.0}
+        for s, (W, X, wq, ws, xq, xs) in zip(self.shapes, self.data):
+            r0 = (self.step_idx * self.req_rows) % s.N
+            a = time.perf_counter()
+            oracle.fp8_quant_weight_block(np.ascontiguousarray(W[r0:r0 + self.req_rows]))
+            t["requant"] += (time.perf_counter() - a) * (s.N / self.req_rows)
+            a = time.perf_counter()
+            oracle.fp8_quant_act_group(X)
+            t["act_quant"] += time.perf_counter() - a
+            m0 = (self.step_idx * self.gemm_rows) % DECODE_M
+            a = time.perf_counter()
+            oracle.fp8_gemm(np.ascontiguousarray(xq[m0:m0 + self.gemm_rows]),
+                            np.ascontiguousarray(xs[:, m0:m0 + self.gemm_rows]), wq, ws)
+            t["gemm"] += (time.perf_counter() - a) * (DECODE_M / self.gemm_rows)
+        self.step_idx += 1
+        return t
+
+    def describe(self):
+        return (f"per sample step: oracle requant of {self.req_rows} rows of each Qwen2.5-7B weight (scaled "
+                f"to all rows), act quant of all four X [64,K], GEMM for {self.gemm_rows} of 64 tokens against "
+                f"the full weights (scaled x{DECODE_M // self.gemm_rows}); single-threaded C oracle; value = "
+                f"full-step algorithmic bytes / extrapolated full-step time")
+
+
+def cpu_baseline(n_steps=3, req_rows=1024, gemm_rows=16):
+    """About 10-20 s of oracle work on the machine's host cores (1 thread)."""
+    o = OracleSample(req_rows=req_rows, gemm_rows=gemm_rows)
+    tot = {"requant": 0.0, "act_quant": 0.0, "gemm": 0.0}
+    for _ in range(n_steps):
+        for k, v in o.step().items():
+            tot[k] += v / n_steps
+    full = sum(tot.values())
+    return {"value": step_bytes(o.shapes, DECODE_M) / full / 1e9, "unit": UNIT, "cores": 1,
+            "kind": "oracle", "sample": o.describe() + f"; mean of {n_steps} sample steps",
+            "full_step_seconds": tot}
+
+
+# ------------------------------------------------------------------ main
+
+def traffic_or_null():
+    src = os.path.join(ROOT, "precision_rl_rollout_gb300", "csrc", "quant.cu")
+    sha = hashlib.sha1(open(src, "rb").read()).hexdigest()
+    if NCU_TRAFFIC["source_sha1"] == sha and NCU_TRAFFIC["bytes_per_launch"]:
+        return NCU_TRAFFIC["bytes_per_launch"]
+    return None
+
+
+def main_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    o = OracleSample(req_rows=128, gemm_rows=1)
+    for _ in range(args.warmup):
+        o.step()
+    t0 = time.perf_counter()
+    full_s = [sum(o.step().values()) for _ in range(args.steps)]
+    wall = time.perf_counter() - t0
+    shapes = synth.QWEN25_7B
+    v = step_bytes(shapes, DECODE_M) / statistics.mean(full_s) / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": step_bytes(shapes, DECODE_M) / (v * 1e9) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+            "data": "synthetic", "config": workload_config(),
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": o.describe()},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": wall}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config():
+    return {"workload": "Qwen2.5-7B-shaped layer set (qkv 3584->4608, o_proj 3584->3584, gate_up "
+                        "3584->37888, down 18944->3584), decode M=64, per-step FP8 128x128 requant",
+            "M": DECODE_M, "layers": [[s.name, s.K, s.N] for s in synth.QWEN25_7B],
+            "copies": COPIES,
+            "l2": "inputs larger than L2: 4 rotating copies (0.7 GB each); GEMM weights written 2 steps earlier",
+            "parallelism": "replicas"}
+
+
+def profile_case(fb, case, dev, reps=3):
+    """Small, self-contained workloads for ncu captures (a few GB at most, a
+    few launches of one kernel)."""
+    if case == "requant":
+        ls = LayerSet(synth.QWEN25_7B, DECODE_M, synth.seed_for(2, 0), dev)
+        for _ in range(reps):
+            run_requant(fb, ls)
+    elif case in ("decode", "act_quant"):
+        ls = LayerSet(synth.QWEN25_7B, DECODE_M, synth.seed_for(2, 0), dev)
+        run_requant(fb, ls)
+        ws = torch.empty(max(1, max(fb.fp8rl_gemm_workspace_bytes(DECODE_M, s.N, s.K) for s in ls.shapes)),
+                         dtype=torch.uint8, device=dev)
+        for _ in range(reps):
+            run_decode(fb, ls, ws)
+    elif case == "prefill":
+        s = synth.QWEN25_32B[0]
+        W = synth.weight_bf16_direct(s.N, s.K, synth.seed_for(4, 0), device=dev)
+        Wq, Ws = fb.fp8rl_quant_weight_block(W)
+        Xq, Xs = fb.fp8rl_quant_act_group(synth.activation(synth.PREFILL_M, s.K, synth.seed_for(4, 1), device=dev))
+        ws = torch.empty(max(1, fb.fp8rl_gemm_workspace_bytes(synth.PREFILL_M, s.N, s.K)), dtype=torch.uint8, device=dev)
+        for _ in range(reps):
+            fb.fp8rl_gemm_w8a8_block(Xq, Xs, Wq, Ws, workspace=ws)
+    elif case == "int8":
+        s = synth.QWEN25_32B[0]
+        W = synth.weight_bf16_direct(s.N, s.K, synth.seed_for(5, 0), device=dev)
+        Wq, Ws = fb.int8rl_quant_weight_channel(W)
+        Xq, Xs = fb.int8rl_quant_act_token(synth.activation(256, s.K, synth.seed_for(5, 1), device=dev))
+        for _ in range(reps):
+            fb.int8rl_gemm_w8a8(Xq, Xs, Wq, Ws)
+    else:
+        raise SystemExit(f"unknown profile case {case}")
+    torch.cuda.synchronize()
+    assert fb.fp8rl_check_device_error() == 0
+    print(f"profile case {case}: ok")
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--extras", default="all", choices=["all", "none"])
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--profile", default=None,
+                    help="run one small case for ncu: requant | decode | prefill | int8")
+    args = ap.parse_args()
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        return main_reference(args, world, rank)
+    if args.warmup < 3:
+        print("note: warm-up raised to the minimum of 3 steps", file=sys.stderr)
+        args.warmup = 3
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    from precision_rl_rollout_gb300 import binding as fb
+    fb.load()
+    if args.profile:
+        return profile_case(fb, args.profile, dev)
+
+    head = time_headline(fb, args, dev, world, rank)
+    shapes = synth.QWEN25_7B
+    sb = step_bytes(shapes, DECODE_M)
+    ms_per_step = head["total_ms"] / args.steps
+    value = world * sb / (ms_per_step * 1e-3) / 1e9
+    peaks = load_peaks()
+    req_b = sum(requant_bytes(s.N, s.K) for s in shapes)
+    req_gbs = req_b / (head["req_ms"] * 1e-3) / 1e9
+    gemm_b = sum(gemm_bytes(DECODE_M, s.N, s.K) for s in shapes)
+    aq_b = sum(act_quant_bytes(DECODE_M, s.K) for s in shapes)
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+            "config": workload_config(),
+            "roofline": {"bound": "hbm", "kernel": "quant_weight_block_kernel (A1 requant, grouped)",
+                         "achieved": req_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": req_gbs / peaks["hbm_gbs"], "traffic": traffic_or_null(),
+                         "algorithmic_bytes_per_launch": req_b,
+                         "peak_source": f"{peaks['source']} hbm_gbs (STREAM-style copy)"},
+            "breakdown": {"requant_ms": head["req_ms"], "requant_gbs": req_gbs,
+                          "act_quant_ms": head["aq_ms"], "act_quant_gbs": aq_b / (head["aq_ms"] * 1e-3) / 1e9,
+                          "gemm_ms": head["gemm_ms"], "gemm_gbs": gemm_b / (head["gemm_ms"] * 1e-3) / 1e9,
+                          "step_bytes": sb},
+            "gpu_launches": head["launches_per_step"] * args.steps,
+            "clocks": head["clocks"]}
+    if not args.no_e2e:
+        line["e2e"] = time_e2e(fb, args, dev)
+    if args.extras == "all" and rank == 0:
+        line["extras"] = extras(fb, dev)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline()
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,179 @@
+/*
+ * fp8rl.h -- C ABI of the 8-bit rollout linear layer for GB300 (sm_103a).
+ *
+ * In RL with 8-bit rollouts the trainer updates the bf16 policy weights every
+ * step, so the rollout engine must quantize them again after every update and
+ * then run its linear layers on 8-bit weights and activations:
+ *   - "FP8-RL: A Practical and Stable Low-Precision Stack for LLM Reinforcement
+ *     Learning", Abstract: policy weights change every step, requiring repeated
+ *     quantization; contribution (i), FP8 W8A8 linear-layer rollout with
+ *     blockwise FP8 quantization.
+ *   - FlashRL news write-up ("FlashRL: 8Bit Rollouts, Full Power RL"), section
+ *     on online quantization (quantizing a model whose parameters are updated)
+ *     and Fig. 1 (INT8 and FP8 rollouts).
+ * The pages fix neither block sizes nor scale rules.  This library reads
+ * "blockwise" as: weight blocks of 128x128 and activation groups of 1x128, one
+ * fp32 scale each, scale = fl32(amax / 448) (an all-zero block gets scale 1),
+ * code = E4M3FN(round-to-nearest-even, saturate to +-448)(fl32(x / scale)).
+ * INT8 uses one symmetric scale per row (weight output channel / token),
+ * scale = fl32(amax / 127), code = clamp(rint(fl32(x / scale)), -127, 127),
+ * int32 accumulation.  E4M3FN is the OCP OFP8 format.
+ *
+ * Conventions shared by every call:
+ *   - Layout is nn.Linear's: W is [N][K] row-major (out x in), X is [M][K],
+ *     Y is [M][N].  bf16 tensors are passed as uint16_t bit patterns.
+ *   - Every data pointer is a DEVICE pointer owned by the caller.  The library
+ *     never allocates, frees or synchronizes (fp8rl_check_device_error is the
+ *     one documented exception: it synchronizes).  All work is enqueued on
+ *     `stream` (a cudaStream_t; NULL is the legacy default stream) and is
+ *     asynchronous.  The calling thread's current device must own the buffers.
+ *   - Validation is synchronous and happens before any launch:
+ *       FP8RL_ERR_NULL   a required pointer is NULL (with a non-empty shape),
+ *       FP8RL_ERR_SHAPE  N or K not a multiple of 128, a negative size, or a
+ *                        leading dimension smaller than the row length,
+ *       FP8RL_ERR_ALIGN  a tensor not 16-byte aligned, or a leading
+ *                        dimension whose row pitch is not a multiple of 16 B,
+ *       FP8RL_ERR_WORKSPACE  workspace smaller than the *_workspace_bytes query,
+ *       FP8RL_ERR_UNSUPPORTED a size above a documented limit.
+ *     A launch failure reported by the runtime returns FP8RL_ERR_CUDA.  Faults
+ *     during execution surface, as usual in CUDA, at the caller's next
+ *     synchronization.
+ *   - M == 0 (an empty batch) is valid and launches nothing.
+ *   - Inputs must be finite; NaN/Inf are not checked on this path.
+ */
+#ifndef FP8RL_H_
+#define FP8RL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP8RL_OK = 0,
+    FP8RL_ERR_NULL = 1,
+    FP8RL_ERR_SHAPE = 2,
+    FP8RL_ERR_ALIGN = 3,
+    FP8RL_ERR_WORKSPACE = 4,
+    FP8RL_ERR_CUDA = 5,
+    FP8RL_ERR_UNSUPPORTED = 6,
+    FP8RL_ERR_TIMEOUT = 7
+} fp8rl_status;
+
+#define FP8RL_ABI_VERSION 1
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* fp8rl_status_string(int status);
+
+/* FP8RL_ABI_VERSION of the loaded library. */
+int fp8rl_abi_version(void);
+
+/* ------------------------------------------------------------------------
+ * FP8 weight requant (FP8-RL, Abstract: repeated quantization every step;
+ * contribution (i): blockwise FP8).  For every 128x128 block (nb, kb) of W:
+ *   amax = max |w| (exact, fp32); s = amax == 0 ? 1 : fl32(amax / 448);
+ *   Wq[n][k] = E4M3FN_rn_satfinite(fl32(W[n][k] / s)); Ws[nb][kb] = s.
+ * W   bf16 [N][ldw], ldw >= K, ldw % 8 == 0, 16-byte aligned.
+ * Wq  e4m3 codes [N][K] (contiguous), 16-byte aligned.
+ * Ws  fp32 [N/128][K/128] row-major, 4-byte aligned.
+ * Output is bit-exact (a pure function of the input bits).
+ * ---------------------------------------------------------------------- */
+int fp8rl_quant_weight_block(const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
+                             uint8_t* Wq, float* Ws, void* stream);
+
+/* One tensor of a grouped requant: the same operation as
+ * fp8rl_quant_weight_block, with the same layout rules per tensor. */
+typedef struct {
+    const uint16_t* W;
+    uint8_t* Wq;
+    float* Ws;
+    int64_t N, K, ldw;
+} fp8rl_wdesc;
+
+/* Requant of n weight tensors (e.g. every linear layer of a model after one
+ * policy update) in as few launches as possible.  `descs` is a HOST array of n
+ * descriptors (read during the call; the caller may reuse it on return); the
+ * pointers inside are device pointers.  Tensors must not overlap.  Any invalid
+ * descriptor fails the whole call before anything is launched. */
+int fp8rl_quant_weight_block_grouped(const fp8rl_wdesc* descs, int n, void* stream);
+
+/* ------------------------------------------------------------------------
+ * FP8 activation quant, 1x128 groups per token (FP8-RL contribution (i), the
+ * A8 of W8A8).  For token m and group g (columns 128g .. 128g+127):
+ *   s = amax == 0 ? 1 : fl32(amax / 448); Xq[m][k] = E4M3FN_rn_satfinite(fl32(X[m][k] / s)).
+ * X   bf16 [M][ldx], ldx >= K, ldx % 8 == 0, 16-byte aligned.
+ * Xq  e4m3 [M][K] contiguous, 16-byte aligned.
+ * Xs  fp32 [K/128][M]: group-major, so that a GEMM reads the scales of
+ *     consecutive tokens contiguously.  4-byte aligned.
+ * Bit-exact.
+ * ---------------------------------------------------------------------- */
+int fp8rl_quant_act_group(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
+                          uint8_t* Xq, float* Xs, void* stream);
+
+/* ------------------------------------------------------------------------
+ * FP8 block-scaled W8A8 GEMM with bf16 output (FP8-RL contribution (i)):
+ *   Y[m][n] = bf16_rn( sum_kb Xs[kb][m] * Ws[n/128][kb] * sum_{k in kb} e4m3(Xq[m][k]) * e4m3(Wq[n][k]) )
+ * computed with fp32 tensor-core partial sums per 128-wide K block and fp32
+ * promotion of each block's scale product.  Accumulation order is not fixed:
+ * the result matches the exact value within |y - y_ref| <= 2^-7 |y_ref| +
+ * 1e-3 rms(y_ref).  The same call serves decode (small M, weight streaming,
+ * HBM-bound) and prefill (large M, tensor-bound); the library picks the kernel.
+ * Xq [M][K] e4m3, Xs [K/128][M] fp32, Wq [N][K] e4m3, Ws [N/128][K/128] fp32,
+ * Y bf16 [M][ldy], ldy >= N, ldy % 8 == 0.  All 16-byte aligned (scales: 4).
+ * workspace: device scratch of at least fp8rl_gemm_workspace_bytes(M, N, K)
+ * bytes (may be NULL when that is 0).  It does not need to be zeroed and holds
+ * nothing between calls, but two calls in flight at once need two workspaces.
+ * ---------------------------------------------------------------------- */
+size_t fp8rl_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+int fp8rl_gemm_w8a8_block(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
+                          const float* Ws, int64_t M, int64_t N, int64_t K,
+                          uint16_t* Y, int64_t ldy, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * INT8 per-row quant (FlashRL write-up, Fig. 1: INT8 rollout).  Per row r:
+ *   s = amax == 0 ? 1 : fl32(amax / 127); Q[r][k] = clamp(rint(fl32(A[r][k] / s)), -127, 127).
+ * The weight variant has one scale per output channel (row of W, Ws [N]); the
+ * activation variant one per token (row of X, Xs [M]).
+ * A bf16 [R][lda], lda >= K, lda % 8 == 0; Q int8 [R][K] contiguous; S fp32 [R].
+ * K <= 32768 (FP8RL_ERR_UNSUPPORTED above).  Bit-exact.
+ * ---------------------------------------------------------------------- */
+int int8rl_quant_weight_channel(const uint16_t* W, int64_t N, int64_t K, int64_t ldw,
+                                int8_t* Wq, float* Ws, void* stream);
+int int8rl_quant_act_token(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
+                           int8_t* Xq, float* Xs, void* stream);
+
+/* ------------------------------------------------------------------------
+ * INT8 W8A8 GEMM (FlashRL INT8 rollout):
+ *   acc[m][n] = sum_k Xq[m][k] * Wq[n][k]  (int32, exact);
+ *   Y[m][n]   = bf16_rn( fl32( fl32(float_rn(acc)) * Xs[m] ) * Ws[n] )  (no FMA).
+ * Bit-exact in both acc and Y.  Requires K * 127^2 < 2^31 (K <= 133143) so
+ * that no accumulator can overflow; larger K returns FP8RL_ERR_UNSUPPORTED.
+ * Xq [M][K] int8, Xs [M] fp32, Wq [N][K] int8, Ws [N] fp32, Y bf16 [M][ldy].
+ * acc_or_null: optional int32 [M][N] copy of the accumulators.
+ * workspace as for the FP8 GEMM (int8rl_gemm_workspace_bytes).
+ * ---------------------------------------------------------------------- */
+size_t int8rl_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+int int8rl_gemm_w8a8(const int8_t* Xq, const float* Xs, const int8_t* Wq, const float* Ws,
+                     int64_t M, int64_t N, int64_t K, uint16_t* Y, int64_t ldy,
+                     int32_t* acc_or_null, void* workspace, size_t workspace_bytes,
+                     void* stream);
+
+/* ------------------------------------------------------------------------
+ * Every wait inside the library's kernels (on an mbarrier filled by TMA or by
+ * the tensor core) is bounded.  A wait that runs out records a code in a
+ * device-side word, abandons the tile and lets the kernel exit, so the CUDA
+ * context stays usable.  This call SYNCHRONIZES the current device, reads and
+ * clears that word, and returns FP8RL_OK or FP8RL_ERR_TIMEOUT.  *detail (may
+ * be NULL) receives the raw word (0 if none: kernel id in bits 24..31, the
+ * wait site in bits 16..23).
+ * ---------------------------------------------------------------------- */
+int fp8rl_check_device_error(uint32_t* detail);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8RL_H_ */

@@ -1,0 +1,174 @@
+// abi.cu -- the extern "C" boundary declared in include/fp8rl.h: synchronous
+// argument validation, then one launch (or a few) on the caller's stream.
+#include <vector>
+
+#include "fp8rl.h"
+#include "internal.h"
+
+namespace fp8rl {
+
+// Word written by a kernel whose bounded wait ran out (see fp8rl.h).
+__device__ uint32_t g_device_error = 0;
+
+cudaError_t read_and_clear_device_error(uint32_t* word) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return e;
+    uint32_t v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof v);
+    if (e != cudaSuccess) return e;
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
+    *word = v;
+    return e;
+}
+
+}  // namespace fp8rl
+
+namespace {
+
+using namespace fp8rl;
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? FP8RL_OK : FP8RL_ERR_CUDA; }
+
+// Common checks of a bf16 [R][ld] source with row length K (K a multiple of 128).
+int check_bf16_src(const uint16_t* A, int64_t R, int64_t K, int64_t ld, bool need_k128) {
+    if (R < 0 || K <= 0 || ld < K) return FP8RL_ERR_SHAPE;
+    if (need_k128 && K % kBlk) return FP8RL_ERR_SHAPE;
+    if (!need_k128 && K % 16) return FP8RL_ERR_SHAPE;
+    if (R > 0 && !A) return FP8RL_ERR_NULL;
+    if (!aligned16(A) || (ld * 2) % 16) return FP8RL_ERR_ALIGN;
+    return FP8RL_OK;
+}
+
+int check_weight_desc(const fp8rl_wdesc& d) {
+    if (d.N < 0 || d.N % kBlk) return FP8RL_ERR_SHAPE;
+    int rc = check_bf16_src(d.W, d.N, d.K, d.ldw, true);
+    if (rc) return rc;
+    if (d.N > 0 && (!d.Wq || !d.Ws)) return FP8RL_ERR_NULL;
+    if (!aligned16(d.Wq) || !aligned4(d.Ws)) return FP8RL_ERR_ALIGN;
+    return FP8RL_OK;
+}
+
+int check_gemm_common(const void* Xq, const float* Xs, const void* Wq, const float* Ws,
+                      int64_t M, int64_t N, int64_t K, const uint16_t* Y, int64_t ldy) {
+    if (M < 0 || N <= 0 || K <= 0 || N % kBlk || K % kBlk || ldy < N) return FP8RL_ERR_SHAPE;
+    if (!Wq || !Ws) return FP8RL_ERR_NULL;
+    if (M > 0 && (!Xq || !Xs || !Y)) return FP8RL_ERR_NULL;
+    if (!aligned16(Xq) || !aligned16(Wq) || !aligned16(Y) || !aligned4(Xs) || !aligned4(Ws))
+        return FP8RL_ERR_ALIGN;
+    if ((ldy * 2) % 16) return FP8RL_ERR_ALIGN;
+    return FP8RL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fp8rl_status_string(int status) {
+    switch (status) {
+        case FP8RL_OK: return "FP8RL_OK";
+        case FP8RL_ERR_NULL: return "FP8RL_ERR_NULL: required pointer is NULL";
+        case FP8RL_ERR_SHAPE: return "FP8RL_ERR_SHAPE: invalid size or leading dimension";
+        case FP8RL_ERR_ALIGN: return "FP8RL_ERR_ALIGN: pointer or row pitch not 16-byte aligned";
+        case FP8RL_ERR_WORKSPACE: return "FP8RL_ERR_WORKSPACE: workspace too small";
+        case FP8RL_ERR_CUDA: return "FP8RL_ERR_CUDA: CUDA runtime reported an error";
+        case FP8RL_ERR_UNSUPPORTED: return "FP8RL_ERR_UNSUPPORTED: size above a documented limit";
+        case FP8RL_ERR_TIMEOUT: return "FP8RL_ERR_TIMEOUT: a bounded device-side wait ran out";
+        default: return "FP8RL_ERR_UNKNOWN";
+    }
+}
+
+int fp8rl_abi_version(void) { return FP8RL_ABI_VERSION; }
+
+int fp8rl_quant_weight_block(const uint16_t* W, int64_t N, int64_t K, int64_t ldw, uint8_t* Wq,
+                             float* Ws, void* stream) {
+    fp8rl_wdesc d{W, Wq, Ws, N, K, ldw};
+    return fp8rl_quant_weight_block_grouped(&d, 1, stream);
+}
+
+int fp8rl_quant_weight_block_grouped(const fp8rl_wdesc* descs, int n, void* stream) {
+    if (n < 0) return FP8RL_ERR_SHAPE;
+    if (n > 0 && !descs) return FP8RL_ERR_NULL;
+    std::vector<WeightDesc> v;
+    v.reserve(n);
+    for (int i = 0; i < n; ++i) {
+        int rc = check_weight_desc(descs[i]);
+        if (rc) return rc;
+        v.push_back({descs[i].W, descs[i].Wq, descs[i].Ws, descs[i].N, descs[i].K, descs[i].ldw});
+    }
+    return cuda_status(launch_quant_weight_block(v.data(), n, as_stream(stream)));
+}
+
+int fp8rl_quant_act_group(const uint16_t* X, int64_t M, int64_t K, int64_t ldx, uint8_t* Xq,
+                          float* Xs, void* stream) {
+    int rc = check_bf16_src(X, M, K, ldx, true);
+    if (rc) return rc;
+    if (M > 0 && (!Xq || !Xs)) return FP8RL_ERR_NULL;
+    if (!aligned16(Xq) || !aligned4(Xs)) return FP8RL_ERR_ALIGN;
+    if (M > 65535LL * 16) return FP8RL_ERR_UNSUPPORTED;
+    return cuda_status(launch_quant_act_group(X, M, K, ldx, Xq, Xs, as_stream(stream)));
+}
+
+size_t fp8rl_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    return gemm_fp8_workspace_bytes(M, N, K);
+}
+
+int fp8rl_gemm_w8a8_block(const uint8_t* Xq, const float* Xs, const uint8_t* Wq, const float* Ws,
+                          int64_t M, int64_t N, int64_t K, uint16_t* Y, int64_t ldy,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_gemm_common(Xq, Xs, Wq, Ws, M, N, K, Y, ldy);
+    if (rc) return rc;
+    if (M > 65535LL * 32) return FP8RL_ERR_UNSUPPORTED;
+    const size_t need = gemm_fp8_workspace_bytes(M, N, K);
+    if (workspace_bytes < need || (need && !workspace)) return FP8RL_ERR_WORKSPACE;
+    if (M == 0) return FP8RL_OK;
+    return cuda_status(launch_gemm_fp8(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, workspace,
+                                       workspace_bytes, as_stream(stream)));
+}
+
+int int8rl_quant_weight_channel(const uint16_t* W, int64_t N, int64_t K, int64_t ldw, int8_t* Wq,
+                                float* Ws, void* stream) {
+    int rc = check_bf16_src(W, N, K, ldw, true);
+    if (rc) return rc;
+    if (K > kInt8MaxK) return FP8RL_ERR_UNSUPPORTED;
+    if (N > 0 && (!Wq || !Ws)) return FP8RL_ERR_NULL;
+    if (!aligned16(Wq) || !aligned4(Ws)) return FP8RL_ERR_ALIGN;
+    return cuda_status(launch_quant_int8_rows(W, N, K, ldw, Wq, Ws, as_stream(stream)));
+}
+
+int int8rl_quant_act_token(const uint16_t* X, int64_t M, int64_t K, int64_t ldx, int8_t* Xq,
+                           float* Xs, void* stream) {
+    return int8rl_quant_weight_channel(X, M, K, ldx, Xq, Xs, stream);
+}
+
+size_t int8rl_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    return gemm_int8_workspace_bytes(M, N, K);
+}
+
+int int8rl_gemm_w8a8(const int8_t* Xq, const float* Xs, const int8_t* Wq, const float* Ws,
+                     int64_t M, int64_t N, int64_t K, uint16_t* Y, int64_t ldy,
+                     int32_t* acc_or_null, void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_gemm_common(Xq, Xs, Wq, Ws, M, N, K, Y, ldy);
+    if (rc) return rc;
+    if (K > 133143) return FP8RL_ERR_UNSUPPORTED;       // 127^2 * K must stay below 2^31
+    if (M > 65535LL * 32) return FP8RL_ERR_UNSUPPORTED;
+    if (acc_or_null && (reinterpret_cast<uintptr_t>(acc_or_null) & 7u)) return FP8RL_ERR_ALIGN;
+    const size_t need = gemm_int8_workspace_bytes(M, N, K);
+    if (workspace_bytes < need || (need && !workspace)) return FP8RL_ERR_WORKSPACE;
+    if (M == 0) return FP8RL_OK;
+    return cuda_status(launch_gemm_int8(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, acc_or_null, workspace,
+                                        workspace_bytes, as_stream(stream)));
+}
+
+int fp8rl_check_device_error(uint32_t* detail) {
+    uint32_t w = 0;
+    cudaError_t e = read_and_clear_device_error(&w);
+    if (detail) *detail = w;
+    if (e != cudaSuccess) return FP8RL_ERR_CUDA;
+    return w ? FP8RL_ERR_TIMEOUT : FP8RL_OK;
+}
+
+}  // extern "C"

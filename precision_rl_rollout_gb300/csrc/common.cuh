@@ -1,0 +1,91 @@
+// common.cuh -- small device helpers shared by the library's kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace fp8rl {
+
+// 16-byte streaming load that bypasses L1 (each byte is read once).
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// bf16 pair packed in a 32-bit word -> the two fp32 values (exact).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Running per-lane maximum of |bf16| as 16-bit integers: for finite values the
+// magnitude bits order like the magnitudes, so integer max == |x| max.
+__device__ __forceinline__ uint32_t absmax2(uint32_t acc, uint32_t w) {
+    return __vmaxu2(acc, w & 0x7FFF7FFFu);
+}
+__device__ __forceinline__ uint32_t absmax_v4(uint32_t acc, uint4 v) {
+    acc = absmax2(acc, v.x);
+    acc = absmax2(acc, v.y);
+    acc = absmax2(acc, v.z);
+    return absmax2(acc, v.w);
+}
+// Fold the two 16-bit lanes and widen to an fp32 value.
+__device__ __forceinline__ float absmax_fold(uint32_t acc) {
+    uint32_t m = max(acc & 0xFFFFu, acc >> 16);
+    return __uint_as_float(m << 16);
+}
+
+// Two fp32 values -> two E4M3FN codes (round to nearest even, saturate to
+// +-448), first argument in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+    return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+}
+
+// Eight bf16 (one 16-byte chunk) divided by s (IEEE, round to nearest) and
+// encoded to eight E4M3FN codes, packed little-endian into 8 bytes.
+__device__ __forceinline__ uint2 quant8_e4m3(uint4 v, float s) {
+    uint2 o;
+    o.x = e4m3x2(__fdiv_rn(bf16_lo(v.x), s), __fdiv_rn(bf16_hi(v.x), s)) |
+          (e4m3x2(__fdiv_rn(bf16_lo(v.y), s), __fdiv_rn(bf16_hi(v.y), s)) << 16);
+    o.y = e4m3x2(__fdiv_rn(bf16_lo(v.z), s), __fdiv_rn(bf16_hi(v.z), s)) |
+          (e4m3x2(__fdiv_rn(bf16_lo(v.w), s), __fdiv_rn(bf16_hi(v.w), s)) << 16);
+    return o;
+}
+
+__device__ __forceinline__ float fp8_scale_from_amax(float amax) {
+    return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
+}
+__device__ __forceinline__ float int8_scale_from_amax(float amax) {
+    return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 127.0f);
+}
+
+// One bf16 -> int8 code: clamp(rint(x / s), -127, 127).
+__device__ __forceinline__ uint32_t q_int8(float x, float s) {
+    int q = __float2int_rn(__fdiv_rn(x, s));
+    q = min(127, max(-127, q));
+    return (uint32_t)(q & 0xFF);
+}
+__device__ __forceinline__ uint2 quant8_int8(uint4 v, float s) {
+    uint2 o;
+    o.x = q_int8(bf16_lo(v.x), s) | (q_int8(bf16_hi(v.x), s) << 8) |
+          (q_int8(bf16_lo(v.y), s) << 16) | (q_int8(bf16_hi(v.y), s) << 24);
+    o.y = q_int8(bf16_lo(v.z), s) | (q_int8(bf16_hi(v.z), s) << 8) |
+          (q_int8(bf16_lo(v.w), s) << 16) | (q_int8(bf16_hi(v.w), s) << 24);
+    return o;
+}
+
+// fp32 -> bf16 bits, round to nearest even (the CUDA intrinsic).
+__device__ __forceinline__ uint32_t f32_to_bf16_bits(float f) {
+    __nv_bfloat16 h = __float2bfloat16_rn(f);
+    return (uint32_t)(*reinterpret_cast<unsigned short*>(&h));
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    return f32_to_bf16_bits(lo) | (f32_to_bf16_bits(hi) << 16);
+}
+
+}  // namespace fp8rl

@@ -1,0 +1,45 @@
+// internal.h -- launchers behind the C ABI (fp8rl.h).  Arguments reaching these
+// functions have been validated by abi.cu; the launchers only size grids and
+// launch on the given stream.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace fp8rl {
+
+constexpr int kBlk = 128;          // weight block edge and activation group length
+constexpr int kMaxGroup = 256;        // tensors per grouped requant launch
+constexpr int64_t kInt8MaxK = 32768;  // row length held in registers by the INT8 quantizer
+
+struct WeightDesc {
+    const uint16_t* W;
+    uint8_t* Wq;
+    float* Ws;
+    int64_t N, K, ldw;
+};
+
+cudaError_t launch_quant_weight_block(const WeightDesc* d, int n, cudaStream_t st);
+cudaError_t launch_quant_act_group(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
+                                   uint8_t* Xq, float* Xs, cudaStream_t st);
+cudaError_t launch_quant_int8_rows(const uint16_t* A, int64_t R, int64_t K, int64_t lda,
+                                   int8_t* Q, float* S, cudaStream_t st);
+
+// FP8 block-scaled GEMM.
+size_t gemm_fp8_workspace_bytes(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_gemm_fp8(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
+                            const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
+                            int64_t ldy, void* ws, size_t ws_bytes, cudaStream_t st);
+
+// INT8 GEMM.
+size_t gemm_int8_workspace_bytes(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_gemm_int8(const int8_t* Xq, const float* Xs, const int8_t* Wq,
+                             const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
+                             int64_t ldy, int32_t* acc, void* ws, size_t ws_bytes,
+                             cudaStream_t st);
+
+// Device-side record of a bounded wait that ran out (0 = none).
+cudaError_t read_and_clear_device_error(uint32_t* word);
+
+}  // namespace fp8rl

@@ -1,0 +1,185 @@
+// quant.cu -- the HBM-bound quantizers of the 8-bit rollout path.
+//
+//  * FP8 weight requant, 128x128 blocks (FP8-RL, Abstract: weights change every
+//    step and are quantized again; contribution (i): blockwise FP8).
+//  * FP8 activation quant, 1x128 groups per token (the A8 of W8A8).
+//  * INT8 per-row quant for weights (per output channel) and activations (per
+//    token) (FlashRL write-up, Fig. 1: INT8 rollout).
+//
+// Every byte of input is read once with 16-byte streaming loads and every code
+// written once; amax is an integer max over the bf16 magnitude bits followed by
+// warp reductions; the division x / s is the IEEE round-to-nearest fp32 divide
+// and the conversion is the hardware E4M3 convert with round-to-nearest-even and
+// saturation, so every output bit is fixed by the input bits.
+#include "common.cuh"
+#include "internal.h"
+
+namespace fp8rl {
+
+// ---------------------------------------------------------------- FP8 weights
+
+// One launch quantizes the 128x128 blocks of up to kMaxGroup tensors.  Block
+// ids are numbered tensor by tensor; block_start[i] is the first block of
+// tensor i and block_start[n] the total.
+struct WeightGroupParams {
+    int n;
+    int64_t block_start[kMaxGroup + 1];
+    const uint16_t* W[kMaxGroup];
+    uint8_t* Wq[kMaxGroup];
+    float* Ws[kMaxGroup];
+    int64_t ldw[kMaxGroup];
+    int64_t K[kMaxGroup];
+};
+
+// 256 threads per 128x128 block.  A block row is 256 B of bf16 = 16 chunks of
+// 16 B; chunk c = i*256 + t (i = 0..7) lies in row c/16 at column 8*(c%16), so
+// a warp reads two full 256-byte row segments per load.
+__global__ void __launch_bounds__(256)
+quant_weight_block_kernel(const __grid_constant__ WeightGroupParams p) {
+    const int64_t b = blockIdx.x;
+    int lo = 0, hi = p.n - 1;                     // tensor that owns block b
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (p.block_start[mid] <= b) lo = mid; else hi = mid - 1;
+    }
+    const int ti = lo;
+    const int64_t K = p.K[ti], ldw = p.ldw[ti];
+    const int64_t KB = K / kBlk;
+    const int64_t local = b - p.block_start[ti];
+    const int64_t nb = local / KB, kb = local - nb * KB;
+
+    const int t = threadIdx.x;
+    const int r0 = t >> 4;                        // row within the block for i = 0
+    const int col = (t & 15) * 8;                 // element column within the block
+    const uint16_t* src = p.W[ti] + (nb * kBlk + r0) * ldw + kb * kBlk + col;
+
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = ld_stream_v4(src + (int64_t)i * 16 * ldw);
+
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = absmax_v4(m, v[i]);
+    m = __reduce_max_sync(0xffffffffu, max(m & 0xFFFFu, m >> 16));
+    __shared__ uint32_t red[8];
+    if ((t & 31) == 0) red[t >> 5] = m;
+    __syncthreads();
+    m = red[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) m = max(m, red[w]);
+    const float s = fp8_scale_from_amax(__uint_as_float(m << 16));
+
+    uint8_t* dst = p.Wq[ti] + (nb * kBlk + r0) * K + kb * kBlk + col;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        *reinterpret_cast<uint2*>(dst + (int64_t)i * 16 * K) = quant8_e4m3(v[i], s);
+    if (t == 0) p.Ws[ti][nb * KB + kb] = s;
+}
+
+cudaError_t launch_quant_weight_block(const WeightDesc* d, int n, cudaStream_t st) {
+    for (int base = 0; base < n; base += kMaxGroup) {
+        WeightGroupParams p;
+        p.n = 0;
+        int64_t total = 0;
+        for (int i = base; i < n && p.n < kMaxGroup; ++i) {
+            const int j = p.n++;
+            p.block_start[j] = total;
+            p.W[j] = d[i].W;
+            p.Wq[j] = d[i].Wq;
+            p.Ws[j] = d[i].Ws;
+            p.ldw[j] = d[i].ldw;
+            p.K[j] = d[i].K;
+            total += (d[i].N / kBlk) * (d[i].K / kBlk);
+        }
+        p.block_start[p.n] = total;
+        if (total == 0) continue;
+        if (total > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+        quant_weight_block_kernel<<<(unsigned)total, 256, 0, st>>>(p);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+// ---------------------------------------------------------------- FP8 activations
+
+// 256 threads = 16 half-warps; half-warp h quantizes group g = blockIdx.x of
+// token m = 16*blockIdx.y + h: each of its 16 lanes holds one 16-byte chunk
+// (8 values) of the 128-value group.
+__global__ void __launch_bounds__(256)
+quant_act_group_kernel(const uint16_t* __restrict__ X, int64_t M, int64_t K, int64_t ldx,
+                       uint8_t* __restrict__ Xq, float* __restrict__ Xs) {
+    const int t = threadIdx.x;
+    const int lane16 = t & 15;
+    const int64_t m = (int64_t)blockIdx.y * 16 + (t >> 4);
+    const int64_t g = blockIdx.x;
+    const bool valid = m < M;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (valid) v = ld_stream_v4(X + m * ldx + g * kBlk + lane16 * 8);
+    uint32_t a = absmax_v4(0u, v);
+    a = max(a & 0xFFFFu, a >> 16);
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) a = max(a, __shfl_xor_sync(0xffffffffu, a, off));
+    const float s = fp8_scale_from_amax(__uint_as_float(a << 16));
+    if (valid) {
+        *reinterpret_cast<uint2*>(Xq + m * K + g * kBlk + lane16 * 8) = quant8_e4m3(v, s);
+        if (lane16 == 0) Xs[g * M + m] = s;
+    }
+}
+
+cudaError_t launch_quant_act_group(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
+                                   uint8_t* Xq, float* Xs, cudaStream_t st) {
+    if (M == 0) return cudaSuccess;
+    dim3 grid((unsigned)(K / kBlk), (unsigned)((M + 15) / 16));
+    quant_act_group_kernel<<<grid, 256, 0, st>>>(X, M, K, ldx, Xq, Xs);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- INT8 rows
+
+// One CTA of 256 threads per row; the row (K <= kInt8MaxK) is held in
+// registers between the amax pass and the quantization pass: chunk c = i*256+t.
+constexpr int kRowChunksPerThread = kInt8MaxK / (256 * 8);
+
+__global__ void __launch_bounds__(256)
+quant_int8_rows_kernel(const uint16_t* __restrict__ A, int64_t K, int64_t lda,
+                       int8_t* __restrict__ Q, float* __restrict__ S) {
+    const int64_t r = blockIdx.x;
+    const int t = threadIdx.x;
+    const int chunks = (int)(K / 8);
+    const uint16_t* src = A + r * lda;
+    uint4 v[kRowChunksPerThread];
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < kRowChunksPerThread; ++i) {
+        const int c = i * 256 + t;
+        v[i] = make_uint4(0, 0, 0, 0);
+        if (c < chunks) v[i] = ld_stream_v4(src + (int64_t)c * 8);
+        m = absmax_v4(m, v[i]);
+    }
+    m = __reduce_max_sync(0xffffffffu, max(m & 0xFFFFu, m >> 16));
+    __shared__ uint32_t red[8];
+    if ((t & 31) == 0) red[t >> 5] = m;
+    __syncthreads();
+    m = red[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) m = max(m, red[w]);
+    const float s = int8_scale_from_amax(__uint_as_float(m << 16));
+    int8_t* dst = Q + r * K;
+#pragma unroll
+    for (int i = 0; i < kRowChunksPerThread; ++i) {
+        const int c = i * 256 + t;
+        if (c < chunks) *reinterpret_cast<uint2*>(dst + (int64_t)c * 8) = quant8_int8(v[i], s);
+    }
+    if (t == 0) S[r] = s;
+}
+
+cudaError_t launch_quant_int8_rows(const uint16_t* A, int64_t R, int64_t K, int64_t lda,
+                                   int8_t* Q, float* S, cudaStream_t st) {
+    if (R == 0) return cudaSuccess;
+    if (R > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    quant_int8_rows_kernel<<<(unsigned)R, 256, 0, st>>>(A, K, lda, Q, S);
+    return cudaGetLastError();
+}
+
+}  // namespace fp8rl

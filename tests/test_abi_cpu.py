@@ -1,0 +1,116 @@
+"""CPU checks of the C ABI: the library loads, exports every function that
+include/fp8rl.h declares, and rejects invalid arguments synchronously, before
+any CUDA call (these paths never touch a device, so they run without a GPU).
+Also checks that the product package never reaches the oracle."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from precision_rl_rollout_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8rl.h")
+A = 0x10000  # a 16-byte-aligned fake device address: validation never dereferences it
+
+
+@pytest.fixture(scope="module")
+def lib():
+    try:
+        build.build()
+    except RuntimeError as e:  # no nvcc on this machine
+        pytest.skip(str(e))
+    return binding.load()
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_binding_exports():
+    assert _declared_functions() == sorted(binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    assert lib.fp8rl_abi_version() == 1
+    for s in range(8):
+        assert lib.fp8rl_status_string(s).decode().startswith(binding.STATUS[s])
+
+
+def test_quant_weight_block_validation(lib):
+    q = lib.fp8rl_quant_weight_block
+    assert q(None, 128, 128, 128, A, A, None) == 1                  # NULL W
+    assert q(A, 100, 128, 128, A, A, None) == 2                     # N % 128
+    assert q(A, 128, 200, 200, A, A, None) == 2                     # K % 128
+    assert q(A, 128, 256, 128, A, A, None) == 2                     # ldw < K
+    assert q(A + 2, 128, 128, 128, A, A, None) == 3                 # misaligned W
+    assert q(A, 128, 128, 132, A, A, None) == 3                     # row pitch 264 B
+    assert q(A, 128, 128, 128, A + 8, A, None) == 3                 # misaligned Wq
+    assert q(A, 128, 128, 128, None, A, None) == 1
+    assert q(A, 0, 128, 128, A, A, None) == 0                       # empty: nothing launched
+
+
+def test_grouped_requant_validates_every_descriptor_first(lib):
+    D = binding.FP8RL_WDESC
+    good = D(A, A, A, 128, 128, 128)
+    bad = D(A, A, A, 128, 100, 128)
+    arr = (D * 3)(good, good, bad)
+    assert lib.fp8rl_quant_weight_block_grouped(arr, 3, None) == 2
+    assert lib.fp8rl_quant_weight_block_grouped(None, 2, None) == 1
+    assert lib.fp8rl_quant_weight_block_grouped(arr, -1, None) == 2
+    empty = (D * 2)(D(A, A, A, 0, 128, 128), D(A, A, A, 0, 256, 256))
+    assert lib.fp8rl_quant_weight_block_grouped(empty, 2, None) == 0
+
+
+def test_act_quant_validation(lib):
+    q = lib.fp8rl_quant_act_group
+    assert q(A, 4, 100, 100, A, A, None) == 2
+    assert q(A, -1, 128, 128, A, A, None) == 2
+    assert q(A, 4, 128, 128, None, A, None) == 1
+    assert q(A, 4, 128, 128, A, A + 2, None) == 3
+    assert q(A, 0, 128, 128, A, A, None) == 0
+
+
+def test_gemm_validation(lib):
+    g = lib.fp8rl_gemm_w8a8_block
+    ws = lib.fp8rl_gemm_workspace_bytes(64, 256, 256)
+    assert g(A, A, A, A, 4, 100, 128, A, 100, None, ws, None) == 2   # N % 128
+    assert g(A, A, A, A, 4, 128, 100, A, 128, None, ws, None) == 2   # K % 128
+    assert g(A, A, A, A, 4, 128, 128, A, 64, None, ws, None) == 2    # ldy < N
+    assert g(A, A, None, A, 4, 128, 128, A, 128, None, ws, None) == 1
+    assert g(A + 4, A, A, A, 4, 128, 128, A, 128, None, ws, None) == 3
+    assert g(A, A, A, A, 4, 128, 128, A, 132, None, ws, None) == 3   # row pitch 264 B
+    assert g(A, A, A, A, 0, 128, 128, A, 128, None, ws, None) == 0   # empty batch
+    i = lib.int8rl_gemm_w8a8
+    assert i(A, A, A, A, 4, 128, 140032, A, 128, None, None, 0, None) == 6  # K * 127^2 >= 2^31
+    assert i(A, A, A, A, 4, 128, 128, A, 128, A + 4, None, 0, None) == 3    # acc alignment
+    assert i(A, A, A, A, 0, 128, 128, A, 128, None, None, 0, None) == 0
+
+
+def test_gemm_workspace_query_is_monotone(lib):
+    for f in (lib.fp8rl_gemm_workspace_bytes, lib.int8rl_gemm_workspace_bytes):
+        a = f(1, 4608, 3584)
+        b = f(256, 4608, 3584)
+        assert 0 <= a <= b or b == 0
+
+
+def test_int8_quant_validation(lib):
+    q = lib.int8rl_quant_weight_channel
+    assert q(A, 4, 65536, 65536, A, A, None) == 6                   # K above the register-resident limit
+    assert q(A, 4, 100, 100, A, A, None) == 2
+    assert lib.int8rl_quant_act_token(A, 4, 128, 128, None, A, None) == 1
+
+
+def test_product_package_never_reaches_the_oracle():
+    pkg = os.path.join(ROOT, "precision_rl_rollout_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp", ".c")):
+                text = open(os.path.join(dirpath, f), errors="ignore").read()
+                assert not re.search(r"(import\s+oracle|from\s+oracle|\boracle\.|liboracle|oracle/)", text), \
+                    f"{f} references the oracle package"

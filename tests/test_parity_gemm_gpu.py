@@ -1,0 +1,116 @@
+"""GPU parity of the GEMMs against the CPU oracle.
+
+FP8: |y - y_ref| <= 2^-7 |y_ref| + 1e-3 rms(y_ref) element by element, y_ref
+the oracle's fp64 dequant-matmul of the same codes (rms over the compared
+rows).  INT8: accumulators and bf16 outputs bit-exact.  Operands are always
+quantized by the oracle (or drawn by the generator), never by the CUDA path."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from precision_rl_rollout_gb300 import binding as fb
+from precision_rl_rollout_gb300 import synth
+from parity_util import (assert_fp8_gemm_close, dev, host, oracle_fp8_act, oracle_fp8_weight,
+                         oracle_int8_act, oracle_int8_weight, sample_rows)
+
+pytestmark = pytest.mark.gpu
+
+
+def _fp8_case(M, N, K, seed_w, seed_x, rows=None, what=""):
+    Wq, Ws = oracle_fp8_weight(N, K, seed_w)
+    Xq, Xs = oracle_fp8_act(M, K, seed_x)
+    Y = fb.fp8rl_gemm_w8a8_block(dev(Xq), dev(Xs), dev(Wq), dev(Ws))
+    Yh = host(Y)
+    if rows is None:
+        rows = np.arange(M)
+    ref = oracle.fp8_gemm(Xq[rows], Xs[:, rows], Wq, Ws)
+    return assert_fp8_gemm_close(Yh[rows], ref, what or f"M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 512, 256), (1, 128, 128), (5, 256, 384), (37, 384, 640),
+                                   (64, 256, 1024), (129, 128, 256), (300, 384, 384)])
+def test_fp8_gemm_small_full(cuda_lib, M, N, K):
+    _fp8_case(M, N, K, 100 + N + K, 200 + M + K)
+
+
+def test_fp8_gemm_tiny_config(cuda_lib):
+    Wq, Ws = oracle_fp8_weight(synth.TINY.N, synth.TINY.K, synth.seed_for(1, 0))
+    from parity_util import act_cpu
+    X = act_cpu(synth.TINY_M, synth.TINY.K, synth.seed_for(1, 1), n_outliers=2)
+    Xq, Xs = oracle.fp8_quant_act_group(synth.bf16_bits(X))
+    Y = fb.fp8rl_gemm_w8a8_block(dev(Xq), dev(Xs), dev(Wq), dev(Ws))
+    assert_fp8_gemm_close(host(Y), oracle.fp8_gemm(Xq, Xs, Wq, Ws), "tiny")
+
+
+def test_fp8_gemm_empty_batch_and_strided_output(cuda_lib):
+    Wq, Ws = oracle_fp8_weight(256, 256, 5)
+    Y0 = fb.fp8rl_gemm_w8a8_block(torch.empty(0, 256, dtype=torch.uint8, device="cuda"),
+                                  torch.empty(2, 0, device="cuda"), dev(Wq), dev(Ws))
+    assert Y0.shape == (0, 256)
+    Xq, Xs = oracle_fp8_act(9, 256, 6)
+    big = torch.full((9, 264), 7.0, dtype=torch.bfloat16, device="cuda")
+    fb.fp8rl_gemm_w8a8_block(dev(Xq), dev(Xs), dev(Wq), dev(Ws), Y=big[:, :256])
+    assert_fp8_gemm_close(host(big[:, :256]), oracle.fp8_gemm(Xq, Xs, Wq, Ws), "strided Y")
+    assert bool((big[:, 256:] == 7.0).all()), "GEMM wrote outside Y"
+
+
+@pytest.mark.parametrize("shape", synth.QWEN25_7B, ids=lambda s: s.name)
+def test_fp8_gemm_qwen7b_decode_m64_sampled(cuda_lib, shape):
+    _fp8_case(64, shape.N, shape.K, synth.seed_for(2, 0), synth.seed_for(2, 1),
+              rows=sample_rows(64, 6, seed=shape.N), what=f"7B {shape.name}")
+
+
+@pytest.mark.parametrize("M", synth.DECODE_M_SWEEP)
+@pytest.mark.parametrize("shape", synth.QWEN25_32B, ids=lambda s: s.name)
+def test_fp8_gemm_qwen32b_decode_sweep_sampled(cuda_lib, shape, M):
+    _fp8_case(M, shape.N, shape.K, synth.seed_for(3, 0), synth.seed_for(3, 1),
+              rows=sample_rows(M, 3, seed=M), what=f"32B {shape.name} M={M}")
+
+
+@pytest.mark.parametrize("shape", synth.QWEN25_32B, ids=lambda s: s.name)
+def test_fp8_gemm_qwen32b_prefill_sampled(cuda_lib, shape):
+    _fp8_case(synth.PREFILL_M, shape.N, shape.K, synth.seed_for(4, 0), synth.seed_for(4, 1),
+              rows=sample_rows(synth.PREFILL_M, 3, seed=shape.K), what=f"prefill {shape.name}")
+
+
+def _int8_case(M, N, K, seed_w, seed_x, rows=None):
+    Wq, Ws = oracle_int8_weight(N, K, seed_w)
+    Xq, Xs = oracle_int8_act(M, K, seed_x)
+    Y, acc = fb.int8rl_gemm_w8a8(dev(Xq), dev(Xs), dev(Wq), dev(Ws), want_acc=True)
+    if rows is None:
+        rows = np.arange(M)
+    want_acc, want_y = oracle.int8_gemm(Xq[rows], Xs[rows], Wq, Ws)
+    got_acc, got_y = host(acc)[rows], host(Y)[rows]
+    assert np.array_equal(got_acc, want_acc), f"acc differs at {np.argwhere(got_acc != want_acc)[:4].tolist()}"
+    assert np.array_equal(got_y, want_y), f"Y differs at {np.argwhere(got_y != want_y)[:4].tolist()}"
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 128), (16, 512, 256), (37, 384, 640), (300, 256, 384)])
+def test_int8_gemm_small_full(cuda_lib, M, N, K):
+    _int8_case(M, N, K, 300 + N, 400 + M)
+
+
+def test_int8_gemm_extreme_codes_exact(cuda_lib):
+    M, N, K = 3, 128, 27648
+    Xq = np.full((M, K), 127, np.int8)
+    Xq[1] = -127
+    Xq[2, ::2] = -127
+    Wq = np.full((N, K), 127, np.int8)
+    Xs = np.array([1.0, 0.5, 3.0], np.float32)
+    Ws = np.linspace(0.001, 2.0, N).astype(np.float32)
+    Y, acc = fb.int8rl_gemm_w8a8(dev(Xq), dev(Xs), dev(Wq), dev(Ws), want_acc=True)
+    want_acc, want_y = oracle.int8_gemm(Xq, Xs, Wq, Ws)
+    assert np.array_equal(host(acc), want_acc) and int(want_acc[0, 0]) == 127 * 127 * K
+    assert np.array_equal(host(Y), want_y)
+
+
+@pytest.mark.parametrize("M", synth.INT8_M_SWEEP)
+@pytest.mark.parametrize("shape", synth.QWEN25_32B, ids=lambda s: s.name)
+def test_int8_gemm_qwen32b_sampled(cuda_lib, shape, M):
+    _int8_case(M, shape.N, shape.K, synth.seed_for(5, 0), synth.seed_for(5, 1),
+               rows=sample_rows(M, 3, seed=M + shape.N))
+
+
+def test_no_device_error_after_gemms(cuda_lib):
+    assert fb.fp8rl_check_device_error() == 0

@@ -1,0 +1,150 @@
+"""GPU parity of the quantizers against the CPU oracle: codes and scales must be
+bit-exact.  Small cases are compared in full (several blocks, ragged token
+counts, strided inputs, planted edge cases); the Qwen2.5-7B/32B shapes are
+compared on sampled blocks/rows plus properties that hold at any size."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from precision_rl_rollout_gb300 import binding as fb
+from precision_rl_rollout_gb300 import synth
+from parity_util import (act_cpu, bits_u32, host, sample_blocks, sample_rows, weight_cpu)
+
+pytestmark = pytest.mark.gpu
+
+
+def _cmp_weight_block(W_cpu: torch.Tensor, Wq_gpu, Ws_gpu, what):
+    want_q, want_s = oracle.fp8_quant_weight_block(synth.bf16_bits(W_cpu))
+    got_q, got_s = host(Wq_gpu), host(Ws_gpu)
+    assert np.array_equal(bits_u32(got_s), bits_u32(want_s)), f"{what}: scales differ"
+    bad = np.argwhere(got_q != want_q)
+    assert bad.size == 0, f"{what}: {len(bad)} codes differ, first {bad[:4].tolist()}"
+
+
+def test_fp8_weight_requant_tiny(cuda_lib):
+    W = weight_cpu(synth.TINY.N, synth.TINY.K, synth.seed_for(1, 0))
+    Wq, Ws = fb.fp8rl_quant_weight_block(W.cuda())
+    _cmp_weight_block(W, Wq, Ws, "tiny")
+
+
+def test_fp8_weight_requant_edge_cases_and_strided_input(cuda_lib):
+    W = synth.edge_case_weight(384, 512, seed=31)
+    wide = torch.zeros(384, 640, dtype=torch.bfloat16)
+    wide[:, :512] = W
+    Wd = wide.cuda()[:, :512]                       # ldw = 640 > K
+    Wq, Ws = fb.fp8rl_quant_weight_block(Wd)
+    _cmp_weight_block(W, Wq, Ws, "edge")
+
+
+@pytest.mark.parametrize("shape", synth.QWEN25_7B, ids=lambda s: s.name)
+def test_fp8_weight_requant_qwen7b_sampled(cuda_lib, shape):
+    W = weight_cpu(shape.N, shape.K, synth.seed_for(2, 0))
+    Wq, Ws = fb.fp8rl_quant_weight_block(W.cuda())
+    torch.cuda.synchronize()
+    # any size: no NaN code, and every block's largest magnitude code is 448 (0x7E)
+    mag = (Wq & 0x7F)
+    assert not bool((mag == 0x7F).any())
+    blkmax = mag.view(shape.N // 128, 128, shape.K // 128, 128).amax(dim=(1, 3))
+    assert bool((blkmax == 0x7E).all())
+    Wq_h, Ws_h = host(Wq), host(Ws)
+    for nb, kb in sample_blocks(shape.N // 128, shape.K // 128, 40, seed=shape.K + shape.N):
+        blk = W[nb * 128:(nb + 1) * 128, kb * 128:(kb + 1) * 128].contiguous()
+        q, s = oracle.fp8_quant_weight_block(synth.bf16_bits(blk))
+        assert bits_u32(Ws_h[nb, kb:kb + 1])[0] == bits_u32(s)[0, 0], (nb, kb)
+        assert np.array_equal(Wq_h[nb * 128:(nb + 1) * 128, kb * 128:(kb + 1) * 128], q), (nb, kb)
+
+
+def test_grouped_requant_matches_oracle_across_launches(cuda_lib):
+    # more tensors than one grouped launch takes, with mixed shapes and pitches
+    rng = np.random.default_rng(8)
+    items, cpu = [], []
+    for i in range(300):
+        N = 128 * int(rng.integers(1, 3))
+        K = 128 * int(rng.integers(1, 4))
+        pad = 8 * int(rng.integers(0, 3))
+        Wc = synth.weight(N, K, 5000 + i, std=float(10.0 ** rng.uniform(-3, 1)))
+        big = torch.zeros(N, K + pad, dtype=torch.bfloat16)
+        big[:, :K] = Wc
+        Wd = big.cuda()[:, :K]
+        items.append((Wd, torch.empty(N, K, dtype=torch.uint8, device="cuda"),
+                      torch.empty(N // 128, K // 128, dtype=torch.float32, device="cuda")))
+        cpu.append(Wc)
+    fb.fp8rl_quant_weight_block_grouped(items)
+    for i in list(range(0, 300, 7)) + [255, 256, 299]:
+        _cmp_weight_block(cpu[i], items[i][1], items[i][2], f"grouped[{i}]")
+
+
+@pytest.mark.parametrize("M,K", [(1, 128), (5, 256), (16, 256), (17, 384), (33, 3584),
+                                 (64, 3584), (257, 640)])
+def test_fp8_act_quant_full(cuda_lib, M, K):
+    X = act_cpu(M, K, synth.seed_for(1, 1) + M)
+    Xq, Xs = fb.fp8rl_quant_act_group(X.cuda())
+    want_q, want_s = oracle.fp8_quant_act_group(synth.bf16_bits(X))
+    assert np.array_equal(bits_u32(host(Xs)), bits_u32(want_s))
+    assert np.array_equal(host(Xq), want_q)
+
+
+def test_fp8_act_quant_edge_rows_and_empty(cuda_lib):
+    X = synth.edge_case_activation(11, 640, seed=3)
+    Xq, Xs = fb.fp8rl_quant_act_group(X.cuda())
+    want_q, want_s = oracle.fp8_quant_act_group(synth.bf16_bits(X))
+    assert np.array_equal(bits_u32(host(Xs)), bits_u32(want_s))
+    assert np.array_equal(host(Xq), want_q)
+    Xq0, Xs0 = fb.fp8rl_quant_act_group(torch.empty(0, 256, dtype=torch.bfloat16, device="cuda"))
+    assert Xq0.shape == (0, 256) and Xs0.shape == (2, 0)
+
+
+@pytest.mark.parametrize("M", synth.DECODE_M_SWEEP)
+@pytest.mark.parametrize("K", [5120, 27648])
+def test_fp8_act_quant_qwen32b_decode(cuda_lib, M, K):
+    X = act_cpu(M, K, synth.seed_for(3, 1))
+    Xq, Xs = fb.fp8rl_quant_act_group(X.cuda())
+    want_q, want_s = oracle.fp8_quant_act_group(synth.bf16_bits(X))
+    assert np.array_equal(bits_u32(host(Xs)), bits_u32(want_s))
+    assert np.array_equal(host(Xq), want_q)
+
+
+def test_fp8_act_quant_prefill_sampled(cuda_lib):
+    M, K = synth.PREFILL_M, 27648
+    X = act_cpu(M, K, synth.seed_for(4, 1))
+    Xq, Xs = fb.fp8rl_quant_act_group(X.cuda())
+    rows = sample_rows(M, 24, seed=4)
+    want_q, want_s = oracle.fp8_quant_act_group(synth.bf16_bits(X[rows]))
+    assert np.array_equal(bits_u32(host(Xs)[:, rows]), bits_u32(want_s))
+    assert np.array_equal(host(Xq)[rows], want_q)
+
+
+@pytest.mark.parametrize("R,K", [(1, 128), (7, 256), (128, 5120), (33, 27648)])
+def test_int8_row_quant_full(cuda_lib, R, K):
+    A = act_cpu(R, K, 77 + R)
+    for fn in (fb.int8rl_quant_weight_channel, fb.int8rl_quant_act_token):
+        Q, S = fn(A.cuda())
+        want_q, want_s = oracle.int8_quant_rows(synth.bf16_bits(A))
+        assert np.array_equal(bits_u32(host(S)), bits_u32(want_s))
+        assert np.array_equal(host(Q), want_q)
+
+
+def test_int8_row_quant_edge_and_strided(cuda_lib):
+    A = synth.edge_case_activation(9, 384, seed=12)
+    wide = torch.zeros(9, 512, dtype=torch.bfloat16)
+    wide[:, :384] = A
+    Q, S = fb.int8rl_quant_act_token(wide.cuda()[:, :384])
+    want_q, want_s = oracle.int8_quant_rows(synth.bf16_bits(A))
+    assert np.array_equal(bits_u32(host(S)), bits_u32(want_s))
+    assert np.array_equal(host(Q), want_q)
+
+
+@pytest.mark.parametrize("shape", synth.QWEN25_32B, ids=lambda s: s.name)
+def test_int8_weight_quant_qwen32b_sampled(cuda_lib, shape):
+    W = weight_cpu(shape.N, shape.K, synth.seed_for(5, 0))
+    Q, S = fb.int8rl_quant_weight_channel(W.cuda())
+    rows = sample_rows(shape.N, 32, seed=shape.N)
+    want_q, want_s = oracle.int8_quant_rows(synth.bf16_bits(W[rows]))
+    assert np.array_equal(bits_u32(host(S)[rows]), bits_u32(want_s))
+    assert np.array_equal(host(Q)[rows], want_q)
+    assert int(Q.abs().amax(dim=1).min()) == 127
+
+
+def test_no_device_error_recorded(cuda_lib):
+    assert fb.fp8rl_check_device_error() == 0
