@@ -5,24 +5,6 @@
 #include "fp8rl.h"
 #include "internal.h"
 
-namespace fp8rl {
-
-// Word written by a kernel whose bounded wait ran out (see fp8rl.h).
-__device__ uint32_t g_device_error = 0;
-
-cudaError_t read_and_clear_device_error(uint32_t* word) {
-    cudaError_t e = cudaDeviceSynchronize();
-    if (e != cudaSuccess) return e;
-    uint32_t v = 0;
-    e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof v);
-    if (e != cudaSuccess) return e;
-    const uint32_t zero = 0;
-    e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
-    *word = v;
-    return e;
-}
-
-}  // namespace fp8rl
 
 namespace {
 

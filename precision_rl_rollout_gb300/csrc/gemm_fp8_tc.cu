@@ -1,0 +1,401 @@
+// gemm_fp8_tc.cu -- block-scaled FP8 W8A8 GEMMs on the 5th-generation tensor
+// cores (tcgen05) of sm_103a, fed by TMA.
+//
+// Math (FP8-RL, Abstract, contribution (i): FP8 W8A8 linear layers with
+// blockwise scales; block 128x128 for W and 1x128 for X in this library):
+//   Y[m][n] = bf16( sum_kb Xs[kb][m] * Ws[n/128][kb] * P_kb[m][n] ),
+//   P_kb[m][n] = sum_{k in block kb} e4m3(Xq[m][k]) * e4m3(Wq[n][k])   (fp32)
+// The block scales are arbitrary fp32 values (amax/448), which the tensor
+// core's own block-scaled MMA kinds (power-of-two / E4M3 scales on 16- or
+// 32-element blocks) cannot express, so each 128-wide K block is one MMA
+// group into its own TMEM buffer and the epilogue warps promote it into fp32
+// registers with that block's scale product.  TMEM buffers are double
+// buffered so the MMAs of block kb+1 overlap the promotion of block kb.
+//
+// Decode kernel (small M, HBM-bound; the long-tail rollout batches of "Taming
+// the Long Tail" (ASPLOS'26 blog), section 3.2 roofline and section 4.3.1):
+// swap-AB -- the MMA's M side is 128 weight rows, its N side the (padded)
+// tokens -- so each CTA streams a disjoint 128-row weight slab exactly once.
+// Split-K CTAs of one slab form a thread-block cluster and add their fp32
+// partials through distributed shared memory in a fixed order
+// (deterministic; no global workspace).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+#include "sm100_ptx.cuh"
+
+namespace fp8rl {
+
+using namespace sm100;
+
+// Word recording the first bounded wait that ran out (fp8rl_check_device_error).
+__device__ uint32_t g_device_error = 0;
+
+cudaError_t read_and_clear_device_error(uint32_t* word) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return e;
+    uint32_t v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof v);
+    if (e != cudaSuccess) return e;
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
+    *word = v;
+    return e;
+}
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
+enum : uint32_t { kKernelDecode = 1, kKernelPrefill = 2 };
+
+__device__ __forceinline__ void record_timeout(uint32_t kernel, uint32_t site, volatile int* abort) {
+    atomicCAS(&g_device_error, 0u, (kernel << 24) | (site << 16) | 1u);
+    *abort = 1;
+}
+
+// ------------------------------------------------------------------ host: tensor maps
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// Row-major byte matrix [rows][cols] (cols contiguous, row pitch `pitch` bytes),
+// loaded in boxes of 128 columns x box_rows rows with the 128-byte swizzle that
+// the UMMA K-major SW128 descriptor expects.  Rows beyond `rows` read as zero.
+bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint64_t pitch,
+                  uint32_t box_rows) {
+    auto enc = get_encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {pitch};
+    cuuint32_t box[2] = {128, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int num_sms() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 148;
+    }
+    return n;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ decode kernel
+
+struct DecodeParams {
+    const float* Xs;   // [KB][M]
+    const float* Ws;   // [N/128][KB]
+    uint16_t* Y;       // [M][ldy]
+    int64_t M, ldy;
+    int KB;            // K / 128
+    int kb_per_split;  // K blocks per split-K CTA
+    int split;         // CTAs per cluster (split-K factor)
+};
+
+template <int MT>
+struct DecodeCfg {
+    static constexpr int kEpiWarps = MT >= 128 ? 8 : 4;
+    static constexpr int kThreads = 64 + 32 * kEpiWarps;
+    static constexpr int kCols = MT / (kEpiWarps / 4);         // TMEM columns per epilogue thread
+    static constexpr int kStageBytes = 16384 + MT * 128;       // W tile + X tile
+    // MT <= 64: two CTAs per SM (2 x (smem + 1 KB reserved) <= 228 KB); larger: one.
+    static constexpr int kStages = MT == 16 ? 6 : MT == 32 ? 5 : MT == 64 ? 4 : MT == 128 ? 5 : 4;
+    static constexpr int kMaxKbPerSplit = 32;                     // K blocks per split-K CTA
+    static constexpr int kScaleBytes = kMaxKbPerSplit * MT * 4;   // per-block scale products
+    static constexpr int kTmemCols = 2 * MT < 32 ? 32 : 2 * MT;
+    static constexpr int kMinBlocks = MT <= 64 ? 2 : 1;             // CTAs per SM the registers allow
+    static constexpr int kChunk = kCols >= 128 ? 16 : (kCols >= 32 ? 32 : 16);  // TMEM load width
+    static constexpr int kBarOffset = kStages * kStageBytes + kScaleBytes;
+    static constexpr int kSmemBytes = kBarOffset + 256 + 1024;   // barriers + alignment slack
+    static_assert(MT * 128 * 4 <= kStages * kStageBytes, "reduction buffer must fit the stage area");
+};
+
+template <int MT>
+__global__ void __launch_bounds__(DecodeCfg<MT>::kThreads, DecodeCfg<MT>::kMinBlocks)
+gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                       const __grid_constant__ DecodeParams p) {
+    using C = DecodeCfg<MT>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* cscale = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
+    // bars: full[S], empty[S], tfull[2], tempty[2]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 4);
+    volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + C::kStages);
+    const uint32_t tfull0 = smem_u32(bars + 2 * C::kStages), tempty0 = smem_u32(bars + 2 * C::kStages + 2);
+
+    const uint32_t warp = warp_id(), lane = lane_id();
+    const int split_idx = blockIdx.x;                  // rank within the cluster
+    const int nt = blockIdx.y, mt = blockIdx.z;
+    const int kb0 = split_idx * p.kb_per_split;
+    const int nkb = min(p.KB, kb0 + p.kb_per_split) - kb0;   // >= 1 by construction
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull0 + 8 * b, 1);
+            mbar_init(tempty0 + 8 * b, C::kEpiWarps);
+        }
+        *abort = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmW);
+        prefetch_tmap(&tmX);
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- TMA producer
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+            int it = 0;
+            for (; it < nkb; ++it) {
+                const int s = it % C::kStages;
+                const uint32_t ph = (it / C::kStages) & 1;
+                if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1, abort, kWaitLimitNs)) {
+                    record_timeout(kKernelDecode, 1, abort);
+                    break;
+                }
+                uint8_t* st = smem + s * C::kStageBytes;
+                mbar_arrive_expect_tx(full0 + 8 * s, C::kStageBytes);
+                tma_load_2d(smem_u32(st), &tmW, full0 + 8 * s, (kb0 + it) * 128, nt * 128, pol_w);
+                tma_load_2d(smem_u32(st + 16384), &tmX, full0 + 8 * s, (kb0 + it) * 128, mt * MT, pol_x);
+            }
+            if (*abort) {   // let copies already in flight land before the CTA can exit
+                for (int j = max(0, it - C::kStages); j < it; ++j)
+                    mbar_wait_bounded(full0 + 8 * (j % C::kStages), (j / C::kStages) & 1, abort, kWaitLimitNs);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer (one thread)
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_e4m3_f32(128, MT);
+            for (int it = 0; it < nkb; ++it) {
+                const int s = it % C::kStages;
+                const uint32_t ph = (it / C::kStages) & 1;
+                const int buf = it & 1;
+                const uint32_t bph = (it >> 1) & 1;
+                if (!mbar_wait_bounded(full0 + 8 * s, ph, abort, kWaitLimitNs)) {
+                    record_timeout(kKernelDecode, 2, abort);
+                    break;
+                }
+                if (!mbar_wait_bounded(tempty0 + 8 * buf, bph ^ 1, abort, kWaitLimitNs)) {
+                    record_timeout(kKernelDecode, 3, abort);
+                    break;
+                }
+                tc_fence_after();
+                const uint8_t* st = smem + s * C::kStageBytes;
+                const uint64_t a = umma_desc_k128_sw128(smem_u32(st));
+                const uint64_t b = umma_desc_k128_sw128(smem_u32(st + 16384));
+                const uint32_t d = tmem_base + buf * MT;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)     // 4 x K=32 per 128-wide block; +32 B = +2 in the address field
+                    mma_f8f6f4(d, a + 2 * k, b + 2 * k, idesc, k > 0 ? 1u : 0u);
+                tc_commit(empty0 + 8 * s);
+                tc_commit(tfull0 + 8 * buf);
+            }
+        }
+    } else {
+        // ---------------- epilogue: per-block promotion in fp32 registers
+        const int e = warp - 2;
+        const int q = warp & 3;                          // TMEM lane quadrant of this warp
+        const int colbase = (e >> 2) * C::kCols;         // token columns of this thread
+        const int n_local = 32 * q + lane;               // weight row within the slab
+        const int et = e * 32 + lane;
+        // c[it][j] = Ws[nt][kb0+it] * Xs[kb0+it][mt*MT + j] (0 beyond M)
+        for (int idx = et; idx < nkb * MT; idx += C::kEpiWarps * 32) {
+            const int it = idx / MT, j = idx - (idx / MT) * MT;
+            const int64_t m = (int64_t)mt * MT + j;
+            const int kb = kb0 + it;
+            cscale[idx] = m < p.M ? p.Ws[(int64_t)nt * p.KB + kb] * p.Xs[(int64_t)kb * p.M + m] : 0.f;
+        }
+        named_bar_sync(1, C::kEpiWarps * 32);
+
+        float acc[C::kCols];
+#pragma unroll
+        for (int j = 0; j < C::kCols; ++j) acc[j] = 0.f;
+        for (int it = 0; it < nkb; ++it) {
+            const int buf = it & 1;
+            const uint32_t bph = (it >> 1) & 1;
+            if (!mbar_wait_bounded(tfull0 + 8 * buf, bph, abort, kWaitLimitNs)) {
+                record_timeout(kKernelDecode, 4, abort);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + buf * MT + colbase;
+            const float* cs = cscale + it * MT + colbase;
+#pragma unroll
+            for (int ch = 0; ch < C::kCols / C::kChunk; ++ch) {
+                uint32_t r[C::kChunk];
+                if constexpr (C::kChunk == 32) tmem_ld_32x32b_x32(taddr + ch * 32, r);
+                else tmem_ld_32x32b_x16(taddr + ch * 16, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < C::kChunk; ++j)
+                    acc[ch * C::kChunk + j] =
+                        fmaf(__uint_as_float(r[j]), cs[ch * C::kChunk + j], acc[ch * C::kChunk + j]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
+        }
+        // every MMA of this CTA has completed: the stage area is free for the
+        // transposed partial tile red[m][n_local]
+        float* red = reinterpret_cast<float*>(smem);
+#pragma unroll
+        for (int j = 0; j < C::kCols; ++j) red[(colbase + j) * 128 + n_local] = acc[j];
+    }
+
+    // ---------------- split-K reduction over the cluster, then bf16 stores
+    tc_fence_before();
+    if (p.split > 1) cluster_sync_all(); else __syncthreads();
+    {
+        const int64_t m_tile0 = (int64_t)mt * MT;
+        const int valid_m = (int)(p.M - m_tile0 < MT ? p.M - m_tile0 : MT);
+        const int total = valid_m * 16;                   // chunks of 8 output channels
+        const int per = (total + p.split - 1) / p.split;
+        const int begin = split_idx * per, end = min(total, begin + per);
+        const uint32_t red_addr = smem_u32(smem);
+        for (int c = begin + (int)threadIdx.x; c < end; c += C::kThreads) {
+            const int m = c >> 4, n8 = c & 15;
+            const uint32_t off = (uint32_t)(m * 128 + n8 * 8) * 4u;
+            float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int r = 0; r < p.split; ++r) {      // fixed order: deterministic
+                float4 v0, v1;
+                if (p.split > 1) {
+                    const uint32_t a = map_to_rank(red_addr + off, (uint32_t)r);
+                    v0 = ld_cluster_v4(a);
+                    v1 = ld_cluster_v4(a + 16);
+                } else {
+                    const float4* l = reinterpret_cast<const float4*>(smem + off);
+                    v0 = l[0];
+                    v1 = l[1];
+                }
+                s[0] += v0.x; s[1] += v0.y; s[2] += v0.z; s[3] += v0.w;
+                s[4] += v1.x; s[5] += v1.y; s[6] += v1.z; s[7] += v1.w;
+            }
+            uint4 o;
+            o.x = pack_bf16x2(s[0], s[1]);
+            o.y = pack_bf16x2(s[2], s[3]);
+            o.z = pack_bf16x2(s[4], s[5]);
+            o.w = pack_bf16x2(s[6], s[7]);
+            *reinterpret_cast<uint4*>(p.Y + (m_tile0 + m) * p.ldy + (int64_t)nt * 128 + n8 * 8) = o;
+        }
+    }
+    if (p.split > 1) cluster_sync_all(); else __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
+// Split-K factor for `tiles` weight slabs of KB blocks: minimise
+// waves x (blocks per CTA + fixed per-CTA overhead), clusters of at most 8.
+static int choose_split(int64_t tiles, int KB, int max_kb_per_split) {
+    const int sms = num_sms();
+    int best = 1;
+    double best_cost = 1e30;
+    for (int s = 1; s <= 8 && s <= KB; ++s) {
+        const int per = (KB + s - 1) / s;
+        if (per > max_kb_per_split) continue;
+        if ((int64_t)(s - 1) * per >= KB) continue;  // no empty split
+        const int64_t ctas = tiles * s;
+        const double waves = (double)((ctas + sms - 1) / sms);
+        const double cost = waves * (per + 2.0);
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best = s;
+        }
+    }
+    return best;
+}
+
+template <int MT>
+static cudaError_t launch_decode_mt(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
+                                    const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
+                                    int64_t ldy, cudaStream_t st) {
+    using C = DecodeCfg<MT>;
+    CUtensorMap tmW, tmX;
+    if (!make_tmap_u8(&tmW, Wq, (uint64_t)N, (uint64_t)K, (uint64_t)K, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap_u8(&tmX, Xq, (uint64_t)M, (uint64_t)K, (uint64_t)K, MT)) return cudaErrorInvalidValue;
+    const int KB = (int)(K / 128);
+    const int64_t mtiles = (M + MT - 1) / MT;
+    const int64_t tiles = (N / 128) * mtiles;
+    int split = choose_split(tiles, KB, C::kMaxKbPerSplit);
+    int per = (KB + split - 1) / split;
+    if (per > C::kMaxKbPerSplit) return cudaErrorInvalidValue;
+    DecodeParams prm{Xs, Ws, Y, M, ldy, KB, per, split};
+
+    auto kern = gemm_fp8_decode_kernel<MT>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)split, (unsigned)(N / 128), (unsigned)mtiles);
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)split;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tmW, tmX, prm);
+}
+
+bool decode_supported(int64_t K) { return K / 128 <= 8 * DecodeCfg<16>::kMaxKbPerSplit; }
+
+cudaError_t launch_gemm_fp8_decode(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
+                                   const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
+                                   int64_t ldy, cudaStream_t st) {
+    if (M <= 16) return launch_decode_mt<16>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
+    if (M <= 32) return launch_decode_mt<32>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
+    if (M <= 64) return launch_decode_mt<64>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
+    if (M <= 128) return launch_decode_mt<128>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
+    return launch_decode_mt<256>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
+}
+
+size_t gemm_fp8_workspace_bytes(int64_t, int64_t, int64_t) { return 0; }
+
+cudaError_t launch_gemm_fp8(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
+                            const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
+                            int64_t ldy, void*, size_t, cudaStream_t st) {
+    if (M <= 256 && decode_supported(K)) return launch_gemm_fp8_decode(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
+    return launch_gemm_fp8_mma_sync(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
+}
+
+}  // namespace fp8rl

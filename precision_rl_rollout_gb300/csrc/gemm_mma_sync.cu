@@ -166,13 +166,6 @@ cudaError_t launch_gemm_int8_mma_sync(const int8_t* Xq, const float* Xs, const i
     return cudaGetLastError();
 }
 
-// Until the tcgen05 kernels are dispatched here, both GEMMs run on this path.
-size_t gemm_fp8_workspace_bytes(int64_t, int64_t, int64_t) { return 0; }
-cudaError_t launch_gemm_fp8(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
-                            const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
-                            int64_t ldy, void*, size_t, cudaStream_t st) {
-    return launch_gemm_fp8_mma_sync(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
-}
 size_t gemm_int8_workspace_bytes(int64_t, int64_t, int64_t) { return 0; }
 cudaError_t launch_gemm_int8(const int8_t* Xq, const float* Xs, const int8_t* Wq,
                              const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,

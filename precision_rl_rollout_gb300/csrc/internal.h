@@ -26,7 +26,13 @@ cudaError_t launch_quant_act_group(const uint16_t* X, int64_t M, int64_t K, int6
 cudaError_t launch_quant_int8_rows(const uint16_t* A, int64_t R, int64_t K, int64_t lda,
                                    int8_t* Q, float* S, cudaStream_t st);
 
-// FP8 block-scaled GEMM.
+// FP8 block-scaled GEMM: dispatch by M (tcgen05 decode kernel for M <= 256).
+cudaError_t launch_gemm_fp8_decode(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
+                                   const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
+                                   int64_t ldy, cudaStream_t st);
+cudaError_t launch_gemm_fp8_mma_sync(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
+                                     const float* Ws, int64_t M, int64_t N, int64_t K,
+                                     uint16_t* Y, int64_t ldy, cudaStream_t st);
 size_t gemm_fp8_workspace_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_gemm_fp8(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
                             const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
