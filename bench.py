@@ -117,7 +117,7 @@ def max_over_ranks(x: float, world: int, device=None) -> float:
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -132,7 +132,7 @@ class ClockSampler:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.smi_id}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -202,6 +202,14 @@ def run_decode(fb, ls, ws):
         fb.fp8rl_gemm_w8a8_block(ls.Xq[i], ls.Xs[i], ls.Wq[i], ls.Ws[i], Y=ls.Y[i], workspace=ws)
 
 
+def capture_graph(fn):
+    """Capture fn's launches (library calls on the current stream) into a CUDA graph."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
 def time_headline(fb, args, dev, world, rank):
     shapes = synth.QWEN25_7B
     M = DECODE_M
@@ -210,22 +218,32 @@ def time_headline(fb, args, dev, world, rank):
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     for c in range(COPIES):                          # every copy has valid codes before step 0
         run_requant(fb, sets[c])
+        run_decode(fb, sets[c], ws)                  # first calls outside capture (one-time set-up)
     torch.cuda.synchronize()
 
+    def aq(ls):
+        for i in range(len(shapes)):
+            fb.fp8rl_quant_act_group(ls.X[i], ls.Xq[i], ls.Xs[i])
+
+    def gemm(ls):
+        for i in range(len(shapes)):
+            fb.fp8rl_gemm_w8a8_block(ls.Xq[i], ls.Xs[i], ls.Wq[i], ls.Ws[i], Y=ls.Y[i], workspace=ws)
+
+    # one graph per part and copy: the launch cost of the host binding stays out of the step
+    g_req = [capture_graph(lambda ls=ls: run_requant(fb, ls)) for ls in sets]
+    g_aq = [capture_graph(lambda ls=ls: aq(ls)) for ls in sets]
+    g_gemm = [capture_graph(lambda ls=ls: gemm(ls)) for ls in sets]
     stream = torch.cuda.current_stream()
-    n_ev = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_ev)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
 
     def step(s, record=None):
-        req, gem = sets[s % COPIES], sets[(s + COPIES // 2) % COPIES]
+        r, d = s % COPIES, (s + COPIES // 2) % COPIES
         if record: record[0].record(stream)
-        run_requant(fb, req)
+        g_req[r].replay()
         if record: record[1].record(stream)
-        for i in range(len(shapes)):
-            fb.fp8rl_quant_act_group(gem.X[i], gem.Xq[i], gem.Xs[i])
+        g_aq[d].replay()
         if record: record[2].record(stream)
-        for i in range(len(shapes)):
-            fb.fp8rl_gemm_w8a8_block(gem.Xq[i], gem.Xs[i], gem.Wq[i], gem.Ws[i], Y=gem.Y[i], workspace=ws)
+        g_gemm[d].replay()
         if record: record[3].record(stream)
 
     for s in range(args.warmup):
@@ -252,7 +270,7 @@ def time_headline(fb, args, dev, world, rank):
     assert fb.fp8rl_check_device_error() == 0
     res = {"total_ms": total_ms, "req_ms": req_ms, "aq_ms": aq_ms, "gemm_ms": gm_ms,
            "clocks": clk.summary(), "launches_per_step": 1 + 2 * len(shapes)}
-    del sets
+    del g_req, g_aq, g_gemm, sets
     torch.cuda.empty_cache()
     return res
 
@@ -305,6 +323,7 @@ def _flush_l2(buf):
 
 
 def _time_op(fn, reps, flush=None, warm=3):
+    """Median time of single launches (for ms-scale kernels), L2 flushed before each."""
     for _ in range(warm):
         fn()
     ts = []
@@ -321,12 +340,36 @@ def _time_op(fn, reps, flush=None, warm=3):
     return statistics.median(ts)
 
 
+def _time_graph(calls, reps=10):
+    """Per-call device time of `calls` (a list of no-arg library calls) captured
+    back to back in one CUDA graph and replayed `reps` times."""
+    for c in calls:
+        c()
+    torch.cuda.synchronize()
+    g = capture_graph(lambda: [c() for c in calls])
+    g.replay()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    b.record()
+    b.synchronize()
+    return a.elapsed_time(b) / (reps * len(calls))
+
+
+def _copies_for(nbytes):
+    """Distinct weight copies so that one pass over them exceeds 3x L2."""
+    return max(2, -(-3 * L2_BYTES // max(1, nbytes)))
+
+
 def extras(fb, dev, reps=5):
     out = {}
     flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     flush = lambda: _flush_l2(flush_buf)  # noqa: E731
 
-    # A3: prefill FP8 GEMM at M=8192 on the 32B shapes
+    # A3: prefill FP8 GEMM at M=8192 on the 32B shapes (ms-scale launches)
     pre = {}
     for s in synth.QWEN25_32B:
         W = synth.weight_bf16_direct(s.N, s.K, synth.seed_for(4, 0), device=dev)
@@ -343,25 +386,29 @@ def extras(fb, dev, reps=5):
         del Wq, Ws, Xq, Xs, Y
     out["prefill_fp8_gemm_m8192"] = pre
 
-    # A2 + A4: 32B decode sweep; the GEMM is timed alone after an L2 flush
+    # A2 + A4: 32B decode sweep; each GEMM walks distinct weight copies (> 3x L2)
     dec = {}
     for s in synth.QWEN25_32B:
         W = synth.weight_bf16_direct(s.N, s.K, synth.seed_for(3, 0), device=dev)
         Wq, Ws = fb.fp8rl_quant_weight_block(W)
         del W
+        nc = _copies_for(s.N * s.K)
+        Wqs = [Wq] + [Wq.clone() for _ in range(nc - 1)]
+        Wss = [Ws] + [Ws.clone() for _ in range(nc - 1)]
         for M in synth.DECODE_M_SWEEP:
             X = synth.activation(M, s.K, synth.seed_for(3, 1), device=dev)
             Xq, Xs = fb.fp8rl_quant_act_group(X)
             Y = torch.empty(M, s.N, dtype=torch.bfloat16, device=dev)
-            ws = torch.empty(max(1, fb.fp8rl_gemm_workspace_bytes(M, s.N, s.K)), dtype=torch.uint8, device=dev)
-            ms = _time_op(lambda: fb.fp8rl_gemm_w8a8_block(Xq, Xs, Wq, Ws, Y=Y, workspace=ws), reps, flush)
-            aq = _time_op(lambda: fb.fp8rl_quant_act_group(X, Xq, Xs), reps, flush)
-            dec[f"{s.name}_M{M}"] = {"gemm_ms": ms, "gemm_gbs": gemm_bytes(M, s.N, s.K) / (ms * 1e-3) / 1e9,
-                                     "act_quant_ms": aq}
-        del Wq, Ws
+            ms = _time_graph([lambda c=c: fb.fp8rl_gemm_w8a8_block(Xq, Xs, Wqs[c], Wss[c], Y=Y)
+                              for c in range(nc)])
+            aq = _time_graph([lambda: fb.fp8rl_quant_act_group(X, Xq, Xs)] * 16)
+            dec[f"{s.name}_M{M}"] = {"gemm_us": ms * 1e3, "gemm_gbs": gemm_bytes(M, s.N, s.K) / (ms * 1e-3) / 1e9,
+                                     "gemm_tflops": 2 * M * s.N * s.K / (ms * 1e-3) / 1e12,
+                                     "act_quant_us": aq * 1e3, "weight_copies": nc}
+        del Wq, Ws, Wqs, Wss
     out["decode_fp8_gemm_32b"] = dec
 
-    # A1 at full-model scale: 64 layers x 4 shapes in grouped launches
+    # A1 at full-model scale: 64 layers x 4 shapes, grouped launches (62 GB in)
     items = []
     for layer in range(synth.QWEN25_32B_LAYERS):
         for i, s in enumerate(synth.QWEN25_32B):
@@ -379,20 +426,27 @@ def extras(fb, dev, reps=5):
     i8 = {}
     for s in synth.QWEN25_32B:
         W = synth.weight_bf16_direct(s.N, s.K, synth.seed_for(5, 0), device=dev)
+        nc = _copies_for(2 * s.N * s.K)
+        Wc = [W] + [W.clone() for _ in range(nc - 1)]
         Wq = torch.empty(s.N, s.K, dtype=torch.int8, device=dev)
         Ws = torch.empty(s.N, dtype=torch.float32, device=dev)
-        wq_ms = _time_op(lambda: fb.int8rl_quant_weight_channel(W, Wq, Ws), reps, flush)
-        i8[f"{s.name}_wquant"] = {"ms": wq_ms, "gbs": (3 * s.N * s.K + 4 * s.N) / (wq_ms * 1e-3) / 1e9}
-        del W
+        wq_ms = _time_graph([lambda c=c: fb.int8rl_quant_weight_channel(Wc[c], Wq, Ws) for c in range(nc)])
+        i8[f"{s.name}_wquant"] = {"us": wq_ms * 1e3, "gbs": (3 * s.N * s.K + 4 * s.N) / (wq_ms * 1e-3) / 1e9}
+        del W, Wc
+        nc = _copies_for(s.N * s.K)
+        Wqs = [Wq] + [Wq.clone() for _ in range(nc - 1)]
         for M in synth.INT8_M_SWEEP:
             X = synth.activation(M, s.K, synth.seed_for(5, 1), device=dev)
             Xq, Xs = fb.int8rl_quant_act_token(X)
             Y = torch.empty(M, s.N, dtype=torch.bfloat16, device=dev)
-            ms = _time_op(lambda: fb.int8rl_gemm_w8a8(Xq, Xs, Wq, Ws, Y=Y), reps, flush)
-            i8[f"{s.name}_M{M}"] = {"gemm_ms": ms,
+            if M <= 256:
+                ms = _time_graph([lambda c=c: fb.int8rl_gemm_w8a8(Xq, Xs, Wqs[c], Ws, Y=Y) for c in range(nc)])
+            else:
+                ms = _time_op(lambda: fb.int8rl_gemm_w8a8(Xq, Xs, Wq, Ws, Y=Y), reps, flush)
+            i8[f"{s.name}_M{M}"] = {"gemm_us": ms * 1e3,
                                     "gemm_gbs": int8_gemm_bytes(M, s.N, s.K) / (ms * 1e-3) / 1e9,
                                     "gemm_tops": 2 * M * s.N * s.K / (ms * 1e-3) / 1e12}
-        del Wq, Ws
+        del Wq, Ws, Wqs
     out["int8_32b"] = i8
     torch.cuda.empty_cache()
     return out
@@ -520,6 +574,15 @@ def profile_case(fb, case, dev, reps=3):
                          dtype=torch.uint8, device=dev)
         for _ in range(reps):
             run_decode(fb, ls, ws)
+    elif case.startswith("decode32b_m"):
+        M = int(case[len("decode32b_m"):])
+        s = synth.QWEN25_32B[2]                         # gate_up 5120 -> 55296
+        W = synth.weight_bf16_direct(s.N, s.K, synth.seed_for(3, 0), device=dev)
+        Wq, Ws = fb.fp8rl_quant_weight_block(W)
+        del W
+        Xq, Xs = fb.fp8rl_quant_act_group(synth.activation(M, s.K, synth.seed_for(3, 1), device=dev))
+        for _ in range(reps):
+            fb.fp8rl_gemm_w8a8_block(Xq, Xs, Wq, Ws)
     elif case == "prefill":
         s = synth.QWEN25_32B[0]
         W = synth.weight_bf16_direct(s.N, s.K, synth.seed_for(4, 0), device=dev)
@@ -546,14 +609,14 @@ def profile_case(fb, case, dev, reps=3):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--extras", default="all", choices=["all", "none"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--profile", default=None,
-                    help="run one small case for ncu: requant | decode | prefill | int8")
+                    help="run one small case for ncu: requant | decode | decode32b_m<M> | prefill | int8")
     args = ap.parse_args()
     world, rank, local = dist_env()
     if args.impl == "reference":

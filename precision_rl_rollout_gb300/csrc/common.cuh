@@ -46,14 +46,52 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
     return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
 }
 
-// Eight bf16 (one 16-byte chunk) divided by s (IEEE, round to nearest) and
-// encoded to eight E4M3FN codes, packed little-endian into 8 bytes.
-__device__ __forceinline__ uint2 quant8_e4m3(uint4 v, float s) {
+// Division of a block's values by its scale s.
+//
+// The quantizers need the IEEE round-to-nearest quotient fl32(x / s) only up to
+// the code it rounds to.  With one scale per block, the reciprocal y = RN(1/s)
+// is computed once and each quotient is refined from it with Markstein's
+// correction (P. Markstein, "Computation of elementary functions on the IBM
+// RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990):
+//     q0 = RN(|x| * y),  r = RN(|x| - q0 * s)  (fused, exact),  q = RN(q0 + r * y),
+// then the sign of x is put back (so -0 and negative values that round to zero
+// keep their sign, as the IEEE quotient does).  For every bf16 x with
+// |x| <= amax and every bf16 amax whose scale s is at least 2^-90 (both
+// families, s = amax/448 and s = amax/127), this gives the same E4M3 code and
+// the same INT8 code as the IEEE quotient; the exhaustive-domain parity tests
+// check exactly that against the CPU reference.  A block with a smaller scale
+// (all |x| < ~2^-81) uses the IEEE division directly.
+struct BlockDivisor {
+    float s, y;
+    bool fast;
+};
+
+__device__ __forceinline__ BlockDivisor make_divisor(float s) {
+    return BlockDivisor{s, __frcp_rn(s), s >= 0x1p-90f};
+}
+
+template <bool kFast>
+__device__ __forceinline__ float div_by_scale(float x, const BlockDivisor& d) {
+    if constexpr (!kFast) {
+        return __fdiv_rn(x, d.s);
+    } else {
+        const float a = fabsf(x);
+        const float q0 = __fmul_rn(a, d.y);
+        const float r = __fmaf_rn(-q0, d.s, a);
+        const float q = __fmaf_rn(r, d.y, q0);
+        return __uint_as_float(__float_as_uint(q) | (__float_as_uint(x) & 0x80000000u));
+    }
+}
+
+// Eight bf16 (one 16-byte chunk) divided by the block scale and encoded to
+// eight E4M3FN codes, packed little-endian into 8 bytes.
+template <bool kFast>
+__device__ __forceinline__ uint2 quant8_e4m3_t(uint4 v, const BlockDivisor& d) {
     uint2 o;
-    o.x = e4m3x2(__fdiv_rn(bf16_lo(v.x), s), __fdiv_rn(bf16_hi(v.x), s)) |
-          (e4m3x2(__fdiv_rn(bf16_lo(v.y), s), __fdiv_rn(bf16_hi(v.y), s)) << 16);
-    o.y = e4m3x2(__fdiv_rn(bf16_lo(v.z), s), __fdiv_rn(bf16_hi(v.z), s)) |
-          (e4m3x2(__fdiv_rn(bf16_lo(v.w), s), __fdiv_rn(bf16_hi(v.w), s)) << 16);
+    o.x = e4m3x2(div_by_scale<kFast>(bf16_lo(v.x), d), div_by_scale<kFast>(bf16_hi(v.x), d)) |
+          (e4m3x2(div_by_scale<kFast>(bf16_lo(v.y), d), div_by_scale<kFast>(bf16_hi(v.y), d)) << 16);
+    o.y = e4m3x2(div_by_scale<kFast>(bf16_lo(v.z), d), div_by_scale<kFast>(bf16_hi(v.z), d)) |
+          (e4m3x2(div_by_scale<kFast>(bf16_lo(v.w), d), div_by_scale<kFast>(bf16_hi(v.w), d)) << 16);
     return o;
 }
 
@@ -65,17 +103,19 @@ __device__ __forceinline__ float int8_scale_from_amax(float amax) {
 }
 
 // One bf16 -> int8 code: clamp(rint(x / s), -127, 127).
-__device__ __forceinline__ uint32_t q_int8(float x, float s) {
-    int q = __float2int_rn(__fdiv_rn(x, s));
+template <bool kFast>
+__device__ __forceinline__ uint32_t q_int8(float x, const BlockDivisor& d) {
+    int q = __float2int_rn(div_by_scale<kFast>(x, d));
     q = min(127, max(-127, q));
     return (uint32_t)(q & 0xFF);
 }
-__device__ __forceinline__ uint2 quant8_int8(uint4 v, float s) {
+template <bool kFast>
+__device__ __forceinline__ uint2 quant8_int8_t(uint4 v, const BlockDivisor& d) {
     uint2 o;
-    o.x = q_int8(bf16_lo(v.x), s) | (q_int8(bf16_hi(v.x), s) << 8) |
-          (q_int8(bf16_lo(v.y), s) << 16) | (q_int8(bf16_hi(v.y), s) << 24);
-    o.y = q_int8(bf16_lo(v.z), s) | (q_int8(bf16_hi(v.z), s) << 8) |
-          (q_int8(bf16_lo(v.w), s) << 16) | (q_int8(bf16_hi(v.w), s) << 24);
+    o.x = q_int8<kFast>(bf16_lo(v.x), d) | (q_int8<kFast>(bf16_hi(v.x), d) << 8) |
+          (q_int8<kFast>(bf16_lo(v.y), d) << 16) | (q_int8<kFast>(bf16_hi(v.y), d) << 24);
+    o.y = q_int8<kFast>(bf16_lo(v.z), d) | (q_int8<kFast>(bf16_hi(v.z), d) << 8) |
+          (q_int8<kFast>(bf16_lo(v.w), d) << 16) | (q_int8<kFast>(bf16_hi(v.w), d) << 24);
     return o;
 }
 

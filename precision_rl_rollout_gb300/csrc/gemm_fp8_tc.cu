@@ -127,6 +127,7 @@ struct DecodeCfg {
     static constexpr int kTmemCols = 2 * MT < 32 ? 32 : 2 * MT;
     static constexpr int kMinBlocks = MT <= 64 ? 2 : 1;             // CTAs per SM the registers allow
     static constexpr int kChunk = kCols >= 128 ? 16 : (kCols >= 32 ? 32 : 16);  // TMEM load width
+    static constexpr int kGroup = kCols >= 128 ? 32 : (kCols < 64 ? kCols : 64);  // columns per tcgen05.wait::ld
     static constexpr int kBarOffset = kStages * kStageBytes + kScaleBytes;
     static constexpr int kSmemBytes = kBarOffset + 256 + 1024;   // barriers + alignment slack
     static_assert(MT * 128 * 4 <= kStages * kStageBytes, "reduction buffer must fit the stage area");
@@ -253,16 +254,23 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
             tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + buf * MT + colbase;
             const float* cs = cscale + it * MT + colbase;
+            // several TMEM loads in flight per wait: the load latency is paid
+            // once per group of up to 64 columns, not once per chunk
 #pragma unroll
-            for (int ch = 0; ch < C::kCols / C::kChunk; ++ch) {
-                uint32_t r[C::kChunk];
-                if constexpr (C::kChunk == 32) tmem_ld_32x32b_x32(taddr + ch * 32, r);
-                else tmem_ld_32x32b_x16(taddr + ch * 16, r);
+            for (int g = 0; g < C::kCols / C::kGroup; ++g) {
+                uint32_t r[C::kGroup];
+#pragma unroll
+                for (int ch = 0; ch < C::kGroup / C::kChunk; ++ch) {
+                    uint32_t(&rc)[C::kChunk] = *reinterpret_cast<uint32_t(*)[C::kChunk]>(r + ch * C::kChunk);
+                    const uint32_t a = taddr + g * C::kGroup + ch * C::kChunk;
+                    if constexpr (C::kChunk == 32) tmem_ld_32x32b_x32(a, rc);
+                    else tmem_ld_32x32b_x16(a, rc);
+                }
                 tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < C::kChunk; ++j)
-                    acc[ch * C::kChunk + j] =
-                        fmaf(__uint_as_float(r[j]), cs[ch * C::kChunk + j], acc[ch * C::kChunk + j]);
+                for (int j = 0; j < C::kGroup; ++j)
+                    acc[g * C::kGroup + j] =
+                        fmaf(__uint_as_float(r[j]), cs[g * C::kGroup + j], acc[g * C::kGroup + j]);
             }
             tc_fence_before();
             __syncwarp();

@@ -8,9 +8,10 @@
 //
 // Every byte of input is read once with 16-byte streaming loads and every code
 // written once; amax is an integer max over the bf16 magnitude bits followed by
-// warp reductions; the division x / s is the IEEE round-to-nearest fp32 divide
-// and the conversion is the hardware E4M3 convert with round-to-nearest-even and
-// saturation, so every output bit is fixed by the input bits.
+// warp reductions; the quotient x / s yields the code of the IEEE round-to-
+// nearest fp32 divide (see BlockDivisor in common.cuh) and the conversion is the
+// hardware E4M3 convert with round-to-nearest-even and saturation, so every
+// output bit is fixed by the input bits.
 #include "common.cuh"
 #include "internal.h"
 
@@ -68,11 +69,18 @@ quant_weight_block_kernel(const __grid_constant__ WeightGroupParams p) {
 #pragma unroll
     for (int w = 1; w < 8; ++w) m = max(m, red[w]);
     const float s = fp8_scale_from_amax(__uint_as_float(m << 16));
+    const BlockDivisor d = make_divisor(s);
 
     uint8_t* dst = p.Wq[ti] + (nb * kBlk + r0) * K + kb * kBlk + col;
+    if (d.fast) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-        *reinterpret_cast<uint2*>(dst + (int64_t)i * 16 * K) = quant8_e4m3(v[i], s);
+        for (int i = 0; i < 8; ++i)
+            *reinterpret_cast<uint2*>(dst + (int64_t)i * 16 * K) = quant8_e4m3_t<true>(v[i], d);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            *reinterpret_cast<uint2*>(dst + (int64_t)i * 16 * K) = quant8_e4m3_t<false>(v[i], d);
+    }
     if (t == 0) p.Ws[ti][nb * KB + kb] = s;
 }
 
@@ -121,8 +129,10 @@ quant_act_group_kernel(const uint16_t* __restrict__ X, int64_t M, int64_t K, int
 #pragma unroll
     for (int off = 8; off > 0; off >>= 1) a = max(a, __shfl_xor_sync(0xffffffffu, a, off));
     const float s = fp8_scale_from_amax(__uint_as_float(a << 16));
+    const BlockDivisor d = make_divisor(s);
     if (valid) {
-        *reinterpret_cast<uint2*>(Xq + m * K + g * kBlk + lane16 * 8) = quant8_e4m3(v, s);
+        uint2 q = d.fast ? quant8_e4m3_t<true>(v, d) : quant8_e4m3_t<false>(v, d);
+        *reinterpret_cast<uint2*>(Xq + m * K + g * kBlk + lane16 * 8) = q;
         if (lane16 == 0) Xs[g * M + m] = s;
     }
 }
@@ -165,11 +175,20 @@ quant_int8_rows_kernel(const uint16_t* __restrict__ A, int64_t K, int64_t lda,
 #pragma unroll
     for (int w = 1; w < 8; ++w) m = max(m, red[w]);
     const float s = int8_scale_from_amax(__uint_as_float(m << 16));
+    const BlockDivisor d = make_divisor(s);
     int8_t* dst = Q + r * K;
+    if (d.fast) {
 #pragma unroll
-    for (int i = 0; i < kRowChunksPerThread; ++i) {
-        const int c = i * 256 + t;
-        if (c < chunks) *reinterpret_cast<uint2*>(dst + (int64_t)c * 8) = quant8_int8(v[i], s);
+        for (int i = 0; i < kRowChunksPerThread; ++i) {
+            const int c = i * 256 + t;
+            if (c < chunks) *reinterpret_cast<uint2*>(dst + (int64_t)c * 8) = quant8_int8_t<true>(v[i], d);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < kRowChunksPerThread; ++i) {
+            const int c = i * 256 + t;
+            if (c < chunks) *reinterpret_cast<uint2*>(dst + (int64_t)c * 8) = quant8_int8_t<false>(v[i], d);
+        }
     }
     if (t == 0) S[r] = s;
 }
