@@ -1,0 +1,261 @@
+// gemm_fp8_prefill.cu -- block-scaled FP8 GEMM for large token counts (prefill),
+// tensor-core bound, on tcgen05 + TMA.
+//
+// Same math as the decode kernel (FP8-RL, Abstract, contribution (i)):
+//   Y[m][n] = bf16( sum_kb Xs[kb][m] * Ws[n/128][kb] * P_kb[m][n] ),
+// with P_kb the fp32 tensor-core product of one 128-wide K block.
+//
+// Persistent kernel, one CTA per SM.  Output tile 128 tokens x 256 channels:
+// one tcgen05.mma M=128 N=256 K=32 group of four per K block into one of two
+// 256-column TMEM buffers (double buffered, all 512 columns).  The two column
+// halves of the tile are exactly two weight blocks, so the scale that promotes
+// a K block's partial product is one fp32 scalar per thread (its token's
+// activation scale times its half's weight scale).
+// Warpgroup 0: warp 0 issues TMA, warp 1 issues the MMAs (and owns TMEM).
+// Warpgroups 1 and 2: epilogue, one per column half; each thread owns one
+// token row and keeps 128 fp32 accumulators in registers, which setmaxnreg
+// moves over from warpgroup 0 (40 -> 232 registers per thread).
+// Tiles go M-fastest, so the CTAs in flight share a few 256-row weight slabs
+// and the (L2-resident) activations.
+#include "common.cuh"
+#include "internal.h"
+#include "sm100_ptx.cuh"
+
+namespace fp8rl {
+
+using namespace sm100;
+
+namespace {
+
+constexpr int kBM = 128, kBN = 256;
+constexpr int kStages = 4;
+constexpr int kABytes = kBM * 128;                  // X tile: 128 tokens x 128 K
+constexpr int kBBytes = kBN * 128;                  // W tile: 256 channels x 128 K
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kThreads = 384;
+constexpr int kBarOffset = kStages * kStageBytes;
+constexpr int kSmemBytes = kBarOffset + 256 + 1024;
+constexpr int kTmemCols = 2 * kBN;
+constexpr int kLaunchRegs = 168, kProdRegs = 40, kEpiRegs = 232;
+static_assert(128 * kProdRegs + 256 * kEpiRegs <= kThreads * kLaunchRegs,
+              "register split must fit the CTA's launch allocation");
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint32_t kKernelPrefill = 2;
+
+struct PrefillParams {
+    uint32_t* err;
+    const float* Xs;   // [KB][M]
+    const float* Ws;   // [N/128][KB]
+    uint16_t* Y;       // [M][ldy]
+    int64_t M, ldy;
+    int KB, NB;        // K/128, N/128
+    int mtiles, ntiles;
+};
+
+__device__ __forceinline__ void record_timeout(uint32_t* err, uint32_t site, volatile int* abort) {
+    atomicCAS(err, 0u, (kKernelPrefill << 24) | (site << 16) | 1u);
+    *abort = 1;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_fp8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                        const __grid_constant__ PrefillParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOffset);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 4);
+    volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
+    const uint32_t tfull0 = smem_u32(bars + 2 * kStages), tempty0 = smem_u32(bars + 2 * kStages + 2);
+    const uint32_t warp = warp_id(), lane = lane_id();
+    const int total_tiles = p.mtiles * p.ntiles;
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull0 + 8 * b, 1);
+            mbar_init(tempty0 + 8 * b, 8);          // one arrival per epilogue warp
+        }
+        *abort = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmX);
+        prefetch_tmap(&tmW);
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    if (warp < 4) {
+        regs_dec<kProdRegs>();
+        if (warp == 0 && lane == 0) {
+            // ---------------- TMA producer
+            const uint64_t pol_x = policy_evict_last(), pol_w = policy_evict_first();
+            uint32_t it = 0;
+            for (int tile = blockIdx.x; tile < total_tiles && !*abort; tile += gridDim.x) {
+                const int mt = tile % p.mtiles, nt = tile / p.mtiles;
+                for (int kb = 0; kb < p.KB; ++kb, ++it) {
+                    const int s = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1;
+                    if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1, abort, kWaitLimitNs)) {
+                        record_timeout(p.err, 1, abort);
+                        break;
+                    }
+                    uint8_t* st = smem + s * kStageBytes;
+                    mbar_arrive_expect_tx(full0 + 8 * s, kStageBytes);
+                    tma_load_2d(smem_u32(st), &tmX, full0 + 8 * s, kb * 128, mt * kBM, pol_x);
+                    tma_load_2d(smem_u32(st + kABytes), &tmW, full0 + 8 * s, kb * 128, nt * kBN, pol_w);
+                }
+            }
+        } else if (warp == 1 && lane == 0) {
+            // ---------------- MMA issuer
+            constexpr uint32_t idesc = idesc_e4m3_f32(kBM, kBN);
+            uint32_t it = 0;
+            for (int tile = blockIdx.x; tile < total_tiles && !*abort; tile += gridDim.x) {
+                for (int kb = 0; kb < p.KB; ++kb, ++it) {
+                    const int s = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1;
+                    const uint32_t buf = it & 1, bph = (it >> 1) & 1;
+                    if (!mbar_wait_bounded(full0 + 8 * s, ph, abort, kWaitLimitNs)) {
+                        record_timeout(p.err, 2, abort);
+                        break;
+                    }
+                    if (!mbar_wait_bounded(tempty0 + 8 * buf, bph ^ 1, abort, kWaitLimitNs)) {
+                        record_timeout(p.err, 3, abort);
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint8_t* st = smem + s * kStageBytes;
+                    const uint64_t a = umma_desc_k128_sw128(smem_u32(st));
+                    const uint64_t b = umma_desc_k128_sw128(smem_u32(st + kABytes));
+                    const uint32_t d = tmem_base + buf * kBN;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) mma_f8f6f4(d, a + 2 * k, b + 2 * k, idesc, k > 0 ? 1u : 0u);
+                    tc_commit(empty0 + 8 * s);
+                    tc_commit(tfull0 + 8 * buf);
+                }
+            }
+        }
+    } else {
+        regs_inc<kEpiRegs>();
+        // ---------------- epilogue: promotion of each K block into fp32 registers
+        const int e = warp - 4;                   // 0..7
+        const int q = warp & 3;                   // TMEM lane quadrant
+        const int h = e >> 2;                     // column half = weight block within the tile
+        const int row = 32 * q + lane;
+        uint32_t it = 0;
+        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+            const int mt = tile % p.mtiles, nt = tile / p.mtiles;
+            const int64_t m = (int64_t)mt * kBM + row;
+            const int nb = 2 * nt + h;
+            const bool live = m < p.M && nb < p.NB;
+            const float* __restrict__ xs = p.Xs + (live ? m : 0);
+            const float* __restrict__ ws = p.Ws + (int64_t)(live ? nb : 0) * p.KB;
+            float acc[128];
+#pragma unroll
+            for (int j = 0; j < 128; ++j) acc[j] = 0.f;
+            float sx = live ? __ldg(xs) : 0.f, sw = live ? __ldg(ws) : 0.f;
+            bool ok = true;
+            for (int kb = 0; kb < p.KB; ++kb, ++it) {
+                const float scale = sx * sw;
+                if (kb + 1 < p.KB && live) {                  // next block's scales, early
+                    sx = __ldg(xs + (int64_t)(kb + 1) * p.M);
+                    sw = __ldg(ws + kb + 1);
+                }
+                const uint32_t buf = it & 1, bph = (it >> 1) & 1;
+                if (!mbar_wait_bounded(tfull0 + 8 * buf, bph, abort, kWaitLimitNs)) {
+                    record_timeout(p.err, 4, abort);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + buf * kBN + h * 128;
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    uint32_t r[64];
+                    tmem_ld_32x32b_x32(taddr + g * 64, *reinterpret_cast<uint32_t(*)[32]>(r));
+                    tmem_ld_32x32b_x32(taddr + g * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) acc[g * 64 + j] = fmaf(__uint_as_float(r[j]), scale, acc[g * 64 + j]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
+            }
+            if (!ok) break;
+            if (live) {
+                uint16_t* y = p.Y + m * p.ldy + (int64_t)nt * kBN + h * 128;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    uint4 o;
+                    o.x = pack_bf16x2(acc[8 * j + 0], acc[8 * j + 1]);
+                    o.y = pack_bf16x2(acc[8 * j + 2], acc[8 * j + 3]);
+                    o.z = pack_bf16x2(acc[8 * j + 4], acc[8 * j + 5]);
+                    o.w = pack_bf16x2(acc[8 * j + 6], acc[8 * j + 7]);
+                    *reinterpret_cast<uint4*>(y + 8 * j) = o;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_fp8_prefill(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
+                                    const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
+                                    int64_t ldy, cudaStream_t st) {
+    // The register split (setmaxnreg) assumes the kernel was built with exactly
+    // kLaunchRegs registers per thread; anything else could make the epilogue's
+    // increase wait forever, so refuse to launch.
+    static int checked = 0;   // 0 unknown, 1 ok, -1 refused
+    if (checked == 0) {
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, gemm_fp8_prefill_kernel) != cudaSuccess) return cudaErrorInvalidValue;
+        checked = (fa.numRegs == kLaunchRegs) ? 1 : -1;
+        if (checked == 1 &&
+            cudaFuncSetAttribute(gemm_fp8_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes) != cudaSuccess)
+            checked = -1;
+    }
+    if (checked != 1) return cudaErrorInvalidDeviceFunction;
+    CUtensorMap tmX, tmW;
+    if (!make_tmap_u8(&tmX, Xq, (uint64_t)M, (uint64_t)K, (uint64_t)K, kBM)) return cudaErrorInvalidValue;
+    if (!make_tmap_u8(&tmW, Wq, (uint64_t)N, (uint64_t)K, (uint64_t)K, kBN)) return cudaErrorInvalidValue;
+    uint32_t* err = device_error_word();
+    if (!err) return cudaErrorInvalidValue;
+    PrefillParams prm{err, Xs, Ws, Y, M, ldy, (int)(K / 128), (int)(N / 128),
+                      (int)((M + kBM - 1) / kBM), (int)((N + kBN - 1) / kBN)};
+    const int tiles = prm.mtiles * prm.ntiles;
+    const int grid = tiles < num_sms() ? tiles : num_sms();
+    return launch_pdl(gemm_fp8_prefill_kernel, dim3(grid), dim3(kThreads), kSmemBytes, st, tmX, tmW, prm);
+}
+
+size_t gemm_fp8_workspace_bytes(int64_t, int64_t, int64_t) { return 0; }
+
+// Decode kernel for small M (weight streaming), prefill kernel otherwise; the
+// warp-MMA kernel covers shapes neither takes (K beyond the decode kernel's
+// split limit at small M).
+cudaError_t launch_gemm_fp8(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
+                            const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
+                            int64_t ldy, void*, size_t, cudaStream_t st) {
+    if (M <= 256) {
+        if (decode_supported(K)) return launch_gemm_fp8_decode(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
+        return launch_gemm_fp8_mma_sync(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
+    }
+    return launch_gemm_fp8_prefill(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
+}
+
+}  // namespace fp8rl

@@ -19,9 +19,6 @@
 // Split-K CTAs of one slab form a thread-block cluster and add their fp32
 // partials through distributed shared memory in a fixed order
 // (deterministic; no global workspace).
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include <algorithm>
 
 #include "common.cuh"
@@ -32,79 +29,19 @@ namespace fp8rl {
 
 using namespace sm100;
 
-// Word recording the first bounded wait that ran out (fp8rl_check_device_error).
-__device__ uint32_t g_device_error = 0;
-
-cudaError_t read_and_clear_device_error(uint32_t* word) {
-    cudaError_t e = cudaDeviceSynchronize();
-    if (e != cudaSuccess) return e;
-    uint32_t v = 0;
-    e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof v);
-    if (e != cudaSuccess) return e;
-    const uint32_t zero = 0;
-    e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
-    *word = v;
-    return e;
-}
-
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
-enum : uint32_t { kKernelDecode = 1, kKernelPrefill = 2 };
+enum : uint32_t { kKernelDecode = 1 };
 
-__device__ __forceinline__ void record_timeout(uint32_t kernel, uint32_t site, volatile int* abort) {
-    atomicCAS(&g_device_error, 0u, (kernel << 24) | (site << 16) | 1u);
+__device__ __forceinline__ void record_timeout(uint32_t* err, uint32_t kernel, uint32_t site,
+                                               volatile int* abort) {
+    atomicCAS(err, 0u, (kernel << 24) | (site << 16) | 1u);
     *abort = 1;
 }
-
-// ------------------------------------------------------------------ host: tensor maps
-
-namespace {
-
-PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        cudaDriverEntryPointQueryResult q;
-        void* p = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
-// Row-major byte matrix [rows][cols] (cols contiguous, row pitch `pitch` bytes),
-// loaded in boxes of 128 columns x box_rows rows with the 128-byte swizzle that
-// the UMMA K-major SW128 descriptor expects.  Rows beyond `rows` read as zero.
-bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint64_t pitch,
-                  uint32_t box_rows) {
-    auto enc = get_encode_fn();
-    if (!enc) return false;
-    cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {pitch};
-    cuuint32_t box[2] = {128, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
-                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
-int num_sms() {
-    static int n = 0;
-    if (!n) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (n <= 0) n = 148;
-    }
-    return n;
-}
-
-}  // namespace
 
 // ------------------------------------------------------------------ decode kernel
 
 struct DecodeParams {
+    uint32_t* err;     // device error word (bounded waits)
     const float* Xs;   // [KB][M]
     const float* Ws;   // [N/128][KB]
     uint16_t* Y;       // [M][ldy]
@@ -116,18 +53,19 @@ struct DecodeParams {
 
 template <int MT>
 struct DecodeCfg {
+    static_assert(MT == 16 || MT == 32 || MT == 64 || MT == 128, "token tile");
     static constexpr int kEpiWarps = MT >= 128 ? 8 : 4;
     static constexpr int kThreads = 64 + 32 * kEpiWarps;
     static constexpr int kCols = MT / (kEpiWarps / 4);         // TMEM columns per epilogue thread
     static constexpr int kStageBytes = 16384 + MT * 128;       // W tile + X tile
     // MT <= 64: two CTAs per SM (2 x (smem + 1 KB reserved) <= 228 KB); larger: one.
-    static constexpr int kStages = MT == 16 ? 6 : MT == 32 ? 5 : MT == 64 ? 4 : MT == 128 ? 5 : 4;
+    static constexpr int kStages = MT == 16 ? 6 : MT == 32 ? 5 : MT == 64 ? 4 : 5;
     static constexpr int kMaxKbPerSplit = 32;                     // K blocks per split-K CTA
     static constexpr int kScaleBytes = kMaxKbPerSplit * MT * 4;   // per-block scale products
     static constexpr int kTmemCols = 2 * MT < 32 ? 32 : 2 * MT;
     static constexpr int kMinBlocks = MT <= 64 ? 2 : 1;             // CTAs per SM the registers allow
-    static constexpr int kChunk = kCols >= 128 ? 16 : (kCols >= 32 ? 32 : 16);  // TMEM load width
-    static constexpr int kGroup = kCols >= 128 ? 32 : (kCols < 64 ? kCols : 64);  // columns per tcgen05.wait::ld
+    static constexpr int kChunk = kCols >= 32 ? 32 : 16;               // TMEM load width
+    static constexpr int kGroup = kCols < 64 ? kCols : 64;             // columns per tcgen05.wait::ld
     static constexpr int kBarOffset = kStages * kStageBytes + kScaleBytes;
     static constexpr int kSmemBytes = kBarOffset + 256 + 1024;   // barriers + alignment slack
     static_assert(MT * 128 * 4 <= kStages * kStageBytes, "reduction buffer must fit the stage area");
@@ -150,7 +88,7 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
 
     const uint32_t warp = warp_id(), lane = lane_id();
     const int split_idx = blockIdx.x;                  // rank within the cluster
-    const int nt = blockIdx.y, mt = blockIdx.z;
+    const int mt = blockIdx.y, nt = blockIdx.z;       // M tiles of one slab are adjacent
     const int kb0 = split_idx * p.kb_per_split;
     const int nkb = min(p.KB, kb0 + p.kb_per_split) - kb0;   // >= 1 by construction
 
@@ -173,6 +111,11 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Programmatic dependent launch: the set-up above overlapped the tail of the
+    // previous kernel in the stream; nothing in global memory is touched before
+    // it has completed.  The next kernel may then be scheduled (it waits the same way).
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     if (warp == 0) {
         // ---------------- TMA producer
@@ -183,7 +126,7 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
                 const int s = it % C::kStages;
                 const uint32_t ph = (it / C::kStages) & 1;
                 if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1, abort, kWaitLimitNs)) {
-                    record_timeout(kKernelDecode, 1, abort);
+                    record_timeout(p.err, kKernelDecode, 1, abort);
                     break;
                 }
                 uint8_t* st = smem + s * C::kStageBytes;
@@ -206,11 +149,11 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
                 const int buf = it & 1;
                 const uint32_t bph = (it >> 1) & 1;
                 if (!mbar_wait_bounded(full0 + 8 * s, ph, abort, kWaitLimitNs)) {
-                    record_timeout(kKernelDecode, 2, abort);
+                    record_timeout(p.err, kKernelDecode, 2, abort);
                     break;
                 }
                 if (!mbar_wait_bounded(tempty0 + 8 * buf, bph ^ 1, abort, kWaitLimitNs)) {
-                    record_timeout(kKernelDecode, 3, abort);
+                    record_timeout(p.err, kKernelDecode, 3, abort);
                     break;
                 }
                 tc_fence_after();
@@ -232,12 +175,26 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
         const int colbase = (e >> 2) * C::kCols;         // token columns of this thread
         const int n_local = 32 * q + lane;               // weight row within the slab
         const int et = e * 32 + lane;
-        // c[it][j] = Ws[nt][kb0+it] * Xs[kb0+it][mt*MT + j] (0 beyond M)
-        for (int idx = et; idx < nkb * MT; idx += C::kEpiWarps * 32) {
-            const int it = idx / MT, j = idx - (idx / MT) * MT;
-            const int64_t m = (int64_t)mt * MT + j;
-            const int kb = kb0 + it;
-            cscale[idx] = m < p.M ? p.Ws[(int64_t)nt * p.KB + kb] * p.Xs[(int64_t)kb * p.M + m] : 0.f;
+        // c[it][j] = Ws[nt][kb0+it] * Xs[kb0+it][mt*MT + j] (0 beyond M); the
+        // loads are issued in batches of 8 so their latencies overlap
+        {
+            const float* __restrict__ ws = p.Ws + (int64_t)nt * p.KB + kb0;
+            const float* __restrict__ xs = p.Xs + (int64_t)kb0 * p.M + (int64_t)mt * MT;
+            const int total = nkb * MT;
+            const int64_t mrem = p.M - (int64_t)mt * MT;
+            constexpr int kStride = C::kEpiWarps * 32;
+            for (int base = et; base < total; base += 8 * kStride) {
+                float v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int idx = base + u * kStride;
+                    const int it = idx / MT, j = idx - it * MT;
+                    v[u] = (idx < total && j < mrem) ? __ldg(ws + it) * __ldg(xs + (int64_t)it * p.M + j) : 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (base + u * kStride < total) cscale[base + u * kStride] = v[u];
+            }
         }
         named_bar_sync(1, C::kEpiWarps * 32);
 
@@ -248,7 +205,7 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
             const int buf = it & 1;
             const uint32_t bph = (it >> 1) & 1;
             if (!mbar_wait_bounded(tfull0 + 8 * buf, bph, abort, kWaitLimitNs)) {
-                record_timeout(kKernelDecode, 4, abort);
+                record_timeout(p.err, kKernelDecode, 4, abort);
                 break;
             }
             tc_fence_after();
@@ -361,7 +318,9 @@ static cudaError_t launch_decode_mt(const uint8_t* Xq, const float* Xs, const ui
     int split = choose_split(tiles, KB, C::kMaxKbPerSplit);
     int per = (KB + split - 1) / split;
     if (per > C::kMaxKbPerSplit) return cudaErrorInvalidValue;
-    DecodeParams prm{Xs, Ws, Y, M, ldy, KB, per, split};
+    uint32_t* err = device_error_word();
+    if (!err) return cudaErrorInvalidValue;
+    DecodeParams prm{err, Xs, Ws, Y, M, ldy, KB, per, split};
 
     auto kern = gemm_fp8_decode_kernel<MT>;
     static bool attr_set = false;
@@ -371,17 +330,19 @@ static cudaError_t launch_decode_mt(const uint8_t* Xq, const float* Xs, const ui
         attr_set = true;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)split, (unsigned)(N / 128), (unsigned)mtiles);
+    cfg.gridDim = dim3((unsigned)split, (unsigned)mtiles, (unsigned)(N / 128));
     cfg.blockDim = dim3(C::kThreads);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)split;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, tmW, tmX, prm);
 }
 
@@ -393,17 +354,7 @@ cudaError_t launch_gemm_fp8_decode(const uint8_t* Xq, const float* Xs, const uin
     if (M <= 16) return launch_decode_mt<16>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
     if (M <= 32) return launch_decode_mt<32>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
     if (M <= 64) return launch_decode_mt<64>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
-    if (M <= 128) return launch_decode_mt<128>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
-    return launch_decode_mt<256>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
-}
-
-size_t gemm_fp8_workspace_bytes(int64_t, int64_t, int64_t) { return 0; }
-
-cudaError_t launch_gemm_fp8(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
-                            const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
-                            int64_t ldy, void*, size_t, cudaStream_t st) {
-    if (M <= 256 && decode_supported(K)) return launch_gemm_fp8_decode(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
-    return launch_gemm_fp8_mma_sync(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
+    return launch_decode_mt<128>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
 }
 
 }  // namespace fp8rl

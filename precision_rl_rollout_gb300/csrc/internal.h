@@ -3,6 +3,7 @@
 // launch on the given stream.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -47,5 +48,17 @@ cudaError_t launch_gemm_int8(const int8_t* Xq, const float* Xs, const int8_t* Wq
 
 // Device-side record of a bounded wait that ran out (0 = none).
 cudaError_t read_and_clear_device_error(uint32_t* word);
+// Address of that word on the current device (passed to kernels that wait).
+uint32_t* device_error_word();
+
+// TMA map of a row-major byte matrix [rows][cols] (row pitch `pitch` bytes),
+// boxes of 128 columns x box_rows rows, 128-byte swizzle, zero fill out of range.
+bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint64_t pitch,
+                  uint32_t box_rows);
+int num_sms();
+bool decode_supported(int64_t K);
+cudaError_t launch_gemm_fp8_prefill(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
+                                    const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
+                                    int64_t ldy, cudaStream_t st);
 
 }  // namespace fp8rl

@@ -37,6 +37,7 @@ struct WeightGroupParams {
 // a warp reads two full 256-byte row segments per load.
 __global__ void __launch_bounds__(256)
 quant_weight_block_kernel(const __grid_constant__ WeightGroupParams p) {
+    pdl_wait_then_release();
     const int64_t b = blockIdx.x;
     int lo = 0, hi = p.n - 1;                     // tensor that owns block b
     while (lo < hi) {
@@ -102,8 +103,7 @@ cudaError_t launch_quant_weight_block(const WeightDesc* d, int n, cudaStream_t s
         p.block_start[p.n] = total;
         if (total == 0) continue;
         if (total > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-        quant_weight_block_kernel<<<(unsigned)total, 256, 0, st>>>(p);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch_pdl(quant_weight_block_kernel, dim3((unsigned)total), dim3(256), 0, st, p);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -117,6 +117,7 @@ cudaError_t launch_quant_weight_block(const WeightDesc* d, int n, cudaStream_t s
 __global__ void __launch_bounds__(256)
 quant_act_group_kernel(const uint16_t* __restrict__ X, int64_t M, int64_t K, int64_t ldx,
                        uint8_t* __restrict__ Xq, float* __restrict__ Xs) {
+    pdl_wait_then_release();
     const int t = threadIdx.x;
     const int lane16 = t & 15;
     const int64_t m = (int64_t)blockIdx.y * 16 + (t >> 4);
@@ -141,8 +142,7 @@ cudaError_t launch_quant_act_group(const uint16_t* X, int64_t M, int64_t K, int6
                                    uint8_t* Xq, float* Xs, cudaStream_t st) {
     if (M == 0) return cudaSuccess;
     dim3 grid((unsigned)(K / kBlk), (unsigned)((M + 15) / 16));
-    quant_act_group_kernel<<<grid, 256, 0, st>>>(X, M, K, ldx, Xq, Xs);
-    return cudaGetLastError();
+    return launch_pdl(quant_act_group_kernel, grid, dim3(256), 0, st, X, M, K, ldx, Xq, Xs);
 }
 
 // ---------------------------------------------------------------- INT8 rows
@@ -154,6 +154,7 @@ constexpr int kRowChunksPerThread = kInt8MaxK / (256 * 8);
 __global__ void __launch_bounds__(256)
 quant_int8_rows_kernel(const uint16_t* __restrict__ A, int64_t K, int64_t lda,
                        int8_t* __restrict__ Q, float* __restrict__ S) {
+    pdl_wait_then_release();
     const int64_t r = blockIdx.x;
     const int t = threadIdx.x;
     const int chunks = (int)(K / 8);
@@ -197,8 +198,7 @@ cudaError_t launch_quant_int8_rows(const uint16_t* A, int64_t R, int64_t K, int6
                                    int8_t* Q, float* S, cudaStream_t st) {
     if (R == 0) return cudaSuccess;
     if (R > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-    quant_int8_rows_kernel<<<(unsigned)R, 256, 0, st>>>(A, K, lda, Q, S);
-    return cudaGetLastError();
+    return launch_pdl(quant_int8_rows_kernel, dim3((unsigned)R), dim3(256), 0, st, A, K, lda, Q, S);
 }
 
 }  // namespace fp8rl

@@ -24,6 +24,22 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 __device__ __forceinline__ uint32_t warp_id() { return threadIdx.x >> 5; }
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31; }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+
+// Block until the grids this one depends on (the previous kernel in the stream,
+// when launched with programmatic stream serialization) have completed and
+// their memory is visible.  A no-op for an ordinary launch.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next kernel in the stream (if launched programmatically) to be
+// scheduled now; it still waits for this grid's completion before touching
+// memory this grid writes.
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -195,6 +211,21 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N) {
            | (0u << 10)           // B format: E4M3
            | ((N >> 3) << 17)     // N / 8
            | ((M >> 4) << 24);    // M / 16
+}
+
+// ------------------------------------------------------------------ register reallocation
+
+// Warpgroup-wide change of the per-thread register budget (all four warps of a
+// warpgroup execute it).  `inc` draws on registers that other warpgroups of the
+// CTA released with `dec`; the caller guarantees the split fits the CTA's
+// launch allocation.
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ------------------------------------------------------------------ cluster

@@ -29,7 +29,8 @@ def _fp8_case(M, N, K, seed_w, seed_x, rows=None, what=""):
 
 
 @pytest.mark.parametrize("M,N,K", [(16, 512, 256), (1, 128, 128), (5, 256, 384), (37, 384, 640),
-                                   (64, 256, 1024), (129, 128, 256), (300, 384, 384)])
+                                   (64, 256, 1024), (129, 128, 256), (256, 640, 512), (257, 384, 128),
+                                   (300, 384, 384), (1000, 768, 1280)])
 def test_fp8_gemm_small_full(cuda_lib, M, N, K):
     _fp8_case(M, N, K, 100 + N + K, 200 + M + K)
 
@@ -114,3 +115,25 @@ def test_int8_gemm_qwen32b_sampled(cuda_lib, shape, M):
 
 def test_no_device_error_after_gemms(cuda_lib):
     assert fb.fp8rl_check_device_error() == 0
+
+
+def test_requant_then_gemm_back_to_back_same_buffers(cuda_lib):
+    """Kernels are launched with programmatic dependent launch; a GEMM issued right
+    after a requant that rewrites its weight buffers must see the new codes."""
+    from parity_util import weight_cpu
+    N, K = 1024, 768
+    seeds = (72, 73, 74)
+    Wd = [weight_cpu(N, K, seed).cuda() for seed in seeds]
+    for M in (8, 300):
+        Xq, Xs = oracle_fp8_act(M, K, 71)
+        Xqd, Xsd = dev(Xq), dev(Xs)
+        Wq = torch.empty(N, K, dtype=torch.uint8, device="cuda")
+        Ws = torch.empty(N // 128, K // 128, dtype=torch.float32, device="cuda")
+        Ys = [torch.empty(M, N, dtype=torch.bfloat16, device="cuda") for _ in seeds]
+        torch.cuda.synchronize()
+        for W, Y in zip(Wd, Ys):                          # requant, GEMM, requant, GEMM, ... back to back
+            fb.fp8rl_quant_weight_block(W, Wq, Ws)        # same weight buffers every time
+            fb.fp8rl_gemm_w8a8_block(Xqd, Xsd, Wq, Ws, Y=Y)
+        for seed, Y in zip(seeds, Ys):
+            wq, ws = oracle_fp8_weight(N, K, seed)
+            assert_fp8_gemm_close(host(Y), oracle.fp8_gemm(Xq, Xs, wq, ws), f"seed {seed} M={M}")
