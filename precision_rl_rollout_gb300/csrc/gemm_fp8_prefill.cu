@@ -33,10 +33,13 @@ constexpr int kABytes = kBM * 128;                  // X tile: 128 tokens x 128 
 constexpr int kBBytes = kBN * 128;                  // W tile: 256 channels x 128 K
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kThreads = 384;
-constexpr int kBarOffset = kStages * kStageBytes;
+constexpr int kOutBytesPerWarp = 32 * 128;          // 32 rows x 64 bf16 output staging
+constexpr int kOutOffset = kStages * kStageBytes;
+constexpr int kBarOffset = kOutOffset + 8 * kOutBytesPerWarp;
 constexpr int kSmemBytes = kBarOffset + 256 + 1024;
 constexpr int kTmemCols = 2 * kBN;
 constexpr int kLaunchRegs = 168, kProdRegs = 40, kEpiRegs = 232;
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 static_assert(128 * kProdRegs + 256 * kEpiRegs <= kThreads * kLaunchRegs,
               "register split must fit the CTA's launch allocation");
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -59,7 +62,7 @@ __device__ __forceinline__ void record_timeout(uint32_t* err, uint32_t site, vol
 
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_fp8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                        const __grid_constant__ PrefillParams p) {
+                        const __grid_constant__ CUtensorMap tmY, const __grid_constant__ PrefillParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOffset);
@@ -83,6 +86,7 @@ gemm_fp8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_co
         fence_mbar_init();
         prefetch_tmap(&tmX);
         prefetch_tmap(&tmW);
+        prefetch_tmap(&tmY);
     }
     if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tc_fence_before();
@@ -190,19 +194,37 @@ gemm_fp8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_co
                 if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
             }
             if (!ok) break;
-            if (live) {
-                uint16_t* y = p.Y + m * p.ldy + (int64_t)nt * kBN + h * 128;
+            // Output: the warp's 32 rows x 128 columns go out as two 32 x 64 boxes,
+            // each staged in this warp's 4 KB buffer with the 128-byte swizzle
+            // and written by one asynchronous TMA store (rows beyond M and
+            // columns beyond N are clipped by the store).
+            if (nb < p.NB) {
+                uint8_t* stage = smem + kOutOffset + e * kOutBytesPerWarp;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    uint4 o;
-                    o.x = pack_bf16x2(acc[8 * j + 0], acc[8 * j + 1]);
-                    o.y = pack_bf16x2(acc[8 * j + 2], acc[8 * j + 3]);
-                    o.z = pack_bf16x2(acc[8 * j + 4], acc[8 * j + 5]);
-                    o.w = pack_bf16x2(acc[8 * j + 6], acc[8 * j + 7]);
-                    *reinterpret_cast<uint4*>(y + 8 * j) = o;
+                for (int c = 0; c < 2; ++c) {
+                    if (lane == 0) bulk_wait_read_all();   // the previous box has left the buffer
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        uint4 o;
+                        const float* a = acc + c * 64 + 8 * j;
+                        o.x = pack_bf16x2(a[0], a[1]);
+                        o.y = pack_bf16x2(a[2], a[3]);
+                        o.z = pack_bf16x2(a[4], a[5]);
+                        o.w = pack_bf16x2(a[6], a[7]);
+                        *reinterpret_cast<uint4*>(stage + lane * 128 + ((j ^ (lane & 7)) << 4)) = o;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmY, smem_u32(stage), nt * kBN + h * 128 + c * 64, mt * kBM + 32 * q);
+                        bulk_commit();
+                    }
                 }
             }
         }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -231,16 +253,17 @@ cudaError_t launch_gemm_fp8_prefill(const uint8_t* Xq, const float* Xs, const ui
             checked = -1;
     }
     if (checked != 1) return cudaErrorInvalidDeviceFunction;
-    CUtensorMap tmX, tmW;
+    CUtensorMap tmX, tmW, tmY;
     if (!make_tmap_u8(&tmX, Xq, (uint64_t)M, (uint64_t)K, (uint64_t)K, kBM)) return cudaErrorInvalidValue;
     if (!make_tmap_u8(&tmW, Wq, (uint64_t)N, (uint64_t)K, (uint64_t)K, kBN)) return cudaErrorInvalidValue;
+    if (!make_tmap_bf16_store(&tmY, Y, (uint64_t)M, (uint64_t)N, (uint64_t)ldy, 64, 32)) return cudaErrorInvalidValue;
     uint32_t* err = device_error_word();
     if (!err) return cudaErrorInvalidValue;
     PrefillParams prm{err, Xs, Ws, Y, M, ldy, (int)(K / 128), (int)(N / 128),
                       (int)((M + kBM - 1) / kBM), (int)((N + kBN - 1) / kBN)};
     const int tiles = prm.mtiles * prm.ntiles;
     const int grid = tiles < num_sms() ? tiles : num_sms();
-    return launch_pdl(gemm_fp8_prefill_kernel, dim3(grid), dim3(kThreads), kSmemBytes, st, tmX, tmW, prm);
+    return launch_pdl(gemm_fp8_prefill_kernel, dim3(grid), dim3(kThreads), kSmemBytes, st, tmX, tmW, tmY, prm);
 }
 
 size_t gemm_fp8_workspace_bytes(int64_t, int64_t, int64_t) { return 0; }

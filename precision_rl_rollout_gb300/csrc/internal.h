@@ -55,6 +55,10 @@ uint32_t* device_error_word();
 // boxes of 128 columns x box_rows rows, 128-byte swizzle, zero fill out of range.
 bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint64_t pitch,
                   uint32_t box_rows);
+// TMA map of a row-major bf16 matrix [rows][cols] (row pitch in elements) for
+// stores of box_cols x box_rows boxes with the 128-byte swizzle (box_cols = 64).
+bool make_tmap_bf16_store(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                          uint64_t pitch_elems, uint32_t box_cols, uint32_t box_rows);
 int num_sms();
 bool decode_supported(int64_t K);
 cudaError_t launch_gemm_fp8_prefill(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
