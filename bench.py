@@ -574,6 +574,15 @@ def profile_case(fb, case, dev, reps=3):
                          dtype=torch.uint8, device=dev)
         for _ in range(reps):
             run_decode(fb, ls, ws)
+    elif case.startswith("decode7b_m"):
+        M = int(case[len("decode7b_m"):])
+        s = synth.QWEN25_7B[2]                          # gate_up 3584 -> 37888
+        W = synth.weight_bf16_direct(s.N, s.K, synth.seed_for(2, 0), device=dev)
+        Wq, Ws = fb.fp8rl_quant_weight_block(W)
+        del W
+        Xq, Xs = fb.fp8rl_quant_act_group(synth.activation(M, s.K, synth.seed_for(2, 1), device=dev))
+        for _ in range(reps):
+            fb.fp8rl_gemm_w8a8_block(Xq, Xs, Wq, Ws)
     elif case.startswith("decode32b_m"):
         M = int(case[len("decode32b_m"):])
         s = synth.QWEN25_32B[2]                         # gate_up 5120 -> 55296
@@ -616,7 +625,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--profile", default=None,
-                    help="run one small case for ncu: requant | decode | decode32b_m<M> | prefill | int8")
+                    help="run one small case for ncu: requant | decode | decode7b_m<M> | decode32b_m<M> | prefill | int8")
     args = ap.parse_args()
     world, rank, local = dist_env()
     if args.impl == "reference":

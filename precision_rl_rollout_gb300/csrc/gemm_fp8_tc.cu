@@ -291,7 +291,7 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
 // (microseconds, roughly): a fixed cost per wave of CTAs, the weight stream of
 // the busiest SM (heavier per block for wide token tiles), and the cluster
 // reduction, which grows with the split and the tile.
-static int choose_split(int64_t tiles, int KB, int MT, int max_kb_per_split) {
+static int choose_split(int64_t tiles, int KB, int MT, int max_kb_per_split, double* cost_out = nullptr) {
     const int sms = num_sms();
     const int per_sm = MT <= 64 ? 2 : 1;              // CTAs of this tile co-resident on one SM
     int best = 1;
@@ -310,7 +310,20 @@ static int choose_split(int64_t tiles, int KB, int MT, int max_kb_per_split) {
             best = s;
         }
     }
+    if (cost_out) *cost_out = best_cost;
     return best;
+}
+
+static int token_tile(int64_t M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128; }
+
+// Estimated decode-kernel time in microseconds (the split model above scaled
+// by 0.8, its median ratio of measured to modelled time on GB300).
+double decode_cost_us(int64_t M, int64_t N, int64_t K) {
+    const int MT = token_tile(M);
+    const int64_t tiles = (N / 128) * ((M + MT - 1) / MT);
+    double c = 1e30;
+    choose_split(tiles, (int)(K / 128), MT, DecodeCfg<16>::kMaxKbPerSplit, &c);
+    return 0.8 * c;
 }
 
 template <int MT>
