@@ -48,7 +48,8 @@ L2_BYTES = 129 * 2 ** 20
 # ncu-measured DRAM traffic of the dominant kernel, valid only for the source it
 # was taken on (checked by hash; null otherwise).  Filled from the committed
 # profile summary of the same workload.
-NCU_TRAFFIC = {"kernel": "quant_weight_block_kernel", "source_sha1": None, "bytes_per_launch": None,
+NCU_TRAFFIC = {"kernel": "quant_weight_block_kernel", "source_sha1": "90389709ba3d55e730702a5d717d6d5d2e9eadef",
+               "bytes_per_launch": 466143744 + 174737152,
                "profile": "profiles/requant_weight_block_qwen7b.md"}
 
 
@@ -521,8 +522,9 @@ def cpu_baseline(n_steps=3, req_rows=1024, gemm_rows=16):
 # ------------------------------------------------------------------ main
 
 def traffic_or_null():
-    src = os.path.join(ROOT, "precision_rl_rollout_gb300", "csrc", "quant.cu")
-    sha = hashlib.sha1(open(src, "rb").read()).hexdigest()
+    csrc = os.path.join(ROOT, "precision_rl_rollout_gb300", "csrc")
+    sha = hashlib.sha1(open(os.path.join(csrc, "quant.cu"), "rb").read() +
+                       open(os.path.join(csrc, "common.cuh"), "rb").read()).hexdigest()
     if NCU_TRAFFIC["source_sha1"] == sha and NCU_TRAFFIC["bytes_per_launch"]:
         return NCU_TRAFFIC["bytes_per_launch"]
     return None
