@@ -423,6 +423,23 @@ def extras(fb, dev, reps=5):
     del items
     torch.cuda.empty_cache()
 
+    # FP8 KV-cache quant with a per-tensor scale recalibrated each step (32B: 8 kv heads x 128)
+    kv = {}
+    for tokens in (8192, 64 * 2048):
+        X = synth.activation(tokens, 1024, synth.seed_for(6, 0), device=dev)
+        Xq = torch.empty(tokens, 1024, dtype=torch.uint8, device=dev)
+        sc = torch.empty(1, dtype=torch.float32, device=dev)
+        wsb = torch.empty(max(1, fb.fp8rl_kv_workspace_bytes(tokens, 1024)), dtype=torch.uint8, device=dev)
+        nc = _copies_for(2 * tokens * 1024)
+        Xc = [X] + [X.clone() for _ in range(nc - 1)]
+        ms = _time_graph([lambda c=c: fb.fp8rl_quant_kv_tensor(Xc[c], Xq, sc, workspace=wsb) for c in range(nc)])
+        ms2 = _time_graph([lambda c=c: fb.fp8rl_quant_kv_with_scale(Xc[c], sc, Xq) for c in range(nc)])
+        b = 3 * tokens * 1024 + 4
+        kv[f"tokens{tokens}"] = {"recalibrate_us": ms * 1e3, "recalibrate_gbs": b / (ms * 1e-3) / 1e9,
+                                 "with_scale_us": ms2 * 1e3, "with_scale_gbs": b / (ms2 * 1e-3) / 1e9}
+        del X, Xc, Xq
+    out["kv_cache_fp8_32b"] = kv
+
     # A5-A7: INT8 on the 32B shapes
     i8 = {}
     for s in synth.QWEN25_32B:

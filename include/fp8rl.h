@@ -162,6 +162,31 @@ int int8rl_gemm_w8a8(const int8_t* Xq, const float* Xs, const int8_t* Wq, const 
                      void* stream);
 
 /* ------------------------------------------------------------------------
+ * FP8 KV-cache quantization with per-step scale recalibration (FP8-RL,
+ * Abstract, contribution (ii): FP8 KV-cache, QKV scales recalibrated every
+ * step).  One fp32 scale per K (or V) tensor, recomputed from the tensor:
+ *   s = amax == 0 ? 1 : fl32(amax / 448) over all R x C values;
+ *   KVq[r][c] = E4M3FN_rn_satfinite(fl32(KV[r][c] / s)); *scale = s.
+ * KV    bf16 [R][ld] (e.g. tokens x kv_heads*head_dim), C % 8 == 0, ld >= C,
+ *       ld % 8 == 0, 16-byte aligned.
+ * KVq   e4m3 [R][C] contiguous, 16-byte aligned.
+ * scale one fp32 in device memory (written by the call).
+ * workspace: device scratch of at least fp8rl_kv_workspace_bytes(R, C) bytes
+ *       (4 bytes per 16384 values); it needs no zeroing and holds nothing
+ *       between calls; calls in flight at the same time need their own.
+ * Bit-exact.  An empty tensor (R == 0) writes scale 1.
+ * ---------------------------------------------------------------------- */
+size_t fp8rl_kv_workspace_bytes(int64_t R, int64_t C);
+int fp8rl_quant_kv_tensor(const uint16_t* KV, int64_t R, int64_t C, int64_t ld, uint8_t* KVq,
+                          float* scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/* The same codes under a scale already fixed for this step (appending new
+ * tokens to a KV cache): KVq = E4M3FN_rn_satfinite(fl32(KV / *scale)).
+ * scale: one fp32 > 0 in device memory (read by the kernel). */
+int fp8rl_quant_kv_with_scale(const uint16_t* KV, int64_t R, int64_t C, int64_t ld,
+                              const float* scale, uint8_t* KVq, void* stream);
+
+/* ------------------------------------------------------------------------
  * Every wait inside the library's kernels (on an mbarrier filled by TMA or by
  * the tensor core) is bounded.  A wait that runs out records a code in a
  * device-side word, abandons the tile and lets the kernel exit, so the CUDA

@@ -73,6 +73,10 @@ def _load():
             lib.oracle_fp8_gemm.argtypes = [P, P, P, P, I, I, I, P]
             lib.oracle_bf16_matmul_f64.argtypes = [P, I, P, I, I, I, I, P]
             lib.oracle_int8_gemm.argtypes = [P, P, P, P, I, I, I, P, P]
+            lib.oracle_fp8_quant_tensor.restype = ctypes.c_int
+            lib.oracle_fp8_quant_tensor.argtypes = [P, I, I, I, P, P]
+            lib.oracle_fp8_quant_with_scale.restype = ctypes.c_int
+            lib.oracle_fp8_quant_with_scale.argtypes = [P, I, I, I, ctypes.c_float, P]
             _lib = lib
     return _lib
 
@@ -159,6 +163,25 @@ def int8_quant_rows(A: np.ndarray):
     _check(_load().oracle_int8_quant_rows(_ptr(A), R, K, K, _ptr(Q), _ptr(S)),
            "int8_quant_rows")
     return Q, S
+
+
+def fp8_quant_tensor(X: np.ndarray):
+    """X uint16 [R,C] -> (Xq uint8 [R,C], scale float32): one scale for the tensor."""
+    X = _bits16(X)
+    R, C = X.shape
+    Xq = np.empty((R, C), np.uint8)
+    sc = np.empty((1,), np.float32)
+    _check(_load().oracle_fp8_quant_tensor(_ptr(X), R, C, C, _ptr(Xq), _ptr(sc)), "fp8_quant_tensor")
+    return Xq, sc[0]
+
+
+def fp8_quant_with_scale(X: np.ndarray, scale: float):
+    X = _bits16(X)
+    R, C = X.shape
+    Xq = np.empty((R, C), np.uint8)
+    _check(_load().oracle_fp8_quant_with_scale(_ptr(X), R, C, C, float(scale), _ptr(Xq)),
+           "fp8_quant_with_scale")
+    return Xq
 
 
 int8_quant_weight_channel = int8_quant_rows

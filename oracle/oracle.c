@@ -179,6 +179,43 @@ int oracle_fp8_quant_act_group(const uint16_t* X, int64_t M, int64_t K, int64_t 
 }
 
 /* ------------------------------------------------------------------ */
+/* FP8 KV-cache quant with a per-tensor scale recalibrated from the tensor
+ * itself (FP8-RL, Abstract, contribution (ii): FP8 KV-cache with per-step QKV
+ * scale recalibration; the reading taken is one scale per K or V tensor,
+ * fl32(amax/448) over the whole tensor, recomputed at every call).         */
+/* ------------------------------------------------------------------ */
+
+/* X: bf16 bits [R][ldx] with row length C.  Xq: e4m3 codes [R][C].
+ * *scale: the tensor's fp32 scale (amax = 0 gives 1). */
+int oracle_fp8_quant_tensor(const uint16_t* X, int64_t R, int64_t C, int64_t ldx,
+                            uint8_t* Xq, float* scale) {
+    if (ldx < C || R < 0 || C < 0) return -1;
+    float amax = 0.0f;
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t c = 0; c < C; ++c) {
+            float x = fabsf(bf16_to_f32(X[r * ldx + c]));
+            if (x > amax) amax = x;
+        }
+    float s = fp8_scale(amax);
+    *scale = s;
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t c = 0; c < C; ++c)
+            Xq[r * C + c] = oracle_e4m3_encode(bf16_to_f32(X[r * ldx + c]) / s);
+    return 0;
+}
+
+/* Codes of X under a given scale s (appending to a KV cache whose scale was
+ * fixed for this step): Xq = E4M3FN_rn_satfinite(fl32(X / s)). */
+int oracle_fp8_quant_with_scale(const uint16_t* X, int64_t R, int64_t C, int64_t ldx, float s,
+                                uint8_t* Xq) {
+    if (ldx < C || R < 0 || C < 0 || !(s > 0.0f)) return -1;
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t c = 0; c < C; ++c)
+            Xq[r * C + c] = oracle_e4m3_encode(bf16_to_f32(X[r * ldx + c]) / s);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
 /* INT8 row quant (FlashRL INT8 rollout, Fig. 1 / Fig. 2): one symmetric
  * scale per row over all K.  Used for the weight (per output channel) and
  * for the activation (per token); the two differ only in which rows they

@@ -28,7 +28,8 @@ EXPORTS = ("fp8rl_status_string", "fp8rl_abi_version", "fp8rl_quant_weight_block
            "fp8rl_quant_weight_block_grouped", "fp8rl_quant_act_group",
            "fp8rl_gemm_workspace_bytes", "fp8rl_gemm_w8a8_block",
            "int8rl_quant_weight_channel", "int8rl_quant_act_token",
-           "int8rl_gemm_workspace_bytes", "int8rl_gemm_w8a8", "fp8rl_check_device_error")
+           "int8rl_gemm_workspace_bytes", "int8rl_gemm_w8a8", "fp8rl_check_device_error",
+           "fp8rl_kv_workspace_bytes", "fp8rl_quant_kv_tensor", "fp8rl_quant_kv_with_scale")
 
 
 class Fp8rlError(RuntimeError):
@@ -79,9 +80,13 @@ def load(path: str | None = None):
         lib.int8rl_gemm_workspace_bytes.argtypes = [I, I, I]
         lib.int8rl_gemm_w8a8.argtypes = [P, P, P, P, I, I, I, P, I, P, P, Z, S]
         lib.fp8rl_check_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+        lib.fp8rl_kv_workspace_bytes.restype = Z
+        lib.fp8rl_kv_workspace_bytes.argtypes = [I, I]
+        lib.fp8rl_quant_kv_tensor.argtypes = [P, I, I, I, P, P, P, Z, S]
+        lib.fp8rl_quant_kv_with_scale.argtypes = [P, I, I, I, P, P, S]
         for name in EXPORTS:
-            if name not in ("fp8rl_status_string", "fp8rl_abi_version",
-                            "fp8rl_gemm_workspace_bytes", "int8rl_gemm_workspace_bytes"):
+            if name not in ("fp8rl_status_string", "fp8rl_abi_version", "fp8rl_gemm_workspace_bytes",
+                            "int8rl_gemm_workspace_bytes", "fp8rl_kv_workspace_bytes"):
                 getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -232,6 +237,38 @@ def int8rl_gemm_w8a8(Xq, Xs, Wq, Ws, Y=None, acc=None, want_acc=False, workspace
     _ck(lib.int8rl_gemm_w8a8(_p(Xq), _p(Xs), _p(Wq), _p(Ws), M, N, K, _p(Y), ldy, _p(acc),
                              _p(workspace), wbytes, _stream(Wq, stream)), "int8rl_gemm_w8a8")
     return (Y, acc) if acc is not None else Y
+
+
+def fp8rl_kv_workspace_bytes(R: int, C: int) -> int:
+    return int(load().fp8rl_kv_workspace_bytes(R, C))
+
+
+def fp8rl_quant_kv_tensor(KV, KVq=None, scale=None, workspace=None, stream=None):
+    """KV bf16 [R,C] -> (KVq uint8 [R,C], scale fp32 [1]): per-tensor scale recalibrated."""
+    lib = load()
+    ld = _rowmajor(KV, "KV")
+    R, C = KV.shape
+    KVq = _need(KVq, (R, C), torch.uint8, KV.device, "KVq")
+    scale = _need(scale, (1,), torch.float32, KV.device, "scale")
+    need = lib.fp8rl_kv_workspace_bytes(R, C)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=KV.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _ck(lib.fp8rl_quant_kv_tensor(_p(KV), R, C, ld, _p(KVq), _p(scale), _p(workspace), wbytes,
+                                  _stream(KV, stream)), "fp8rl_quant_kv_tensor")
+    return KVq, scale
+
+
+def fp8rl_quant_kv_with_scale(KV, scale, KVq=None, stream=None):
+    """KV bf16 [R,C], scale fp32 [1] (device) -> KVq uint8 [R,C]."""
+    lib = load()
+    ld = _rowmajor(KV, "KV")
+    R, C = KV.shape
+    KVq = _need(KVq, (R, C), torch.uint8, KV.device, "KVq")
+    _need(scale, (1,), torch.float32, KV.device, "scale")
+    _ck(lib.fp8rl_quant_kv_with_scale(_p(KV), R, C, ld, _p(scale), _p(KVq), _stream(KV, stream)),
+        "fp8rl_quant_kv_with_scale")
+    return KVq
 
 
 def fp8rl_check_device_error() -> int:

@@ -145,6 +145,39 @@ int int8rl_gemm_w8a8(const int8_t* Xq, const float* Xs, const int8_t* Wq, const 
                                         workspace_bytes, as_stream(stream)));
 }
 
+static int check_kv(const uint16_t* KV, int64_t R, int64_t C, int64_t ld, const uint8_t* KVq) {
+    if (R < 0 || C <= 0 || C % 8 || ld < C) return FP8RL_ERR_SHAPE;
+    if (R > 0 && (!KV || !KVq)) return FP8RL_ERR_NULL;
+    if (!aligned16(KV) || !aligned16(KVq) || (ld * 2) % 16) return FP8RL_ERR_ALIGN;
+    return FP8RL_OK;
+}
+
+size_t fp8rl_kv_workspace_bytes(int64_t R, int64_t C) {
+    if (R <= 0 || C <= 0) return 0;
+    return (size_t)kv_partials(R, C) * sizeof(uint32_t);
+}
+
+int fp8rl_quant_kv_tensor(const uint16_t* KV, int64_t R, int64_t C, int64_t ld, uint8_t* KVq,
+                          float* scale, void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_kv(KV, R, C, ld, KVq);
+    if (rc) return rc;
+    if (!scale) return FP8RL_ERR_NULL;
+    if (!aligned4(scale) || !aligned4(workspace)) return FP8RL_ERR_ALIGN;
+    const size_t need = fp8rl_kv_workspace_bytes(R, C);
+    if (workspace_bytes < need || (need && !workspace)) return FP8RL_ERR_WORKSPACE;
+    return cuda_status(launch_quant_kv_tensor(KV, R, C, ld, KVq, scale,
+                                              static_cast<uint32_t*>(workspace), as_stream(stream)));
+}
+
+int fp8rl_quant_kv_with_scale(const uint16_t* KV, int64_t R, int64_t C, int64_t ld,
+                              const float* scale, uint8_t* KVq, void* stream) {
+    int rc = check_kv(KV, R, C, ld, KVq);
+    if (rc) return rc;
+    if (!scale) return FP8RL_ERR_NULL;
+    if (!aligned4(scale)) return FP8RL_ERR_ALIGN;
+    return cuda_status(launch_quant_kv_with_scale(KV, R, C, ld, scale, KVq, as_stream(stream)));
+}
+
 int fp8rl_check_device_error(uint32_t* detail) {
     uint32_t w = 0;
     cudaError_t e = read_and_clear_device_error(&w);

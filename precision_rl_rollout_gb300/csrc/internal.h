@@ -27,6 +27,13 @@ cudaError_t launch_quant_act_group(const uint16_t* X, int64_t M, int64_t K, int6
 cudaError_t launch_quant_int8_rows(const uint16_t* A, int64_t R, int64_t K, int64_t lda,
                                    int8_t* Q, float* S, cudaStream_t st);
 
+// FP8 KV-cache per-tensor quant (three launches; `partial` holds kv_partials(R, C) words).
+int64_t kv_partials(int64_t R, int64_t C);
+cudaError_t launch_quant_kv_tensor(const uint16_t* X, int64_t R, int64_t C, int64_t ld, uint8_t* Xq,
+                                   float* scale, uint32_t* partial, cudaStream_t st);
+cudaError_t launch_quant_kv_with_scale(const uint16_t* X, int64_t R, int64_t C, int64_t ld,
+                                       const float* scale, uint8_t* Xq, cudaStream_t st);
+
 // FP8 block-scaled GEMM: dispatch by M (tcgen05 decode kernel for M <= 256).
 cudaError_t launch_gemm_fp8_decode(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
                                    const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,

@@ -147,10 +147,11 @@ cudaError_t launch_quant_act_group(const uint16_t* X, int64_t M, int64_t K, int6
 
 // ---------------------------------------------------------------- INT8 rows
 
-// One CTA of 256 threads per row; the row (K <= kInt8MaxK) is held in
-// registers between the amax pass and the quantization pass: chunk c = i*256+t.
-constexpr int kRowChunksPerThread = kInt8MaxK / (256 * 8);
-
+// One CTA of 256 threads per row; the row is held in registers between the
+// amax pass and the quantization pass: chunk c = i*256 + t for i < CPT.  CPT
+// (chunks of 8 values per thread) is the smallest instantiation that covers
+// the row, so short rows keep few registers and many CTAs in flight.
+template <int CPT>
 __global__ void __launch_bounds__(256)
 quant_int8_rows_kernel(const uint16_t* __restrict__ A, int64_t K, int64_t lda,
                        int8_t* __restrict__ Q, float* __restrict__ S) {
@@ -159,10 +160,10 @@ quant_int8_rows_kernel(const uint16_t* __restrict__ A, int64_t K, int64_t lda,
     const int t = threadIdx.x;
     const int chunks = (int)(K / 8);
     const uint16_t* src = A + r * lda;
-    uint4 v[kRowChunksPerThread];
+    uint4 v[CPT];
     uint32_t m = 0;
 #pragma unroll
-    for (int i = 0; i < kRowChunksPerThread; ++i) {
+    for (int i = 0; i < CPT; ++i) {
         const int c = i * 256 + t;
         v[i] = make_uint4(0, 0, 0, 0);
         if (c < chunks) v[i] = ld_stream_v4(src + (int64_t)c * 8);
@@ -180,13 +181,13 @@ quant_int8_rows_kernel(const uint16_t* __restrict__ A, int64_t K, int64_t lda,
     int8_t* dst = Q + r * K;
     if (d.fast) {
 #pragma unroll
-        for (int i = 0; i < kRowChunksPerThread; ++i) {
+        for (int i = 0; i < CPT; ++i) {
             const int c = i * 256 + t;
             if (c < chunks) *reinterpret_cast<uint2*>(dst + (int64_t)c * 8) = quant8_int8_t<true>(v[i], d);
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < kRowChunksPerThread; ++i) {
+        for (int i = 0; i < CPT; ++i) {
             const int c = i * 256 + t;
             if (c < chunks) *reinterpret_cast<uint2*>(dst + (int64_t)c * 8) = quant8_int8_t<false>(v[i], d);
         }
@@ -194,11 +195,26 @@ quant_int8_rows_kernel(const uint16_t* __restrict__ A, int64_t K, int64_t lda,
     if (t == 0) S[r] = s;
 }
 
+template <int CPT>
+static cudaError_t launch_int8_rows_cpt(const uint16_t* A, int64_t R, int64_t K, int64_t lda, int8_t* Q,
+                                        float* S, cudaStream_t st) {
+    return launch_pdl(quant_int8_rows_kernel<CPT>, dim3((unsigned)R), dim3(256), 0, st, A, K, lda, Q, S);
+}
+
 cudaError_t launch_quant_int8_rows(const uint16_t* A, int64_t R, int64_t K, int64_t lda,
                                    int8_t* Q, float* S, cudaStream_t st) {
     if (R == 0) return cudaSuccess;
     if (R > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-    return launch_pdl(quant_int8_rows_kernel, dim3((unsigned)R), dim3(256), 0, st, A, K, lda, Q, S);
+    const int64_t need = (K / 8 + 255) / 256;          // chunks per thread
+    static_assert(kInt8MaxK / (256 * 8) == 16, "largest instantiation covers kInt8MaxK");
+    if (need <= 1) return launch_int8_rows_cpt<1>(A, R, K, lda, Q, S, st);
+    if (need <= 2) return launch_int8_rows_cpt<2>(A, R, K, lda, Q, S, st);
+    if (need <= 3) return launch_int8_rows_cpt<3>(A, R, K, lda, Q, S, st);
+    if (need <= 4) return launch_int8_rows_cpt<4>(A, R, K, lda, Q, S, st);
+    if (need <= 6) return launch_int8_rows_cpt<6>(A, R, K, lda, Q, S, st);
+    if (need <= 8) return launch_int8_rows_cpt<8>(A, R, K, lda, Q, S, st);
+    if (need <= 12) return launch_int8_rows_cpt<12>(A, R, K, lda, Q, S, st);
+    return launch_int8_rows_cpt<16>(A, R, K, lda, Q, S, st);
 }
 
 }  // namespace fp8rl

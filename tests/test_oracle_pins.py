@@ -393,3 +393,35 @@ def test_tiny_config_inputs_have_requested_structure():
     assert int((amax_per_ch > 10).sum()) == 2
     W = synth.weight(synth.TINY.N, synth.TINY.K, synth.seed_for(1, 0))
     assert abs(float(W.float().std()) - 0.02) < 0.002
+
+
+# ------------------------------------------------------------------ KV-cache per-tensor quant
+
+def test_per_tensor_quant_reduces_to_single_block_quant():
+    # a 128x128 tensor is one weight block: the per-tensor quantizer must agree
+    # with the (pinned) block quantizer on codes and scale
+    Wb = _weight_with_block_magnitudes(128, 128, 31)
+    q1, s1 = oracle.fp8_quant_tensor(synth.bf16_bits(Wb))
+    q2, s2 = oracle.fp8_quant_weight_block(synth.bf16_bits(Wb))
+    assert np.array_equal(q1, q2) and s1.view(np.uint32) == s2[0, 0].view(np.uint32)
+
+
+def test_per_tensor_quant_uses_the_global_amax():
+    g = torch.Generator().manual_seed(41)
+    X = torch.randn(300, 1024, generator=g) * 0.1
+    X[217, 901] = -7.5                                   # the tensor's amax, far from row/column 0
+    Xb = X.to(torch.bfloat16)
+    q, s = oracle.fp8_quant_tensor(synth.bf16_bits(Xb))
+    assert s.view(np.uint32) == (np.float32(7.5) / np.float32(448)).view(np.uint32)
+    assert q[217, 901] == 0xFE and np.sum((q & 0x7F) == 0x7E) == 1
+    dq = oracle.e4m3_decode_table()[q]
+    v = Xb.double().numpy() / float(s)
+    bound = 0.5 * _ulp_e4m3(np.maximum(np.abs(v), np.abs(dq))) + np.abs(v) * 2.0 ** -23
+    assert np.all(np.abs(v - dq) <= bound)
+    # with that scale given explicitly, the with-scale quantizer gives the same codes
+    assert np.array_equal(oracle.fp8_quant_with_scale(synth.bf16_bits(Xb), float(s)), q)
+
+
+def test_per_tensor_quant_zero_tensor():
+    q, s = oracle.fp8_quant_tensor(np.zeros((3, 16), np.uint16))
+    assert s == 1.0 and not q.any()

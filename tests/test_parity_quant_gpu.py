@@ -148,3 +148,40 @@ def test_int8_weight_quant_qwen32b_sampled(cuda_lib, shape):
 
 def test_no_device_error_recorded(cuda_lib):
     assert fb.fp8rl_check_device_error() == 0
+
+
+# ------------------------------------------------------------------ FP8 KV-cache, per-tensor scale
+
+@pytest.mark.parametrize("R,C,ld", [(1, 8, 8), (3, 136, 144), (64, 1024, 1024), (300, 1024, 1032),
+                                    (2049, 1024, 1024), (8192, 1024, 1024)])
+def test_fp8_kv_tensor_quant_full(cuda_lib, R, C, ld):
+    X = act_cpu(R, C, 9000 + R + C)
+    wide = torch.zeros(R, ld, dtype=torch.bfloat16)
+    wide[:, :C] = X
+    KVq, scale = fb.fp8rl_quant_kv_tensor(wide.cuda()[:, :C])
+    want_q, want_s = oracle.fp8_quant_tensor(synth.bf16_bits(X))
+    assert bits_u32(host(scale))[0] == np.float32(want_s).view(np.uint32)
+    assert np.array_equal(host(KVq), want_q)
+    # the with-scale entry point on the same scale gives the same codes
+    KVq2 = fb.fp8rl_quant_kv_with_scale(wide.cuda()[:, :C], scale)
+    assert np.array_equal(host(KVq2), want_q)
+
+
+def test_fp8_kv_tensor_quant_edge_rows_and_empty(cuda_lib):
+    X = synth.edge_case_activation(11, 640, seed=13)
+    KVq, scale = fb.fp8rl_quant_kv_tensor(X.cuda())
+    want_q, want_s = oracle.fp8_quant_tensor(synth.bf16_bits(X))
+    assert bits_u32(host(scale))[0] == np.float32(want_s).view(np.uint32)
+    assert np.array_equal(host(KVq), want_q)
+    KVq0, s0 = fb.fp8rl_quant_kv_tensor(torch.empty(0, 64, dtype=torch.bfloat16, device="cuda"))
+    assert KVq0.shape == (0, 64) and float(s0[0]) == 1.0
+
+
+def test_fp8_kv_tensor_quant_qwen32b_cache_sampled(cuda_lib):
+    # a rollout-sized K cache: 64 sequences x 2048 tokens, 8 kv heads x 128
+    R, C = 64 * 2048, 1024
+    X = synth.activation(R, C, synth.seed_for(6, 0), device="cuda")
+    KVq, scale = fb.fp8rl_quant_kv_tensor(X)
+    want_q, want_s = oracle.fp8_quant_tensor(synth.bf16_bits(X))
+    assert bits_u32(host(scale))[0] == np.float32(want_s).view(np.uint32)
+    assert np.array_equal(host(KVq), want_q)
