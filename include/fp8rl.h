@@ -187,6 +187,30 @@ int fp8rl_quant_kv_with_scale(const uint16_t* KV, int64_t R, int64_t C, int64_t 
                               const float* scale, uint8_t* KVq, void* stream);
 
 /* ------------------------------------------------------------------------
+ * fp8rl_quant_kv_tensor without a workspace.  The paper has no counterpart:
+ * this is a calling convention, not part of the method.  It computes exactly
+ * what fp8rl_quant_kv_tensor computes, for callers that cannot allocate the
+ * workspace -- e.g. an inference engine that reserves nearly all GPU memory
+ * for its KV-cache pool at start-up and allows no allocation outside it, or a
+ * serving loop that must not call cudaMalloc / cudaFree because they
+ * synchronize the device and stall queued work.  It allocates nothing and
+ * calls no allocating routine.
+ * Scratch: a 64 KB array in device memory owned by the library (a file-scope
+ * __device__ array), held by every GPU that loads the library until the
+ * process exits.  Limit: R * C <= 268435456 (16384 x 16384) values; larger
+ * tensors return FP8RL_ERR_UNSUPPORTED (use fp8rl_quant_kv_tensor instead).
+ * The first call on a device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream
+ * capture.  Every call shares the one array: nothing in it needs to start at
+ * zero (a call writes every slot it reads before reading it), and two calls
+ * whose kernels overlap on the GPU (different streams) race on it -- issue
+ * them in one stream, or use fp8rl_quant_kv_tensor with separate workspaces.
+ * Other arguments, layouts and errors as for fp8rl_quant_kv_tensor.
+ * ---------------------------------------------------------------------- */
+int fp8rl_quant_kv_tensor_noalloc(const uint16_t* KV, int64_t R, int64_t C, int64_t ld,
+                                  uint8_t* KVq, float* scale, void* stream);
+
+/* ------------------------------------------------------------------------
  * Every wait inside the library's kernels (on an mbarrier filled by TMA or by
  * the tensor core) is bounded.  A wait that runs out records a code in a
  * device-side word, abandons the tile and lets the kernel exit, so the CUDA

@@ -29,7 +29,8 @@ EXPORTS = ("fp8rl_status_string", "fp8rl_abi_version", "fp8rl_quant_weight_block
            "fp8rl_gemm_workspace_bytes", "fp8rl_gemm_w8a8_block",
            "int8rl_quant_weight_channel", "int8rl_quant_act_token",
            "int8rl_gemm_workspace_bytes", "int8rl_gemm_w8a8", "fp8rl_check_device_error",
-           "fp8rl_kv_workspace_bytes", "fp8rl_quant_kv_tensor", "fp8rl_quant_kv_with_scale")
+           "fp8rl_kv_workspace_bytes", "fp8rl_quant_kv_tensor", "fp8rl_quant_kv_with_scale",
+           "fp8rl_quant_kv_tensor_noalloc")
 
 
 class Fp8rlError(RuntimeError):
@@ -84,6 +85,7 @@ def load(path: str | None = None):
         lib.fp8rl_kv_workspace_bytes.argtypes = [I, I]
         lib.fp8rl_quant_kv_tensor.argtypes = [P, I, I, I, P, P, P, Z, S]
         lib.fp8rl_quant_kv_with_scale.argtypes = [P, I, I, I, P, P, S]
+        lib.fp8rl_quant_kv_tensor_noalloc.argtypes = [P, I, I, I, P, P, S]
         for name in EXPORTS:
             if name not in ("fp8rl_status_string", "fp8rl_abi_version", "fp8rl_gemm_workspace_bytes",
                             "int8rl_gemm_workspace_bytes", "fp8rl_kv_workspace_bytes"):
@@ -269,6 +271,19 @@ def fp8rl_quant_kv_with_scale(KV, scale, KVq=None, stream=None):
     _ck(lib.fp8rl_quant_kv_with_scale(_p(KV), R, C, ld, _p(scale), _p(KVq), _stream(KV, stream)),
         "fp8rl_quant_kv_with_scale")
     return KVq
+
+
+def fp8rl_quant_kv_tensor_noalloc(KV, KVq, scale, stream=None):
+    """As fp8rl_quant_kv_tensor, but with the library's own scratch instead of a
+    workspace, for callers that cannot allocate; KVq and scale must be given."""
+    lib = load()
+    ld = _rowmajor(KV, "KV")
+    R, C = KV.shape
+    _need(KVq, (R, C), torch.uint8, KV.device, "KVq")
+    _need(scale, (1,), torch.float32, KV.device, "scale")
+    _ck(lib.fp8rl_quant_kv_tensor_noalloc(_p(KV), R, C, ld, _p(KVq), _p(scale), _stream(KV, stream)),
+        "fp8rl_quant_kv_tensor_noalloc")
+    return KVq, scale
 
 
 def fp8rl_check_device_error() -> int:

@@ -178,6 +178,16 @@ int fp8rl_quant_kv_with_scale(const uint16_t* KV, int64_t R, int64_t C, int64_t 
     return cuda_status(launch_quant_kv_with_scale(KV, R, C, ld, scale, KVq, as_stream(stream)));
 }
 
+int fp8rl_quant_kv_tensor_noalloc(const uint16_t* KV, int64_t R, int64_t C, int64_t ld, uint8_t* KVq,
+                                  float* scale, void* stream) {
+    int rc = check_kv(KV, R, C, ld, KVq);
+    if (rc) return rc;
+    if (!scale) return FP8RL_ERR_NULL;
+    if (!aligned4(scale)) return FP8RL_ERR_ALIGN;
+    if (R > 0 && R > kv_noalloc_max_values() / C) return FP8RL_ERR_UNSUPPORTED;   // R * C above the limit
+    return cuda_status(launch_quant_kv_tensor_noalloc(KV, R, C, ld, KVq, scale, as_stream(stream)));
+}
+
 int fp8rl_check_device_error(uint32_t* detail) {
     uint32_t w = 0;
     cudaError_t e = read_and_clear_device_error(&w);

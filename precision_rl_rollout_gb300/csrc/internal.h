@@ -33,6 +33,10 @@ cudaError_t launch_quant_kv_tensor(const uint16_t* X, int64_t R, int64_t C, int6
                                    float* scale, uint32_t* partial, cudaStream_t st);
 cudaError_t launch_quant_kv_with_scale(const uint16_t* X, int64_t R, int64_t C, int64_t ld,
                                        const float* scale, uint8_t* Xq, cudaStream_t st);
+// The same with the partial maxima in a library-owned device array (no workspace).
+int64_t kv_noalloc_max_values();
+cudaError_t launch_quant_kv_tensor_noalloc(const uint16_t* X, int64_t R, int64_t C, int64_t ld,
+                                           uint8_t* Xq, float* scale, cudaStream_t st);
 
 // FP8 block-scaled GEMM: dispatch by M (tcgen05 decode kernel for M <= 256).
 cudaError_t launch_gemm_fp8_decode(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,

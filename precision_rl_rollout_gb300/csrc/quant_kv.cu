@@ -13,6 +13,8 @@
 // Deterministic (no atomics, nothing to zero).  Above L2 size the tensor is
 // read twice (6.6 B of DRAM traffic per 3 algorithmic bytes); below it the
 // second read comes from L2.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -118,6 +120,48 @@ cudaError_t launch_quant_kv_tensor(const uint16_t* X, int64_t R, int64_t C, int6
     e = launch_pdl(kv_scale_kernel, dim3(1), dim3(1024), 0, st, (const uint32_t*)partial, P, scale);
     if (e != cudaSuccess) return e;
     return launch_quant_kv_with_scale(X, R, C, ld, scale, Xq, st);
+}
+
+// ---------------------------------------------------------------- no-allocation variant
+//
+// Some callers cannot hand the library a workspace: an inference engine that
+// reserves almost all GPU memory for its KV-cache pool when it starts and
+// allows no allocation outside that pool afterwards, or a serving loop that
+// must not call cudaMalloc / cudaFree because those calls synchronize the
+// device and would stall the work already queued.  For them the partial maxima
+// live in this file-scope device array instead of a caller workspace.  Every
+// GPU that loads the library holds the array (64 KB) until the process exits.
+
+constexpr int64_t kKvNoAllocSlots = 16384;   // partial maxima: tensors up to 16384 x 16384 values
+static __device__ __align__(256) uint32_t g_kv_noalloc_partials[kKvNoAllocSlots];
+
+int64_t kv_noalloc_max_values() { return kKvNoAllocSlots * kKvChunksPerCta * 8; }
+
+// Device address of the array on the current device.  The host-side name of a
+// __device__ variable is only a stand-in, never a device address, so it is
+// resolved once per device with cudaGetSymbolAddress (with that device
+// current) and cached.  Returns nullptr if the runtime reports an error.
+static uint32_t* kv_noalloc_scratch() {
+    constexpr int kMaxDevices = 64;
+    static uint32_t* cache[kMaxDevices] = {nullptr};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_kv_noalloc_partials) != cudaSuccess || !p) return nullptr;
+        cache[dev] = static_cast<uint32_t*>(p);
+    }
+    return cache[dev];
+}
+
+cudaError_t launch_quant_kv_tensor_noalloc(const uint16_t* X, int64_t R, int64_t C, int64_t ld,
+                                           uint8_t* Xq, float* scale, cudaStream_t st) {
+    if (kv_partials(R, C) > kKvNoAllocSlots) return cudaErrorInvalidValue;
+    uint32_t* partial = kv_noalloc_scratch();
+    if (!partial) return cudaErrorInvalidDevicePointer;
+    return launch_quant_kv_tensor(X, R, C, ld, Xq, scale, partial, st);
 }
 
 }  // namespace fp8rl
