@@ -440,6 +440,22 @@ def extras(fb, dev, reps=5):
         del X, Xc, Xq
     out["kv_cache_fp8_32b"] = kv
 
+    # token-level TIS / MIS weights for a rollout batch (1024 sequences x 16384 tokens)
+    n = 1024 * 16384
+    g = torch.Generator(device=dev)
+    g.manual_seed(synth.seed_for(7, 0))
+    lt = torch.randn(n, device=dev, generator=g) - 2.0
+    lr = lt + 0.3 * torch.randn(n, device=dev, generator=g)
+    mask = torch.ones(n, dtype=torch.uint8, device=dev)
+    w = torch.empty(n, dtype=torch.float32, device=dev)
+    st = torch.empty(4, dtype=torch.float64, device=dev)
+    wsb = torch.empty(max(1, fb.fp8rl_rollout_is_workspace_bytes(n)), dtype=torch.uint8, device=dev)
+    out["rollout_is"] = {}
+    for mode, name in ((0, "tis"), (1, "mis")):
+        ms = _time_graph([lambda: fb.fp8rl_rollout_is_weights(lt, lr, mask, 0.6931472, mode, w, st, wsb)] * 4)
+        out["rollout_is"][name] = {"tokens": n, "us": ms * 1e3, "gbs": 13 * n / (ms * 1e-3) / 1e9}
+    del lt, lr, mask, w
+
     # A5-A7: INT8 on the 32B shapes
     i8 = {}
     for s in synth.QWEN25_32B:

@@ -187,6 +187,35 @@ int fp8rl_quant_kv_with_scale(const uint16_t* KV, int64_t R, int64_t C, int64_t 
                               const float* scale, uint8_t* KVq, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Token-level importance-sampling rollout correction (FP8-RL, Abstract,
+ * contribution (iii): token-level TIS/MIS; FlashRL write-up, section on
+ * truncated importance sampling).  For n sampled tokens with log-probabilities
+ * under the trainer's policy (logp_train) and under the 8-bit rollout policy
+ * (logp_rollout), d = fl32(logp_train - logp_rollout) and, with the threshold
+ * C given as log_clip = ln C:
+ *   mode FP8RL_IS_TRUNCATE (TIS): w = exp(min(d, log_clip))
+ *   mode FP8RL_IS_MASK     (MIS): w = d > log_clip ? 0 : exp(d)
+ * Tokens whose mask byte is 0 (padding) get w = 0 and are not counted; mask may
+ * be NULL (every token valid).  The clip decision is an fp32 comparison (exact
+ * count); w is within a few ulp of exp (CUDA expf).
+ * logp_train, logp_rollout, weights: fp32 [n], 4-byte aligned; mask: u8 [n].
+ * stats: 4 doubles in device memory: [0] valid tokens, [1] tokens truncated
+ * (TIS) or masked (MIS), [2] sum of w, [3] sum of d over valid tokens (its
+ * mean is the sample estimate of KL(rollout || train) when the tokens are drawn
+ * from the rollout policy).  The sums are reduced in a fixed order
+ * (deterministic run to run).
+ * workspace: at least fp8rl_rollout_is_workspace_bytes(n) bytes, 8-byte
+ * aligned (32 bytes per 4096 tokens).
+ * ---------------------------------------------------------------------- */
+#define FP8RL_IS_TRUNCATE 0
+#define FP8RL_IS_MASK 1
+size_t fp8rl_rollout_is_workspace_bytes(int64_t n);
+int fp8rl_rollout_is_weights(const float* logp_train, const float* logp_rollout,
+                             const uint8_t* mask, int64_t n, float log_clip, int mode,
+                             float* weights, double* stats, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * fp8rl_quant_kv_tensor without a workspace.  The paper has no counterpart:
  * this is a calling convention, not part of the method.  It computes exactly
  * what fp8rl_quant_kv_tensor computes, for callers that cannot allocate the

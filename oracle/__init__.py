@@ -77,6 +77,8 @@ def _load():
             lib.oracle_fp8_quant_tensor.argtypes = [P, I, I, I, P, P]
             lib.oracle_fp8_quant_with_scale.restype = ctypes.c_int
             lib.oracle_fp8_quant_with_scale.argtypes = [P, I, I, I, ctypes.c_float, P]
+            lib.oracle_rollout_is.restype = ctypes.c_int
+            lib.oracle_rollout_is.argtypes = [P, P, P, I, ctypes.c_float, ctypes.c_int, P, P]
             _lib = lib
     return _lib
 
@@ -236,3 +238,19 @@ def fp8_gemm_tolerance(y_ref: np.ndarray) -> np.ndarray:
     whole [M,N] output (the tolerance the library's FP8 GEMM is held to)."""
     rms = float(np.sqrt(np.mean(np.square(y_ref)))) if y_ref.size else 0.0
     return np.abs(y_ref) * 2.0 ** -7 + 1e-3 * rms
+
+
+# ---------------------------------------------------------------- rollout correction
+
+def rollout_is(logp_train, logp_rollout, mask, log_clip: float, mode: int):
+    """Token-level TIS (mode 0) / MIS (mode 1) weights (float64) and stats
+    [valid, clipped_or_masked, sum_w, sum_logratio]."""
+    lt = np.ascontiguousarray(logp_train, np.float32).ravel()
+    lr = np.ascontiguousarray(logp_rollout, np.float32).ravel()
+    mk = np.ascontiguousarray(mask, np.uint8).ravel()
+    n = lt.size
+    w = np.empty(n, np.float64)
+    st = np.empty(4, np.float64)
+    _check(_load().oracle_rollout_is(_ptr(lt), _ptr(lr), _ptr(mk), n, float(log_clip), int(mode),
+                                     _ptr(w), _ptr(st)), "rollout_is")
+    return w.reshape(np.shape(logp_train)), st

@@ -321,3 +321,35 @@ int oracle_int8_gemm(const int8_t* Xq, const float* Xs, const int8_t* Wq, const 
         }
     return rc;
 }
+
+/* ------------------------------------------------------------------ */
+/* Token-level importance-sampling rollout correction (FP8-RL, Abstract,
+ * contribution (iii): token-level TIS/MIS; FlashRL write-up, section on TIS,
+ * whose formula is missing from the extracted page).  Reading taken: for a
+ * sampled token with log-probabilities lt under the trainer's policy and lr
+ * under the 8-bit rollout policy, d = fl32(lt - lr) is the log importance
+ * ratio; with a threshold C given as log_clip = ln C,
+ *   truncated (TIS): w = exp(min(d, log_clip)),
+ *   masked    (MIS): w = d > log_clip ? 0 : exp(d);
+ * tokens with mask 0 (padding) get w = 0 and are not counted.  The decision
+ * d > log_clip is taken in fp32 (the precision the library uses for it).
+ * stats: [0] valid tokens, [1] tokens clipped (TIS) or masked (MIS),
+ *        [2] sum of w, [3] sum of d over valid tokens (fp64).             */
+/* ------------------------------------------------------------------ */
+int oracle_rollout_is(const float* lt, const float* lr, const uint8_t* mask, int64_t n,
+                      float log_clip, int mode, double* w, double* stats) {
+    if (n < 0 || (mode != 0 && mode != 1)) return -1;
+    double nv = 0, nc = 0, sw = 0, sd = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        if (!mask[i]) { w[i] = 0.0; continue; }
+        float d = lt[i] - lr[i];
+        int clipped = d > log_clip;
+        double wi;
+        if (mode == 0) wi = exp((double)(clipped ? log_clip : d));
+        else wi = clipped ? 0.0 : exp((double)d);
+        w[i] = wi;
+        nv += 1; nc += clipped; sw += wi; sd += (double)d;
+    }
+    stats[0] = nv; stats[1] = nc; stats[2] = sw; stats[3] = sd;
+    return 0;
+}

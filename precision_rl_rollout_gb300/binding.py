@@ -30,7 +30,8 @@ EXPORTS = ("fp8rl_status_string", "fp8rl_abi_version", "fp8rl_quant_weight_block
            "int8rl_quant_weight_channel", "int8rl_quant_act_token",
            "int8rl_gemm_workspace_bytes", "int8rl_gemm_w8a8", "fp8rl_check_device_error",
            "fp8rl_kv_workspace_bytes", "fp8rl_quant_kv_tensor", "fp8rl_quant_kv_with_scale",
-           "fp8rl_quant_kv_tensor_noalloc")
+           "fp8rl_quant_kv_tensor_noalloc", "fp8rl_rollout_is_workspace_bytes",
+           "fp8rl_rollout_is_weights")
 
 
 class Fp8rlError(RuntimeError):
@@ -86,9 +87,13 @@ def load(path: str | None = None):
         lib.fp8rl_quant_kv_tensor.argtypes = [P, I, I, I, P, P, P, Z, S]
         lib.fp8rl_quant_kv_with_scale.argtypes = [P, I, I, I, P, P, S]
         lib.fp8rl_quant_kv_tensor_noalloc.argtypes = [P, I, I, I, P, P, S]
+        lib.fp8rl_rollout_is_workspace_bytes.restype = Z
+        lib.fp8rl_rollout_is_workspace_bytes.argtypes = [I]
+        lib.fp8rl_rollout_is_weights.argtypes = [P, P, P, I, ctypes.c_float, ctypes.c_int, P, P, P, Z, S]
         for name in EXPORTS:
             if name not in ("fp8rl_status_string", "fp8rl_abi_version", "fp8rl_gemm_workspace_bytes",
-                            "int8rl_gemm_workspace_bytes", "fp8rl_kv_workspace_bytes"):
+                            "int8rl_gemm_workspace_bytes", "fp8rl_kv_workspace_bytes",
+                            "fp8rl_rollout_is_workspace_bytes"):
                 getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -284,6 +289,36 @@ def fp8rl_quant_kv_tensor_noalloc(KV, KVq, scale, stream=None):
     _ck(lib.fp8rl_quant_kv_tensor_noalloc(_p(KV), R, C, ld, _p(KVq), _p(scale), _stream(KV, stream)),
         "fp8rl_quant_kv_tensor_noalloc")
     return KVq, scale
+
+
+FP8RL_IS_TRUNCATE = 0
+FP8RL_IS_MASK = 1
+
+
+def fp8rl_rollout_is_workspace_bytes(n: int) -> int:
+    return int(load().fp8rl_rollout_is_workspace_bytes(n))
+
+
+def fp8rl_rollout_is_weights(logp_train, logp_rollout, mask=None, log_clip: float = 0.6931472,
+                             mode: int = FP8RL_IS_TRUNCATE, weights=None, stats=None, workspace=None,
+                             stream=None):
+    """fp32 log-probs [...] (same shape, contiguous) -> (weights fp32 [...], stats fp64 [4])."""
+    lib = load()
+    if logp_train.shape != logp_rollout.shape or not logp_train.is_contiguous() or not logp_rollout.is_contiguous():
+        raise ValueError("logp_train and logp_rollout must be contiguous tensors of the same shape")
+    n = logp_train.numel()
+    weights = _need(weights, tuple(logp_train.shape), torch.float32, logp_train.device, "weights")
+    stats = _need(stats, (4,), torch.float64, logp_train.device, "stats")
+    if mask is not None and (mask.dtype != torch.uint8 or mask.numel() != n or not mask.is_contiguous()):
+        raise ValueError("mask must be a contiguous uint8 tensor with one byte per token")
+    need = lib.fp8rl_rollout_is_workspace_bytes(n)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=logp_train.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _ck(lib.fp8rl_rollout_is_weights(_p(logp_train), _p(logp_rollout), _p(mask), n, float(log_clip), int(mode),
+                                     _p(weights), _p(stats), _p(workspace), wbytes,
+                                     _stream(logp_train, stream)), "fp8rl_rollout_is_weights")
+    return weights, stats
 
 
 def fp8rl_check_device_error() -> int:

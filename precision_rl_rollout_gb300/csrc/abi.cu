@@ -178,6 +178,25 @@ int fp8rl_quant_kv_with_scale(const uint16_t* KV, int64_t R, int64_t C, int64_t 
     return cuda_status(launch_quant_kv_with_scale(KV, R, C, ld, scale, KVq, as_stream(stream)));
 }
 
+size_t fp8rl_rollout_is_workspace_bytes(int64_t n) {
+    if (n <= 0) return 0;
+    return (size_t)rollout_is_partials(n) * rollout_is_partial_bytes();
+}
+
+int fp8rl_rollout_is_weights(const float* logp_train, const float* logp_rollout, const uint8_t* mask,
+                             int64_t n, float log_clip, int mode, float* weights, double* stats,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+    if (n < 0 || (mode != FP8RL_IS_TRUNCATE && mode != FP8RL_IS_MASK)) return FP8RL_ERR_SHAPE;
+    if (!stats || (n > 0 && (!logp_train || !logp_rollout || !weights))) return FP8RL_ERR_NULL;
+    if (!aligned4(logp_train) || !aligned4(logp_rollout) || !aligned4(weights) ||
+        (reinterpret_cast<uintptr_t>(stats) & 7u) || (reinterpret_cast<uintptr_t>(workspace) & 7u))
+        return FP8RL_ERR_ALIGN;
+    const size_t need = fp8rl_rollout_is_workspace_bytes(n);
+    if (workspace_bytes < need || (need && !workspace)) return FP8RL_ERR_WORKSPACE;
+    return cuda_status(launch_rollout_is(logp_train, logp_rollout, mask, n, log_clip, mode, weights,
+                                         stats, workspace, as_stream(stream)));
+}
+
 int fp8rl_quant_kv_tensor_noalloc(const uint16_t* KV, int64_t R, int64_t C, int64_t ld, uint8_t* KVq,
                                   float* scale, void* stream) {
     int rc = check_kv(KV, R, C, ld, KVq);

@@ -38,6 +38,13 @@ int64_t kv_noalloc_max_values();
 cudaError_t launch_quant_kv_tensor_noalloc(const uint16_t* X, int64_t R, int64_t C, int64_t ld,
                                            uint8_t* Xq, float* scale, cudaStream_t st);
 
+// Token-level TIS/MIS weights and statistics (two launches, partial records in `ws`).
+int64_t rollout_is_partials(int64_t n);
+size_t rollout_is_partial_bytes();
+cudaError_t launch_rollout_is(const float* lt, const float* lr, const uint8_t* mask, int64_t n,
+                              float log_clip, int mode, float* w, double* stats, void* ws,
+                              cudaStream_t st);
+
 // FP8 block-scaled GEMM: dispatch by M (tcgen05 decode kernel for M <= 256).
 cudaError_t launch_gemm_fp8_decode(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
                                    const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,

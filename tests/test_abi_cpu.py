@@ -128,3 +128,13 @@ def test_kv_quant_validation(lib):
     w = lib.fp8rl_quant_kv_with_scale
     assert w(A, 64, 1024, 1024, None, A, None) == 1
     assert w(A, 0, 1024, 1024, A, A, None) == 0                          # empty: nothing launched
+
+
+def test_rollout_is_validation(lib):
+    f = lib.fp8rl_rollout_is_weights
+    ws = lib.fp8rl_rollout_is_workspace_bytes(10000)
+    assert ws == 3 * 32
+    assert f(A, A, None, 10000, ctypes.c_float(0.5), 2, A, A, A, ws, None) == 2      # bad mode
+    assert f(A, A, None, 10000, ctypes.c_float(0.5), 0, A, None, A, ws, None) == 1   # stats NULL
+    assert f(A, A, None, 10000, ctypes.c_float(0.5), 0, A, A + 4, A, ws, None) == 3  # stats alignment
+    assert f(A, A, None, 10000, ctypes.c_float(0.5), 0, A, A, A, ws - 8, None) == 4  # workspace

@@ -425,3 +425,41 @@ def test_per_tensor_quant_uses_the_global_amax():
 def test_per_tensor_quant_zero_tensor():
     q, s = oracle.fp8_quant_tensor(np.zeros((3, 16), np.uint16))
     assert s == 1.0 and not q.any()
+
+
+# ------------------------------------------------------------------ TIS / MIS rollout correction
+
+def test_rollout_is_closed_forms():
+    lt = np.array([-1.0, -2.0, -0.5, -3.0, -1.0, -7.0], np.float32)
+    lr = np.array([-1.0, -2.0 - np.log(2.0), -0.5 + np.log(4.0), -1.0, -1.0, -7.0], np.float32)
+    mask = np.array([1, 1, 1, 1, 0, 1], np.uint8)
+    log_clip = np.float32(np.log(3.0))
+    d = lt - lr                                           # 0, ln2, -ln4, -2, (masked), 0
+    w, st = oracle.rollout_is(lt, lr, mask, log_clip, 0)
+    assert w[0] == 1.0 and abs(w[1] - 2.0) < 1e-6 and abs(w[2] - 0.25) < 1e-6
+    assert abs(w[3] - np.exp(-2.0)) < 1e-7 and w[4] == 0.0 and w[5] == 1.0
+    assert st[0] == 5 and st[1] == 0
+    assert abs(st[3] - float(np.sum(d[mask == 1].astype(np.float64)))) < 1e-12
+    # a ratio above the threshold: TIS truncates it to C, MIS drops it
+    lt2 = np.array([0.0, -0.1], np.float32)
+    lr2 = np.array([-2.0, -0.1], np.float32)              # ratio e^2 > 3, and 1
+    w2, st2 = oracle.rollout_is(lt2, lr2, np.ones(2, np.uint8), log_clip, 0)
+    assert abs(w2[0] - 3.0) < 1e-6 and w2[1] == 1.0 and st2[1] == 1 and abs(st2[2] - 4.0) < 1e-6
+    w3, st3 = oracle.rollout_is(lt2, lr2, np.ones(2, np.uint8), log_clip, 1)
+    assert w3[0] == 0.0 and w3[1] == 1.0 and st3[1] == 1 and st3[2] == 1.0
+
+
+def test_rollout_is_matches_library_exp_and_counts():
+    rng = np.random.default_rng(12)
+    lt = rng.normal(-2.0, 1.0, 5000).astype(np.float32)
+    lr = (lt + rng.normal(0.0, 0.3, 5000)).astype(np.float32)
+    mask = (rng.random(5000) < 0.9).astype(np.uint8)
+    log_clip = np.float32(np.log(2.0))
+    d = (lt - lr).astype(np.float32)
+    for mode in (0, 1):
+        w, st = oracle.rollout_is(lt, lr, mask, log_clip, mode)
+        clipped = (d > log_clip) & (mask == 1)
+        keep = np.exp(d.astype(np.float64))
+        want = np.where(mask == 0, 0.0, np.where(clipped, np.exp(float(log_clip)) if mode == 0 else 0.0, keep))
+        assert np.allclose(w, want, rtol=1e-12, atol=0)
+        assert st[0] == mask.sum() and st[1] == clipped.sum()

@@ -1,0 +1,48 @@
+"""GPU parity of the token-level TIS/MIS rollout correction against the CPU
+oracle: clipped/masked and valid counts exact, weights within 4 ulp of the
+fp64 exp, sums within fp32 accumulation error."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity_util import host
+from precision_rl_rollout_gb300 import binding as fb
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(n, seed, sigma=0.3):
+    g = torch.Generator().manual_seed(seed)
+    lt = torch.randn(n, generator=g) * 1.5 - 2.0
+    lr = lt + torch.randn(n, generator=g) * sigma
+    mask = (torch.rand(n, generator=g) < 0.9).to(torch.uint8)
+    return lt.float(), lr.float(), mask
+
+
+@pytest.mark.parametrize("n", [0, 1, 7, 4096, 4097, 100003, 1 << 20])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_rollout_is_matches_oracle(cuda_lib, n, mode):
+    lt, lr, mask = _inputs(n, 100 + n)
+    log_clip = float(np.float32(math.log(2.0)))
+    w, stats = fb.fp8rl_rollout_is_weights(lt.cuda(), lr.cuda(), mask.cuda(), log_clip, mode)
+    want_w, want_st = oracle.rollout_is(lt.numpy(), lr.numpy(), mask.numpy(), log_clip, mode)
+    got_w, got_st = host(w).astype(np.float64), host(stats)
+    assert got_st[0] == want_st[0] and got_st[1] == want_st[1]      # exact counts
+    assert np.all(np.abs(got_w - want_w) <= 4 * 2.0 ** -23 * np.abs(want_w))
+    tol = 1e-6 * max(1.0, float(np.sum(np.abs(want_w))))
+    assert abs(got_st[2] - want_st[2]) <= tol
+    d = np.abs(lt.numpy() - lr.numpy()).astype(np.float64)
+    assert abs(got_st[3] - want_st[3]) <= 1e-6 * max(1.0, float(np.sum(d)))
+
+
+def test_rollout_is_no_mask_and_deterministic(cuda_lib):
+    n = 3 * 4096 + 5
+    lt, lr, _ = _inputs(n, 9, sigma=1.0)
+    runs = [fb.fp8rl_rollout_is_weights(lt.cuda(), lr.cuda(), None, 0.0, 0) for _ in range(2)]
+    want_w, want_st = oracle.rollout_is(lt.numpy(), lr.numpy(), np.ones(n, np.uint8), 0.0, 0)
+    assert host(runs[0][1])[0] == n and host(runs[0][1])[1] == want_st[1]
+    assert np.array_equal(host(runs[0][1]), host(runs[1][1]))        # same bits run to run
+    assert np.all(host(runs[0][0]) <= 1.0)                           # C = 1 truncates to <= 1
