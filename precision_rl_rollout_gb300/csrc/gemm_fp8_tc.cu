@@ -198,9 +198,9 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
         }
         named_bar_sync(1, C::kEpiWarps * 32);
 
-        float acc[C::kCols];
+        uint64_t acc[C::kCols / 2];              // fp32 accumulators as packed pairs
 #pragma unroll
-        for (int j = 0; j < C::kCols; ++j) acc[j] = 0.f;
+        for (int j = 0; j < C::kCols / 2; ++j) acc[j] = 0ull;
         for (int it = 0; it < nkb; ++it) {
             const int buf = it & 1;
             const uint32_t bph = (it >> 1) & 1;
@@ -224,10 +224,10 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
                     else tmem_ld_32x32b_x16(a, rc);
                 }
                 tmem_wait_ld();
+                const uint64_t* cs2 = reinterpret_cast<const uint64_t*>(cs + g * C::kGroup);
 #pragma unroll
-                for (int j = 0; j < C::kGroup; ++j)
-                    acc[g * C::kGroup + j] =
-                        fmaf(__uint_as_float(r[j]), cs[g * C::kGroup + j], acc[g * C::kGroup + j]);
+                for (int j = 0; j < C::kGroup / 2; ++j)
+                    fma_f32x2(acc[g * C::kGroup / 2 + j], f32x2_pack(r[2 * j], r[2 * j + 1]), cs2[j]);
             }
             tc_fence_before();
             __syncwarp();
@@ -237,7 +237,11 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
         // transposed partial tile red[m][n_local]
         float* red = reinterpret_cast<float*>(smem);
 #pragma unroll
-        for (int j = 0; j < C::kCols; ++j) red[(colbase + j) * 128 + n_local] = acc[j];
+        for (int j = 0; j < C::kCols / 2; ++j) {
+            const float2 v = f32x2_unpack(acc[j]);
+            red[(colbase + 2 * j) * 128 + n_local] = v.x;
+            red[(colbase + 2 * j + 1) * 128 + n_local] = v.y;
+        }
     }
 
     // ---------------- split-K reduction over the cluster, then bf16 stores

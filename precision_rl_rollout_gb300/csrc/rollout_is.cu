@@ -11,8 +11,8 @@
 // padding tokens (mask 0) get w = 0.  The clip decision is an fp32 comparison,
 // so the clipped/masked count is exact; the weights use the CUDA expf.
 // Two launches: every CTA writes the weights of its 4096 tokens and one
-// partial record (valid, clipped, sum w, sum d); one CTA then adds the records
-// in a fixed order (deterministic statistics).
+// partial record (valid, clipped, sum w, sum d; fp32 sums inside the CTA); one
+// CTA then adds the records in fp64 in a fixed order (deterministic statistics).
 #include "common.cuh"
 #include "internal.h"
 
@@ -34,6 +34,15 @@ __device__ __forceinline__ double warp_sum(double v) {
     return v;
 }
 
+__device__ __forceinline__ float is_weight(float d, float log_clip, int mode, bool& clipped) {
+    clipped = d > log_clip;
+    return mode == 0 ? expf(clipped ? log_clip : d) : (clipped ? 0.f : expf(d));
+}
+
+// Every thread owns 16 tokens of its CTA's 4096: in the vector form, four
+// groups of four consecutive tokens (16-byte loads of both log-prob arrays and
+// a 4-byte load of the mask, all issued before any is used).
+template <bool kVec>
 __global__ void __launch_bounds__(kIsThreads)
 rollout_is_kernel(const float* __restrict__ lt, const float* __restrict__ lr,
                   const uint8_t* __restrict__ mask, int64_t n, float log_clip, int mode,
@@ -42,35 +51,79 @@ rollout_is_kernel(const float* __restrict__ lt, const float* __restrict__ lr,
     const int64_t base = (int64_t)blockIdx.x * kIsPerCta;
     int nv = 0, nc = 0;
     float sw = 0.f, sd = 0.f;
-#pragma unroll 4
-    for (int j = 0; j < kIsPerThread; ++j) {
-        const int64_t i = base + j * kIsThreads + threadIdx.x;
-        if (i >= n) break;
-        const bool valid = mask == nullptr || mask[i] != 0;
-        float wi = 0.f;
-        if (valid) {
-            const float d = __fsub_rn(lt[i], lr[i]);
-            const bool clipped = d > log_clip;
-            wi = mode == 0 ? expf(clipped ? log_clip : d) : (clipped ? 0.f : expf(d));
-            nv += 1;
-            nc += clipped;
-            sw += wi;
-            sd += d;
+    if (kVec && base + kIsPerCta <= n) {
+        float4 a[4], b[4];
+        uint32_t mk[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const int64_t i = base + (int64_t)(g * kIsThreads + threadIdx.x) * 4;
+            a[g] = *reinterpret_cast<const float4*>(lt + i);
+            b[g] = *reinterpret_cast<const float4*>(lr + i);
+            mk[g] = mask ? *reinterpret_cast<const uint32_t*>(mask + i) : 0x01010101u;
         }
-        w[i] = wi;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const float x[4] = {a[g].x, a[g].y, a[g].z, a[g].w};
+            const float y[4] = {b[g].x, b[g].y, b[g].z, b[g].w};
+            float o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                o[e] = 0.f;
+                if ((mk[g] >> (8 * e)) & 0xFFu) {
+                    const float d = __fsub_rn(x[e], y[e]);
+                    bool clipped;
+                    o[e] = is_weight(d, log_clip, mode, clipped);
+                    nv += 1;
+                    nc += clipped;
+                    sw += o[e];
+                    sd += d;
+                }
+            }
+            const int64_t i = base + (int64_t)(g * kIsThreads + threadIdx.x) * 4;
+            *reinterpret_cast<float4*>(w + i) = make_float4(o[0], o[1], o[2], o[3]);
+        }
+    } else {
+        for (int j = 0; j < kIsPerThread; ++j) {
+            const int64_t i = base + j * kIsThreads + threadIdx.x;
+            if (i >= n) break;
+            float wi = 0.f;
+            if (mask == nullptr || mask[i] != 0) {
+                const float d = __fsub_rn(lt[i], lr[i]);
+                bool clipped;
+                wi = is_weight(d, log_clip, mode, clipped);
+                nv += 1;
+                nc += clipped;
+                sw += wi;
+                sd += d;
+            }
+            w[i] = wi;
+        }
     }
-    double v0 = warp_sum((double)nv), v1 = warp_sum((double)nc), v2 = warp_sum((double)sw),
-           v3 = warp_sum((double)sd);
-    __shared__ double red[kIsThreads / 32][4];
+    // In-CTA reduction in fp32 (counts exactly, as integers): fp64 arithmetic is
+    // a small fraction of the fp32 rate on this GPU.  Only the per-CTA record is
+    // widened to fp64.
+    nv = __reduce_add_sync(0xffffffffu, nv);
+    nc = __reduce_add_sync(0xffffffffu, nc);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        sw += __shfl_xor_sync(0xffffffffu, sw, off);
+        sd += __shfl_xor_sync(0xffffffffu, sd, off);
+    }
+    __shared__ int ired[kIsThreads / 32][2];
+    __shared__ float fred[kIsThreads / 32][2];
     const int wid = threadIdx.x >> 5;
     if ((threadIdx.x & 31) == 0) {
-        red[wid][0] = v0; red[wid][1] = v1; red[wid][2] = v2; red[wid][3] = v3;
+        ired[wid][0] = nv; ired[wid][1] = nc;
+        fred[wid][0] = sw; fred[wid][1] = sd;
     }
     __syncthreads();
-    if (threadIdx.x < 4) {
-        double t = 0.0;
-        for (int k = 0; k < kIsThreads / 32; ++k) t += red[k][threadIdx.x];
-        reinterpret_cast<double*>(&part[blockIdx.x])[threadIdx.x] = t;
+    if (threadIdx.x == 0) {
+        int a = 0, b = 0;
+        float c = 0.f, e = 0.f;
+        for (int k = 0; k < kIsThreads / 32; ++k) {
+            a += ired[k][0]; b += ired[k][1]; c += fred[k][0]; e += fred[k][1];
+        }
+        part[blockIdx.x] = IsPartial{(double)a, (double)b, (double)c, (double)e};
     }
 }
 
@@ -110,8 +163,13 @@ cudaError_t launch_rollout_is(const float* lt, const float* lr, const uint8_t* m
     IsPartial* part = static_cast<IsPartial*>(ws);
     cudaError_t e;
     if (P > 0) {
-        e = launch_pdl(rollout_is_kernel, dim3((unsigned)P), dim3(kIsThreads), 0, st, lt, lr, mask, n,
-                       log_clip, mode, w, part);
+        const bool vec = ((reinterpret_cast<uintptr_t>(lt) | reinterpret_cast<uintptr_t>(lr) |
+                           reinterpret_cast<uintptr_t>(w)) & 15u) == 0 &&
+                         (reinterpret_cast<uintptr_t>(mask) & 3u) == 0;
+        e = vec ? launch_pdl(rollout_is_kernel<true>, dim3((unsigned)P), dim3(kIsThreads), 0, st, lt, lr,
+                             mask, n, log_clip, mode, w, part)
+                : launch_pdl(rollout_is_kernel<false>, dim3((unsigned)P), dim3(kIsThreads), 0, st, lt, lr,
+                             mask, n, log_clip, mode, w, part);
         if (e != cudaSuccess) return e;
     }
     return launch_pdl(rollout_is_stats_kernel, dim3(1), dim3(1024), 0, st, (const IsPartial*)part, P,

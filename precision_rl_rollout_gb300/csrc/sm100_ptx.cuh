@@ -208,6 +208,38 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
         : "r"(taddr));
 }
 
+// ------------------------------------------------------------------ packed fp32 pairs
+
+// Two fp32 values in one 64-bit register pair (low = first).
+__device__ __forceinline__ uint64_t f32x2_pack(uint32_t lo, uint32_t hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ __forceinline__ float2 f32x2_unpack(uint64_t v) {
+    float2 f;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(v));
+    return f;
+}
+// acc = a * b + acc on both halves, each an IEEE fma rounded to nearest (one
+// instruction for two lanes of work).
+__device__ __forceinline__ void fma_f32x2(uint64_t& acc, uint64_t a, uint64_t b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+
+// (a0, a1) += (x0, x1) * (s, s) with one packed instruction; operands stay in
+// ordinary fp32 registers (the pairing is left to the register allocator).
+__device__ __forceinline__ void fma2_scalar(float& a0, float& a1, uint32_t x0, uint32_t x1, float s) {
+    asm("{\n.reg .b64 a, x, t;\n"
+        "mov.b64 a, {%0, %1};\n"
+        "mov.b64 x, {%2, %3};\n"
+        "mov.b64 t, {%4, %4};\n"
+        "fma.rn.f32x2 a, x, t, a;\n"
+        "mov.b64 {%0, %1}, a;\n}\n"
+        : "+f"(a0), "+f"(a1)
+        : "r"(x0), "r"(x1), "f"(s));
+}
+
 // ------------------------------------------------------------------ descriptors
 
 // UMMA shared-memory descriptor of a K-major operand tile stored with the
