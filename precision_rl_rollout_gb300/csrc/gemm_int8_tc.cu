@@ -1,0 +1,391 @@
+// gemm_int8_tc.cu -- exact INT8 W8A8 GEMM on the 5th-generation tensor cores.
+//
+// FlashRL write-up (Fig. 1, INT8 rollout): acc[m][n] = sum_k Xq[m][k] Wq[n][k]
+// exactly (int32), y = bf16_rn((float(acc) * Xs[m]) * Ws[n]).
+//
+// sm_103a has no tcgen05 INT8 MMA kind and its legacy INT8 warp MMA is slow, so
+// the integer product runs on the fp16 tensor path with exact arithmetic:
+//   * every int8 code v (|v| <= 127) is an exact fp16; the conversion is the
+//     offset-binary identity fp16(0x6400 | (v ^ 0x80)) = 1152 + v followed by
+//     one packed fp16 subtraction of 1152 (exact: the result needs <= 8 bits);
+//   * each product is an integer below 2^14, exact in the fp32 accumulator;
+//   * a TMEM accumulator collects at most 4 K blocks (512 products per output,
+//     |sum| <= 512 * 127^2 < 2^23) so every partial sum is an integer well
+//     inside fp32's 24-bit significand and no rounding can occur; it is then
+//     converted to int32 (exact) and added in int32 registers.
+// The bit-exact parity tests against the int64 CPU reference include the
+// extreme case of every code at +-127.
+//
+// Layout (swap-AB, as the FP8 decode kernel): the MMA's M side is 128 weight
+// rows, its N side a tile of MT tokens; each CTA streams one 128-row weight
+// slab.  Warp 0 issues TMA (raw int8 tiles, 128-byte swizzle), warp 1 the
+// MMAs, warps 2-5 convert raw tiles to fp16 operand tiles in the UMMA K-major
+// 128-byte-swizzle layout (a 128-wide K block is two 64-wide atoms), warps 6-9
+// promote and hold the int32 accumulators.  Split-K CTAs of one slab form a
+// cluster and add their int32 partials through distributed shared memory.
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "sm100_ptx.cuh"
+
+namespace fp8rl {
+
+using namespace sm100;
+
+namespace {
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint32_t kKernelInt8 = 3;
+constexpr int kGroupKb = 4;   // K blocks accumulated in TMEM before promotion (exactness bound)
+
+struct Int8Params {
+    uint32_t* err;
+    const float* Xs;   // [M]
+    const float* Ws;   // [N]
+    uint16_t* Y;       // [M][ldy]
+    int32_t* acc;      // [M][N] or null
+    int64_t M, N, ldy;
+    int KB;
+    int kb_per_split;
+    int split;
+};
+
+template <int MT>
+struct I8Cfg {
+    static_assert(MT == 16 || MT == 32 || MT == 64, "token tile");
+    static constexpr int kThreads = 320;                       // 10 warps
+    static constexpr int kRawW = 128 * 128, kRawX = MT * 128;  // int8 tiles
+    static constexpr int kRawStage = kRawW + kRawX;
+    static constexpr int kRawStages = 4;
+    static constexpr int kCvtW = 2 * 128 * 128, kCvtX = 2 * MT * 128;   // fp16: two 64-wide atoms
+    static constexpr int kCvtStage = kCvtW + kCvtX;
+    static constexpr int kCvtStages = 2;
+    static constexpr int kCvtOffset = kRawStages * kRawStage;
+    static constexpr int kBarOffset = kCvtOffset + kCvtStages * kCvtStage;
+    static constexpr int kSmemBytes = kBarOffset + 256 + 1024;
+    static constexpr int kTmemCols = 2 * MT < 32 ? 32 : 2 * MT;
+    static constexpr int kChunk = MT >= 32 ? 32 : 16;
+    static_assert(MT * 128 * 4 <= kRawStages * kRawStage, "reduction buffer must fit the raw stages");
+    static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+};
+
+__device__ __forceinline__ void record_timeout(uint32_t* err, uint32_t site, volatile int* abort) {
+    atomicCAS(err, 0u, (kKernelInt8 << 24) | (site << 16) | 1u);
+    *abort = 1;
+}
+
+// 4 int8 codes (one 32-bit word) -> 4 fp16 values in two words (exact).
+__device__ __forceinline__ void i8x4_to_f16x4(uint32_t x, uint32_t& lo, uint32_t& hi) {
+    const uint32_t y = x ^ 0x80808080u;
+    lo = __byte_perm(y, 0x64646464u, 0x4140);   // [y0, 0x64, y1, 0x64]
+    hi = __byte_perm(y, 0x64646464u, 0x4342);   // [y2, 0x64, y3, 0x64]
+    const __half2 off = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+    __half2 a = __hsub2(*reinterpret_cast<__half2*>(&lo), off);
+    __half2 b = __hsub2(*reinterpret_cast<__half2*>(&hi), off);
+    lo = *reinterpret_cast<uint32_t*>(&a);
+    hi = *reinterpret_cast<uint32_t*>(&b);
+}
+
+// Row r of a raw int8 tile (128 B, 128-byte swizzle) -> the fp16 operand tile
+// (two atoms of 64 K, each 128 B per row, 128-byte swizzle).
+__device__ __forceinline__ void convert_row(const uint8_t* raw, uint8_t* cvt, int r, int atom_bytes) {
+    const int sw = r & 7;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(raw + r * 128 + ((c ^ sw) << 4));
+        uint4 o0, o1;
+        i8x4_to_f16x4(v.x, o0.x, o0.y);
+        i8x4_to_f16x4(v.y, o0.z, o0.w);
+        i8x4_to_f16x4(v.z, o1.x, o1.y);
+        i8x4_to_f16x4(v.w, o1.z, o1.w);
+        uint8_t* dst = cvt + (c >> 2) * atom_bytes + r * 128;
+        const int j = 2 * (c & 3);
+        *reinterpret_cast<uint4*>(dst + ((j ^ sw) << 4)) = o0;
+        *reinterpret_cast<uint4*>(dst + (((j + 1) ^ sw) << 4)) = o1;
+    }
+}
+
+template <int MT>
+__global__ void __launch_bounds__(I8Cfg<MT>::kThreads, 1)
+gemm_int8_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                    const __grid_constant__ Int8Params p) {
+    using C = I8Cfg<MT>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
+    // raw_full[R], raw_empty[R], cvt_full[V], cvt_empty[V], tfull[2], tempty[2]
+    constexpr int R = C::kRawStages, V = C::kCvtStages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * R + 2 * V + 4);
+    volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const uint32_t rfull0 = smem_u32(bars), rempty0 = smem_u32(bars + R);
+    const uint32_t cfull0 = smem_u32(bars + 2 * R), cempty0 = smem_u32(bars + 2 * R + V);
+    const uint32_t tfull0 = smem_u32(bars + 2 * R + 2 * V), tempty0 = smem_u32(bars + 2 * R + 2 * V + 2);
+
+    const uint32_t warp = warp_id(), lane = lane_id();
+    const int split_idx = blockIdx.x;
+    const int mt = blockIdx.y, nt = blockIdx.z;
+    const int kb0 = split_idx * p.kb_per_split;
+    const int nkb = min(p.KB, kb0 + p.kb_per_split) - kb0;
+    const int ngroups = (nkb + kGroupKb - 1) / kGroupKb;
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < R; ++s) {
+            mbar_init(rfull0 + 8 * s, 1);
+            mbar_init(rempty0 + 8 * s, 4);           // the four converter warps
+        }
+        for (int s = 0; s < V; ++s) {
+            mbar_init(cfull0 + 8 * s, 4);
+            mbar_init(cempty0 + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull0 + 8 * b, 1);
+            mbar_init(tempty0 + 8 * b, 4);           // the four epilogue warps
+        }
+        *abort = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmW);
+        prefetch_tmap(&tmX);
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    if (warp == 0) {
+        // ---------------- TMA producer: raw int8 tiles
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+            int it = 0;
+            for (; it < nkb; ++it) {
+                const int s = it % R;
+                const uint32_t ph = (it / R) & 1;
+                if (!mbar_wait_bounded(rempty0 + 8 * s, ph ^ 1, abort, kWaitLimitNs)) {
+                    record_timeout(p.err, 1, abort);
+                    break;
+                }
+                uint8_t* st = smem + s * C::kRawStage;
+                mbar_arrive_expect_tx(rfull0 + 8 * s, C::kRawStage);
+                tma_load_2d(smem_u32(st), &tmW, rfull0 + 8 * s, (kb0 + it) * 128, nt * 128, pol_w);
+                tma_load_2d(smem_u32(st + C::kRawW), &tmX, rfull0 + 8 * s, (kb0 + it) * 128, mt * MT, pol_x);
+            }
+            if (*abort)
+                for (int j = max(0, it - R); j < it; ++j)
+                    mbar_wait_bounded(rfull0 + 8 * (j % R), (j / R) & 1, abort, kWaitLimitNs);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer: 8 x (M=128, N=MT, K=16) fp16 MMAs per K block
+        if (lane == 0) {
+            constexpr uint32_t idesc = (1u << 4) | ((uint32_t)(MT >> 3) << 17) | ((128u >> 4) << 24);  // f16 x f16 -> f32
+            for (int it = 0; it < nkb; ++it) {
+                const int s = it % V;
+                const uint32_t ph = (it / V) & 1;
+                const int g = it / kGroupKb;
+                const uint32_t buf = g & 1, bph = (g >> 1) & 1;
+                const bool first = (it % kGroupKb) == 0;
+                const bool last = (it % kGroupKb) == kGroupKb - 1 || it == nkb - 1;
+                if (!mbar_wait_bounded(cfull0 + 8 * s, ph, abort, kWaitLimitNs)) {
+                    record_timeout(p.err, 2, abort);
+                    break;
+                }
+                if (first && !mbar_wait_bounded(tempty0 + 8 * buf, bph ^ 1, abort, kWaitLimitNs)) {
+                    record_timeout(p.err, 3, abort);
+                    break;
+                }
+                tc_fence_after();
+                const uint8_t* st = smem + C::kCvtOffset + s * C::kCvtStage;
+                const uint32_t d = tmem_base + buf * MT;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {        // K = 16 fp16 = 32 bytes per step; 4 steps per atom
+                    const uint64_t a = umma_desc_k128_sw128(smem_u32(st + (k >> 2) * (128 * 128))) + 2 * (k & 3);
+                    const uint64_t b = umma_desc_k128_sw128(smem_u32(st + C::kCvtW + (k >> 2) * (MT * 128))) + 2 * (k & 3);
+                    mma_f16(d, a, b, idesc, (first && k == 0) ? 0u : 1u);
+                }
+                tc_commit(cempty0 + 8 * s);
+                if (last) tc_commit(tfull0 + 8 * buf);
+            }
+        }
+    } else if (warp < 6) {
+        // ---------------- converters: raw int8 -> fp16 operand tiles
+        const int t = (warp - 2) * 32 + lane;        // 0..127
+        for (int it = 0; it < nkb; ++it) {
+            const int rs = it % R, cs = it % V;
+            const uint32_t rph = (it / R) & 1, cph = (it / V) & 1;
+            if (!mbar_wait_bounded(rfull0 + 8 * rs, rph, abort, kWaitLimitNs) ||
+                !mbar_wait_bounded(cempty0 + 8 * cs, cph ^ 1, abort, kWaitLimitNs)) {
+                record_timeout(p.err, 4, abort);
+                break;
+            }
+            const uint8_t* raw = smem + rs * C::kRawStage;
+            uint8_t* cvt = smem + C::kCvtOffset + cs * C::kCvtStage;
+            convert_row(raw, cvt, t, 128 * 128);                               // weight row t
+            if (t < MT) convert_row(raw + C::kRawW, cvt + C::kCvtW, t, MT * 128);   // token row t
+            fence_proxy_async_smem();                // generic writes -> tensor-core reads
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(cfull0 + 8 * cs);
+                mbar_arrive(rempty0 + 8 * rs);
+            }
+        }
+    } else {
+        // ---------------- epilogue: exact promotion into int32 registers
+        const int q = warp & 3;
+        const int n_local = 32 * q + lane;
+        int32_t acc[MT];
+#pragma unroll
+        for (int j = 0; j < MT; ++j) acc[j] = 0;
+        for (int g = 0; g < ngroups; ++g) {
+            const uint32_t buf = g & 1, bph = (g >> 1) & 1;
+            if (!mbar_wait_bounded(tfull0 + 8 * buf, bph, abort, kWaitLimitNs)) {
+                record_timeout(p.err, 5, abort);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + buf * MT;
+#pragma unroll
+            for (int ch = 0; ch < MT / C::kChunk; ++ch) {
+                uint32_t r[C::kChunk];
+                if constexpr (C::kChunk == 32) tmem_ld_32x32b_x32(taddr + ch * 32, r);
+                else tmem_ld_32x32b_x16(taddr + ch * 16, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < C::kChunk; ++j) acc[ch * C::kChunk + j] += __float2int_rn(__uint_as_float(r[j]));
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
+        }
+        // every MMA has completed: the raw stages hold the transposed partial tile
+        int32_t* red = reinterpret_cast<int32_t*>(smem);
+#pragma unroll
+        for (int j = 0; j < MT; ++j) red[j * 128 + n_local] = acc[j];
+    }
+
+    // ---------------- split-K reduction over the cluster (int32: exact), epilogue stores
+    tc_fence_before();
+    if (p.split > 1) cluster_sync_all(); else __syncthreads();
+    {
+        const int64_t m_tile0 = (int64_t)mt * MT;
+        const int valid_m = (int)(p.M - m_tile0 < MT ? p.M - m_tile0 : MT);
+        const int total = valid_m * 16;
+        const int per = (total + p.split - 1) / p.split;
+        const int begin = split_idx * per, end = min(total, begin + per);
+        const uint32_t red_addr = smem_u32(smem);
+        for (int c = begin + (int)threadIdx.x; c < end; c += C::kThreads) {
+            const int m = c >> 4, n8 = c & 15;
+            const uint32_t off = (uint32_t)(m * 128 + n8 * 8) * 4u;
+            int32_t s[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            for (int rk = 0; rk < p.split; ++rk) {
+                float4 v0, v1;
+                if (p.split > 1) {
+                    const uint32_t a = map_to_rank(red_addr + off, (uint32_t)rk);
+                    v0 = ld_cluster_v4(a);
+                    v1 = ld_cluster_v4(a + 16);
+                } else {
+                    const float4* l = reinterpret_cast<const float4*>(smem + off);
+                    v0 = l[0];
+                    v1 = l[1];
+                }
+                s[0] += __float_as_int(v0.x); s[1] += __float_as_int(v0.y);
+                s[2] += __float_as_int(v0.z); s[3] += __float_as_int(v0.w);
+                s[4] += __float_as_int(v1.x); s[5] += __float_as_int(v1.y);
+                s[6] += __float_as_int(v1.z); s[7] += __float_as_int(v1.w);
+            }
+            const int64_t mg = m_tile0 + m, n0 = (int64_t)nt * 128 + n8 * 8;
+            const float xs = p.Xs[mg];
+            float y[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) y[e] = __fmul_rn(__fmul_rn(__int2float_rn(s[e]), xs), p.Ws[n0 + e]);
+            uint4 o;
+            o.x = pack_bf16x2(y[0], y[1]);
+            o.y = pack_bf16x2(y[2], y[3]);
+            o.z = pack_bf16x2(y[4], y[5]);
+            o.w = pack_bf16x2(y[6], y[7]);
+            *reinterpret_cast<uint4*>(p.Y + mg * p.ldy + n0) = o;
+            if (p.acc) {                             // 8-byte stores: the ABI guarantees 8-byte alignment
+                int2* a2 = reinterpret_cast<int2*>(p.acc + mg * p.N + n0);
+                a2[0] = make_int2(s[0], s[1]);
+                a2[1] = make_int2(s[2], s[3]);
+                a2[2] = make_int2(s[4], s[5]);
+                a2[3] = make_int2(s[6], s[7]);
+            }
+        }
+    }
+    if (p.split > 1) cluster_sync_all(); else __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
+// Split-K factor: fill the GPU (one CTA per SM) without starving each CTA.
+int choose_split_i8(int64_t tiles, int KB) {
+    const int sms = num_sms();
+    int best = 1;
+    double best_cost = 1e30;
+    for (int s = 1; s <= 8 && s <= KB; ++s) {
+        const int per = (KB + s - 1) / s;
+        if ((int64_t)(s - 1) * per >= KB) continue;
+        const int64_t ctas = tiles * s;
+        const int64_t busiest = (ctas + sms - 1) / sms;
+        const double cost = 3.0 * busiest + 0.55 * busiest * per + 1.0 * s;
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best = s;
+        }
+    }
+    return best;
+}
+
+template <int MT>
+cudaError_t launch_i8_mt(const int8_t* Xq, const float* Xs, const int8_t* Wq, const float* Ws, int64_t M,
+                         int64_t N, int64_t K, uint16_t* Y, int64_t ldy, int32_t* acc, cudaStream_t st) {
+    using C = I8Cfg<MT>;
+    CUtensorMap tmW, tmX;
+    if (!make_tmap_u8(&tmW, Wq, (uint64_t)N, (uint64_t)K, (uint64_t)K, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap_u8(&tmX, Xq, (uint64_t)M, (uint64_t)K, (uint64_t)K, MT)) return cudaErrorInvalidValue;
+    const int KB = (int)(K / 128);
+    const int64_t mtiles = (M + MT - 1) / MT;
+    const int split = choose_split_i8((N / 128) * mtiles, KB);
+    const int per = (KB + split - 1) / split;
+    uint32_t* err = device_error_word();
+    if (!err) return cudaErrorInvalidValue;
+    Int8Params prm{err, Xs, Ws, Y, acc, M, N, ldy, KB, per, split};
+    auto kern = gemm_int8_tc_kernel<MT>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)split, (unsigned)mtiles, (unsigned)(N / 128));
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)split;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kern, tmW, tmX, prm);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_int8_tc(const int8_t* Xq, const float* Xs, const int8_t* Wq, const float* Ws,
+                                int64_t M, int64_t N, int64_t K, uint16_t* Y, int64_t ldy, int32_t* acc,
+                                cudaStream_t st) {
+    if (M <= 16) return launch_i8_mt<16>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, acc, st);
+    if (M <= 32) return launch_i8_mt<32>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, acc, st);
+    return launch_i8_mt<64>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, acc, st);
+}
+
+}  // namespace fp8rl

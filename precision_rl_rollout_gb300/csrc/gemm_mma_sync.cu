@@ -170,6 +170,7 @@ size_t gemm_int8_workspace_bytes(int64_t, int64_t, int64_t) { return 0; }
 cudaError_t launch_gemm_int8(const int8_t* Xq, const float* Xs, const int8_t* Wq,
                              const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
                              int64_t ldy, int32_t* acc, void*, size_t, cudaStream_t st) {
+    if (M <= 256) return launch_gemm_int8_tc(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, acc, st);
     return launch_gemm_int8_mma_sync(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, acc, st);
 }
 
