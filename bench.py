@@ -627,6 +627,24 @@ def profile_case(fb, case, dev, reps=3):
         Xq, Xs = fb.fp8rl_quant_act_group(synth.activation(M, s.K, synth.seed_for(3, 1), device=dev))
         for _ in range(reps):
             fb.fp8rl_gemm_w8a8_block(Xq, Xs, Wq, Ws)
+    elif case == "int8_m32":
+        s = synth.QWEN25_32B[2]                          # gate_up 5120 -> 55296
+        W = synth.weight_bf16_direct(s.N, s.K, synth.seed_for(5, 0), device=dev)
+        Wq, Ws = fb.int8rl_quant_weight_channel(W)
+        del W
+        Xq, Xs = fb.int8rl_quant_act_token(synth.activation(32, s.K, synth.seed_for(5, 1), device=dev))
+        for _ in range(reps):
+            fb.int8rl_gemm_w8a8(Xq, Xs, Wq, Ws)
+    elif case == "kv":
+        X = synth.activation(64 * 2048, 1024, synth.seed_for(6, 0), device=dev)
+        for _ in range(reps):
+            fb.fp8rl_quant_kv_tensor(X)
+    elif case == "tis":
+        n = 1024 * 16384
+        lt = torch.randn(n, device=dev) - 2.0
+        lr = lt + 0.3 * torch.randn(n, device=dev)
+        for _ in range(reps):
+            fb.fp8rl_rollout_is_weights(lt, lr, None, 0.6931472, 0)
     elif case == "prefill":
         s = synth.QWEN25_32B[0]
         W = synth.weight_bf16_direct(s.N, s.K, synth.seed_for(4, 0), device=dev)
@@ -660,7 +678,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--profile", default=None,
-                    help="run one small case for ncu: requant | decode | decode7b_m<M> | decode32b_m<M> | prefill | int8")
+                    help="run one small case for ncu: requant | decode | decode7b_m<M> | decode32b_m<M> | prefill | int8 | int8_m32 | kv | tis")
     args = ap.parse_args()
     world, rank, local = dist_env()
     if args.impl == "reference":

@@ -57,7 +57,9 @@ struct I8Cfg {
     static constexpr int kThreads = 320;                       // 10 warps
     static constexpr int kRawW = 128 * 128, kRawX = MT * 128;  // int8 tiles
     static constexpr int kRawStage = kRawW + kRawX;
-    static constexpr int kRawStages = 4;
+    // raw int8 stages fill what the two fp16 stages leave of ~220 KB: the weight
+    // bytes in flight per SM are what keeps the HBM stream going
+    static constexpr int kRawStages = MT == 16 ? 8 : MT == 32 ? 7 : 5;
     static constexpr int kCvtW = 2 * 128 * 128, kCvtX = 2 * MT * 128;   // fp16: two 64-wide atoms
     static constexpr int kCvtStage = kCvtW + kCvtX;
     static constexpr int kCvtStages = 2;
