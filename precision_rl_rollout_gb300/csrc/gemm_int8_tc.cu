@@ -19,9 +19,10 @@
 // Layout (swap-AB, as the FP8 decode kernel): the MMA's M side is 128 weight
 // rows, its N side a tile of MT tokens; each CTA streams one 128-row weight
 // slab.  Warp 0 issues TMA (raw int8 tiles, 128-byte swizzle), warp 1 the
-// MMAs, warps 2-5 convert raw tiles to fp16 operand tiles in the UMMA K-major
-// 128-byte-swizzle layout (a 128-wide K block is two 64-wide atoms), warps 6-9
-// promote and hold the int32 accumulators.  Split-K CTAs of one slab form a
+// MMAs, warps 2-9 (two groups, alternate K blocks) convert raw tiles to fp16
+// operand tiles in the UMMA K-major 128-byte-swizzle layout (a 128-wide K
+// block is two 64-wide atoms), warps 10-13 promote and hold the int32
+// accumulators.  Split-K CTAs of one slab form a
 // cluster and add their int32 partials through distributed shared memory.
 #include <cuda_fp16.h>
 
@@ -54,7 +55,7 @@ struct Int8Params {
 template <int MT>
 struct I8Cfg {
     static_assert(MT == 16 || MT == 32 || MT == 64, "token tile");
-    static constexpr int kThreads = 320;                       // 10 warps
+    static constexpr int kThreads = 448;                       // 14 warps
     static constexpr int kRawW = 128 * 128, kRawX = MT * 128;  // int8 tiles
     static constexpr int kRawStage = kRawW + kRawX;
     // raw int8 stages fill what the two fp16 stages leave of ~220 KB: the weight
@@ -210,10 +211,13 @@ gemm_int8_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
                 if (last) tc_commit(tfull0 + 8 * buf);
             }
         }
-    } else if (warp < 6) {
-        // ---------------- converters: raw int8 -> fp16 operand tiles
-        const int t = (warp - 2) * 32 + lane;        // 0..127
-        for (int it = 0; it < nkb; ++it) {
+    } else if (warp < 10) {
+        // ---------------- converters: raw int8 -> fp16 operand tiles.  Two
+        // groups of four warps take alternate K blocks (each group always fills
+        // the same fp16 stage), so two blocks are converted concurrently.
+        const int grp = (warp - 2) >> 2;
+        const int t = ((warp - 2) & 3) * 32 + lane;  // 0..127
+        for (int it = grp; it < nkb; it += 2) {
             const int rs = it % R, cs = it % V;
             const uint32_t rph = (it / R) & 1, cph = (it / V) & 1;
             if (!mbar_wait_bounded(rfull0 + 8 * rs, rph, abort, kWaitLimitNs) ||
