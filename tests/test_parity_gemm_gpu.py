@@ -30,7 +30,8 @@ def _fp8_case(M, N, K, seed_w, seed_x, rows=None, what=""):
 
 @pytest.mark.parametrize("M,N,K", [(16, 512, 256), (1, 128, 128), (5, 256, 384), (37, 384, 640),
                                    (64, 256, 1024), (129, 128, 256), (256, 640, 512), (257, 384, 128),
-                                   (300, 384, 384), (1000, 768, 1280)])
+                                   (300, 384, 384), (1000, 768, 1280), (512, 256, 128), (700, 640, 384),
+                                   (1537, 1152, 640)])
 def test_fp8_gemm_small_full(cuda_lib, M, N, K):
     _fp8_case(M, N, K, 100 + N + K, 200 + M + K)
 
