@@ -296,8 +296,6 @@ cudaError_t launch_gemm_fp8(const uint8_t* Xq, const float* Xs, const uint8_t* W
             return launch_gemm_fp8_mma_sync(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
         }
     }
-    if (M >= 512 && prefill_pair_available())     // 256-row pair tiles are well filled
-        return launch_gemm_fp8_prefill_pair(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
     return launch_gemm_fp8_prefill(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
 }
 

@@ -88,10 +88,6 @@ bool make_tmap_bf16_store(CUtensorMap* m, const void* base, uint64_t rows, uint6
 int num_sms();
 bool decode_supported(int64_t K);
 double decode_cost_us(int64_t M, int64_t N, int64_t K);
-bool prefill_pair_available();
-cudaError_t launch_gemm_fp8_prefill_pair(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
-                                         const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
-                                         int64_t ldy, cudaStream_t st);
 cudaError_t launch_gemm_fp8_prefill(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
                                     const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
                                     int64_t ldy, cudaStream_t st);
