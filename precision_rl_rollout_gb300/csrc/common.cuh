@@ -158,4 +158,15 @@ __device__ __forceinline__ void pdl_wait_then_release() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// For short kernels whose successor reads inputs of its own first (the GEMM
+// after the activation quantizer streams its weights): let the next kernel be
+// scheduled at once, then wait for the previous one.  The successor still
+// waits for this kernel's completion before it reads what this kernel writes,
+// and this kernel completes only after its own wait, so the ordering of the
+// stream is kept.
+__device__ __forceinline__ void pdl_release_then_wait() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 }  // namespace fp8rl

@@ -61,6 +61,8 @@ struct DecodeCfg {
     // MT <= 64: two CTAs per SM (2 x (smem + 1 KB reserved) <= 228 KB); larger: one.
     static constexpr int kStages = MT == 16 ? 6 : MT == 32 ? 5 : MT == 64 ? 4 : 5;
     static constexpr int kMaxKbPerSplit = 32;                     // K blocks per split-K CTA
+    static constexpr int kMaxSplit = 8;                           // portable cluster size
+    static constexpr int kPrefetchKb = 8;                         // weight blocks sent to L2 early
     static constexpr int kScaleBytes = kMaxKbPerSplit * MT * 4;   // per-block scale products
     static constexpr int kTmemCols = 2 * MT < 32 ? 32 : 2 * MT;
     static constexpr int kMinBlocks = MT <= 64 ? 2 : 1;             // CTAs per SM the registers allow
@@ -105,6 +107,11 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
         fence_mbar_init();
         prefetch_tmap(&tmW);
         prefetch_tmap(&tmX);
+        // The first weight blocks of this slab start moving into L2 while the
+        // previous kernel of the stream finishes (the weights are read-only
+        // here; an L2 prefetch cannot return stale data).
+        const int npf = nkb < C::kPrefetchKb ? nkb : C::kPrefetchKb;
+        for (int it = 0; it < npf; ++it) tma_prefetch_l2_2d(&tmW, (kb0 + it) * 128, nt * 128);
     }
     if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
     tc_fence_before();
@@ -258,17 +265,26 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
             const int m = c >> 4, n8 = c & 15;
             const uint32_t off = (uint32_t)(m * 128 + n8 * 8) * 4u;
             float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int r = 0; r < p.split; ++r) {      // fixed order: deterministic
-                float4 v0, v1;
-                if (p.split > 1) {
-                    const uint32_t a = map_to_rank(red_addr + off, (uint32_t)r);
-                    v0 = ld_cluster_v4(a);
-                    v1 = ld_cluster_v4(a + 16);
-                } else {
-                    const float4* l = reinterpret_cast<const float4*>(smem + off);
-                    v0 = l[0];
-                    v1 = l[1];
-                }
+            if (p.split > 1) {
+                // every rank's loads are in flight before the first add: one
+                // distributed-shared-memory round trip per chunk, not one per rank
+                float4 v[C::kMaxSplit][2];
+#pragma unroll
+                for (int r = 0; r < C::kMaxSplit; ++r)
+                    if (r < p.split) {
+                        const uint32_t a = map_to_rank(red_addr + off, (uint32_t)r);
+                        v[r][0] = ld_cluster_v4(a);
+                        v[r][1] = ld_cluster_v4(a + 16);
+                    }
+#pragma unroll
+                for (int r = 0; r < C::kMaxSplit; ++r)   // fixed order: deterministic
+                    if (r < p.split) {
+                        s[0] += v[r][0].x; s[1] += v[r][0].y; s[2] += v[r][0].z; s[3] += v[r][0].w;
+                        s[4] += v[r][1].x; s[5] += v[r][1].y; s[6] += v[r][1].z; s[7] += v[r][1].w;
+                    }
+            } else {
+                const float4* l = reinterpret_cast<const float4*>(smem + off);
+                const float4 v0 = l[0], v1 = l[1];
                 s[0] += v0.x; s[1] += v0.y; s[2] += v0.z; s[3] += v0.w;
                 s[4] += v1.x; s[5] += v1.y; s[6] += v1.z; s[7] += v1.w;
             }
@@ -300,7 +316,7 @@ static int choose_split(int64_t tiles, int KB, int MT, int max_kb_per_split, dou
     const int per_sm = MT <= 64 ? 2 : 1;              // CTAs of this tile co-resident on one SM
     int best = 1;
     double best_cost = 1e30;
-    for (int s = 1; s <= 8 && s <= KB; ++s) {
+    for (int s = 1; s <= DecodeCfg<16>::kMaxSplit && s <= KB; ++s) {
         const int per = (KB + s - 1) / s;
         if (per > max_kb_per_split) continue;
         if ((int64_t)(s - 1) * per >= KB) continue;  // no empty split

@@ -117,7 +117,7 @@ cudaError_t launch_quant_weight_block(const WeightDesc* d, int n, cudaStream_t s
 __global__ void __launch_bounds__(256)
 quant_act_group_kernel(const uint16_t* __restrict__ X, int64_t M, int64_t K, int64_t ldx,
                        uint8_t* __restrict__ Xq, float* __restrict__ Xs) {
-    pdl_wait_then_release();
+    pdl_release_then_wait();
     const int t = threadIdx.x;
     const int lane16 = t & 15;
     const int64_t m = (int64_t)blockIdx.y * 16 + (t >> 4);

@@ -102,6 +102,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
         : "memory");
 }
 
+// Prefetch one 2-D tile of a tensor map into L2 (no shared memory, no
+// completion).  The L2 is the coherence point of device memory, so this is
+// safe even before the kernel's dependency wait: a later store by an earlier
+// kernel updates the cached line.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t c0, int32_t c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
+
 // 2-D tiled TMA store from this CTA's shared memory (bulk-group completion).
 // Elements of the box outside the tensor are not written.
 __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int32_t c0, int32_t c1) {
