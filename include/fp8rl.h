@@ -62,7 +62,7 @@ typedef enum {
     FP8RL_ERR_TIMEOUT = 7
 } fp8rl_status;
 
-#define FP8RL_ABI_VERSION 1
+#define FP8RL_ABI_VERSION 2
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* fp8rl_status_string(int status);
@@ -131,6 +131,31 @@ int fp8rl_gemm_w8a8_block(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
                           const float* Ws, int64_t M, int64_t N, int64_t K,
                           uint16_t* Y, int64_t ldy, void* workspace,
                           size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * The whole 8-bit linear layer from bf16 activations: the activation quant
+ * above followed by the block-scaled GEMM above, in one call (FP8-RL
+ * contribution (i): W8A8 rollout linear layers; the activation side is
+ * quantized on the fly, token by token).  The result is
+ *   Y = fp8rl_gemm_w8a8_block(Xq, Xs, Wq, Ws)  with  (Xq, Xs) = fp8rl_quant_act_group(X):
+ * the same codes and scales (bit-exact) and Y within the GEMM's tolerance.
+ * Two kernels run back to back on `stream`; the GEMM is scheduled while the
+ * quantizer runs and prefetches its first weight blocks meanwhile.
+ * X   bf16 [M][ldx], ldx >= K, ldx % 8 == 0, 16-byte aligned.
+ * Wq, Ws, Y, ldy as for fp8rl_gemm_w8a8_block.
+ * Xq_or_null, Xs_or_null: both NULL, or both given ([M][K] e4m3 contiguous,
+ *     16-byte aligned; [K/128][M] fp32, 4-byte aligned) to receive the
+ *     activation codes and scales; then no workspace is needed.
+ * workspace: otherwise at least fp8rl_linear_workspace_bytes(M, N, K) bytes
+ *     (the codes and scales), 16-byte aligned; no zeroing needed; calls in
+ *     flight at once need their own.
+ * Limit: M <= 1048560 (FP8RL_ERR_UNSUPPORTED above).
+ * ---------------------------------------------------------------------- */
+size_t fp8rl_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
+int fp8rl_linear_w8a8_block(const uint16_t* X, int64_t ldx, const uint8_t* Wq, const float* Ws,
+                            int64_t M, int64_t N, int64_t K, uint16_t* Y, int64_t ldy,
+                            uint8_t* Xq_or_null, float* Xs_or_null, void* workspace,
+                            size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
  * INT8 per-row quant (FlashRL write-up, Fig. 1: INT8 rollout).  Per row r:

@@ -27,6 +27,7 @@ STATUS = {0: "FP8RL_OK", 1: "FP8RL_ERR_NULL", 2: "FP8RL_ERR_SHAPE", 3: "FP8RL_ER
 EXPORTS = ("fp8rl_status_string", "fp8rl_abi_version", "fp8rl_quant_weight_block",
            "fp8rl_quant_weight_block_grouped", "fp8rl_quant_act_group",
            "fp8rl_gemm_workspace_bytes", "fp8rl_gemm_w8a8_block",
+           "fp8rl_linear_workspace_bytes", "fp8rl_linear_w8a8_block",
            "int8rl_quant_weight_channel", "int8rl_quant_act_token",
            "int8rl_gemm_workspace_bytes", "int8rl_gemm_w8a8", "fp8rl_check_device_error",
            "fp8rl_kv_workspace_bytes", "fp8rl_quant_kv_tensor", "fp8rl_quant_kv_with_scale",
@@ -76,6 +77,9 @@ def load(path: str | None = None):
         lib.fp8rl_gemm_workspace_bytes.restype = Z
         lib.fp8rl_gemm_workspace_bytes.argtypes = [I, I, I]
         lib.fp8rl_gemm_w8a8_block.argtypes = [P, P, P, P, I, I, I, P, I, P, Z, S]
+        lib.fp8rl_linear_workspace_bytes.restype = Z
+        lib.fp8rl_linear_workspace_bytes.argtypes = [I, I, I]
+        lib.fp8rl_linear_w8a8_block.argtypes = [P, I, P, P, I, I, I, P, I, P, P, P, Z, S]
         lib.int8rl_quant_weight_channel.argtypes = [P, I, I, I, P, P, S]
         lib.int8rl_quant_act_token.argtypes = [P, I, I, I, P, P, S]
         lib.int8rl_gemm_workspace_bytes.restype = Z
@@ -93,7 +97,7 @@ def load(path: str | None = None):
         for name in EXPORTS:
             if name not in ("fp8rl_status_string", "fp8rl_abi_version", "fp8rl_gemm_workspace_bytes",
                             "int8rl_gemm_workspace_bytes", "fp8rl_kv_workspace_bytes",
-                            "fp8rl_rollout_is_workspace_bytes"):
+                            "fp8rl_rollout_is_workspace_bytes", "fp8rl_linear_workspace_bytes"):
                 getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -198,6 +202,32 @@ def fp8rl_gemm_w8a8_block(Xq, Xs, Wq, Ws, Y=None, workspace=None, stream=None):
                                   _p(workspace), wbytes, _stream(Wq, stream)),
         "fp8rl_gemm_w8a8_block")
     return Y
+
+
+def fp8rl_linear_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load().fp8rl_linear_workspace_bytes(M, N, K))
+
+
+def fp8rl_linear_w8a8_block(X, Wq, Ws, Y=None, Xq=None, Xs=None, want_codes=False, workspace=None,
+                            stream=None):
+    """X bf16 [M,K] -> Y bf16 [M,N] (and (Xq, Xs) when want_codes or Xq/Xs are given)."""
+    lib = load()
+    ldx = _rowmajor(X, "X")
+    M, K = X.shape
+    N = Wq.shape[0]
+    Y = Y if Y is not None else torch.empty((M, N), dtype=torch.bfloat16, device=Wq.device)
+    ldy = _rowmajor(Y, "Y") if M > 0 else N
+    if want_codes or Xq is not None or Xs is not None:
+        Xq = _need(Xq, (M, K), torch.uint8, X.device, "Xq")
+        Xs = _need(Xs, (K // 128, M), torch.float32, X.device, "Xs")
+    need = lib.fp8rl_linear_workspace_bytes(M, N, K)
+    if workspace is None and need and Xq is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=Wq.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _ck(lib.fp8rl_linear_w8a8_block(_p(X), ldx, _p(Wq), _p(Ws), M, N, K, _p(Y), ldy, _p(Xq), _p(Xs),
+                                    _p(workspace), wbytes, _stream(Wq, stream)),
+        "fp8rl_linear_w8a8_block")
+    return (Y, Xq, Xs) if Xq is not None else Y
 
 
 def int8rl_quant_weight_channel(W, Wq=None, Ws=None, stream=None):

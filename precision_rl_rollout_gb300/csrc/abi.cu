@@ -111,6 +111,30 @@ int fp8rl_gemm_w8a8_block(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
                                        workspace_bytes, as_stream(stream)));
 }
 
+size_t fp8rl_linear_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    return linear_workspace_bytes(M, N, K);
+}
+
+int fp8rl_linear_w8a8_block(const uint16_t* X, int64_t ldx, const uint8_t* Wq, const float* Ws,
+                            int64_t M, int64_t N, int64_t K, uint16_t* Y, int64_t ldy,
+                            uint8_t* Xq_or_null, float* Xs_or_null, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+    int rc = check_bf16_src(X, M, K, ldx, true);
+    if (rc) return rc;
+    if (N <= 0 || N % kBlk || ldy < N) return FP8RL_ERR_SHAPE;
+    if (!Wq || !Ws || (M > 0 && !Y)) return FP8RL_ERR_NULL;
+    if ((Xq_or_null == nullptr) != (Xs_or_null == nullptr)) return FP8RL_ERR_NULL;
+    if (!aligned16(Wq) || !aligned16(Y) || !aligned4(Ws) || (ldy * 2) % 16) return FP8RL_ERR_ALIGN;
+    if (!aligned16(Xq_or_null) || !aligned4(Xs_or_null) || !aligned16(workspace)) return FP8RL_ERR_ALIGN;
+    if (M > 65535LL * 16) return FP8RL_ERR_UNSUPPORTED;
+    const size_t need = fp8rl_linear_workspace_bytes(M, N, K);
+    if (!Xq_or_null && (workspace_bytes < need || (need && !workspace))) return FP8RL_ERR_WORKSPACE;
+    if (M == 0) return FP8RL_OK;
+    return cuda_status(launch_linear_fp8(X, ldx, Wq, Ws, M, N, K, Y, ldy, Xq_or_null, Xs_or_null,
+                                         workspace, as_stream(stream)));
+}
+
 int int8rl_quant_weight_channel(const uint16_t* W, int64_t N, int64_t K, int64_t ldw, int8_t* Wq,
                                 float* Ws, void* stream) {
     int rc = check_bf16_src(W, N, K, ldw, true);

@@ -211,8 +211,9 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
         for (int it = 0; it < nkb; ++it) {
             const int buf = it & 1;
             const uint32_t bph = (it >> 1) & 1;
-            if (!mbar_wait_bounded(tfull0 + 8 * buf, bph, abort, kWaitLimitNs)) {
-                record_timeout(p.err, kKernelDecode, 4, abort);
+            // the verdict is made warp-uniform: the TMEM loads below are warp-collective
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(tfull0 + 8 * buf, bph, abort, kWaitLimitNs))) {
+                if (lane == 0) record_timeout(p.err, kKernelDecode, 4, abort);
                 break;
             }
             tc_fence_after();
@@ -365,11 +366,15 @@ static cudaError_t launch_decode_mt(const uint8_t* Xq, const float* Xs, const ui
     DecodeParams prm{err, Xs, Ws, Y, M, ldy, KB, per, split};
 
     auto kern = gemm_fp8_decode_kernel<MT>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    static bool attr_set[64] = {};     // the attribute belongs to the current device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        attr_set[dev] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)split, (unsigned)mtiles, (unsigned)(N / 128));
@@ -397,6 +402,29 @@ cudaError_t launch_gemm_fp8_decode(const uint8_t* Xq, const float* Xs, const uin
     if (M <= 32) return launch_decode_mt<32>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
     if (M <= 64) return launch_decode_mt<64>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
     return launch_decode_mt<128>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
+}
+
+// ------------------------------------------------------------------ linear layer
+
+size_t linear_codes_bytes(int64_t M, int64_t K) { return ((size_t)M * (size_t)K + 255) & ~(size_t)255; }
+
+size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    (void)N;
+    if (M <= 0) return 0;
+    return linear_codes_bytes(M, K) + (size_t)M * (size_t)(K / 128) * 4;
+}
+
+// The activation quantizer releases its dependent at launch, so the GEMM's
+// CTAs are resident and have started pulling their first weight blocks into L2
+// while the activations are quantized; the GEMM then reads the codes from L2.
+cudaError_t launch_linear_fp8(const uint16_t* X, int64_t ldx, const uint8_t* Wq, const float* Ws, int64_t M,
+                              int64_t N, int64_t K, uint16_t* Y, int64_t ldy, uint8_t* Xq_out,
+                              float* Xs_out, void* ws, cudaStream_t st) {
+    uint8_t* Xq = Xq_out ? Xq_out : static_cast<uint8_t*>(ws);
+    float* Xs = Xs_out ? Xs_out : reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + linear_codes_bytes(M, K));
+    cudaError_t e = launch_quant_act_group(X, M, K, ldx, Xq, Xs, st);
+    if (e != cudaSuccess) return e;
+    return launch_gemm_fp8(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, nullptr, 0, st);
 }
 
 }  // namespace fp8rl

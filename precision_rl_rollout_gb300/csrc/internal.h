@@ -72,6 +72,13 @@ cudaError_t launch_gemm_int8(const int8_t* Xq, const float* Xs, const int8_t* Wq
                              int64_t ldy, int32_t* acc, void* ws, size_t ws_bytes,
                              cudaStream_t st);
 
+// The linear layer from bf16 activations: the activation quantizer, then the GEMM.
+size_t linear_codes_bytes(int64_t M, int64_t K);
+size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_linear_fp8(const uint16_t* X, int64_t ldx, const uint8_t* Wq, const float* Ws, int64_t M,
+                              int64_t N, int64_t K, uint16_t* Y, int64_t ldy, uint8_t* Xq_out,
+                              float* Xs_out, void* ws, cudaStream_t st);
+
 // Device-side record of a bounded wait that ran out (0 = none).
 cudaError_t read_and_clear_device_error(uint32_t* word);
 // Address of that word on the current device (passed to kernels that wait).

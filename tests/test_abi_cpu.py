@@ -37,7 +37,8 @@ def test_header_declares_the_binding_exports():
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared_functions():
         assert hasattr(lib, name), name
-    assert lib.fp8rl_abi_version() == 1
+    version = int(re.search(r"#define FP8RL_ABI_VERSION (\d+)", open(HEADER).read()).group(1))
+    assert lib.fp8rl_abi_version() == version
     for s in range(8):
         assert lib.fp8rl_status_string(s).decode().startswith(binding.STATUS[s])
 
@@ -74,6 +75,30 @@ def test_act_quant_validation(lib):
     assert q(A, 4, 128, 128, None, A, None) == 1
     assert q(A, 4, 128, 128, A, A + 2, None) == 3
     assert q(A, 0, 128, 128, A, A, None) == 0
+
+
+def test_linear_validation(lib):
+    f = lib.fp8rl_linear_w8a8_block
+    #      X  ldx  Wq Ws  M   N    K   Y  ldy  Xq  Xs  ws   bytes
+    assert f(A, 128, A, A, 8, 128, 256, A, 128, None, None, None, 0, None) == 2  # ldx < K
+    assert f(A, 256, A, A, 8, 100, 256, A, 128, None, None, None, 0, None) == 2  # N % 128
+    assert f(A, 256, A, A, 8, 128, 200, A, 128, None, None, None, 0, None) == 2  # K % 128
+    assert f(A, 256, A, A, 8, 256, 256, A, 128, None, None, None, 0, None) == 2  # ldy < N
+    assert f(None, 256, A, A, 8, 128, 256, A, 128, None, None, None, 0, None) == 1
+    assert f(A, 256, None, A, 8, 128, 256, A, 128, None, None, None, 0, None) == 1
+    assert f(A, 256, A, A, 8, 128, 256, None, 128, None, None, None, 0, None) == 1
+    assert f(A, 256, A, A, 8, 128, 256, A, 128, A, None, None, 0, None) == 1    # Xq without Xs
+    assert f(A + 2, 256, A, A, 8, 128, 256, A, 128, None, None, None, 0, None) == 3
+    assert f(A, 260, A, A, 8, 128, 256, A, 128, None, None, None, 0, None) == 3  # row pitch 520 B
+    assert f(A, 256, A, A, 8, 128, 256, A, 128, A + 8, A, None, 0, None) == 3
+    assert f(A, 256, A, A, 2 ** 21, 128, 256, A, 128, A, A, None, 0, None) == 6  # above the M limit
+    assert f(A, 256, A, A, 0, 128, 256, A, 128, None, None, None, 0, None) == 0  # empty batch
+    # the workspace holds the codes and scales unless the caller passes Xq and Xs
+    assert lib.fp8rl_linear_workspace_bytes(0, 128, 256) == 0
+    need = lib.fp8rl_linear_workspace_bytes(65, 128, 256)
+    assert need >= 65 * 256 + 65 * 2 * 4
+    assert f(A, 256, A, A, 65, 128, 256, A, 128, None, None, A, need - 1, None) == 4
+    assert f(A, 256, A, A, 65, 128, 256, A, 128, None, None, None, 0, None) == 4
 
 
 def test_gemm_validation(lib):
