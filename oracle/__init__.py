@@ -207,6 +207,27 @@ def fp8_gemm(Xq, Xs, Wq, Ws) -> np.ndarray:
     return Y
 
 
+def fp8_gemm_grouped(Xq, Xs, Wq, Ws, offsets) -> np.ndarray:
+    """Grouped (mixture-of-experts) block-scaled FP8 GEMM (FP8-RL, Abstract: the
+    FP8 rollout stack serves dense and MoE models).  The T token rows of Xq are
+    grouped by expert: rows offsets[e] .. offsets[e+1]-1 go through expert e's
+    weights Wq[e] [N,K] with scales Ws[e] [N/128, K/128], which is the dense GEMM
+    above applied to each group.  Xs is [K/128, T].  Returns Y float64 [T, N]."""
+    Wq = np.ascontiguousarray(Wq, np.uint8)
+    Ws = np.ascontiguousarray(Ws, np.float32)
+    E, N, K = Wq.shape
+    T = Xq.shape[0]
+    off = np.asarray(offsets, np.int64)
+    assert off.shape == (E + 1,) and off[0] == 0 and off[-1] == T and np.all(np.diff(off) >= 0)
+    assert Ws.shape == (E, N // 128, K // 128)
+    Y = np.zeros((T, N), np.float64)
+    for e in range(E):
+        a, b = int(off[e]), int(off[e + 1])
+        if b > a:
+            Y[a:b] = fp8_gemm(Xq[a:b], Xs[:, a:b], Wq[e], Ws[e])
+    return Y
+
+
 def bf16_matmul_f64(X: np.ndarray, W: np.ndarray) -> np.ndarray:
     X = _bits16(X)
     W = _bits16(W)

@@ -379,6 +379,45 @@ def test_fp8_gemm_within_quantization_bound_of_unquantized_matmul():
     assert np.abs(Y - Ytrue).max() < 0.2 * np.abs(Ytrue).max()
 
 
+def _e4m3_code(v: float) -> int:
+    return int(torch.tensor([v]).to(torch.float8_e4m3fn).view(torch.uint8)[0])
+
+
+def test_fp8_gemm_grouped_routes_each_token_to_its_expert():
+    # Expert e's weights are all the E4M3 value (e+1) with scale 2^-kb on K block
+    # kb; activations are small integers with unit scales.  So for a token t of
+    # expert e, y[t, n] = (e+1) * sum_kb 2^-kb * sum_{k in kb} x[t, k] for every n:
+    # a token sent to the wrong expert, a wrong expert's scale row or a shifted
+    # token range changes the multiplier.
+    E, N, K = 4, 256, 384
+    KB = K // 128
+    rng = np.random.default_rng(5)
+    offsets = np.array([0, 3, 3, 8, 9])                     # expert 1 has no tokens
+    T = offsets[-1]
+    xv = rng.integers(-3, 4, size=(T, K)).astype(np.float64)
+    Xq = np.array([[_e4m3_code(v) for v in row] for row in xv], np.uint8)
+    Xs = np.ones((KB, T), np.float32)
+    Wq = np.stack([np.full((N, K), _e4m3_code(e + 1.0), np.uint8) for e in range(E)])
+    Ws = np.stack([np.tile((2.0 ** -np.arange(KB)).astype(np.float32), (N // 128, 1)) for _ in range(E)])
+    Y = oracle.fp8_gemm_grouped(Xq, Xs, Wq, Ws, offsets)
+    blk = (xv.reshape(T, KB, 128).sum(axis=2) * 2.0 ** -np.arange(KB)).sum(axis=1)
+    expert_of = np.repeat(np.arange(E), np.diff(offsets))
+    want = ((expert_of + 1) * blk)[:, None] * np.ones((1, N))
+    assert np.array_equal(Y, want)
+
+
+def test_fp8_gemm_grouped_all_tokens_in_one_expert_is_the_dense_gemm_of_that_expert():
+    # closed form again: one expert holds every token; the others (empty) must not
+    # contribute, and the result is the single-term dequantized product
+    E, N, K, T = 3, 128, 256, 5
+    Xq = np.full((T, K), _e4m3_code(2.0), np.uint8)
+    Xs = np.full((K // 128, T), 0.5, np.float32)
+    Wq = np.stack([np.full((N, K), _e4m3_code(v), np.uint8) for v in (1.0, 3.0, 5.0)])
+    Ws = np.full((E, N // 128, K // 128), 0.25, np.float32)
+    Y = oracle.fp8_gemm_grouped(Xq, Xs, Wq, Ws, [0, 0, T, T])
+    assert np.array_equal(Y, np.full((T, N), K * (2.0 * 0.5) * (3.0 * 0.25)))
+
+
 def test_bf16_matmul_f64_matches_library():
     g = torch.Generator().manual_seed(9)
     X = torch.randn(4, 256, generator=g).to(torch.bfloat16)
