@@ -409,6 +409,34 @@ def extras(fb, dev, reps=5):
         del Wq, Ws, Wqs, Wss
     out["decode_fp8_gemm_32b"] = dec
 
+    # Grouped MoE GEMM: 64 decode tokens routed top-8 over 128 experts of a
+    # hidden-2048 / expert-FFN-768 MoE layer (gate_up N=1536 K=2048, down
+    # N=2048 K=768); bytes = the active experts' weights + scales + X + Y
+    moe = {}
+    E, topk = 128, 8
+    rng = torch.Generator().manual_seed(synth.seed_for(8, 0))
+    picks = torch.stack([torch.randperm(E, generator=rng)[:topk] for _ in range(DECODE_M)])
+    counts = torch.bincount(picks.flatten(), minlength=E)
+    offs = torch.cat([torch.zeros(1, dtype=torch.int64), counts.cumsum(0)]).to(torch.int32).to(dev)
+    T, active, bound = int(counts.sum()), int((counts > 0).sum()), int(counts.max())
+    for name, N, K in (("gate_up", 1536, 2048), ("down", 2048, 768)):
+        W = synth.weight_bf16_direct(E * N, K, synth.seed_for(8, 1), device=dev)
+        Wq, Ws = fb.fp8rl_quant_weight_block(W)          # stacked experts: per-expert blocks
+        del W
+        nc = _copies_for(active * N * K)
+        Wqs = [Wq.view(E, N, K)] + [Wq.view(E, N, K).clone() for _ in range(nc - 1)]
+        Wss = [Ws.view(E, N // 128, K // 128)] + [Ws.view(E, N // 128, K // 128).clone() for _ in range(nc - 1)]
+        X = synth.activation(T, K, synth.seed_for(8, 2), device=dev)
+        Xq, Xs = fb.fp8rl_quant_act_group(X)
+        Y = torch.empty(T, N, dtype=torch.bfloat16, device=dev)
+        ms = _time_graph([lambda c=c: fb.fp8rl_gemm_w8a8_block_grouped(Xq, Xs, Wqs[c], Wss[c], offs, bound, Y=Y)
+                          for c in range(nc)])
+        nbytes = active * (N * K + 4 * (N // 128) * (K // 128)) + T * K + 4 * T * (K // 128) + 2 * T * N
+        moe[name] = {"us": ms * 1e3, "gbs": nbytes / (ms * 1e-3) / 1e9, "experts": E, "experts_active": active,
+                     "routed_rows": T, "max_rows_per_expert": bound, "weight_copies": nc}
+        del Wq, Ws, Wqs, Wss, X, Xq, Xs, Y
+    out["moe_fp8_grouped_decode"] = moe
+
     # A1 at full-model scale: 64 layers x 4 shapes, grouped launches (62 GB in)
     items = []
     for layer in range(synth.QWEN25_32B_LAYERS):

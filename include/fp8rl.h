@@ -59,7 +59,8 @@ typedef enum {
     FP8RL_ERR_WORKSPACE = 4,
     FP8RL_ERR_CUDA = 5,
     FP8RL_ERR_UNSUPPORTED = 6,
-    FP8RL_ERR_TIMEOUT = 7
+    FP8RL_ERR_TIMEOUT = 7,
+    FP8RL_ERR_DEVICE = 8
 } fp8rl_status;
 
 #define FP8RL_ABI_VERSION 2
@@ -131,6 +132,31 @@ int fp8rl_gemm_w8a8_block(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
                           const float* Ws, int64_t M, int64_t N, int64_t K,
                           uint16_t* Y, int64_t ldy, void* workspace,
                           size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Grouped block-scaled FP8 GEMM for mixture-of-experts layers (FP8-RL,
+ * Abstract: the FP8 rollout stack serves dense and MoE models).  The T token
+ * rows are grouped by expert: rows expert_offsets[e] .. expert_offsets[e+1]-1
+ * of Xq go through expert e's weights, and for those rows
+ *   Y = fp8rl_gemm_w8a8_block(Xq[rows], Xs[:, rows], Wq[e], Ws[e])
+ * (same arithmetic and tolerance).  Experts without tokens read none of their
+ * weights.  Built on the decode kernel: meant for decode-sized groups.
+ * Xq [T][K] e4m3, Xs [K/128][T] fp32, Y bf16 [T][ldy] (ldy >= N, ldy % 8 == 0).
+ * Wq  e4m3 [E][N][K] (experts stacked), Ws fp32 [E][N/128][K/128].
+ * expert_offsets: DEVICE int32 [E+1], non-decreasing, [0] = 0, [E] = T (the
+ *     kernel clamps every range into [0, T], so bad offsets cannot make it
+ *     read or write outside the tensors).  It may be written by the previous
+ *     kernel in the stream (e.g. a router).
+ * max_tokens_per_expert: a host-side bound, 1 <= bound <= T, on every expert's
+ *     token count; the grid covers that many rows per expert.  Rows of an
+ *     expert beyond it are not computed and the device records it
+ *     (fp8rl_check_device_error returns FP8RL_ERR_DEVICE).
+ * Limits: K <= 32768 and E * N / 128 <= 65535 (FP8RL_ERR_UNSUPPORTED).
+ * ---------------------------------------------------------------------- */
+int fp8rl_gemm_w8a8_block_grouped(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
+                                  const float* Ws, const int32_t* expert_offsets, int64_t E,
+                                  int64_t T, int64_t N, int64_t K, int64_t max_tokens_per_expert,
+                                  uint16_t* Y, int64_t ldy, void* stream);
 
 /* ------------------------------------------------------------------------
  * The whole 8-bit linear layer from bf16 activations: the activation quant
@@ -269,9 +295,11 @@ int fp8rl_quant_kv_tensor_noalloc(const uint16_t* KV, int64_t R, int64_t C, int6
  * the tensor core) is bounded.  A wait that runs out records a code in a
  * device-side word, abandons the tile and lets the kernel exit, so the CUDA
  * context stays usable.  This call SYNCHRONIZES the current device, reads and
- * clears that word, and returns FP8RL_OK or FP8RL_ERR_TIMEOUT.  *detail (may
- * be NULL) receives the raw word (0 if none: kernel id in bits 24..31, the
- * wait site in bits 16..23).
+ * clears that word, and returns FP8RL_OK, FP8RL_ERR_TIMEOUT (a wait ran out)
+ * or FP8RL_ERR_DEVICE (a device-side check of the data failed: an expert of
+ * the grouped GEMM with more tokens than max_tokens_per_expert).  *detail
+ * (may be NULL) receives the raw word (0 if none: kernel id in bits 24..31,
+ * the site in bits 16..23, 1 = timeout / 2 = data check in bits 0..15).
  * ---------------------------------------------------------------------- */
 int fp8rl_check_device_error(uint32_t* detail);
 

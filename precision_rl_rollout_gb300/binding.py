@@ -21,12 +21,12 @@ from . import build as _build
 
 STATUS = {0: "FP8RL_OK", 1: "FP8RL_ERR_NULL", 2: "FP8RL_ERR_SHAPE", 3: "FP8RL_ERR_ALIGN",
           4: "FP8RL_ERR_WORKSPACE", 5: "FP8RL_ERR_CUDA", 6: "FP8RL_ERR_UNSUPPORTED",
-          7: "FP8RL_ERR_TIMEOUT"}
+          7: "FP8RL_ERR_TIMEOUT", 8: "FP8RL_ERR_DEVICE"}
 
 # Every symbol the header declares (the CPU test checks the library exports them).
 EXPORTS = ("fp8rl_status_string", "fp8rl_abi_version", "fp8rl_quant_weight_block",
            "fp8rl_quant_weight_block_grouped", "fp8rl_quant_act_group",
-           "fp8rl_gemm_workspace_bytes", "fp8rl_gemm_w8a8_block",
+           "fp8rl_gemm_workspace_bytes", "fp8rl_gemm_w8a8_block", "fp8rl_gemm_w8a8_block_grouped",
            "fp8rl_linear_workspace_bytes", "fp8rl_linear_w8a8_block",
            "int8rl_quant_weight_channel", "int8rl_quant_act_token",
            "int8rl_gemm_workspace_bytes", "int8rl_gemm_w8a8", "fp8rl_check_device_error",
@@ -77,6 +77,7 @@ def load(path: str | None = None):
         lib.fp8rl_gemm_workspace_bytes.restype = Z
         lib.fp8rl_gemm_workspace_bytes.argtypes = [I, I, I]
         lib.fp8rl_gemm_w8a8_block.argtypes = [P, P, P, P, I, I, I, P, I, P, Z, S]
+        lib.fp8rl_gemm_w8a8_block_grouped.argtypes = [P, P, P, P, P, I, I, I, I, I, P, I, S]
         lib.fp8rl_linear_workspace_bytes.restype = Z
         lib.fp8rl_linear_workspace_bytes.argtypes = [I, I, I]
         lib.fp8rl_linear_w8a8_block.argtypes = [P, I, P, P, I, I, I, P, I, P, P, P, Z, S]
@@ -201,6 +202,26 @@ def fp8rl_gemm_w8a8_block(Xq, Xs, Wq, Ws, Y=None, workspace=None, stream=None):
     _ck(lib.fp8rl_gemm_w8a8_block(_p(Xq), _p(Xs), _p(Wq), _p(Ws), M, N, K, _p(Y), ldy,
                                   _p(workspace), wbytes, _stream(Wq, stream)),
         "fp8rl_gemm_w8a8_block")
+    return Y
+
+
+def fp8rl_gemm_w8a8_block_grouped(Xq, Xs, Wq, Ws, expert_offsets, max_tokens_per_expert=None, Y=None,
+                                  stream=None):
+    """Mixture-of-experts GEMM.  Xq [T,K] (rows grouped by expert), Xs [K/128,T],
+    Wq [E,N,K], Ws [E,N/128,K/128], expert_offsets int32 [E+1] on the device.
+    max_tokens_per_expert: host-side bound on any expert's token count (T if None).
+    -> Y bf16 [T,N]."""
+    lib = load()
+    T, K = Xq.shape
+    E, N = Wq.shape[0], Wq.shape[1]
+    if expert_offsets.dtype != torch.int32 or not expert_offsets.is_cuda or expert_offsets.numel() != E + 1:
+        raise ValueError("expert_offsets must be a CUDA int32 tensor of E+1 entries")
+    Y = Y if Y is not None else torch.empty((T, N), dtype=torch.bfloat16, device=Wq.device)
+    ldy = _rowmajor(Y, "Y") if T > 0 else N
+    bound = T if max_tokens_per_expert is None else int(max_tokens_per_expert)
+    _ck(lib.fp8rl_gemm_w8a8_block_grouped(_p(Xq), _p(Xs), _p(Wq), _p(Ws), _p(expert_offsets), E, T, N, K,
+                                          bound, _p(Y), ldy, _stream(Wq, stream)),
+        "fp8rl_gemm_w8a8_block_grouped")
     return Y
 
 
@@ -356,6 +377,6 @@ def fp8rl_check_device_error() -> int:
     lib = load()
     w = ctypes.c_uint32(0)
     rc = lib.fp8rl_check_device_error(ctypes.byref(w))
-    if rc not in (0, 7):
+    if rc not in (0, 7, 8):
         raise Fp8rlError(rc, "fp8rl_check_device_error")
     return int(w.value)

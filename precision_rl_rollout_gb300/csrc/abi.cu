@@ -59,6 +59,7 @@ const char* fp8rl_status_string(int status) {
         case FP8RL_ERR_CUDA: return "FP8RL_ERR_CUDA: CUDA runtime reported an error";
         case FP8RL_ERR_UNSUPPORTED: return "FP8RL_ERR_UNSUPPORTED: size above a documented limit";
         case FP8RL_ERR_TIMEOUT: return "FP8RL_ERR_TIMEOUT: a bounded device-side wait ran out";
+        case FP8RL_ERR_DEVICE: return "FP8RL_ERR_DEVICE: a device-side check of the data failed";
         default: return "FP8RL_ERR_UNKNOWN";
     }
 }
@@ -109,6 +110,22 @@ int fp8rl_gemm_w8a8_block(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
     if (M == 0) return FP8RL_OK;
     return cuda_status(launch_gemm_fp8(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, workspace,
                                        workspace_bytes, as_stream(stream)));
+}
+
+int fp8rl_gemm_w8a8_block_grouped(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
+                                  const float* Ws, const int32_t* expert_offsets, int64_t E,
+                                  int64_t T, int64_t N, int64_t K, int64_t max_tokens_per_expert,
+                                  uint16_t* Y, int64_t ldy, void* stream) {
+    if (E < 1 || T < 0) return FP8RL_ERR_SHAPE;
+    int rc = check_gemm_common(Xq, Xs, Wq, Ws, T, N, K, Y, ldy);
+    if (rc) return rc;
+    if (!expert_offsets) return FP8RL_ERR_NULL;
+    if (!aligned4(expert_offsets)) return FP8RL_ERR_ALIGN;
+    if (T > 0 && (max_tokens_per_expert < 1 || max_tokens_per_expert > T)) return FP8RL_ERR_SHAPE;
+    if (!decode_supported(K) || E * (N / kBlk) > 65535 || T > 0x7FFFFFFFLL) return FP8RL_ERR_UNSUPPORTED;
+    if (T == 0) return FP8RL_OK;
+    return cuda_status(launch_gemm_fp8_grouped(Xq, Xs, Wq, Ws, expert_offsets, E, T, N, K,
+                                               max_tokens_per_expert, Y, ldy, as_stream(stream)));
 }
 
 size_t fp8rl_linear_workspace_bytes(int64_t M, int64_t N, int64_t K) {
@@ -236,7 +253,8 @@ int fp8rl_check_device_error(uint32_t* detail) {
     cudaError_t e = read_and_clear_device_error(&w);
     if (detail) *detail = w;
     if (e != cudaSuccess) return FP8RL_ERR_CUDA;
-    return w ? FP8RL_ERR_TIMEOUT : FP8RL_OK;
+    if (!w) return FP8RL_OK;
+    return (w & 0xFFFFu) == 2u ? FP8RL_ERR_DEVICE : FP8RL_ERR_TIMEOUT;
 }
 
 }  // extern "C"

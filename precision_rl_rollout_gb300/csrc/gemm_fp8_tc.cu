@@ -19,6 +19,13 @@
 // Split-K CTAs of one slab form a thread-block cluster and add their fp32
 // partials through distributed shared memory in a fixed order
 // (deterministic; no global workspace).
+//
+// Grouped form (mixture-of-experts layers; FP8-RL, Abstract: dense and MoE
+// models): the weights of E experts are stacked as [E*N][K] and the token rows
+// are grouped by expert, expert e owning rows offsets[e] .. offsets[e+1]-1.
+// Grid z runs over (expert, 128-row slab); each CTA reads its expert's token
+// range after the dependency wait (the router may have just written it), and
+// a CTA whose token tile is empty streams nothing.
 #include <algorithm>
 
 #include "common.cuh"
@@ -49,6 +56,10 @@ struct DecodeParams {
     int KB;            // K / 128
     int kb_per_split;  // K blocks per split-K CTA
     int split;         // CTAs per cluster (split-K factor)
+    // grouped form only (offs == nullptr: one dense GEMM; M is then the token count)
+    const int32_t* offs;   // [E+1] first token row of each expert, device memory
+    int ntiles;            // 128-row weight slabs per expert (N / 128)
+    int64_t tok_bound;     // token rows per expert the grid covers (M tiles * MT)
 };
 
 template <int MT>
@@ -90,7 +101,9 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
 
     const uint32_t warp = warp_id(), lane = lane_id();
     const int split_idx = blockIdx.x;                  // rank within the cluster
-    const int mt = blockIdx.y, nt = blockIdx.z;       // M tiles of one slab are adjacent
+    const int mt = blockIdx.y;                        // M tiles of one slab are adjacent
+    const int z = blockIdx.z;                         // weight slab: rows 128 z .. of [E*N][K]
+    const int nt = p.offs ? z % p.ntiles : z;         // output column block
     const int kb0 = split_idx * p.kb_per_split;
     const int nkb = min(p.KB, kb0 + p.kb_per_split) - kb0;   // >= 1 by construction
 
@@ -110,8 +123,9 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
         // The first weight blocks of this slab start moving into L2 while the
         // previous kernel of the stream finishes (the weights are read-only
         // here; an L2 prefetch cannot return stale data).
-        const int npf = nkb < C::kPrefetchKb ? nkb : C::kPrefetchKb;
-        for (int it = 0; it < npf; ++it) tma_prefetch_l2_2d(&tmW, (kb0 + it) * 128, nt * 128);
+        // (grouped form: not before the expert is known to have tokens here)
+        const int npf = p.offs ? 0 : (nkb < C::kPrefetchKb ? nkb : C::kPrefetchKb);
+        for (int it = 0; it < npf; ++it) tma_prefetch_l2_2d(&tmW, (kb0 + it) * 128, z * 128);
     }
     if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
     tc_fence_before();
@@ -124,12 +138,27 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
     grid_dependency_wait();
     grid_launch_dependents();
 
+    // this CTA's token rows: row0 .. row0 + rows - 1 (rows <= 0: nothing to do;
+    // the decision is the same for every CTA of a cluster)
+    int64_t row0 = (int64_t)mt * MT, rows = p.M - row0;
+    if (p.offs) {
+        const int e = z / p.ntiles;
+        int64_t b = p.offs[e], en = p.offs[e + 1];
+        b = b < 0 ? 0 : (b > p.M ? p.M : b);
+        en = en < b ? b : (en > p.M ? p.M : en);
+        row0 = b + (int64_t)mt * MT;
+        rows = en - row0;
+        if (mt == 0 && split_idx == 0 && nt == 0 && threadIdx.x == 0 && en - b > p.tok_bound)
+            atomicCAS(p.err, 0u, (kKernelDecode << 24) | (7u << 16) | 2u);   // tokens beyond the bound
+    }
+    const int nrun = rows > 0 ? nkb : 0;
+
     if (warp == 0) {
         // ---------------- TMA producer
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
             int it = 0;
-            for (; it < nkb; ++it) {
+            for (; it < nrun; ++it) {
                 const int s = it % C::kStages;
                 const uint32_t ph = (it / C::kStages) & 1;
                 if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1, abort, kWaitLimitNs)) {
@@ -138,8 +167,8 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
                 }
                 uint8_t* st = smem + s * C::kStageBytes;
                 mbar_arrive_expect_tx(full0 + 8 * s, C::kStageBytes);
-                tma_load_2d(smem_u32(st), &tmW, full0 + 8 * s, (kb0 + it) * 128, nt * 128, pol_w);
-                tma_load_2d(smem_u32(st + 16384), &tmX, full0 + 8 * s, (kb0 + it) * 128, mt * MT, pol_x);
+                tma_load_2d(smem_u32(st), &tmW, full0 + 8 * s, (kb0 + it) * 128, z * 128, pol_w);
+                tma_load_2d(smem_u32(st + 16384), &tmX, full0 + 8 * s, (kb0 + it) * 128, (int32_t)row0, pol_x);
             }
             if (*abort) {   // let copies already in flight land before the CTA can exit
                 for (int j = max(0, it - C::kStages); j < it; ++j)
@@ -150,7 +179,7 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
         // ---------------- MMA issuer (one thread)
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_e4m3_f32(128, MT);
-            for (int it = 0; it < nkb; ++it) {
+            for (int it = 0; it < nrun; ++it) {
                 const int s = it % C::kStages;
                 const uint32_t ph = (it / C::kStages) & 1;
                 const int buf = it & 1;
@@ -182,13 +211,13 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
         const int colbase = (e >> 2) * C::kCols;         // token columns of this thread
         const int n_local = 32 * q + lane;               // weight row within the slab
         const int et = e * 32 + lane;
-        // c[it][j] = Ws[nt][kb0+it] * Xs[kb0+it][mt*MT + j] (0 beyond M); the
-        // loads are issued in batches of 8 so their latencies overlap
+        // c[it][j] = Ws[z][kb0+it] * Xs[kb0+it][row0 + j] (0 beyond the tile's
+        // rows); the loads are issued in batches of 8 so their latencies overlap
         {
-            const float* __restrict__ ws = p.Ws + (int64_t)nt * p.KB + kb0;
-            const float* __restrict__ xs = p.Xs + (int64_t)kb0 * p.M + (int64_t)mt * MT;
-            const int total = nkb * MT;
-            const int64_t mrem = p.M - (int64_t)mt * MT;
+            const float* __restrict__ ws = p.Ws + (int64_t)z * p.KB + kb0;
+            const float* __restrict__ xs = p.Xs + (int64_t)kb0 * p.M + row0;
+            const int total = nrun * MT;
+            const int64_t mrem = rows;
             constexpr int kStride = C::kEpiWarps * 32;
             for (int base = et; base < total; base += 8 * kStride) {
                 float v[8];
@@ -208,7 +237,7 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
         uint64_t acc[C::kCols / 2];              // fp32 accumulators as packed pairs
 #pragma unroll
         for (int j = 0; j < C::kCols / 2; ++j) acc[j] = 0ull;
-        for (int it = 0; it < nkb; ++it) {
+        for (int it = 0; it < nrun; ++it) {
             const int buf = it & 1;
             const uint32_t bph = (it >> 1) & 1;
             // the verdict is made warp-uniform: the TMEM loads below are warp-collective
@@ -256,8 +285,8 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
     tc_fence_before();
     if (p.split > 1) cluster_sync_all(); else __syncthreads();
     {
-        const int64_t m_tile0 = (int64_t)mt * MT;
-        const int valid_m = (int)(p.M - m_tile0 < MT ? p.M - m_tile0 : MT);
+        const int64_t m_tile0 = row0;
+        const int valid_m = rows <= 0 ? 0 : (int)(rows < MT ? rows : MT);
         const int total = valid_m * 16;                   // chunks of 8 output channels
         const int per = (total + p.split - 1) / p.split;
         const int begin = split_idx * per, end = min(total, begin + per);
@@ -347,23 +376,27 @@ double decode_cost_us(int64_t M, int64_t N, int64_t K) {
     return 0.8 * c;
 }
 
+// M: token rows (all experts together in the grouped form); rows_per_group:
+// the token rows one weight matrix may have (M, or the per-expert bound);
+// groups: experts (1 for the dense GEMM, offs == nullptr).
 template <int MT>
 static cudaError_t launch_decode_mt(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
                                     const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
-                                    int64_t ldy, cudaStream_t st) {
+                                    int64_t ldy, const int32_t* offs, int64_t groups, int64_t rows_per_group,
+                                    cudaStream_t st) {
     using C = DecodeCfg<MT>;
     CUtensorMap tmW, tmX;
-    if (!make_tmap_u8(&tmW, Wq, (uint64_t)N, (uint64_t)K, (uint64_t)K, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap_u8(&tmW, Wq, (uint64_t)(groups * N), (uint64_t)K, (uint64_t)K, 128)) return cudaErrorInvalidValue;
     if (!make_tmap_u8(&tmX, Xq, (uint64_t)M, (uint64_t)K, (uint64_t)K, MT)) return cudaErrorInvalidValue;
     const int KB = (int)(K / 128);
-    const int64_t mtiles = (M + MT - 1) / MT;
-    const int64_t tiles = (N / 128) * mtiles;
+    const int64_t mtiles = (rows_per_group + MT - 1) / MT;
+    const int64_t tiles = groups * (N / 128) * mtiles;
     int split = choose_split(tiles, KB, MT, C::kMaxKbPerSplit);
     int per = (KB + split - 1) / split;
     if (per > C::kMaxKbPerSplit) return cudaErrorInvalidValue;
     uint32_t* err = device_error_word();
     if (!err) return cudaErrorInvalidValue;
-    DecodeParams prm{err, Xs, Ws, Y, M, ldy, KB, per, split};
+    DecodeParams prm{err, Xs, Ws, Y, M, ldy, KB, per, split, offs, (int)(N / 128), mtiles * MT};
 
     auto kern = gemm_fp8_decode_kernel<MT>;
     static bool attr_set[64] = {};     // the attribute belongs to the current device
@@ -377,7 +410,7 @@ static cudaError_t launch_decode_mt(const uint8_t* Xq, const float* Xs, const ui
         attr_set[dev] = true;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)split, (unsigned)mtiles, (unsigned)(N / 128));
+    cfg.gridDim = dim3((unsigned)split, (unsigned)mtiles, (unsigned)(groups * (N / 128)));
     cfg.blockDim = dim3(C::kThreads);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = st;
@@ -398,10 +431,22 @@ bool decode_supported(int64_t K) { return K / 128 <= 8 * DecodeCfg<16>::kMaxKbPe
 cudaError_t launch_gemm_fp8_decode(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
                                    const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
                                    int64_t ldy, cudaStream_t st) {
-    if (M <= 16) return launch_decode_mt<16>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
-    if (M <= 32) return launch_decode_mt<32>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
-    if (M <= 64) return launch_decode_mt<64>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
-    return launch_decode_mt<128>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
+    if (M <= 16) return launch_decode_mt<16>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, nullptr, 1, M, st);
+    if (M <= 32) return launch_decode_mt<32>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, nullptr, 1, M, st);
+    if (M <= 64) return launch_decode_mt<64>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, nullptr, 1, M, st);
+    return launch_decode_mt<128>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, nullptr, 1, M, st);
+}
+
+cudaError_t launch_gemm_fp8_grouped(const uint8_t* Xq, const float* Xs, const uint8_t* Wq, const float* Ws,
+                                    const int32_t* offs, int64_t E, int64_t T, int64_t N, int64_t K,
+                                    int64_t max_rows, uint16_t* Y, int64_t ldy, cudaStream_t st) {
+    if (max_rows <= 16)
+        return launch_decode_mt<16>(Xq, Xs, Wq, Ws, T, N, K, Y, ldy, offs, E, max_rows, st);
+    if (max_rows <= 32)
+        return launch_decode_mt<32>(Xq, Xs, Wq, Ws, T, N, K, Y, ldy, offs, E, max_rows, st);
+    if (max_rows <= 64)
+        return launch_decode_mt<64>(Xq, Xs, Wq, Ws, T, N, K, Y, ldy, offs, E, max_rows, st);
+    return launch_decode_mt<128>(Xq, Xs, Wq, Ws, T, N, K, Y, ldy, offs, E, max_rows, st);
 }
 
 // ------------------------------------------------------------------ linear layer

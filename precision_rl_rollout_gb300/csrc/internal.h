@@ -49,6 +49,11 @@ cudaError_t launch_rollout_is(const float* lt, const float* lr, const uint8_t* m
 cudaError_t launch_gemm_fp8_decode(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
                                    const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
                                    int64_t ldy, cudaStream_t st);
+// Grouped (mixture-of-experts) form of the decode kernel: experts' weights
+// stacked [E*N][K], token rows grouped by expert at offs[0..E] (device).
+cudaError_t launch_gemm_fp8_grouped(const uint8_t* Xq, const float* Xs, const uint8_t* Wq, const float* Ws,
+                                    const int32_t* offs, int64_t E, int64_t T, int64_t N, int64_t K,
+                                    int64_t max_rows, uint16_t* Y, int64_t ldy, cudaStream_t st);
 cudaError_t launch_gemm_fp8_mma_sync(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
                                      const float* Ws, int64_t M, int64_t N, int64_t K,
                                      uint16_t* Y, int64_t ldy, cudaStream_t st);

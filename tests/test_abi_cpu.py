@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
     version = int(re.search(r"#define FP8RL_ABI_VERSION (\d+)", open(HEADER).read()).group(1))
     assert lib.fp8rl_abi_version() == version
-    for s in range(8):
+    for s in range(9):
         assert lib.fp8rl_status_string(s).decode().startswith(binding.STATUS[s])
 
 
@@ -99,6 +99,21 @@ def test_linear_validation(lib):
     assert need >= 65 * 256 + 65 * 2 * 4
     assert f(A, 256, A, A, 65, 128, 256, A, 128, None, None, A, need - 1, None) == 4
     assert f(A, 256, A, A, 65, 128, 256, A, 128, None, None, None, 0, None) == 4
+
+
+def test_grouped_gemm_validation(lib):
+    g = lib.fp8rl_gemm_w8a8_block_grouped
+    #      Xq Xs Wq Ws off E  T   N    K    bound Y  ldy
+    assert g(A, A, A, A, A, 0, 8, 128, 256, 8, A, 128, None) == 2      # no experts
+    assert g(A, A, A, A, A, 4, -1, 128, 256, 8, A, 128, None) == 2     # negative T
+    assert g(A, A, A, A, A, 4, 8, 100, 256, 8, A, 128, None) == 2      # N % 128
+    assert g(A, A, A, A, A, 4, 8, 128, 256, 0, A, 128, None) == 2      # bound < 1
+    assert g(A, A, A, A, A, 4, 8, 128, 256, 9, A, 128, None) == 2      # bound > T
+    assert g(A, A, A, A, None, 4, 8, 128, 256, 8, A, 128, None) == 1   # offsets
+    assert g(A, A, A, A, A + 2, 4, 8, 128, 256, 8, A, 128, None) == 3
+    assert g(A, A, A, A, A, 4, 8, 128, 33024, 8, A, 128, None) == 6    # K above the decode limit
+    assert g(A, A, A, A, A, 70000, 8, 128, 256, 8, A, 128, None) == 6  # grid z above 65535
+    assert g(A, A, A, A, A, 4, 0, 128, 256, 8, A, 128, None) == 0      # no tokens: nothing launched
 
 
 def test_gemm_validation(lib):
