@@ -77,6 +77,8 @@ def _load():
             lib.oracle_fp8_quant_tensor.argtypes = [P, I, I, I, P, P]
             lib.oracle_fp8_quant_with_scale.restype = ctypes.c_int
             lib.oracle_fp8_quant_with_scale.argtypes = [P, I, I, I, ctypes.c_float, P]
+            lib.oracle_logits_kl.restype = ctypes.c_int
+            lib.oracle_logits_kl.argtypes = [P, I, P, I, I, I, P]
             lib.oracle_rollout_is.restype = ctypes.c_int
             lib.oracle_rollout_is.argtypes = [P, P, P, I, ctypes.c_float, ctypes.c_int, P, P]
             _lib = lib
@@ -275,3 +277,18 @@ def rollout_is(logp_train, logp_rollout, mask, log_clip: float, mode: int):
     _check(_load().oracle_rollout_is(_ptr(lt), _ptr(lr), _ptr(mk), n, float(log_clip), int(mode),
                                      _ptr(w), _ptr(st)), "rollout_is")
     return w.reshape(np.shape(logp_train)), st
+
+
+# ---------------------------------------------------------------- mismatch
+
+def logits_kl(P, Q) -> np.ndarray:
+    """Per-row KL(softmax(P) || softmax(Q)) in fp64 for bf16 logits (uint16 bits)
+    [M, V]: the train-inference mismatch of a quantized rollout (FlashRL write-up,
+    Fig. 2, right), P the higher-precision logits, Q the quantized ones."""
+    P = _bits16(P)
+    Q = _bits16(Q)
+    assert P.shape == Q.shape and P.ndim == 2
+    M, V = P.shape
+    kl = np.empty(M, np.float64)
+    _check(_load().oracle_logits_kl(_ptr(P), V, _ptr(Q), V, M, V, _ptr(kl)), "logits_kl")
+    return kl

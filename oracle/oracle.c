@@ -353,3 +353,46 @@ int oracle_rollout_is(const float* lt, const float* lr, const uint8_t* mask, int
     stats[0] = nv; stats[1] = nc; stats[2] = sw; stats[3] = sd;
     return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* Train-inference mismatch of a quantized rollout (FlashRL write-up,
+ * Fig. 2, right: the KL divergence between the trainer's policy and the
+ * rollout engine's policy, larger for INT8 rollouts than for FP8 ones).
+ * The pages do not give the estimator; this oracle takes the full-vocabulary
+ * KL of the two next-token distributions, per token row m:
+ *   p = softmax(P[m][:]), q = softmax(Q[m][:]),
+ *   kl[m] = sum_v p_v (log p_v - log q_v),
+ * P being the higher-precision policy's logits and Q the quantized one's,
+ * both bf16 [M][ld].  Plain fp64 log-softmax (max-shifted log-sum-exp).   */
+/* ------------------------------------------------------------------ */
+static double log_sum_exp_row(const uint16_t* r, int64_t V, double* mx_out) {
+    double mx = -INFINITY;
+    for (int64_t v = 0; v < V; ++v) {
+        double x = (double)oracle_bf16_to_f32(r[v]);
+        if (x > mx) mx = x;
+    }
+    double s = 0.0;
+    for (int64_t v = 0; v < V; ++v) s += exp((double)oracle_bf16_to_f32(r[v]) - mx);
+    *mx_out = mx;
+    return mx + log(s);
+}
+
+int oracle_logits_kl(const uint16_t* P, int64_t ldp, const uint16_t* Q, int64_t ldq, int64_t M, int64_t V,
+                     double* kl) {
+    if (M < 0 || V < 1 || ldp < V || ldq < V) return -1;
+    for (int64_t m = 0; m < M; ++m) {
+        const uint16_t* a = P + m * ldp;
+        const uint16_t* b = Q + m * ldq;
+        double ma, mb;
+        double za = log_sum_exp_row(a, V, &ma);
+        double zb = log_sum_exp_row(b, V, &mb);
+        double acc = 0.0;
+        for (int64_t v = 0; v < V; ++v) {
+            double lp = (double)oracle_bf16_to_f32(a[v]) - za;
+            double lq = (double)oracle_bf16_to_f32(b[v]) - zb;
+            acc += exp(lp) * (lp - lq);
+        }
+        kl[m] = acc;
+    }
+    return 0;
+}

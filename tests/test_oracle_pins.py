@@ -502,3 +502,50 @@ def test_rollout_is_matches_library_exp_and_counts():
         want = np.where(mask == 0, 0.0, np.where(clipped, np.exp(float(log_clip)) if mode == 0 else 0.0, keep))
         assert np.allclose(w, want, rtol=1e-12, atol=0)
         assert st[0] == mask.sum() and st[1] == clipped.sum()
+
+
+# ------------------------------------------------------------------ mismatch KL
+
+def _bf16(v):
+    return oracle.f32_to_bf16_rn(np.asarray(v, np.float32))
+
+
+def test_logits_kl_two_symbol_closed_form():
+    # V = 2: the softmax is a Bernoulli with p = sigmoid(a0 - a1), so the KL is
+    # p log(p/q) + (1-p) log((1-p)/(1-q)); the inputs are exact in bf16
+    a = np.array([[1.5, -0.25], [0.0, 0.0], [3.0, 1.0]], np.float32)
+    b = np.array([[0.5, 0.5], [2.0, -1.0], [-1.0, 4.0]], np.float32)
+    kl = oracle.logits_kl(_bf16(a), _bf16(b))
+    for m in range(3):
+        p = 1.0 / (1.0 + math.exp(-(float(a[m, 0]) - float(a[m, 1]))))
+        q = 1.0 / (1.0 + math.exp(-(float(b[m, 0]) - float(b[m, 1]))))
+        want = p * math.log(p / q) + (1 - p) * math.log((1 - p) / (1 - q))
+        assert abs(kl[m] - want) <= 1e-14 * max(1.0, abs(want))
+
+
+def test_logits_kl_uniform_against_one_raised_logit_closed_form():
+    # p uniform over V; q puts logit c on symbol 0 and 0 elsewhere:
+    # KL = -log V - (1/V) [log q0 + (V-1) log q1], q0 = e^c / Z, q1 = 1 / Z, Z = e^c + V - 1
+    V, c = 1000, 2.5
+    a = np.zeros((1, V), np.float32)
+    b = np.zeros((1, V), np.float32)
+    b[0, 0] = c
+    Z = math.exp(c) + V - 1
+    want = -math.log(V) - (math.log(math.exp(c) / Z) + (V - 1) * math.log(1 / Z)) / V
+    kl = oracle.logits_kl(_bf16(a), _bf16(b))
+    assert abs(kl[0] - want) <= 1e-12
+
+
+def test_logits_kl_zero_for_equal_rows_positive_otherwise_and_shift_invariant():
+    rng = np.random.default_rng(3)
+    a = _bf16(rng.normal(0, 2, size=(4, 513)))
+    assert np.all(np.abs(oracle.logits_kl(a, a)) <= 1e-14)
+    b = _bf16(oracle.bf16_to_f32(a) + rng.normal(0, 0.05, size=a.shape).astype(np.float32))
+    kl = oracle.logits_kl(a, b)
+    assert np.all(kl > 0)
+    # a shift by a power of two keeps small integers exact in bf16, and the
+    # softmax does not see a constant added to every logit of a row
+    ai = _bf16(rng.integers(-8, 9, size=(3, 257)).astype(np.float32))
+    bi = _bf16(rng.integers(-8, 9, size=(3, 257)).astype(np.float32))
+    shifted = _bf16(oracle.bf16_to_f32(bi) + np.float32(16.0))
+    assert np.allclose(oracle.logits_kl(ai, bi), oracle.logits_kl(ai, shifted), rtol=1e-12, atol=1e-14)
