@@ -15,7 +15,9 @@ earlier, so every weight byte comes from HBM, not from L2.
 
 Other rows are measured as sub-benchmarks under "extras" (not in `value`):
 prefill FP8 GEMM TFLOP/s at M=8192 (Qwen2.5-32B shapes), the 32B decode sweep
-M in {1,8,32,128,256}, the 64-layer 32B requant, and the INT8 W8A8 path.
+M in {1,8,32,128,256}, the grouped MoE GEMM, the FP8-vs-INT8 rollout mismatch
+KL, the 64-layer 32B requant, the FP8 KV-cache quant, the TIS/MIS weights and
+the INT8 W8A8 path.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--extras all|none]
     python bench.py --impl reference ...     # the CPU oracle on a bounded sample
@@ -436,6 +438,34 @@ def extras(fb, dev, reps=5):
                      "routed_rows": T, "max_rows_per_expert": bound, "weight_copies": nc}
         del Wq, Ws, Wqs, Wss, X, Xq, Xs, Y
     out["moe_fp8_grouped_decode"] = moe
+
+    # Rollout mismatch (FlashRL write-up, Fig. 2, right): KL between the bf16
+    # policy's next-token distribution and the FP8 / INT8 rollout's, on a
+    # synthetic Qwen2.5-7B LM head (hidden 3584 -> vocab 152064), 64 tokens.  The
+    # bf16 reference logits stand for the trainer's forward (torch matmul); the
+    # 8-bit logits and the KL come from this library.
+    V, K = 152064, 3584
+    W = synth.weight_bf16_direct(V, K, synth.seed_for(9, 0), device=dev)
+    X = synth.activation(DECODE_M, K, synth.seed_for(9, 1), device=dev)
+    R = X @ W.t()
+    Wq, Ws = fb.fp8rl_quant_weight_block(W)
+    Y8 = fb.fp8rl_linear_w8a8_block(X, Wq, Ws)
+    del Wq, Ws
+    Wi, Wsi = fb.int8rl_quant_weight_channel(W)
+    Xi, Xsi = fb.int8rl_quant_act_token(X)
+    Yi = fb.int8rl_gemm_w8a8(Xi, Xsi, Wi, Wsi)
+    del W, Wi
+    kl8 = fb.fp8rl_logits_kl(R, Y8)
+    kli = fb.fp8rl_logits_kl(R, Yi)
+    klw = torch.empty(max(1, fb.fp8rl_logits_kl_workspace_bytes(DECODE_M, V)), dtype=torch.uint8, device=dev)
+    ms = _time_graph([lambda: fb.fp8rl_logits_kl(R, Y8, kl8, workspace=klw)] * 8)
+    out["mismatch_kl_lm_head_7b"] = {
+        "tokens": DECODE_M, "vocab": V, "hidden": K,
+        "kl_fp8_mean": float(kl8.double().mean()), "kl_int8_mean": float(kli.double().mean()),
+        "kl_fp8_max": float(kl8.max()), "kl_int8_max": float(kli.max()),
+        "int8_over_fp8": float(kli.double().mean() / kl8.double().mean()),
+        "kl_kernel_us": ms * 1e3, "kl_kernel_gbs": 4 * DECODE_M * V / (ms * 1e-3) / 1e9}
+    del R, Y8, Yi, X, Xi
 
     # A1 at full-model scale: 64 layers x 4 shapes, grouped launches (62 GB in)
     items = []

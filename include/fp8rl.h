@@ -267,6 +267,25 @@ int fp8rl_rollout_is_weights(const float* logp_train, const float* logp_rollout,
                              size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Train-inference mismatch of a quantized rollout (FlashRL write-up, Fig. 2,
+ * right: the KL divergence between the trainer's policy and the rollout
+ * engine's, larger for INT8 rollouts than for FP8 ones).  For every token row
+ * m of two logit matrices -- P from the higher-precision policy, Q from the
+ * quantized one (e.g. the output of an LM-head GEMM) --
+ *   kl[m] = sum_v softmax(P[m])_v * (log softmax(P[m])_v - log softmax(Q[m])_v).
+ * P [M][ldp], Q [M][ldq] bf16, V >= 1 logits per row, ld >= V, ld % 8 == 0,
+ * 16-byte aligned; kl fp32 [M], 4-byte aligned.  Logits must be finite and
+ * |P - Q| < 32 elementwise (keeps every fp32 term finite).  Accuracy: |kl - kl_exact| <= 1e-4 kl_exact + 1e-7
+ * (fp32 elementwise terms, fp64 combination; see mismatch_kl.cu).
+ * Deterministic.  workspace: at least fp8rl_logits_kl_workspace_bytes(M, V)
+ * bytes, 16-byte aligned, no zeroing needed (32 bytes per 8192 logits).
+ * Limit: M <= 65535 (FP8RL_ERR_UNSUPPORTED).
+ * ---------------------------------------------------------------------- */
+size_t fp8rl_logits_kl_workspace_bytes(int64_t M, int64_t V);
+int fp8rl_logits_kl(const uint16_t* P, int64_t ldp, const uint16_t* Q, int64_t ldq, int64_t M,
+                    int64_t V, float* kl, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * fp8rl_quant_kv_tensor without a workspace.  The paper has no counterpart:
  * this is a calling convention, not part of the method.  It computes exactly
  * what fp8rl_quant_kv_tensor computes, for callers that cannot allocate the

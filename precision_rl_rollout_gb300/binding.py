@@ -32,7 +32,7 @@ EXPORTS = ("fp8rl_status_string", "fp8rl_abi_version", "fp8rl_quant_weight_block
            "int8rl_gemm_workspace_bytes", "int8rl_gemm_w8a8", "fp8rl_check_device_error",
            "fp8rl_kv_workspace_bytes", "fp8rl_quant_kv_tensor", "fp8rl_quant_kv_with_scale",
            "fp8rl_quant_kv_tensor_noalloc", "fp8rl_rollout_is_workspace_bytes",
-           "fp8rl_rollout_is_weights")
+           "fp8rl_rollout_is_weights", "fp8rl_logits_kl_workspace_bytes", "fp8rl_logits_kl")
 
 
 class Fp8rlError(RuntimeError):
@@ -92,13 +92,17 @@ def load(path: str | None = None):
         lib.fp8rl_quant_kv_tensor.argtypes = [P, I, I, I, P, P, P, Z, S]
         lib.fp8rl_quant_kv_with_scale.argtypes = [P, I, I, I, P, P, S]
         lib.fp8rl_quant_kv_tensor_noalloc.argtypes = [P, I, I, I, P, P, S]
+        lib.fp8rl_logits_kl_workspace_bytes.restype = Z
+        lib.fp8rl_logits_kl_workspace_bytes.argtypes = [I, I]
+        lib.fp8rl_logits_kl.argtypes = [P, I, P, I, I, I, P, P, Z, S]
         lib.fp8rl_rollout_is_workspace_bytes.restype = Z
         lib.fp8rl_rollout_is_workspace_bytes.argtypes = [I]
         lib.fp8rl_rollout_is_weights.argtypes = [P, P, P, I, ctypes.c_float, ctypes.c_int, P, P, P, Z, S]
         for name in EXPORTS:
             if name not in ("fp8rl_status_string", "fp8rl_abi_version", "fp8rl_gemm_workspace_bytes",
                             "int8rl_gemm_workspace_bytes", "fp8rl_kv_workspace_bytes",
-                            "fp8rl_rollout_is_workspace_bytes", "fp8rl_linear_workspace_bytes"):
+                            "fp8rl_rollout_is_workspace_bytes", "fp8rl_linear_workspace_bytes",
+                            "fp8rl_logits_kl_workspace_bytes"):
                 getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -380,3 +384,24 @@ def fp8rl_check_device_error() -> int:
     if rc not in (0, 7, 8):
         raise Fp8rlError(rc, "fp8rl_check_device_error")
     return int(w.value)
+
+
+def fp8rl_logits_kl_workspace_bytes(M: int, V: int) -> int:
+    return int(load().fp8rl_logits_kl_workspace_bytes(M, V))
+
+
+def fp8rl_logits_kl(P, Q, kl=None, workspace=None, stream=None):
+    """Per-row KL(softmax(P) || softmax(Q)) of bf16 logits [M, V] -> fp32 [M]."""
+    lib = load()
+    ldp, ldq = _rowmajor(P, "P"), _rowmajor(Q, "Q")
+    if P.shape != Q.shape:
+        raise ValueError("P and Q must have the same shape")
+    M, V = P.shape
+    kl = _need(kl, (M,), torch.float32, P.device, "kl")
+    need = lib.fp8rl_logits_kl_workspace_bytes(M, V)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=P.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _ck(lib.fp8rl_logits_kl(_p(P), ldp, _p(Q), ldq, M, V, _p(kl), _p(workspace), wbytes, _stream(P, stream)),
+        "fp8rl_logits_kl")
+    return kl

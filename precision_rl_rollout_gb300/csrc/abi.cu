@@ -238,6 +238,25 @@ int fp8rl_rollout_is_weights(const float* logp_train, const float* logp_rollout,
                                          stats, workspace, as_stream(stream)));
 }
 
+size_t fp8rl_logits_kl_workspace_bytes(int64_t M, int64_t V) {
+    if (M <= 0 || V <= 0) return 0;
+    return (size_t)M * (size_t)kl_chunks(V) * kl_partial_bytes();
+}
+
+int fp8rl_logits_kl(const uint16_t* P, int64_t ldp, const uint16_t* Q, int64_t ldq, int64_t M,
+                    int64_t V, float* kl, void* workspace, size_t workspace_bytes, void* stream) {
+    if (M < 0 || V < 1 || ldp < V || ldq < V) return FP8RL_ERR_SHAPE;
+    if (M > 0 && (!P || !Q || !kl)) return FP8RL_ERR_NULL;
+    if (!aligned16(P) || !aligned16(Q) || (ldp * 2) % 16 || (ldq * 2) % 16 || !aligned4(kl) ||
+        !aligned16(workspace))
+        return FP8RL_ERR_ALIGN;
+    if (M > 65535) return FP8RL_ERR_UNSUPPORTED;
+    const size_t need = fp8rl_logits_kl_workspace_bytes(M, V);
+    if (workspace_bytes < need || (need && !workspace)) return FP8RL_ERR_WORKSPACE;
+    if (M == 0) return FP8RL_OK;
+    return cuda_status(launch_logits_kl(P, ldp, Q, ldq, M, V, kl, workspace, as_stream(stream)));
+}
+
 int fp8rl_quant_kv_tensor_noalloc(const uint16_t* KV, int64_t R, int64_t C, int64_t ld, uint8_t* KVq,
                                   float* scale, void* stream) {
     int rc = check_kv(KV, R, C, ld, KVq);

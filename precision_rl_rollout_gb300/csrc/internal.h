@@ -45,6 +45,12 @@ cudaError_t launch_rollout_is(const float* lt, const float* lr, const uint8_t* m
                               float log_clip, int mode, float* w, double* stats, void* ws,
                               cudaStream_t st);
 
+// Per-token KL between two logit matrices (two launches, partial records in `ws`).
+int kl_chunks(int64_t V);
+size_t kl_partial_bytes();
+cudaError_t launch_logits_kl(const uint16_t* P, int64_t ldp, const uint16_t* Q, int64_t ldq, int64_t M,
+                             int64_t V, float* kl, void* ws, cudaStream_t st);
+
 // FP8 block-scaled GEMM: dispatch by M (tcgen05 decode kernel for M <= 256).
 cudaError_t launch_gemm_fp8_decode(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
                                    const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,

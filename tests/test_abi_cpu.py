@@ -116,6 +116,23 @@ def test_grouped_gemm_validation(lib):
     assert g(A, A, A, A, A, 4, 0, 128, 256, 8, A, 128, None) == 0      # no tokens: nothing launched
 
 
+def test_logits_kl_validation(lib):
+    f = lib.fp8rl_logits_kl
+    ws = lib.fp8rl_logits_kl_workspace_bytes(4, 1000)
+    assert ws == 4 * 1 * 32
+    assert lib.fp8rl_logits_kl_workspace_bytes(2, 8193) == 2 * 2 * 32
+    #      P  ldp  Q  ldq  M  V     kl ws bytes
+    assert f(A, 1000, A, 1000, 4, 0, A, A, ws, None) == 2         # V < 1
+    assert f(A, 996, A, 1000, 4, 1000, A, A, ws, None) == 2       # ldp < V
+    assert f(None, 1000, A, 1000, 4, 1000, A, A, ws, None) == 1
+    assert f(A, 1000, A, 1000, 4, 1000, None, A, ws, None) == 1
+    assert f(A, 1004, A, 1004, 4, 1000, A, A, ws, None) == 3      # row pitch 2008 B
+    assert f(A, 1000, A + 2, 1000, 4, 1000, A, A, ws, None) == 3
+    assert f(A, 1000, A, 1000, 4, 1000, A, A, ws - 1, None) == 4
+    assert f(A, 1000, A, 1000, 70000, 1000, A, A, 1 << 40, None) == 6
+    assert f(A, 1000, A, 1000, 0, 1000, A, None, 0, None) == 0    # nothing to do
+
+
 def test_gemm_validation(lib):
     g = lib.fp8rl_gemm_w8a8_block
     ws = lib.fp8rl_gemm_workspace_bytes(64, 256, 256)
