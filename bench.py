@@ -50,8 +50,8 @@ L2_BYTES = 129 * 2 ** 20
 # ncu-measured DRAM traffic of the dominant kernel, valid only for the source it
 # was taken on (checked by hash; null otherwise).  Filled from the committed
 # profile summary of the same workload.
-NCU_TRAFFIC = {"kernel": "quant_weight_block_kernel", "source_sha1": "90389709ba3d55e730702a5d717d6d5d2e9eadef",
-               "bytes_per_launch": 466143744 + 174737152,
+NCU_TRAFFIC = {"kernel": "quant_weight_block_kernel", "source_sha1": "41ce679f08cedbd2a78d584ca50789218d072b18",
+               "bytes_per_launch": 466135040 + 174086144,
                "profile": "profiles/requant_weight_block_qwen7b.md"}
 
 
@@ -685,6 +685,27 @@ def profile_case(fb, case, dev, reps=3):
         Xq, Xs = fb.fp8rl_quant_act_group(synth.activation(M, s.K, synth.seed_for(3, 1), device=dev))
         for _ in range(reps):
             fb.fp8rl_gemm_w8a8_block(Xq, Xs, Wq, Ws)
+    elif case == "moe":
+        E, N, K = 128, 1536, 2048                         # MoE gate_up, top-8 of 64 tokens
+        rng = torch.Generator().manual_seed(synth.seed_for(8, 0))
+        picks = torch.stack([torch.randperm(E, generator=rng)[:8] for _ in range(DECODE_M)])
+        counts = torch.bincount(picks.flatten(), minlength=E)
+        offs = torch.cat([torch.zeros(1, dtype=torch.int64), counts.cumsum(0)]).to(torch.int32).to(dev)
+        W = synth.weight_bf16_direct(E * N, K, synth.seed_for(8, 1), device=dev)
+        Wq, Ws = fb.fp8rl_quant_weight_block(W)
+        del W
+        Xq, Xs = fb.fp8rl_quant_act_group(synth.activation(int(counts.sum()), K, synth.seed_for(8, 2), device=dev))
+        for _ in range(reps):
+            fb.fp8rl_gemm_w8a8_block_grouped(Xq, Xs, Wq.view(E, N, K), Ws.view(E, N // 128, K // 128), offs,
+                                             int(counts.max()))
+    elif case == "kl":
+        V = 152064
+        g = torch.Generator(device=dev)
+        g.manual_seed(synth.seed_for(9, 2))
+        R = (2.0 * torch.randn(DECODE_M, V, device=dev, generator=g)).to(torch.bfloat16)
+        Q = (R.float() + 0.02 * torch.randn(DECODE_M, V, device=dev, generator=g)).to(torch.bfloat16)
+        for _ in range(reps):
+            fb.fp8rl_logits_kl(R, Q)
     elif case == "int8_m32":
         s = synth.QWEN25_32B[2]                          # gate_up 5120 -> 55296
         W = synth.weight_bf16_direct(s.N, s.K, synth.seed_for(5, 0), device=dev)

@@ -15,11 +15,11 @@
 // weight >= 1/S_j on x = 0), then for five fp32 sums over x = d - c_j:
 //   S = sum w, X = sum w x, F = sum w f(x), U = sum w expm1(-x), G = sum w exp(-x),
 // with f(x) = x + expm1(-x) >= 0 (its Taylor series for |x| < 1/16, so no
-// cancellation).  Per chunk, r_j = log E[exp(-x)] + E[x] >= 0 is taken as
-// F/S + log1p(U/S) - U/S when |U/S| < 1/2 and as X/S + log(G/S) otherwise,
-// and z_j = X/S + c_j - c - r_j.  A second launch combines the chunks of a row
-// in fp64, in a fixed order (deterministic), with pi_j = S_j exp(m_j - m) / S
-// and c the centre of the chunk holding the row's largest logit:
+// cancellation).  Per chunk, in fp64, r_j = log E[exp(-x)] + E[x] >= 0 is taken
+// as F/S + log1p(U/S) - U/S when |U/S| < 1/2 and as X/S + log(G/S) otherwise,
+// and z_j = X/S + c_j - r_j.  A second launch (one warp per row) combines the
+// chunks of a row in fp64 with pi_j = S_j exp(m_j - m) / S, m the row's
+// largest logit, in a fixed reduction order (deterministic):
 //   kl = sum_j pi_j r_j + log1p( sum_j pi_j expm1(-(z_j - zbar)) ),  zbar = sum_j pi_j z_j,
 // which is the same quantity with every cancellation left to fp64.
 #include <math.h>
@@ -36,21 +36,10 @@ constexpr int64_t kKlChunk = 8192;                          // logits per CTA (3
 constexpr int kKlPer = (int)(kKlChunk / kKlThreads);        // 32 per thread
 
 struct KlPartial {
-    float m, c, S, X, F, U, G, pad;
+    double r, z;       // the chunk's Jensen gap and centred mean (see above)
+    float m, S;        // its largest logit and sum of weights
+    float pad[2];
 };
-
-// f(x) = x + expm1(-x), given u = expm1(-x)
-__device__ __forceinline__ float kl_f(float x, float u) {
-    if (fabsf(x) < 0.0625f) {
-        // x^2/2 - x^3/6 + x^4/24 - x^5/120 + x^6/720 (next term below 1e-9 relative)
-        float t = fmaf(-x, 1.f / 720.f, 1.f / 120.f);
-        t = fmaf(-x, t, 1.f / 24.f);
-        t = fmaf(-x, t, 1.f / 6.f);
-        t = fmaf(-x, t, 0.5f);
-        return x * x * t;
-    }
-    return x + u;
-}
 
 __device__ __forceinline__ float bf16f(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
 
@@ -113,12 +102,26 @@ kl_partial_kernel(const uint16_t* __restrict__ P, int64_t ldp, const uint16_t* _
             const float pv = bf16f(sp[e]);
             const float wv = expf(pv - mx);
             const float x = (pv - bf16f(sq[e])) - c;
-            const float u = expm1f(-x);
+            const float ex = expf(-x);
+            float u, f;
+            if (fabsf(x) < 0.0625f) {
+                // expm1(-x) and x + expm1(-x) by their Taylor series (terms past x^6
+                // are below 1e-9 of the result)
+                float t = fmaf(-x, 1.f / 720.f, 1.f / 120.f);
+                t = fmaf(-x, t, 1.f / 24.f);
+                t = fmaf(-x, t, 1.f / 6.f);
+                t = fmaf(-x, t, 0.5f);
+                f = x * x * t;
+                u = fmaf(x * x, t, -x);
+            } else {
+                u = ex - 1.f;                              // |u| >= 0.06: no cancellation
+                f = x + u;
+            }
             S += wv;
             X = fmaf(wv, x, X);
-            F = fmaf(wv, kl_f(x, u), F);
+            F = fmaf(wv, f, F);
             U = fmaf(wv, u, U);
-            G = fmaf(wv, expf(-x), G);
+            G = fmaf(wv, ex, G);
         }
     }
     float t[5] = {S, X, F, U, G};
@@ -135,39 +138,49 @@ kl_partial_kernel(const uint16_t* __restrict__ P, int64_t ldp, const uint16_t* _
             r[q] = 0.f;
             for (int k = 0; k < kKlThreads / 32; ++k) r[q] += wsum[q][k];   // fixed order
         }
-        part[row * chunks + blockIdx.x] = KlPartial{mx, c, r[0], r[1], r[2], r[3], r[4], 0.f};
+        const double Sj = r[0], xb = r[1] / Sj, u = r[3] / Sj;
+        const double rj = fabs(u) < 0.5 ? r[2] / Sj + (log1p(u) - u) : xb + log(r[4] / Sj);
+        part[row * chunks + blockIdx.x] = KlPartial{rj, xb + (double)c - rj, mx, r[0], {0.f, 0.f}};
     }
 }
 
-// One thread per row: the row's chunks in order, in fp64.
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+// One warp per row: lane l takes chunks l, l+32, ...; fixed shuffle trees.
 __global__ void __launch_bounds__(128)
 kl_combine_kernel(const KlPartial* __restrict__ part, int64_t M, int chunks, float* __restrict__ kl) {
     pdl_wait_then_release();
-    const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (row >= M) return;
+    const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= M) return;                                 // whole warps only
     const KlPartial* r = part + row * chunks;
-    int top = 0;
-    for (int j = 1; j < chunks; ++j)
-        if (r[j].m > r[top].m) top = j;
-    const double m = r[top].m, c = r[top].c;
+    float mf = -INFINITY;
+    for (int j = lane; j < chunks; j += 32) mf = fmaxf(mf, r[j].m);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mf = fmaxf(mf, __shfl_xor_sync(0xffffffffu, mf, off));
+    const double m = mf;
     double S = 0.0;
-    for (int j = 0; j < chunks; ++j) S += (double)r[j].S * exp((double)r[j].m - m);
-    double sr = 0.0, zbar = 0.0;
-    for (int j = 0; j < chunks; ++j) {
-        const double Sj = r[j].S, pi = Sj * exp((double)r[j].m - m) / S;
-        const double u = r[j].U / Sj, xb = r[j].X / Sj;
-        const double rj = fabs(u) < 0.5 ? r[j].F / Sj + (log1p(u) - u) : xb + log(r[j].G / Sj);
-        sr += pi * rj;
-        zbar += pi * (xb + ((double)r[j].c - c) - rj);
+    for (int j = lane; j < chunks; j += 32) S += (double)r[j].S * exp((double)r[j].m - m);
+    S = warp_sum_d(S);
+    double sr = 0.0, zb = 0.0;
+    for (int j = lane; j < chunks; j += 32) {
+        const double pi = (double)r[j].S * exp((double)r[j].m - m) / S;
+        sr += pi * r[j].r;
+        zb += pi * r[j].z;
     }
+    sr = warp_sum_d(sr);
+    zb = warp_sum_d(zb);
     double g = 0.0;
-    for (int j = 0; j < chunks; ++j) {
-        const double Sj = r[j].S, pi = Sj * exp((double)r[j].m - m) / S;
-        const double u = r[j].U / Sj, xb = r[j].X / Sj;
-        const double rj = fabs(u) < 0.5 ? r[j].F / Sj + (log1p(u) - u) : xb + log(r[j].G / Sj);
-        g += pi * expm1(-((xb + ((double)r[j].c - c) - rj) - zbar));
+    for (int j = lane; j < chunks; j += 32) {
+        const double pi = (double)r[j].S * exp((double)r[j].m - m) / S;
+        g += pi * expm1(-(r[j].z - zb));
     }
-    kl[row] = (float)(sr + log1p(g));
+    g = warp_sum_d(g);
+    if (lane == 0) kl[row] = (float)(sr + log1p(g));
 }
 
 }  // namespace
@@ -182,7 +195,7 @@ cudaError_t launch_logits_kl(const uint16_t* P, int64_t ldp, const uint16_t* Q, 
     cudaError_t e = launch_pdl(kl_partial_kernel, dim3((unsigned)chunks, (unsigned)M), dim3(kKlThreads), 0, st, P,
                                ldp, Q, ldq, V, chunks, part);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kl_combine_kernel, dim3((unsigned)((M + 127) / 128)), dim3(128), 0, st,
+    return launch_pdl(kl_combine_kernel, dim3((unsigned)((M + 3) / 4)), dim3(128), 0, st,
                       (const KlPartial*)part, M, chunks, kl);
 }
 
