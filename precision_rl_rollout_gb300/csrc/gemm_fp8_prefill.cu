@@ -11,7 +11,8 @@
 // halves of the tile are exactly two weight blocks, so the scale that promotes
 // a K block's partial product is one fp32 scalar per thread (its token's
 // activation scale times its half's weight scale).
-// Warpgroup 0: warp 0 issues TMA, warp 1 issues the MMAs (and owns TMEM).
+// Warpgroup 0: warp 0 issues TMA, warps 1 and 2 issue the MMAs of alternate K
+// blocks (warp 1 owns TMEM).
 // Warpgroups 1 and 2: epilogue, one per column half; each thread owns one
 // token row and keeps 128 fp32 accumulators in registers, which setmaxnreg
 // moves over from warpgroup 0 (40 -> 232 registers per thread).
@@ -117,12 +118,16 @@ gemm_fp8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_co
                     tma_load_2d(smem_u32(st + kABytes), &tmW, full0 + 8 * s, kb * 128, nt * kBN, pol_w);
                 }
             }
-        } else if (warp == 1 && lane == 0) {
-            // ---------------- MMA issuer
+        } else if ((warp == 1 || warp == 2) && lane == 0) {
+            // ---------------- MMA issuers: warp 1 issues the K blocks that go to
+            // TMEM buffer 0, warp 2 those of buffer 1, so one thread's barrier
+            // waits and commits overlap the other's MMAs
             constexpr uint32_t idesc = idesc_e4m3_f32(kBM, kBN);
+            const uint32_t mine = warp - 1;
             uint32_t it = 0;
             for (int tile = blockIdx.x; tile < total_tiles && !*abort; tile += gridDim.x) {
                 for (int kb = 0; kb < p.KB; ++kb, ++it) {
+                    if ((it & 1) != mine) continue;
                     const int s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1;
                     const uint32_t buf = it & 1, bph = (it >> 1) & 1;
