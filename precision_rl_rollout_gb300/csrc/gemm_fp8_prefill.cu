@@ -185,18 +185,22 @@ gemm_fp8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_co
                 }
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + buf * kBN + h * 128;
+                // The buffer is released as soon as its last columns are in
+                // registers; the second half's promotion runs after the release.
+                uint32_t r[64];
+                tmem_ld_32x32b_x32(taddr, *reinterpret_cast<uint32_t(*)[32]>(r));
+                tmem_ld_32x32b_x32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
+                tmem_wait_ld();
 #pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    uint32_t r[64];
-                    tmem_ld_32x32b_x32(taddr + g * 64, *reinterpret_cast<uint32_t(*)[32]>(r));
-                    tmem_ld_32x32b_x32(taddr + g * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 64; ++j) acc[g * 64 + j] = fmaf(__uint_as_float(r[j]), scale, acc[g * 64 + j]);
-                }
+                for (int j = 0; j < 64; ++j) acc[j] = fmaf(__uint_as_float(r[j]), scale, acc[j]);
+                tmem_ld_32x32b_x32(taddr + 64, *reinterpret_cast<uint32_t(*)[32]>(r));
+                tmem_ld_32x32b_x32(taddr + 96, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
+                tmem_wait_ld();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
+#pragma unroll
+                for (int j = 0; j < 64; ++j) acc[64 + j] = fmaf(__uint_as_float(r[j]), scale, acc[64 + j]);
             }
             if (!ok) break;
             // Output: the warp's 32 rows x 128 columns go out as two 32 x 64 boxes,
