@@ -248,27 +248,26 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
             tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + buf * MT + colbase;
             const float* cs = cscale + it * MT + colbase;
-            // several TMEM loads in flight per wait: the load latency is paid
-            // once per group of up to 64 columns, not once per chunk
+            // all of this thread's columns (<= 64) in flight under one wait; the
+            // buffer is released as soon as they are in registers, before the
+            // promotion, so the next MMAs into it need not wait for the FMAs
+            static_assert(C::kCols == C::kGroup, "one load group per block");
+            uint32_t r[C::kGroup];
 #pragma unroll
-            for (int g = 0; g < C::kCols / C::kGroup; ++g) {
-                uint32_t r[C::kGroup];
-#pragma unroll
-                for (int ch = 0; ch < C::kGroup / C::kChunk; ++ch) {
-                    uint32_t(&rc)[C::kChunk] = *reinterpret_cast<uint32_t(*)[C::kChunk]>(r + ch * C::kChunk);
-                    const uint32_t a = taddr + g * C::kGroup + ch * C::kChunk;
-                    if constexpr (C::kChunk == 32) tmem_ld_32x32b_x32(a, rc);
-                    else tmem_ld_32x32b_x16(a, rc);
-                }
-                tmem_wait_ld();
-                const uint64_t* cs2 = reinterpret_cast<const uint64_t*>(cs + g * C::kGroup);
-#pragma unroll
-                for (int j = 0; j < C::kGroup / 2; ++j)
-                    fma_f32x2(acc[g * C::kGroup / 2 + j], f32x2_pack(r[2 * j], r[2 * j + 1]), cs2[j]);
+            for (int ch = 0; ch < C::kGroup / C::kChunk; ++ch) {
+                uint32_t(&rc)[C::kChunk] = *reinterpret_cast<uint32_t(*)[C::kChunk]>(r + ch * C::kChunk);
+                const uint32_t a = taddr + ch * C::kChunk;
+                if constexpr (C::kChunk == 32) tmem_ld_32x32b_x32(a, rc);
+                else tmem_ld_32x32b_x16(a, rc);
             }
+            tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
+            const uint64_t* cs2 = reinterpret_cast<const uint64_t*>(cs);
+#pragma unroll
+            for (int j = 0; j < C::kGroup / 2; ++j)
+                fma_f32x2(acc[j], f32x2_pack(r[2 * j], r[2 * j + 1]), cs2[j]);
         }
         // every MMA of this CTA has completed: the stage area is free for the
         // transposed partial tile red[m][n_local]

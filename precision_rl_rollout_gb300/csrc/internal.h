@@ -40,6 +40,7 @@ cudaError_t launch_quant_kv_tensor_noalloc(const uint16_t* X, int64_t R, int64_t
 
 // Token-level TIS/MIS weights and statistics (two launches, partial records in `ws`).
 int64_t rollout_is_partials(int64_t n);
+int64_t rollout_is_max_partials(int64_t n);
 size_t rollout_is_partial_bytes();
 cudaError_t launch_rollout_is(const float* lt, const float* lr, const uint8_t* mask, int64_t n,
                               float log_clip, int mode, float* w, double* stats, void* ws,

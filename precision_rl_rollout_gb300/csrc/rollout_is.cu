@@ -10,9 +10,10 @@
 //   masked    (MIS): w = d > log_clip ? 0 : exp(d);
 // padding tokens (mask 0) get w = 0.  The clip decision is an fp32 comparison,
 // so the clipped/masked count is exact; the weights use the CUDA expf.
-// Two launches: every CTA writes the weights of its 4096 tokens and one
-// partial record (valid, clipped, sum w, sum d; fp32 sums inside the CTA); one
-// CTA then adds the records in fp64 in a fixed order (deterministic statistics).
+// Two launches: every CTA of a persistent grid writes the weights of its token
+// range and one partial record (valid, clipped, sum w, sum d; fp32 sums inside
+// the CTA); one CTA then adds the records in fp64 in a fixed order
+// (deterministic statistics for a given GPU).
 #include "common.cuh"
 #include "internal.h"
 
@@ -39,64 +40,71 @@ __device__ __forceinline__ float is_weight(float d, float log_clip, int mode, bo
     return mode == 0 ? expf(clipped ? log_clip : d) : (clipped ? 0.f : expf(d));
 }
 
-// Every thread owns 16 tokens of its CTA's 4096: in the vector form, four
-// groups of four consecutive tokens (16-byte loads of both log-prob arrays and
-// a 4-byte load of the mask, all issued before any is used).
+// A persistent grid (a few CTAs per SM): CTA c owns the contiguous token range
+// [c*per, (c+1)*per), per a multiple of 4096, so every CTA streams the same
+// amount and there is no tail wave.  Within the range a thread takes 16
+// tokens per step: four groups of four consecutive tokens (16-byte loads of
+// both log-prob arrays and a 4-byte load of the mask, all issued before any is
+// used).  Ranges that are not whole 4096-token steps, or unaligned pointers,
+// take the scalar path.
 template <bool kVec>
 __global__ void __launch_bounds__(kIsThreads)
 rollout_is_kernel(const float* __restrict__ lt, const float* __restrict__ lr,
-                  const uint8_t* __restrict__ mask, int64_t n, float log_clip, int mode,
+                  const uint8_t* __restrict__ mask, int64_t n, int64_t per, float log_clip, int mode,
                   float* __restrict__ w, IsPartial* __restrict__ part) {
     pdl_wait_then_release();
-    const int64_t base = (int64_t)blockIdx.x * kIsPerCta;
+    const int64_t r0 = (int64_t)blockIdx.x * per;
+    const int64_t r1 = r0 + per < n ? r0 + per : n;
     int nv = 0, nc = 0;
     float sw = 0.f, sd = 0.f;
-    if (kVec && base + kIsPerCta <= n) {
-        float4 a[4], b[4];
-        uint32_t mk[4];
+    for (int64_t base = r0; base < r1; base += kIsPerCta) {
+        if (kVec && base + kIsPerCta <= r1) {
+            float4 a[4], b[4];
+            uint32_t mk[4];
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-            const int64_t i = base + (int64_t)(g * kIsThreads + threadIdx.x) * 4;
-            a[g] = *reinterpret_cast<const float4*>(lt + i);
-            b[g] = *reinterpret_cast<const float4*>(lr + i);
-            mk[g] = mask ? *reinterpret_cast<const uint32_t*>(mask + i) : 0x01010101u;
-        }
+            for (int g = 0; g < 4; ++g) {
+                const int64_t i = base + (int64_t)(g * kIsThreads + threadIdx.x) * 4;
+                a[g] = *reinterpret_cast<const float4*>(lt + i);
+                b[g] = *reinterpret_cast<const float4*>(lr + i);
+                mk[g] = mask ? *reinterpret_cast<const uint32_t*>(mask + i) : 0x01010101u;
+            }
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-            const float x[4] = {a[g].x, a[g].y, a[g].z, a[g].w};
-            const float y[4] = {b[g].x, b[g].y, b[g].z, b[g].w};
-            float o[4];
+            for (int g = 0; g < 4; ++g) {
+                const float x[4] = {a[g].x, a[g].y, a[g].z, a[g].w};
+                const float y[4] = {b[g].x, b[g].y, b[g].z, b[g].w};
+                float o[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                o[e] = 0.f;
-                if ((mk[g] >> (8 * e)) & 0xFFu) {
-                    const float d = __fsub_rn(x[e], y[e]);
+                for (int e = 0; e < 4; ++e) {
+                    o[e] = 0.f;
+                    if ((mk[g] >> (8 * e)) & 0xFFu) {
+                        const float d = __fsub_rn(x[e], y[e]);
+                        bool clipped;
+                        o[e] = is_weight(d, log_clip, mode, clipped);
+                        nv += 1;
+                        nc += clipped;
+                        sw += o[e];
+                        sd += d;
+                    }
+                }
+                const int64_t i = base + (int64_t)(g * kIsThreads + threadIdx.x) * 4;
+                *reinterpret_cast<float4*>(w + i) = make_float4(o[0], o[1], o[2], o[3]);
+            }
+        } else {
+            for (int j = 0; j < kIsPerThread; ++j) {
+                const int64_t i = base + j * kIsThreads + threadIdx.x;
+                if (i >= r1) break;
+                float wi = 0.f;
+                if (mask == nullptr || mask[i] != 0) {
+                    const float d = __fsub_rn(lt[i], lr[i]);
                     bool clipped;
-                    o[e] = is_weight(d, log_clip, mode, clipped);
+                    wi = is_weight(d, log_clip, mode, clipped);
                     nv += 1;
                     nc += clipped;
-                    sw += o[e];
+                    sw += wi;
                     sd += d;
                 }
+                w[i] = wi;
             }
-            const int64_t i = base + (int64_t)(g * kIsThreads + threadIdx.x) * 4;
-            *reinterpret_cast<float4*>(w + i) = make_float4(o[0], o[1], o[2], o[3]);
-        }
-    } else {
-        for (int j = 0; j < kIsPerThread; ++j) {
-            const int64_t i = base + j * kIsThreads + threadIdx.x;
-            if (i >= n) break;
-            float wi = 0.f;
-            if (mask == nullptr || mask[i] != 0) {
-                const float d = __fsub_rn(lt[i], lr[i]);
-                bool clipped;
-                wi = is_weight(d, log_clip, mode, clipped);
-                nv += 1;
-                nc += clipped;
-                sw += wi;
-                sd += d;
-            }
-            w[i] = wi;
         }
     }
     // In-CTA reduction in fp32 (counts exactly, as integers): fp64 arithmetic is
@@ -152,7 +160,20 @@ rollout_is_stats_kernel(const IsPartial* __restrict__ part, int64_t P, double* _
 
 }  // namespace
 
-int64_t rollout_is_partials(int64_t n) { return (n + kIsPerCta - 1) / kIsPerCta; }
+// Partial records the workspace must hold: one per 4096 tokens at most (the
+// grid never has more CTAs than that).
+int64_t rollout_is_max_partials(int64_t n) { return (n + kIsPerCta - 1) / kIsPerCta; }
+
+// CTAs of the persistent grid: up to 4 per SM, each with at least one 4096-token step.
+int64_t rollout_is_partials(int64_t n) {
+    const int64_t steps = (n + kIsPerCta - 1) / kIsPerCta;
+    const int64_t cap = 4 * (int64_t)num_sms();
+    return steps < cap ? steps : cap;
+}
+static int64_t rollout_is_per(int64_t n, int64_t ctas) {
+    const int64_t steps = (n + kIsPerCta - 1) / kIsPerCta;
+    return ((steps + ctas - 1) / ctas) * kIsPerCta;
+}
 size_t rollout_is_partial_bytes() { return sizeof(IsPartial); }
 
 cudaError_t launch_rollout_is(const float* lt, const float* lr, const uint8_t* mask, int64_t n,
@@ -166,10 +187,11 @@ cudaError_t launch_rollout_is(const float* lt, const float* lr, const uint8_t* m
         const bool vec = ((reinterpret_cast<uintptr_t>(lt) | reinterpret_cast<uintptr_t>(lr) |
                            reinterpret_cast<uintptr_t>(w)) & 15u) == 0 &&
                          (reinterpret_cast<uintptr_t>(mask) & 3u) == 0;
+        const int64_t per = rollout_is_per(n, P);
         e = vec ? launch_pdl(rollout_is_kernel<true>, dim3((unsigned)P), dim3(kIsThreads), 0, st, lt, lr,
-                             mask, n, log_clip, mode, w, part)
+                             mask, n, per, log_clip, mode, w, part)
                 : launch_pdl(rollout_is_kernel<false>, dim3((unsigned)P), dim3(kIsThreads), 0, st, lt, lr,
-                             mask, n, log_clip, mode, w, part);
+                             mask, n, per, log_clip, mode, w, part);
         if (e != cudaSuccess) return e;
     }
     return launch_pdl(rollout_is_stats_kernel, dim3(1), dim3(1024), 0, st, (const IsPartial*)part, P,
