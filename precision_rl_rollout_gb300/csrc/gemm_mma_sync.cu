@@ -1,17 +1,15 @@
-// gemm_mma_sync.cu -- warp-level mma.sync GEMMs for the 8-bit rollout layer.
+// gemm_mma_sync.cu -- warp-level mma.sync FP8 GEMM for the one case the tcgen05
+// kernels do not take: fewer than 64 tokens with K beyond the decode kernel's
+// split range (K > 32768).
 //
 // FP8 (FP8-RL, Abstract (i)): Y = sum over 128-wide K blocks of
 //   Xs[kb][m] * Ws[nb][kb] * (Xq . Wq over the block),
 // partial sums per block from m16n8k32 e4m3 MMAs in fp32, promoted into an
 // fp32 accumulator with the block's scale product.
-// INT8 (FlashRL write-up, Fig. 1): exact s8 x s8 -> s32 MMAs over all of K, then
-// y = bf16_rn((float(acc) * Xs[m]) * Ws[n]) with two rounded multiplies.
 //
 // CTA tile: 32 tokens x 128 output channels (one weight block row), 4 warps of
 // 16 x 64.  Fragments are read straight from global memory (L1/L2 serve the
-// reuse); this is the portable warp-MMA path that the tcgen05 kernels replace
-// on the hot shapes, and the path for the INT8 GEMM, whose tcgen05 kind is not
-// available on sm_103a.
+// reuse).
 #include "common.cuh"
 #include "internal.h"
 
@@ -27,15 +25,6 @@ __device__ __forceinline__ void mma_e4m3(float (&d)[4], const uint32_t (&a)[4], 
         "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void mma_s8(int (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                       uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 "
-        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
-        : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
@@ -108,70 +97,6 @@ cudaError_t launch_gemm_fp8_mma_sync(const uint8_t* Xq, const float* Xs, const u
     dim3 grid((unsigned)(N / kBlk), (unsigned)((M + 31) / 32));
     gemm_fp8_mma_sync_kernel<<<grid, 128, 0, st>>>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy);
     return cudaGetLastError();
-}
-
-__global__ void __launch_bounds__(128)
-gemm_int8_mma_sync_kernel(const int8_t* __restrict__ Xq, const float* __restrict__ Xs,
-                          const int8_t* __restrict__ Wq, const float* __restrict__ Ws,
-                          int64_t M, int64_t N, int64_t K, uint16_t* __restrict__ Y, int64_t ldy,
-                          int32_t* __restrict__ acc_out) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, t4 = lane & 3;
-    const int64_t n_base = (int64_t)blockIdx.x * kBlk + (warp >> 1) * 64;
-    const int64_t m0 = (int64_t)blockIdx.y * 32 + (warp & 1) * 16 + g, m1 = m0 + 8;
-    const bool v0 = m0 < M, v1 = m1 < M;
-    const uint8_t* x0 = reinterpret_cast<const uint8_t*>(Xq) + (v0 ? m0 : 0) * K;
-    const uint8_t* x1 = reinterpret_cast<const uint8_t*>(Xq) + (v1 ? m1 : 0) * K;
-    const uint8_t* wq = reinterpret_cast<const uint8_t*>(Wq);
-
-    int acc[8][4];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0;
-    for (int64_t k0 = 0; k0 < K; k0 += 32) {
-        const int64_t k = k0 + t4 * 4;
-        uint32_t a[4];
-        load_a_frag(a, x0, x1, v0, v1, k);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const uint8_t* w = wq + (n_base + j * 8 + g) * K + k;
-            mma_s8(acc[j], a, ld32(w), ld32(w + 16));
-        }
-    }
-    const float xs0 = v0 ? Xs[m0] : 0.f, xs1 = v1 ? Xs[m1] : 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int64_t n = n_base + j * 8 + t4 * 2;
-        const float w0 = Ws[n], w1 = Ws[n + 1];
-        if (v0) {
-            const float y0 = __fmul_rn(__fmul_rn(__int2float_rn(acc[j][0]), xs0), w0);
-            const float y1 = __fmul_rn(__fmul_rn(__int2float_rn(acc[j][1]), xs0), w1);
-            *reinterpret_cast<uint32_t*>(Y + m0 * ldy + n) = pack_bf16x2(y0, y1);
-            if (acc_out) *reinterpret_cast<int2*>(acc_out + m0 * N + n) = make_int2(acc[j][0], acc[j][1]);
-        }
-        if (v1) {
-            const float y0 = __fmul_rn(__fmul_rn(__int2float_rn(acc[j][2]), xs1), w0);
-            const float y1 = __fmul_rn(__fmul_rn(__int2float_rn(acc[j][3]), xs1), w1);
-            *reinterpret_cast<uint32_t*>(Y + m1 * ldy + n) = pack_bf16x2(y0, y1);
-            if (acc_out) *reinterpret_cast<int2*>(acc_out + m1 * N + n) = make_int2(acc[j][2], acc[j][3]);
-        }
-    }
-}
-
-cudaError_t launch_gemm_int8_mma_sync(const int8_t* Xq, const float* Xs, const int8_t* Wq,
-                                      const float* Ws, int64_t M, int64_t N, int64_t K,
-                                      uint16_t* Y, int64_t ldy, int32_t* acc, cudaStream_t st) {
-    if (M == 0) return cudaSuccess;
-    dim3 grid((unsigned)(N / kBlk), (unsigned)((M + 31) / 32));
-    gemm_int8_mma_sync_kernel<<<grid, 128, 0, st>>>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, acc);
-    return cudaGetLastError();
-}
-
-size_t gemm_int8_workspace_bytes(int64_t, int64_t, int64_t) { return 0; }
-cudaError_t launch_gemm_int8(const int8_t* Xq, const float* Xs, const int8_t* Wq,
-                             const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
-                             int64_t ldy, int32_t* acc, void*, size_t, cudaStream_t st) {
-    if (M <= 256) return launch_gemm_int8_tc(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, acc, st);
-    return launch_gemm_int8_mma_sync(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, acc, st);
 }
 
 }  // namespace fp8rl

@@ -69,14 +69,10 @@ cudaError_t launch_gemm_fp8(const uint8_t* Xq, const float* Xs, const uint8_t* W
                             const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
                             int64_t ldy, void* ws, size_t ws_bytes, cudaStream_t st);
 
-// INT8 GEMM: exact integer arithmetic on the fp16 tensor path (tcgen05) for
-// decode-sized M, warp MMA otherwise.
+// INT8 GEMM: exact integer arithmetic on the fp16 tensor path (tcgen05).
 cudaError_t launch_gemm_int8_tc(const int8_t* Xq, const float* Xs, const int8_t* Wq, const float* Ws,
                                 int64_t M, int64_t N, int64_t K, uint16_t* Y, int64_t ldy, int32_t* acc,
                                 cudaStream_t st);
-cudaError_t launch_gemm_int8_mma_sync(const int8_t* Xq, const float* Xs, const int8_t* Wq,
-                                      const float* Ws, int64_t M, int64_t N, int64_t K,
-                                      uint16_t* Y, int64_t ldy, int32_t* acc, cudaStream_t st);
 // INT8 GEMM.
 size_t gemm_int8_workspace_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_gemm_int8(const int8_t* Xq, const float* Xs, const int8_t* Wq,

@@ -88,7 +88,8 @@ def _int8_case(M, N, K, seed_w, seed_x, rows=None):
     assert np.array_equal(got_y, want_y), f"Y differs at {np.argwhere(got_y != want_y)[:4].tolist()}"
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 128, 128), (16, 512, 256), (37, 384, 640), (300, 256, 384)])
+@pytest.mark.parametrize("M,N,K", [(1, 128, 128), (16, 512, 256), (37, 384, 640), (300, 256, 384),
+                                   (513, 256, 640), (1000, 384, 128)])
 def test_int8_gemm_small_full(cuda_lib, M, N, K):
     _int8_case(M, N, K, 300 + N, 400 + M)
 
