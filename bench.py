@@ -402,7 +402,8 @@ def extras(fb, dev, reps=5):
             X = synth.activation(M, s.K, synth.seed_for(3, 1), device=dev)
             Xq, Xs = fb.fp8rl_quant_act_group(X)
             Y = torch.empty(M, s.N, dtype=torch.bfloat16, device=dev)
-            ms = _time_graph([lambda c=c: fb.fp8rl_gemm_w8a8_block(Xq, Xs, Wqs[c], Wss[c], Y=Y)
+            gws = torch.empty(max(16, fb.fp8rl_gemm_workspace_bytes(M, s.N, s.K)), dtype=torch.uint8, device=dev)
+            ms = _time_graph([lambda c=c: fb.fp8rl_gemm_w8a8_block(Xq, Xs, Wqs[c], Wss[c], Y=Y, workspace=gws)
                               for c in range(nc)])
             aq = _time_graph([lambda: fb.fp8rl_quant_act_group(X, Xq, Xs)] * 16)
             dec[f"{s.name}_M{M}"] = {"gemm_us": ms * 1e3, "gemm_gbs": gemm_bytes(M, s.N, s.K) / (ms * 1e-3) / 1e9,

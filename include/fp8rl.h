@@ -123,8 +123,12 @@ int fp8rl_quant_act_group(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
  * HBM-bound) and prefill (large M, tensor-bound); the library picks the kernel.
  * Xq [M][K] e4m3, Xs [K/128][M] fp32, Wq [N][K] e4m3, Ws [N/128][K/128] fp32,
  * Y bf16 [M][ldy], ldy >= N, ldy % 8 == 0.  All 16-byte aligned (scales: 4).
- * workspace: device scratch of at least fp8rl_gemm_workspace_bytes(M, N, K)
- * bytes (may be NULL when that is 0).  It does not need to be zeroed and holds
+ * workspace: device scratch, 16-byte aligned, of fp8rl_gemm_workspace_bytes(M,
+ * N, K) bytes.  That is nonzero only for shapes with too few output tiles to
+ * fill the GPU but a long K (e.g. a few hundred tokens against a 27648-wide
+ * layer): the K dimension is then split and the fp32 partial tiles are added
+ * in a second launch, in a fixed order.  With less workspace (or NULL) the call
+ * still succeeds, without the split.  It does not need to be zeroed and holds
  * nothing between calls, but two calls in flight at once need two workspaces.
  * ---------------------------------------------------------------------- */
 size_t fp8rl_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
@@ -171,10 +175,11 @@ int fp8rl_gemm_w8a8_block_grouped(const uint8_t* Xq, const float* Xs, const uint
  * Wq, Ws, Y, ldy as for fp8rl_gemm_w8a8_block.
  * Xq_or_null, Xs_or_null: both NULL, or both given ([M][K] e4m3 contiguous,
  *     16-byte aligned; [K/128][M] fp32, 4-byte aligned) to receive the
- *     activation codes and scales; then no workspace is needed.
- * workspace: otherwise at least fp8rl_linear_workspace_bytes(M, N, K) bytes
- *     (the codes and scales), 16-byte aligned; no zeroing needed; calls in
- *     flight at once need their own.
+ *     activation codes and scales.
+ * workspace: at least fp8rl_linear_workspace_bytes(M, N, K) bytes, 16-byte
+ *     aligned: room for the codes and scales (unused when Xq/Xs are given)
+ *     followed by the GEMM's own workspace (see fp8rl_gemm_w8a8_block); no
+ *     zeroing needed; calls in flight at once need their own.
  * Limit: M <= 1048560 (FP8RL_ERR_UNSUPPORTED above).
  * ---------------------------------------------------------------------- */
 size_t fp8rl_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);

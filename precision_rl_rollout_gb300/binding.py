@@ -246,7 +246,7 @@ def fp8rl_linear_w8a8_block(X, Wq, Ws, Y=None, Xq=None, Xs=None, want_codes=Fals
         Xq = _need(Xq, (M, K), torch.uint8, X.device, "Xq")
         Xs = _need(Xs, (K // 128, M), torch.float32, X.device, "Xs")
     need = lib.fp8rl_linear_workspace_bytes(M, N, K)
-    if workspace is None and need and Xq is None:
+    if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=Wq.device)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _ck(lib.fp8rl_linear_w8a8_block(_p(X), ldx, _p(Wq), _p(Ws), M, N, K, _p(Y), ldy, _p(Xq), _p(Xs),

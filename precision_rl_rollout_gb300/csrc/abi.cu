@@ -105,11 +105,11 @@ int fp8rl_gemm_w8a8_block(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
     int rc = check_gemm_common(Xq, Xs, Wq, Ws, M, N, K, Y, ldy);
     if (rc) return rc;
     if (M > 65535LL * 32) return FP8RL_ERR_UNSUPPORTED;
-    const size_t need = gemm_fp8_workspace_bytes(M, N, K);
-    if (workspace_bytes < need || (need && !workspace)) return FP8RL_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return FP8RL_ERR_ALIGN;
     if (M == 0) return FP8RL_OK;
+    // less workspace than the query only gives up split-K (see the header)
     return cuda_status(launch_gemm_fp8(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, workspace,
-                                       workspace_bytes, as_stream(stream)));
+                                       workspace ? workspace_bytes : 0, as_stream(stream)));
 }
 
 int fp8rl_gemm_w8a8_block_grouped(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
@@ -146,7 +146,7 @@ int fp8rl_linear_w8a8_block(const uint16_t* X, int64_t ldx, const uint8_t* Wq, c
     if (!aligned16(Xq_or_null) || !aligned4(Xs_or_null) || !aligned16(workspace)) return FP8RL_ERR_ALIGN;
     if (M > 65535LL * 16) return FP8RL_ERR_UNSUPPORTED;
     const size_t need = fp8rl_linear_workspace_bytes(M, N, K);
-    if (!Xq_or_null && (workspace_bytes < need || (need && !workspace))) return FP8RL_ERR_WORKSPACE;
+    if (workspace_bytes < need || (need && !workspace)) return FP8RL_ERR_WORKSPACE;
     if (M == 0) return FP8RL_OK;
     return cuda_status(launch_linear_fp8(X, ldx, Wq, Ws, M, N, K, Y, ldy, Xq_or_null, Xs_or_null,
                                          workspace, as_stream(stream)));

@@ -18,6 +18,10 @@
 // moves over from warpgroup 0 (40 -> 232 registers per thread).
 // Tiles go M-fastest, so the CTAs in flight share a few 256-row weight slabs
 // and the (L2-resident) activations.
+// Split-K (shapes with fewer tiles than SMs and long K, e.g. a few hundred
+// tokens): a work unit is (tile, K range); each split writes its fp32 partial
+// tile to the caller's workspace by TMA, and a second launch adds the splits
+// of every tile in a fixed order (deterministic) and rounds to bf16.
 #include "common.cuh"
 #include "internal.h"
 #include "sm100_ptx.cuh"
@@ -54,6 +58,7 @@ struct PrefillParams {
     int64_t M, ldy;
     int KB, NB;        // K/128, N/128
     int mtiles, ntiles;
+    int split, kb_per;  // K ranges per tile and K blocks per range (split 1: no workspace)
 };
 
 __device__ __forceinline__ void record_timeout(uint32_t* err, uint32_t site, volatile int* abort) {
@@ -61,9 +66,11 @@ __device__ __forceinline__ void record_timeout(uint32_t* err, uint32_t site, vol
     *abort = 1;
 }
 
+template <bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_fp8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                        const __grid_constant__ CUtensorMap tmY, const __grid_constant__ PrefillParams p) {
+                        const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmP,
+                        const __grid_constant__ PrefillParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOffset);
@@ -72,7 +79,8 @@ gemm_fp8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_co
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
     const uint32_t tfull0 = smem_u32(bars + 2 * kStages), tempty0 = smem_u32(bars + 2 * kStages + 2);
     const uint32_t warp = warp_id(), lane = lane_id();
-    const int total_tiles = p.mtiles * p.ntiles;
+    const int split = kSplit ? p.split : 1;              // (kSplit = false: the split code is compiled out)
+    const int total_units = p.mtiles * p.ntiles * split;
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -88,6 +96,7 @@ gemm_fp8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_co
         prefetch_tmap(&tmX);
         prefetch_tmap(&tmW);
         prefetch_tmap(&tmY);
+        if (kSplit) prefetch_tmap(&tmP);
     }
     if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tc_fence_before();
@@ -103,9 +112,12 @@ gemm_fp8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_co
             // ---------------- TMA producer
             const uint64_t pol_x = policy_evict_last(), pol_w = policy_evict_first();
             uint32_t it = 0;
-            for (int tile = blockIdx.x; tile < total_tiles && !*abort; tile += gridDim.x) {
+            for (int u = blockIdx.x; u < total_units && !*abort; u += gridDim.x) {
+                const int tile = u / split, sp = u - tile * split;
                 const int mt = tile % p.mtiles, nt = tile / p.mtiles;
-                for (int kb = 0; kb < p.KB; ++kb, ++it) {
+                const int kb_beg = kSplit ? sp * p.kb_per : 0;
+                const int kb_end = kSplit ? min(p.KB, kb_beg + p.kb_per) : p.KB;
+                for (int kb = kb_beg; kb < kb_end; ++kb, ++it) {
                     const int s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1;
                     if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1, abort, kWaitLimitNs)) {
@@ -125,8 +137,10 @@ gemm_fp8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_co
             constexpr uint32_t idesc = idesc_e4m3_f32(kBM, kBN);
             const uint32_t mine = warp - 1;
             uint32_t it = 0;
-            for (int tile = blockIdx.x; tile < total_tiles && !*abort; tile += gridDim.x) {
-                for (int kb = 0; kb < p.KB; ++kb, ++it) {
+            for (int u = blockIdx.x; u < total_units && !*abort; u += gridDim.x) {
+                const int sp = u % split;
+                const int nkb = kSplit ? min(p.KB, (sp + 1) * p.kb_per) - sp * p.kb_per : p.KB;
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
                     if ((it & 1) != mine) continue;
                     const int s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1;
@@ -159,8 +173,11 @@ gemm_fp8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_co
         const int h = e >> 2;                     // column half = weight block within the tile
         const int row = 32 * q + lane;
         uint32_t it = 0;
-        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+        for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+            const int tile = u / split, sp = u - tile * split;
             const int mt = tile % p.mtiles, nt = tile / p.mtiles;
+            const int kb_beg = kSplit ? sp * p.kb_per : 0;
+            const int kb_end = kSplit ? min(p.KB, kb_beg + p.kb_per) : p.KB;
             const int64_t m = (int64_t)mt * kBM + row;
             const int nb = 2 * nt + h;
             const bool live = m < p.M && nb < p.NB;
@@ -169,11 +186,11 @@ gemm_fp8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_co
             float acc[128];
 #pragma unroll
             for (int j = 0; j < 128; ++j) acc[j] = 0.f;
-            float sx = live ? __ldg(xs) : 0.f, sw = live ? __ldg(ws) : 0.f;
+            float sx = live ? __ldg(xs + (int64_t)kb_beg * p.M) : 0.f, sw = live ? __ldg(ws + kb_beg) : 0.f;
             bool ok = true;
-            for (int kb = 0; kb < p.KB; ++kb, ++it) {
+            for (int kb = kb_beg; kb < kb_end; ++kb, ++it) {
                 const float scale = sx * sw;
-                if (kb + 1 < p.KB && live) {                  // next block's scales, early
+                if (kb + 1 < kb_end && live) {                // next block's scales, early
                     sx = __ldg(xs + (int64_t)(kb + 1) * p.M);
                     sw = __ldg(ws + kb + 1);
                 }
@@ -203,6 +220,31 @@ gemm_fp8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_co
                 for (int j = 0; j < 64; ++j) acc[64 + j] = fmaf(__uint_as_float(r[j]), scale, acc[64 + j]);
             }
             if (!ok) break;
+            if constexpr (kSplit) {
+                // fp32 partial of this K range: the warp's 32 rows x 128 columns as
+                // four 32 x 32 boxes (128-byte rows, 128-byte swizzle) into the
+                // workspace's slot (tile, sp), rows slot*128 .. +127
+                uint8_t* stage = smem + kOutOffset + e * kOutBytesPerWarp;
+                const int slot_row = (tile * split + sp) * kBM + 32 * q;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    if (lane == 0) bulk_wait_read_all();   // the previous box has left the buffer
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float* a = acc + c * 32 + 4 * j;
+                        *reinterpret_cast<float4*>(stage + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                            make_float4(a[0], a[1], a[2], a[3]);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmP, smem_u32(stage), h * 128 + c * 32, slot_row);
+                        bulk_commit();
+                    }
+                }
+                continue;
+            }
             // Output: the warp's 32 rows x 128 columns go out as two 32 x 64 boxes,
             // each staged in this warp's 4 KB buffer with the 128-byte swizzle
             // and written by one asynchronous TMA store (rows beyond M and
@@ -243,69 +285,153 @@ gemm_fp8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_co
     }
 }
 
+// Split-K reduction: one thread per (tile row, 8 output columns); the splits
+// are added in order in fp32, then rounded to bf16 once.
+__global__ void __launch_bounds__(256)
+prefill_splitk_reduce_kernel(const float* __restrict__ part, int64_t M, int64_t N, int mtiles, int split,
+                             int64_t units8, uint16_t* __restrict__ Y, int64_t ldy) {
+    pdl_wait_then_release();
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= units8) return;
+    const int64_t tile = t >> 12;                     // 128 rows x 32 eight-column chunks per tile
+    const int r = (int)((t >> 5) & 127), c8 = (int)(t & 31);
+    const int mt = (int)(tile % mtiles), nt = (int)(tile / mtiles);
+    const int64_t m = (int64_t)mt * kBM + r, n = (int64_t)nt * kBN + c8 * 8;
+    if (m >= M || n >= N) return;
+    float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int sp = 0; sp < split; ++sp) {
+        const float4* src = reinterpret_cast<const float4*>(part + ((tile * split + sp) * kBM + r) * kBN + c8 * 8);
+        const float4 a = src[0], b = src[1];
+        s[0] += a.x; s[1] += a.y; s[2] += a.z; s[3] += a.w;
+        s[4] += b.x; s[5] += b.y; s[6] += b.z; s[7] += b.w;
+    }
+    uint4 o;
+    o.x = pack_bf16x2(s[0], s[1]);
+    o.y = pack_bf16x2(s[2], s[3]);
+    o.z = pack_bf16x2(s[4], s[5]);
+    o.w = pack_bf16x2(s[6], s[7]);
+    *reinterpret_cast<uint4*>(Y + m * ldy + n) = o;
+}
+
 }  // namespace
+
+// K ranges per tile: when the tiles cannot fill the GPU, split K so that about
+// one wave of CTAs runs, keeping at least 8 K blocks per range.
+static int prefill_split(int64_t M, int64_t N, int64_t K) {
+    const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
+    const int sms = num_sms();
+    if (tiles * 4 >= (int64_t)sms * 3) return 1;
+    int s = (int)(sms / tiles);
+    const int kb = (int)(K / 128);
+    if (s > kb / 8) s = kb / 8;
+    if (s > 8) s = 8;
+    return s < 1 ? 1 : s;
+}
+
+static size_t prefill_ws_bytes(int64_t M, int64_t N, int64_t K, int split) {
+    if (split <= 1) return 0;
+    const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
+    return (size_t)tiles * (size_t)split * kBM * kBN * sizeof(float);
+}
+
+// The register split (setmaxnreg) assumes the kernel was built with exactly
+// kLaunchRegs registers per thread; anything else could make the epilogue's
+// increase wait forever, so such a build is refused.  Checked (and the shared
+// memory attribute set) once per device.
+template <bool kSplit>
+static int prefill_ready(int dev) {
+    static int checked[64] = {};   // 0 unknown, 1 ok, -1 refused
+    if (checked[dev] == 0) {
+        cudaFuncAttributes fa;
+        checked[dev] = (cudaFuncGetAttributes(&fa, gemm_fp8_prefill_kernel<kSplit>) == cudaSuccess &&
+                        fa.numRegs == kLaunchRegs &&
+                        cudaFuncSetAttribute(gemm_fp8_prefill_kernel<kSplit>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) == cudaSuccess)
+                           ? 1
+                           : -1;
+    }
+    return checked[dev];
+}
 
 cudaError_t launch_gemm_fp8_prefill(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
                                     const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
-                                    int64_t ldy, cudaStream_t st) {
-    // The register split (setmaxnreg) assumes the kernel was built with exactly
-    // kLaunchRegs registers per thread; anything else could make the epilogue's
-    // increase wait forever, so refuse to launch.
-    static int checked = 0;   // 0 unknown, 1 ok, -1 refused
-    if (checked == 0) {
-        cudaFuncAttributes fa;
-        if (cudaFuncGetAttributes(&fa, gemm_fp8_prefill_kernel) != cudaSuccess) return cudaErrorInvalidValue;
-        checked = (fa.numRegs == kLaunchRegs) ? 1 : -1;
-        if (checked == 1 &&
-            cudaFuncSetAttribute(gemm_fp8_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes) != cudaSuccess)
-            checked = -1;
-    }
-    if (checked != 1) return cudaErrorInvalidDeviceFunction;
-    CUtensorMap tmX, tmW, tmY;
+                                    int64_t ldy, void* ws, size_t ws_bytes, cudaStream_t st) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (prefill_ready<false>(dev) != 1 || prefill_ready<true>(dev) != 1) return cudaErrorInvalidDeviceFunction;
+    int split = prefill_split(M, N, K);
+    // with less workspace than the split needs, run without split-K
+    if (split > 1 && (ws == nullptr || ws_bytes < prefill_ws_bytes(M, N, K, split))) split = 1;
+    CUtensorMap tmX, tmW, tmY, tmP;
     if (!make_tmap_u8(&tmX, Xq, (uint64_t)M, (uint64_t)K, (uint64_t)K, kBM)) return cudaErrorInvalidValue;
     if (!make_tmap_u8(&tmW, Wq, (uint64_t)N, (uint64_t)K, (uint64_t)K, kBN)) return cudaErrorInvalidValue;
     if (!make_tmap_bf16_store(&tmY, Y, (uint64_t)M, (uint64_t)N, (uint64_t)ldy, 64, 32)) return cudaErrorInvalidValue;
     uint32_t* err = device_error_word();
     if (!err) return cudaErrorInvalidValue;
-    PrefillParams prm{err, Xs, Ws, Y, M, ldy, (int)(K / 128), (int)(N / 128),
-                      (int)((M + kBM - 1) / kBM), (int)((N + kBN - 1) / kBN)};
-    const int tiles = prm.mtiles * prm.ntiles;
-    const int grid = tiles < num_sms() ? tiles : num_sms();
-    return launch_pdl(gemm_fp8_prefill_kernel, dim3(grid), dim3(kThreads), kSmemBytes, st, tmX, tmW, tmY, prm);
+    const int KB = (int)(K / 128);
+    PrefillParams prm{err, Xs, Ws, Y, M, ldy, KB, (int)(N / 128),
+                      (int)((M + kBM - 1) / kBM), (int)((N + kBN - 1) / kBN), split, (KB + split - 1) / split};
+    const int64_t tiles = (int64_t)prm.mtiles * prm.ntiles;
+    if (split > 1) {
+        if (!make_tmap_f32_store(&tmP, ws, (uint64_t)(tiles * split * kBM), (uint64_t)kBN, (uint64_t)kBN, 32, 32))
+            return cudaErrorInvalidValue;
+    } else {
+        tmP = tmY;                                   // not used
+    }
+    const int64_t units = tiles * split;
+    const int grid = units < num_sms() ? (int)units : num_sms();
+    cudaError_t e = split > 1 ? launch_pdl(gemm_fp8_prefill_kernel<true>, dim3(grid), dim3(kThreads), kSmemBytes,
+                                           st, tmX, tmW, tmY, tmP, prm)
+                              : launch_pdl(gemm_fp8_prefill_kernel<false>, dim3(grid), dim3(kThreads), kSmemBytes,
+                                           st, tmX, tmW, tmY, tmP, prm);
+    if (e != cudaSuccess || split == 1) return e;
+    const int64_t units8 = tiles * kBM * 32;
+    return launch_pdl(prefill_splitk_reduce_kernel, dim3((unsigned)((units8 + 255) / 256)), dim3(256), 0, st,
+                      (const float*)ws, M, N, prm.mtiles, split, units8, Y, ldy);
 }
 
-size_t gemm_fp8_workspace_bytes(int64_t, int64_t, int64_t) { return 0; }
+// The dispatch below takes the prefill kernel for this shape (same rule).
+static bool takes_prefill(int64_t M, int64_t N, int64_t K);
+
+size_t gemm_fp8_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    if (M <= 0 || !takes_prefill(M, N, K)) return 0;
+    return prefill_ws_bytes(M, N, K, prefill_split(M, N, K));
+}
 
 // Estimated prefill-kernel time in microseconds: a fixed 3 us plus the larger of
-// the tensor-core time (waves of 128x256 tiles, 0.55 us per 128-wide K block)
-// and the HBM time at 5.5 TB/s; fitted to GB300 measurements of the
-// Qwen2.5-7B/32B shapes at M = 32..256 (4.5% mean error).
+// the tensor-core time (waves of 128x256 work units, about 0.5 us per 128-wide K
+// block) and the HBM time at 5.5 TB/s, plus, with split-K, the partial tiles'
+// round trip through L2 and the reduction launch.
 static double prefill_cost_us(int64_t M, int64_t N, int64_t K) {
     const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
-    const int64_t waves = (tiles + num_sms() - 1) / num_sms();
-    const double compute = (double)waves * (double)(K / 128) * 0.55;
+    const int split = prefill_split(M, N, K);
+    const int64_t kb = (K / 128 + split - 1) / split;
+    const int64_t waves = (tiles * split + num_sms() - 1) / num_sms();
+    const double compute = (double)waves * (double)kb * 0.5;
     const double memory = (double)(N * K + M * K + 2 * M * N) / 5.5e6;
-    return 3.0 + (compute > memory ? compute : memory);
+    const double reduce = split > 1 ? 3.0 + (double)prefill_ws_bytes(M, N, K, split) / 3e6 : 0.0;
+    return 3.0 + (compute > memory ? compute : memory) + reduce;
 }
 
 // Up to 256 tokens both tcgen05 kernels apply: the split-K weight-streaming
 // decode kernel wins for few, deep weight slabs, the 128x256-tile kernel once
-// there are enough tiles to fill the GPU; the cheaper estimate is taken.  The
-// warp-MMA kernel covers small-M shapes whose K exceeds the decode kernel's
-// split limit when the tile kernel is not cheaper.
+// there are enough tiles (or enough K to split) to fill the GPU; the cheaper
+// estimate is taken.  The warp-MMA kernel covers small-M shapes whose K exceeds
+// the decode kernel's split limit.
+static bool takes_prefill(int64_t M, int64_t N, int64_t K) {
+    if (M > 256) return true;
+    if (decode_supported(K)) return prefill_cost_us(M, N, K) < decode_cost_us(M, N, K);
+    return M >= 64;
+}
+
 cudaError_t launch_gemm_fp8(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
                             const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
-                            int64_t ldy, void*, size_t, cudaStream_t st) {
-    if (M <= 256) {
-        if (decode_supported(K)) {
-            if (decode_cost_us(M, N, K) <= prefill_cost_us(M, N, K))
-                return launch_gemm_fp8_decode(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
-        } else if (M < 64) {
-            return launch_gemm_fp8_mma_sync(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
-        }
+                            int64_t ldy, void* ws, size_t ws_bytes, cudaStream_t st) {
+    if (!takes_prefill(M, N, K)) {
+        if (decode_supported(K)) return launch_gemm_fp8_decode(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
+        return launch_gemm_fp8_mma_sync(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
     }
-    return launch_gemm_fp8_prefill(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
+    return launch_gemm_fp8_prefill(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, ws, ws_bytes, st);
 }
 
 }  // namespace fp8rl

@@ -452,10 +452,14 @@ cudaError_t launch_gemm_fp8_grouped(const uint8_t* Xq, const float* Xs, const ui
 
 size_t linear_codes_bytes(int64_t M, int64_t K) { return ((size_t)M * (size_t)K + 255) & ~(size_t)255; }
 
+static size_t linear_codes_and_scales_bytes(int64_t M, int64_t K) {
+    return linear_codes_bytes(M, K) + (((size_t)M * (size_t)(K / 128) * 4 + 255) & ~(size_t)255);
+}
+
+// [codes | scales | the GEMM's workspace], each part 256-byte aligned
 size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-    (void)N;
     if (M <= 0) return 0;
-    return linear_codes_bytes(M, K) + (size_t)M * (size_t)(K / 128) * 4;
+    return linear_codes_and_scales_bytes(M, K) + gemm_fp8_workspace_bytes(M, N, K);
 }
 
 // The activation quantizer releases its dependent at launch, so the GEMM's
@@ -464,11 +468,14 @@ size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K) {
 cudaError_t launch_linear_fp8(const uint16_t* X, int64_t ldx, const uint8_t* Wq, const float* Ws, int64_t M,
                               int64_t N, int64_t K, uint16_t* Y, int64_t ldy, uint8_t* Xq_out,
                               float* Xs_out, void* ws, cudaStream_t st) {
-    uint8_t* Xq = Xq_out ? Xq_out : static_cast<uint8_t*>(ws);
-    float* Xs = Xs_out ? Xs_out : reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + linear_codes_bytes(M, K));
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    uint8_t* Xq = Xq_out ? Xq_out : base;
+    float* Xs = Xs_out ? Xs_out : reinterpret_cast<float*>(base + linear_codes_bytes(M, K));
     cudaError_t e = launch_quant_act_group(X, M, K, ldx, Xq, Xs, st);
     if (e != cudaSuccess) return e;
-    return launch_gemm_fp8(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, nullptr, 0, st);
+    const size_t g = gemm_fp8_workspace_bytes(M, N, K);
+    void* gws = (base && g) ? base + linear_codes_and_scales_bytes(M, K) : nullptr;
+    return launch_gemm_fp8(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, gws, gws ? g : 0, st);
 }
 
 }  // namespace fp8rl

@@ -100,11 +100,15 @@ bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols
 // stores of box_cols x box_rows boxes with the 128-byte swizzle (box_cols = 64).
 bool make_tmap_bf16_store(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
                           uint64_t pitch_elems, uint32_t box_cols, uint32_t box_rows);
+// TMA map of a row-major fp32 matrix [rows][cols] (row pitch in elements) for
+// stores of box_cols x box_rows boxes with the 128-byte swizzle (box_cols = 32).
+bool make_tmap_f32_store(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                         uint64_t pitch_elems, uint32_t box_cols, uint32_t box_rows);
 int num_sms();
 bool decode_supported(int64_t K);
 double decode_cost_us(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_gemm_fp8_prefill(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
                                     const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
-                                    int64_t ldy, cudaStream_t st);
+                                    int64_t ldy, void* ws, size_t ws_bytes, cudaStream_t st);
 
 }  // namespace fp8rl

@@ -57,6 +57,20 @@ bool make_tmap_bf16_store(CUtensorMap* m, const void* base, uint64_t rows, uint6
     return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_f32_store(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                         uint64_t pitch_elems, uint32_t box_cols, uint32_t box_rows) {
+    auto enc = get_encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {pitch_elems * 4};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int num_sms() {
     static int cache[kMaxDevices] = {0};
     int dev = 0;

@@ -31,9 +31,26 @@ def _fp8_case(M, N, K, seed_w, seed_x, rows=None, what=""):
 @pytest.mark.parametrize("M,N,K", [(16, 512, 256), (1, 128, 128), (5, 256, 384), (37, 384, 640),
                                    (64, 256, 1024), (129, 128, 256), (256, 640, 512), (257, 384, 128),
                                    (300, 384, 384), (1000, 768, 1280), (512, 256, 128), (700, 640, 384),
-                                   (1537, 1152, 640)])
+                                   (1537, 1152, 640),
+                                   # few tiles, long K: split-K with the fp32 partials in the workspace
+                                   (300, 256, 4096), (520, 512, 8192), (260, 384, 2048)])
 def test_fp8_gemm_small_full(cuda_lib, M, N, K):
     _fp8_case(M, N, K, 100 + N + K, 200 + M + K)
+
+
+def test_fp8_gemm_split_k_without_workspace_matches(cuda_lib):
+    # a split-K shape run with and without the workspace it asks for: both
+    # within tolerance of the oracle (the call without it gives up the split)
+    M, N, K = 300, 256, 4096
+    assert fb.fp8rl_gemm_workspace_bytes(M, N, K) > 0
+    Wq, Ws = oracle_fp8_weight(N, K, 91)
+    Xq, Xs = oracle_fp8_act(M, K, 92)
+    ref = oracle.fp8_gemm(Xq, Xs, Wq, Ws)
+    Y1 = fb.fp8rl_gemm_w8a8_block(dev(Xq), dev(Xs), dev(Wq), dev(Ws))
+    Y2 = fb.fp8rl_gemm_w8a8_block(dev(Xq), dev(Xs), dev(Wq), dev(Ws),
+                                  workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
+    assert_fp8_gemm_close(host(Y1), ref, "split-K")
+    assert_fp8_gemm_close(host(Y2), ref, "no split")
 
 
 def test_fp8_gemm_tiny_config(cuda_lib):
