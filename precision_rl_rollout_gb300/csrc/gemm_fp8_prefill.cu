@@ -394,7 +394,8 @@ cudaError_t launch_gemm_fp8_prefill(const uint8_t* Xq, const float* Xs, const ui
 static bool takes_prefill(int64_t M, int64_t N, int64_t K);
 
 size_t gemm_fp8_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-    if (M <= 0 || !takes_prefill(M, N, K)) return 0;
+    if (M <= 0) return 0;
+    if (!takes_prefill(M, N, K)) return decode_workspace_bytes(M, N, K);
     return prefill_ws_bytes(M, N, K, prefill_split(M, N, K));
 }
 
@@ -428,7 +429,7 @@ cudaError_t launch_gemm_fp8(const uint8_t* Xq, const float* Xs, const uint8_t* W
                             const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
                             int64_t ldy, void* ws, size_t ws_bytes, cudaStream_t st) {
     if (!takes_prefill(M, N, K)) {
-        if (decode_supported(K)) return launch_gemm_fp8_decode(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
+        if (decode_supported(K)) return launch_gemm_fp8_decode(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, ws, ws_bytes, st);
         return launch_gemm_fp8_mma_sync(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
     }
     return launch_gemm_fp8_prefill(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, ws, ws_bytes, st);

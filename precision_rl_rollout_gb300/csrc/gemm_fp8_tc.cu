@@ -60,6 +60,9 @@ struct DecodeParams {
     const int32_t* offs;   // [E+1] first token row of each expert, device memory
     int ntiles;            // 128-row weight slabs per expert (N / 128)
     int64_t tok_bound;     // token rows per expert the grid covers (M tiles * MT)
+    // split-K without a cluster: fp32 partial tiles [slabs * M tiles * split][MT][128]
+    // for a second launch to add (nullptr: the split CTAs form a cluster)
+    float* part;
 };
 
 template <int MT>
@@ -282,8 +285,28 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
 
     // ---------------- split-K reduction over the cluster, then bf16 stores
     tc_fence_before();
-    if (p.split > 1) cluster_sync_all(); else __syncthreads();
-    {
+    const bool in_cluster = p.split > 1 && p.part == nullptr;
+    // self-check: the launch shape this reduction relies on (a cluster of
+    // exactly `split` CTAs, ranked by blockIdx.x); a mismatch is recorded and
+    // the distributed-shared-memory reads are skipped
+    const bool shape_ok = gridDim.x == (unsigned)p.split &&
+                          (!in_cluster || (cluster_nctarank() == (uint32_t)p.split &&
+                                           cluster_ctarank() == (uint32_t)split_idx));
+    if (!shape_ok && threadIdx.x == 0) atomicCAS(p.err, 0u, (kKernelDecode << 24) | (8u << 16) | 2u);
+    const int64_t ncols = (int64_t)(p.offs ? p.ntiles : (int)gridDim.z) * 128;   // output columns
+    if (p.part != nullptr) {
+        // no cluster: this CTA's partial rows go to its workspace slot (coalesced
+        // 16-byte stores of red[m][0..127]); the reduction launch adds the slots
+        __syncthreads();
+        const int valid_m = rows <= 0 ? 0 : (int)(rows < MT ? rows : MT);
+        float4* dst = reinterpret_cast<float4*>(
+            p.part + (((int64_t)z * gridDim.y + mt) * p.split + split_idx) * (MT * 128));
+        const float4* src = reinterpret_cast<const float4*>(smem);
+        if (shape_ok)
+            for (int i = threadIdx.x; i < valid_m * 32; i += C::kThreads) dst[i] = src[i];
+    } else {
+    if (in_cluster) cluster_sync_all(); else __syncthreads();
+    if (shape_ok) {
         const int64_t m_tile0 = row0;
         const int valid_m = rows <= 0 ? 0 : (int)(rows < MT ? rows : MT);
         const int total = valid_m * 16;                   // chunks of 8 output channels
@@ -294,7 +317,7 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
             const int m = c >> 4, n8 = c & 15;
             const uint32_t off = (uint32_t)(m * 128 + n8 * 8) * 4u;
             float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            if (p.split > 1) {
+            if (in_cluster) {
                 // every rank's loads are in flight before the first add: one
                 // distributed-shared-memory round trip per chunk, not one per rank
                 float4 v[C::kMaxSplit][2];
@@ -322,14 +345,49 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
             o.y = pack_bf16x2(s[2], s[3]);
             o.z = pack_bf16x2(s[4], s[5]);
             o.w = pack_bf16x2(s[6], s[7]);
-            *reinterpret_cast<uint4*>(p.Y + (m_tile0 + m) * p.ldy + (int64_t)nt * 128 + n8 * 8) = o;
+            const int64_t col = (int64_t)nt * 128 + n8 * 8;
+            if (m_tile0 + m < p.M && col + 8 <= ncols)        // self-check of the output index
+                *reinterpret_cast<uint4*>(p.Y + (m_tile0 + m) * p.ldy + col) = o;
+            else
+                atomicCAS(p.err, 0u, (kKernelDecode << 24) | (9u << 16) | 2u);
         }
     }
-    if (p.split > 1) cluster_sync_all(); else __syncthreads();
+    }
+    if (in_cluster) cluster_sync_all(); else __syncthreads();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, C::kTmemCols);
     }
+}
+
+// Split-K without a cluster: one thread per (slab, token row, 8 channels) adds
+// the split partials in order and rounds to bf16 once.
+template <int MT>
+__global__ void __launch_bounds__(256)
+decode_splitk_reduce_kernel(const float* __restrict__ part, int64_t M, int mtiles, int split, int64_t units,
+                            uint16_t* __restrict__ Y, int64_t ldy) {
+    pdl_wait_then_release();
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= units) return;
+    const int64_t tile = t / (MT * 16);
+    const int rem = (int)(t - tile * (MT * 16));
+    const int m = rem >> 4, c8 = rem & 15;
+    const int64_t z = tile / mtiles, mt = tile - z * mtiles;
+    const int64_t row = mt * MT + m;
+    if (row >= M) return;
+    float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int sp = 0; sp < split; ++sp) {
+        const float4* src = reinterpret_cast<const float4*>(part + ((tile * split + sp) * MT + m) * 128 + c8 * 8);
+        const float4 a = src[0], b = src[1];
+        s[0] += a.x; s[1] += a.y; s[2] += a.z; s[3] += a.w;
+        s[4] += b.x; s[5] += b.y; s[6] += b.z; s[7] += b.w;
+    }
+    uint4 o;
+    o.x = pack_bf16x2(s[0], s[1]);
+    o.y = pack_bf16x2(s[2], s[3]);
+    o.z = pack_bf16x2(s[4], s[5]);
+    o.w = pack_bf16x2(s[6], s[7]);
+    *reinterpret_cast<uint4*>(Y + row * ldy + z * 128 + c8 * 8) = o;
 }
 
 // Split-K factor for `tiles` weight slabs of KB blocks and a token tile of MT.
@@ -375,14 +433,100 @@ double decode_cost_us(int64_t M, int64_t N, int64_t K) {
     return 0.8 * c;
 }
 
+template <int MT>
+static cudaError_t set_decode_smem(int dev) {
+    static bool attr_set[64] = {};     // the attribute belongs to the device
+    if (!attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_fp8_decode_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             DecodeCfg<MT>::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    return cudaSuccess;
+}
+
+// Clusters of `split` CTAs of this kernel that can run at once on the device
+// (the occupancy API counts one CTA of a cluster per SM; this kernel fits
+// kMinBlocks per SM, so that many times more run).  0 if unknown.
+template <int MT>
+static int64_t clusters_per_wave(int split) {
+    static int cache[64][9] = {};      // device x split; -1: unknown
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || split < 1 || split > 8) return 0;
+    if (cache[dev][split] == 0) {
+        int n = -1;
+        if (set_decode_smem<MT>(dev) == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)split, 1, 1024);
+            cfg.blockDim = dim3(DecodeCfg<MT>::kThreads);
+            cfg.dynamicSmemBytes = DecodeCfg<MT>::kSmemBytes;
+            cudaLaunchAttribute a[1];
+            a[0].id = cudaLaunchAttributeClusterDimension;
+            a[0].val.clusterDim.x = (unsigned)split;
+            a[0].val.clusterDim.y = 1;
+            a[0].val.clusterDim.z = 1;
+            cfg.attrs = a;
+            cfg.numAttrs = 1;
+            int c = 0;
+            if (cudaOccupancyMaxActiveClusters(&c, gemm_fp8_decode_kernel<MT>, &cfg) == cudaSuccess && c > 0) n = c;
+        }
+        cudaGetLastError();            // a failed query leaves no sticky error
+        cache[dev][split] = n;
+    }
+    return cache[dev][split] > 0 ? (int64_t)cache[dev][split] * DecodeCfg<MT>::kMinBlocks : 0;
+}
+
+// Split-K plan of the dense decode GEMM.  The cluster plan comes from the cost
+// model; when its clusters cannot all run at once (long K on few slabs: the
+// 27648-wide down projection), the split CTAs run without a cluster instead,
+// as many per slab as one wave holds, and add their partials through the
+// workspace in a second launch.
+struct DecodePlan {
+    int split;
+    bool global;
+};
+
+template <int MT>
+static DecodePlan decode_plan(int64_t tiles, int KB) {
+    using C = DecodeCfg<MT>;
+    DecodePlan pl{choose_split(tiles, KB, MT, C::kMaxKbPerSplit), false};
+    if (pl.split > 1) {
+        const int64_t cpw = clusters_per_wave<MT>(pl.split);
+        if (cpw > 0 && tiles > cpw) {
+            const int64_t slots = (int64_t)num_sms() * C::kMinBlocks;
+            int gs = (int)(slots / tiles);
+            if (gs > 16) gs = 16;
+            if (gs >= 2 && (KB + gs - 1) / gs <= C::kMaxKbPerSplit && (int64_t)(gs - 1) * ((KB + gs - 1) / gs) < KB)
+                pl = DecodePlan{gs, true};
+        }
+    }
+    return pl;
+}
+
+template <int MT>
+static size_t decode_ws_bytes_mt(int64_t M, int64_t N, int64_t K) {
+    const int64_t mtiles = (M + MT - 1) / MT, tiles = (N / 128) * mtiles;
+    const DecodePlan pl = decode_plan<MT>(tiles, (int)(K / 128));
+    return pl.global ? (size_t)tiles * pl.split * MT * 128 * sizeof(float) : 0;
+}
+
+size_t decode_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    if (M <= 0 || !decode_supported(K)) return 0;
+    if (M <= 16) return decode_ws_bytes_mt<16>(M, N, K);
+    if (M <= 32) return decode_ws_bytes_mt<32>(M, N, K);
+    if (M <= 64) return decode_ws_bytes_mt<64>(M, N, K);
+    return decode_ws_bytes_mt<128>(M, N, K);
+}
+
 // M: token rows (all experts together in the grouped form); rows_per_group:
 // the token rows one weight matrix may have (M, or the per-expert bound);
-// groups: experts (1 for the dense GEMM, offs == nullptr).
+// groups: experts (1 for the dense GEMM, offs == nullptr).  ws: workspace for
+// split-K without a cluster (dense form only; may be too small or NULL).
 template <int MT>
 static cudaError_t launch_decode_mt(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
                                     const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
                                     int64_t ldy, const int32_t* offs, int64_t groups, int64_t rows_per_group,
-                                    cudaStream_t st) {
+                                    void* ws, size_t ws_bytes, cudaStream_t st) {
     using C = DecodeCfg<MT>;
     CUtensorMap tmW, tmX;
     if (!make_tmap_u8(&tmW, Wq, (uint64_t)(groups * N), (uint64_t)K, (uint64_t)K, 128)) return cudaErrorInvalidValue;
@@ -390,62 +534,65 @@ static cudaError_t launch_decode_mt(const uint8_t* Xq, const float* Xs, const ui
     const int KB = (int)(K / 128);
     const int64_t mtiles = (rows_per_group + MT - 1) / MT;
     const int64_t tiles = groups * (N / 128) * mtiles;
-    int split = choose_split(tiles, KB, MT, C::kMaxKbPerSplit);
-    int per = (KB + split - 1) / split;
+    DecodePlan pl = offs ? DecodePlan{choose_split(tiles, KB, MT, C::kMaxKbPerSplit), false}
+                         : decode_plan<MT>(tiles, KB);
+    if (pl.global && (ws == nullptr || ws_bytes < (size_t)tiles * pl.split * MT * 128 * sizeof(float)))
+        pl = DecodePlan{choose_split(tiles, KB, MT, C::kMaxKbPerSplit), false};
+    const int split = pl.split;
+    const int per = (KB + split - 1) / split;
     if (per > C::kMaxKbPerSplit) return cudaErrorInvalidValue;
     uint32_t* err = device_error_word();
     if (!err) return cudaErrorInvalidValue;
-    DecodeParams prm{err, Xs, Ws, Y, M, ldy, KB, per, split, offs, (int)(N / 128), mtiles * MT};
-
-    auto kern = gemm_fp8_decode_kernel<MT>;
-    static bool attr_set[64] = {};     // the attribute belongs to the current device
+    DecodeParams prm{err, Xs, Ws, Y, M, ldy, KB, per, split, offs, (int)(N / 128), mtiles * MT,
+                     pl.global ? static_cast<float*>(ws) : nullptr};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
-    }
+    e = set_decode_smem<MT>(dev);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)split, (unsigned)mtiles, (unsigned)(groups * (N / 128)));
     cfg.blockDim = dim3(C::kThreads);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)split;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)split;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kern, tmW, tmX, prm);
+    cfg.numAttrs = pl.global ? 1 : 2;
+    e = cudaLaunchKernelEx(&cfg, gemm_fp8_decode_kernel<MT>, tmW, tmX, prm);
+    if (e != cudaSuccess || !pl.global) return e;
+    const int64_t units = tiles * MT * 16;
+    return launch_pdl(decode_splitk_reduce_kernel<MT>, dim3((unsigned)((units + 255) / 256)), dim3(256), 0, st,
+                      (const float*)ws, M, (int)mtiles, split, units, Y, ldy);
 }
 
 bool decode_supported(int64_t K) { return K / 128 <= 8 * DecodeCfg<16>::kMaxKbPerSplit; }
 
 cudaError_t launch_gemm_fp8_decode(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
                                    const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
-                                   int64_t ldy, cudaStream_t st) {
-    if (M <= 16) return launch_decode_mt<16>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, nullptr, 1, M, st);
-    if (M <= 32) return launch_decode_mt<32>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, nullptr, 1, M, st);
-    if (M <= 64) return launch_decode_mt<64>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, nullptr, 1, M, st);
-    return launch_decode_mt<128>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, nullptr, 1, M, st);
+                                   int64_t ldy, void* ws, size_t ws_bytes, cudaStream_t st) {
+    if (M <= 16) return launch_decode_mt<16>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, nullptr, 1, M, ws, ws_bytes, st);
+    if (M <= 32) return launch_decode_mt<32>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, nullptr, 1, M, ws, ws_bytes, st);
+    if (M <= 64) return launch_decode_mt<64>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, nullptr, 1, M, ws, ws_bytes, st);
+    return launch_decode_mt<128>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, nullptr, 1, M, ws, ws_bytes, st);
 }
 
 cudaError_t launch_gemm_fp8_grouped(const uint8_t* Xq, const float* Xs, const uint8_t* Wq, const float* Ws,
                                     const int32_t* offs, int64_t E, int64_t T, int64_t N, int64_t K,
                                     int64_t max_rows, uint16_t* Y, int64_t ldy, cudaStream_t st) {
     if (max_rows <= 16)
-        return launch_decode_mt<16>(Xq, Xs, Wq, Ws, T, N, K, Y, ldy, offs, E, max_rows, st);
+        return launch_decode_mt<16>(Xq, Xs, Wq, Ws, T, N, K, Y, ldy, offs, E, max_rows, nullptr, 0, st);
     if (max_rows <= 32)
-        return launch_decode_mt<32>(Xq, Xs, Wq, Ws, T, N, K, Y, ldy, offs, E, max_rows, st);
+        return launch_decode_mt<32>(Xq, Xs, Wq, Ws, T, N, K, Y, ldy, offs, E, max_rows, nullptr, 0, st);
     if (max_rows <= 64)
-        return launch_decode_mt<64>(Xq, Xs, Wq, Ws, T, N, K, Y, ldy, offs, E, max_rows, st);
-    return launch_decode_mt<128>(Xq, Xs, Wq, Ws, T, N, K, Y, ldy, offs, E, max_rows, st);
+        return launch_decode_mt<64>(Xq, Xs, Wq, Ws, T, N, K, Y, ldy, offs, E, max_rows, nullptr, 0, st);
+    return launch_decode_mt<128>(Xq, Xs, Wq, Ws, T, N, K, Y, ldy, offs, E, max_rows, nullptr, 0, st);
 }
 
 // ------------------------------------------------------------------ linear layer

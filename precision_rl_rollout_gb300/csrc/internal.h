@@ -55,7 +55,8 @@ cudaError_t launch_logits_kl(const uint16_t* P, int64_t ldp, const uint16_t* Q, 
 // FP8 block-scaled GEMM: dispatch by M (tcgen05 decode kernel for M <= 256).
 cudaError_t launch_gemm_fp8_decode(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
                                    const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
-                                   int64_t ldy, cudaStream_t st);
+                                   int64_t ldy, void* ws, size_t ws_bytes, cudaStream_t st);
+size_t decode_workspace_bytes(int64_t M, int64_t N, int64_t K);
 // Grouped (mixture-of-experts) form of the decode kernel: experts' weights
 // stacked [E*N][K], token rows grouped by expert at offs[0..E] (device).
 cudaError_t launch_gemm_fp8_grouped(const uint8_t* Xq, const float* Xs, const uint8_t* Wq, const float* Ws,
