@@ -124,13 +124,14 @@ int fp8rl_quant_act_group(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
  * Xq [M][K] e4m3, Xs [K/128][M] fp32, Wq [N][K] e4m3, Ws [N/128][K/128] fp32,
  * Y bf16 [M][ldy], ldy >= N, ldy % 8 == 0.  All 16-byte aligned (scales: 4).
  * workspace: device scratch, 16-byte aligned, of fp8rl_gemm_workspace_bytes(M,
- * N, K) bytes.  That is nonzero only for shapes whose K is split over more
- * work units than can share partial sums on chip: too few output tiles to fill
- * the GPU but a long K (e.g. a few hundred tokens against a 27648-wide layer),
- * or a small batch on a long-K layer with few 128-row weight slabs (the
- * 27648-wide down projection of a 5120-wide model).  The fp32 partial tiles
- * are then added in a second launch, in a fixed order (deterministic).  With
- * less workspace (or NULL) the call still succeeds, without that split.  It does not need to be zeroed and holds
+ * N, K) bytes.  It is nonzero for shapes whose K the library splits through
+ * memory: most batches of 17..256 tokens on layers with few 128-row weight
+ * slabs, small batches on long-K layers (the 27648-wide down projection of a
+ * 5120-wide model), and a few hundred tokens against a long K.  The fp32
+ * partial tiles are then added in a second launch, in a fixed order
+ * (deterministic), so the call launches two kernels instead of one.  With less
+ * workspace (or NULL) the call still succeeds, on a split that keeps its
+ * partial sums on chip (slower for those shapes).  It does not need to be zeroed and holds
  * nothing between calls, but two calls in flight at once need two workspaces.
  * ---------------------------------------------------------------------- */
 size_t fp8rl_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);

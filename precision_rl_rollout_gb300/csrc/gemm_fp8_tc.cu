@@ -9,8 +9,9 @@
 // core's own block-scaled MMA kinds (power-of-two / E4M3 scales on 16- or
 // 32-element blocks) cannot express, so each 128-wide K block is one MMA
 // group into its own TMEM buffer and the epilogue warps promote it into fp32
-// registers with that block's scale product.  TMEM buffers are double
-// buffered so the MMAs of block kb+1 overlap the promotion of block kb.
+// registers with that block's scale product.  Several TMEM buffers (two in
+// the prefill kernel, four to eight here) let the MMAs of later blocks run
+// while the epilogue promotes earlier ones.
 //
 // Decode kernel (small M, HBM-bound; the long-tail rollout batches of "Taming
 // the Long Tail" (ASPLOS'26 blog), section 3.2 roofline and section 4.3.1):
@@ -78,12 +79,20 @@ struct DecodeCfg {
     static constexpr int kMaxSplit = 8;                           // portable cluster size
     static constexpr int kPrefetchKb = 8;                         // weight blocks sent to L2 early
     static constexpr int kScaleBytes = kMaxKbPerSplit * MT * 4;   // per-block scale products
-    static constexpr int kTmemCols = 2 * MT < 32 ? 32 : 2 * MT;
+    // TMEM accumulator buffers: enough that the MMAs of several K blocks are in
+    // flight while the epilogue drains earlier ones (a block's four dependent
+    // MMAs take far longer to complete than to issue); the columns of two
+    // co-resident CTAs (MT <= 64) or of one (MT = 128) fill at most 512
+    static constexpr int kTmemBufs = MT <= 32 ? 8 : 4;
+    static constexpr int kTmemCols = kTmemBufs * MT;
     static constexpr int kMinBlocks = MT <= 64 ? 2 : 1;             // CTAs per SM the registers allow
     static constexpr int kChunk = kCols >= 32 ? 32 : 16;               // TMEM load width
     static constexpr int kGroup = kCols < 64 ? kCols : 64;             // columns per tcgen05.wait::ld
     static constexpr int kBarOffset = kStages * kStageBytes + kScaleBytes;
     static constexpr int kSmemBytes = kBarOffset + 256 + 1024;   // barriers + alignment slack
+    static_assert((2 * kStages + 2 * kTmemBufs) * 8 + 8 <= 256, "barrier area");
+    static_assert(kTmemCols >= 32 && (kTmemCols & (kTmemCols - 1)) == 0 &&
+                      kTmemCols * (MT <= 64 ? 2 : 1) <= 512, "TMEM allocation");
     static_assert(MT * 128 * 4 <= kStages * kStageBytes, "reduction buffer must fit the stage area");
 };
 
@@ -96,11 +105,12 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float* cscale = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
-    // bars: full[S], empty[S], tfull[2], tempty[2]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 4);
+    // bars: full[S], empty[S], tfull[B], tempty[B] (B TMEM buffers)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 2 * C::kTmemBufs);
     volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + C::kStages);
-    const uint32_t tfull0 = smem_u32(bars + 2 * C::kStages), tempty0 = smem_u32(bars + 2 * C::kStages + 2);
+    const uint32_t tfull0 = smem_u32(bars + 2 * C::kStages);
+    const uint32_t tempty0 = smem_u32(bars + 2 * C::kStages + C::kTmemBufs);
 
     const uint32_t warp = warp_id(), lane = lane_id();
     const int split_idx = blockIdx.x;                  // rank within the cluster
@@ -115,7 +125,7 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < C::kTmemBufs; ++b) {
             mbar_init(tfull0 + 8 * b, 1);
             mbar_init(tempty0 + 8 * b, C::kEpiWarps);
         }
@@ -185,8 +195,8 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
             for (int it = 0; it < nrun; ++it) {
                 const int s = it % C::kStages;
                 const uint32_t ph = (it / C::kStages) & 1;
-                const int buf = it & 1;
-                const uint32_t bph = (it >> 1) & 1;
+                const int buf = it % C::kTmemBufs;
+                const uint32_t bph = (it / C::kTmemBufs) & 1;
                 if (!mbar_wait_bounded(full0 + 8 * s, ph, abort, kWaitLimitNs)) {
                     record_timeout(p.err, kKernelDecode, 2, abort);
                     break;
@@ -241,8 +251,8 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
 #pragma unroll
         for (int j = 0; j < C::kCols / 2; ++j) acc[j] = 0ull;
         for (int it = 0; it < nrun; ++it) {
-            const int buf = it & 1;
-            const uint32_t bph = (it >> 1) & 1;
+            const int buf = it % C::kTmemBufs;
+            const uint32_t bph = (it / C::kTmemBufs) & 1;
             // the verdict is made warp-uniform: the TMEM loads below are warp-collective
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(tfull0 + 8 * buf, bph, abort, kWaitLimitNs))) {
                 if (lane == 0) record_timeout(p.err, kKernelDecode, 4, abort);
@@ -391,9 +401,11 @@ decode_splitk_reduce_kernel(const float* __restrict__ part, int64_t M, int mtile
 }
 
 // Split-K factor for `tiles` weight slabs of KB blocks and a token tile of MT.
-// Cost model fitted to a sweep of splits 1..8 over the Qwen2.5-7B/32B decode
-// shapes at M = 1..256 on GB300 (within 2% of the best split on average,
-// 10% in the worst case):
+// Cost model fitted to a sweep of cluster splits 1..8 over the Qwen2.5-7B/32B
+// decode shapes at M = 1..256 on GB300.  It underrates larger splits on short
+// weight streams (up to 20% slower than the best split at M = 1), so the dense
+// GEMM's plan below uses it only as a fallback; it also prices the decode
+// kernel for the decode/prefill dispatch and sets the grouped form's split:
 //   cost = 3 * waves + busiest-SM CTAs * blocks per CTA * (0.4 + 0.3 MT/128) + 2 * split * MT/128
 // (microseconds, roughly): a fixed cost per wave of CTAs, the weight stream of
 // the busiest SM (heavier per block for wide token tiles), and the cluster
@@ -476,37 +488,61 @@ static int64_t clusters_per_wave(int split) {
     return cache[dev][split] > 0 ? (int64_t)cache[dev][split] * DecodeCfg<MT>::kMinBlocks : 0;
 }
 
-// Split-K plan of the dense decode GEMM.  The cluster plan comes from the cost
-// model; when its clusters cannot all run at once (long K on few slabs: the
-// 27648-wide down projection), the split CTAs run without a cluster instead,
-// as many per slab as one wave holds, and add their partials through the
-// workspace in a second launch.
+// Split-K plan of the dense decode GEMM, from a sweep of splits 1..16 with and
+// without clusters over the Qwen2.5-7B/32B decode shapes at M = 1..128 on
+// GB300 (in the order tried):
+//  - token tiles of 32 or more, with a workspace: the split CTAs run without a
+//    cluster and add their partials through the workspace in a second launch,
+//    about one CTA per SM (1.5 for 32-token tiles).  Their exchange moves 16-64 KB
+//    per CTA, which the distributed-shared-memory reduction does slowly;
+//  - otherwise, for token tiles of up to 32, a cluster of the largest split
+//    whose clusters all run at once (per the occupancy API): more, shorter
+//    weight streams per slab, as long as a second wave of clusters is not
+//    needed;
+//  - when no such split exists (long K on few slabs: the 27648-wide down
+//    projection), through the workspace again, as many CTAs per slab as one
+//    wave holds;
+//  - else the cost model above (without a workspace, tiles of 64 and more: it
+//    picks the best cluster split there).
 struct DecodePlan {
     int split;
     bool global;
 };
 
+static bool split_fits(int KB, int s, int max_per) {
+    const int per = (KB + s - 1) / s;
+    return per <= max_per && (s - 1) * per < KB;   // no empty split
+}
+
 template <int MT>
-static DecodePlan decode_plan(int64_t tiles, int KB) {
+static DecodePlan decode_plan(int64_t tiles, int KB, bool may_use_memory) {
     using C = DecodeCfg<MT>;
-    DecodePlan pl{choose_split(tiles, KB, MT, C::kMaxKbPerSplit), false};
-    if (pl.split > 1) {
-        const int64_t cpw = clusters_per_wave<MT>(pl.split);
-        if (cpw > 0 && tiles > cpw) {
-            const int64_t slots = (int64_t)num_sms() * C::kMinBlocks;
-            int gs = (int)(slots / tiles);
-            if (gs > 16) gs = 16;
-            if (gs >= 2 && (KB + gs - 1) / gs <= C::kMaxKbPerSplit && (int64_t)(gs - 1) * ((KB + gs - 1) / gs) < KB)
-                pl = DecodePlan{gs, true};
-        }
+    constexpr int kMaxMemSplit = 16;
+    const int64_t sms = num_sms();
+    if (may_use_memory && MT >= 32) {
+        int64_t t = (MT == 32 ? 3 * sms / 2 : sms) / tiles;
+        int s = (int)(t < kMaxMemSplit ? t : kMaxMemSplit);
+        while (s >= 2 && !split_fits(KB, s, C::kMaxKbPerSplit)) --s;
+        if (s >= 2) return DecodePlan{s, true};
     }
-    return pl;
+    for (int s = C::kMaxSplit; MT <= 32 && s >= 1; --s) {
+        if (!split_fits(KB, s, C::kMaxKbPerSplit)) continue;
+        const int64_t cpw = clusters_per_wave<MT>(s);
+        if (cpw > 0 && tiles <= cpw) return DecodePlan{s, false};
+    }
+    if (may_use_memory && clusters_per_wave<MT>(1) > 0) {   // occupancy known: clusters did not fit
+        int64_t t = sms * C::kMinBlocks / tiles;
+        int s = (int)(t < kMaxMemSplit ? t : kMaxMemSplit);
+        while (s >= 2 && !split_fits(KB, s, C::kMaxKbPerSplit)) --s;
+        if (s >= 2) return DecodePlan{s, true};
+    }
+    return DecodePlan{choose_split(tiles, KB, MT, C::kMaxKbPerSplit), false};
 }
 
 template <int MT>
 static size_t decode_ws_bytes_mt(int64_t M, int64_t N, int64_t K) {
     const int64_t mtiles = (M + MT - 1) / MT, tiles = (N / 128) * mtiles;
-    const DecodePlan pl = decode_plan<MT>(tiles, (int)(K / 128));
+    const DecodePlan pl = decode_plan<MT>(tiles, (int)(K / 128), true);
     return pl.global ? (size_t)tiles * pl.split * MT * 128 * sizeof(float) : 0;
 }
 
@@ -535,9 +571,9 @@ static cudaError_t launch_decode_mt(const uint8_t* Xq, const float* Xs, const ui
     const int64_t mtiles = (rows_per_group + MT - 1) / MT;
     const int64_t tiles = groups * (N / 128) * mtiles;
     DecodePlan pl = offs ? DecodePlan{choose_split(tiles, KB, MT, C::kMaxKbPerSplit), false}
-                         : decode_plan<MT>(tiles, KB);
+                         : decode_plan<MT>(tiles, KB, true);
     if (pl.global && (ws == nullptr || ws_bytes < (size_t)tiles * pl.split * MT * 128 * sizeof(float)))
-        pl = DecodePlan{choose_split(tiles, KB, MT, C::kMaxKbPerSplit), false};
+        pl = decode_plan<MT>(tiles, KB, false);
     const int split = pl.split;
     const int per = (KB + split - 1) / split;
     if (per > C::kMaxKbPerSplit) return cudaErrorInvalidValue;
