@@ -18,10 +18,13 @@
 // moves over from warpgroup 0 (40 -> 232 registers per thread).
 // Tiles go M-fastest, so the CTAs in flight share a few 256-row weight slabs
 // and the (L2-resident) activations.
-// Split-K (shapes with fewer tiles than SMs and long K, e.g. a few hundred
-// tokens): a work unit is (tile, K range); each split writes its fp32 partial
-// tile to the caller's workspace by TMA, and a second launch adds the splits
-// of every tile in a fixed order (deterministic) and rounds to bf16.
+// Split-K: a work unit is (tile, K range); each range writes its fp32 partial
+// tile to the caller's workspace by TMA, and a second launch adds the ranges
+// of a tile in a fixed order (deterministic) and rounds to bf16.  It serves
+// two cases: shapes with fewer tiles than SMs and a long K (a few hundred
+// tokens: every tile is split), and the last, partial wave of tiles (only the
+// tiles after the last full wave are split, so that wave finishes in a
+// fraction of a tile's time; e.g. 1280 tiles on 152 SMs leave 64).
 #include "common.cuh"
 #include "internal.h"
 #include "sm100_ptx.cuh"
@@ -58,8 +61,24 @@ struct PrefillParams {
     int64_t M, ldy;
     int KB, NB;        // K/128, N/128
     int mtiles, ntiles;
-    int split, kb_per;  // K ranges per tile and K blocks per range (split 1: no workspace)
+    int split, kb_per;  // K ranges per split tile and K blocks per range (split 1: no workspace)
+    int full_tiles;     // tiles [0, full_tiles) are not split (all of them when split == 1)
 };
+
+// Work unit u: tile, K range [kb_beg, kb_end), and the range's index (-1: the
+// whole tile, written as bf16).  Units [0, full_tiles) are whole tiles; each
+// later tile is `split` consecutive units.
+struct PrefillUnit {
+    int tile, sp, kb_beg, kb_end;
+};
+
+template <bool kSplit>
+__device__ __forceinline__ PrefillUnit prefill_unit(int u, const PrefillParams& p) {
+    if (!kSplit || u < p.full_tiles) return PrefillUnit{u, -1, 0, p.KB};
+    const int v = u - p.full_tiles, t = v / p.split, sp = v - t * p.split;
+    const int kb_beg = sp * p.kb_per;
+    return PrefillUnit{p.full_tiles + t, sp, kb_beg, min(p.KB, kb_beg + p.kb_per)};
+}
 
 __device__ __forceinline__ void record_timeout(uint32_t* err, uint32_t site, volatile int* abort) {
     atomicCAS(err, 0u, (kKernelPrefill << 24) | (site << 16) | 1u);
@@ -79,8 +98,9 @@ gemm_fp8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_co
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
     const uint32_t tfull0 = smem_u32(bars + 2 * kStages), tempty0 = smem_u32(bars + 2 * kStages + 2);
     const uint32_t warp = warp_id(), lane = lane_id();
-    const int split = kSplit ? p.split : 1;              // (kSplit = false: the split code is compiled out)
-    const int total_units = p.mtiles * p.ntiles * split;
+    // (kSplit = false: the split code is compiled out)
+    const int total_units = kSplit ? p.full_tiles + (p.mtiles * p.ntiles - p.full_tiles) * p.split
+                                   : p.mtiles * p.ntiles;
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -113,11 +133,9 @@ gemm_fp8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_co
             const uint64_t pol_x = policy_evict_last(), pol_w = policy_evict_first();
             uint32_t it = 0;
             for (int u = blockIdx.x; u < total_units && !*abort; u += gridDim.x) {
-                const int tile = u / split, sp = u - tile * split;
-                const int mt = tile % p.mtiles, nt = tile / p.mtiles;
-                const int kb_beg = kSplit ? sp * p.kb_per : 0;
-                const int kb_end = kSplit ? min(p.KB, kb_beg + p.kb_per) : p.KB;
-                for (int kb = kb_beg; kb < kb_end; ++kb, ++it) {
+                const PrefillUnit un = prefill_unit<kSplit>(u, p);
+                const int mt = un.tile % p.mtiles, nt = un.tile / p.mtiles;
+                for (int kb = un.kb_beg; kb < un.kb_end; ++kb, ++it) {
                     const int s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1;
                     if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1, abort, kWaitLimitNs)) {
@@ -138,8 +156,8 @@ gemm_fp8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_co
             const uint32_t mine = warp - 1;
             uint32_t it = 0;
             for (int u = blockIdx.x; u < total_units && !*abort; u += gridDim.x) {
-                const int sp = u % split;
-                const int nkb = kSplit ? min(p.KB, (sp + 1) * p.kb_per) - sp * p.kb_per : p.KB;
+                const PrefillUnit un = prefill_unit<kSplit>(u, p);
+                const int nkb = un.kb_end - un.kb_beg;
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     if ((it & 1) != mine) continue;
                     const int s = it % kStages;
@@ -174,10 +192,10 @@ gemm_fp8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_co
         const int row = 32 * q + lane;
         uint32_t it = 0;
         for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
-            const int tile = u / split, sp = u - tile * split;
+            const PrefillUnit un = prefill_unit<kSplit>(u, p);
+            const int tile = un.tile, sp = un.sp;
             const int mt = tile % p.mtiles, nt = tile / p.mtiles;
-            const int kb_beg = kSplit ? sp * p.kb_per : 0;
-            const int kb_end = kSplit ? min(p.KB, kb_beg + p.kb_per) : p.KB;
+            const int kb_beg = un.kb_beg, kb_end = un.kb_end;
             const int64_t m = (int64_t)mt * kBM + row;
             const int nb = 2 * nt + h;
             const bool live = m < p.M && nb < p.NB;
@@ -220,12 +238,12 @@ gemm_fp8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_co
                 for (int j = 0; j < 64; ++j) acc[64 + j] = fmaf(__uint_as_float(r[j]), scale, acc[64 + j]);
             }
             if (!ok) break;
-            if constexpr (kSplit) {
+            if (kSplit && sp >= 0) {
                 // fp32 partial of this K range: the warp's 32 rows x 128 columns as
                 // four 32 x 32 boxes (128-byte rows, 128-byte swizzle) into the
                 // workspace's slot (tile, sp), rows slot*128 .. +127
                 uint8_t* stage = smem + kOutOffset + e * kOutBytesPerWarp;
-                const int slot_row = (tile * split + sp) * kBM + 32 * q;
+                const int slot_row = ((tile - p.full_tiles) * p.split + sp) * kBM + 32 * q;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     if (lane == 0) bulk_wait_read_all();   // the previous box has left the buffer
@@ -289,18 +307,19 @@ gemm_fp8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_co
 // are added in order in fp32, then rounded to bf16 once.
 __global__ void __launch_bounds__(256)
 prefill_splitk_reduce_kernel(const float* __restrict__ part, int64_t M, int64_t N, int mtiles, int split,
-                             int64_t units8, uint16_t* __restrict__ Y, int64_t ldy) {
+                             int tile0, int64_t units8, uint16_t* __restrict__ Y, int64_t ldy) {
     pdl_wait_then_release();
     const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= units8) return;
-    const int64_t tile = t >> 12;                     // 128 rows x 32 eight-column chunks per tile
+    const int64_t slot = t >> 12;                     // 128 rows x 32 eight-column chunks per tile
+    const int64_t tile = tile0 + slot;                // split tiles start at tile0
     const int r = (int)((t >> 5) & 127), c8 = (int)(t & 31);
     const int mt = (int)(tile % mtiles), nt = (int)(tile / mtiles);
     const int64_t m = (int64_t)mt * kBM + r, n = (int64_t)nt * kBN + c8 * 8;
     if (m >= M || n >= N) return;
     float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int sp = 0; sp < split; ++sp) {
-        const float4* src = reinterpret_cast<const float4*>(part + ((tile * split + sp) * kBM + r) * kBN + c8 * 8);
+        const float4* src = reinterpret_cast<const float4*>(part + ((slot * split + sp) * kBM + r) * kBN + c8 * 8);
         const float4 a = src[0], b = src[1];
         s[0] += a.x; s[1] += a.y; s[2] += a.z; s[3] += a.w;
         s[4] += b.x; s[5] += b.y; s[6] += b.z; s[7] += b.w;
@@ -315,23 +334,47 @@ prefill_splitk_reduce_kernel(const float* __restrict__ part, int64_t M, int64_t 
 
 }  // namespace
 
-// K ranges per tile: when the tiles cannot fill the GPU, split K so that about
-// one wave of CTAs runs, keeping at least 8 K blocks per range.
-static int prefill_split(int64_t M, int64_t N, int64_t K) {
+// Which tiles are split into K ranges, and into how many (split 1: none).
+//  - Fewer tiles than about one wave: every tile, so that about one wave of
+//    CTAs runs, keeping at least 8 K blocks per range.
+//  - Otherwise the tiles after the last full wave, when they fill at most half
+//    a wave: into as many ranges as fill it (at least 8 K blocks each), if the
+//    part of a tile's time saved (at about 0.45 us per K block) exceeds what
+//    the partial tiles' round trip and the reduction launch cost (3 us plus
+//    the partials at 1.4 GB/ms, measured on the 32B shapes at M = 2048 and
+//    8192: the 27648-wide down projection gains 3.5% and 27%, the 5120-wide
+//    o_proj 6% at M = 2048 and would lose 3% at M = 8192).
+struct PrefillPlan {
+    int split;        // K ranges per split tile
+    int full_tiles;   // tiles [0, full_tiles) run whole
+};
+
+static PrefillPlan prefill_plan(int64_t M, int64_t N, int64_t K) {
     const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
-    const int sms = num_sms();
-    if (tiles * 4 >= (int64_t)sms * 3) return 1;
-    int s = (int)(sms / tiles);
+    const int64_t sms = num_sms();
     const int kb = (int)(K / 128);
+    const PrefillPlan none{1, (int)tiles};
+    if (tiles * 4 < sms * 3) {
+        int64_t s = sms / tiles;
+        if (s > kb / 8) s = kb / 8;
+        if (s > 8) s = 8;
+        return s < 2 ? none : PrefillPlan{(int)s, 0};
+    }
+    const int64_t full = tiles / sms * sms, tail = tiles - full;
+    if (tail == 0 || tail * 2 > sms) return none;
+    int64_t s = sms / tail;
     if (s > kb / 8) s = kb / 8;
     if (s > 8) s = 8;
-    return s < 1 ? 1 : s;
+    if (s < 2) return none;
+    const double saved = (1.0 - 1.0 / (double)s) * kb * 0.45;
+    const double cost = 3.0 + (double)(tail * s) * kBM * kBN * sizeof(float) / 1.4e6;
+    return saved > cost ? PrefillPlan{(int)s, (int)full} : none;
 }
 
-static size_t prefill_ws_bytes(int64_t M, int64_t N, int64_t K, int split) {
-    if (split <= 1) return 0;
+static size_t prefill_ws_bytes(int64_t M, int64_t N, int64_t K, const PrefillPlan& pl) {
+    if (pl.split <= 1) return 0;
     const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
-    return (size_t)tiles * (size_t)split * kBM * kBN * sizeof(float);
+    return (size_t)(tiles - pl.full_tiles) * (size_t)pl.split * kBM * kBN * sizeof(float);
 }
 
 // The register split (setmaxnreg) assumes the kernel was built with exactly
@@ -359,9 +402,11 @@ cudaError_t launch_gemm_fp8_prefill(const uint8_t* Xq, const float* Xs, const ui
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (prefill_ready<false>(dev) != 1 || prefill_ready<true>(dev) != 1) return cudaErrorInvalidDeviceFunction;
-    int split = prefill_split(M, N, K);
+    PrefillPlan pl = prefill_plan(M, N, K);
+    const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
     // with less workspace than the split needs, run without split-K
-    if (split > 1 && (ws == nullptr || ws_bytes < prefill_ws_bytes(M, N, K, split))) split = 1;
+    if (pl.split > 1 && (ws == nullptr || ws_bytes < prefill_ws_bytes(M, N, K, pl))) pl = PrefillPlan{1, (int)tiles};
+    const int split = pl.split;
     CUtensorMap tmX, tmW, tmY, tmP;
     if (!make_tmap_u8(&tmX, Xq, (uint64_t)M, (uint64_t)K, (uint64_t)K, kBM)) return cudaErrorInvalidValue;
     if (!make_tmap_u8(&tmW, Wq, (uint64_t)N, (uint64_t)K, (uint64_t)K, kBN)) return cudaErrorInvalidValue;
@@ -370,24 +415,26 @@ cudaError_t launch_gemm_fp8_prefill(const uint8_t* Xq, const float* Xs, const ui
     if (!err) return cudaErrorInvalidValue;
     const int KB = (int)(K / 128);
     PrefillParams prm{err, Xs, Ws, Y, M, ldy, KB, (int)(N / 128),
-                      (int)((M + kBM - 1) / kBM), (int)((N + kBN - 1) / kBN), split, (KB + split - 1) / split};
-    const int64_t tiles = (int64_t)prm.mtiles * prm.ntiles;
+                      (int)((M + kBM - 1) / kBM), (int)((N + kBN - 1) / kBN), split, (KB + split - 1) / split,
+                      pl.full_tiles};
+    const int64_t split_tiles = tiles - pl.full_tiles;
     if (split > 1) {
-        if (!make_tmap_f32_store(&tmP, ws, (uint64_t)(tiles * split * kBM), (uint64_t)kBN, (uint64_t)kBN, 32, 32))
+        if (!make_tmap_f32_store(&tmP, ws, (uint64_t)(split_tiles * split * kBM), (uint64_t)kBN, (uint64_t)kBN, 32,
+                                 32))
             return cudaErrorInvalidValue;
     } else {
         tmP = tmY;                                   // not used
     }
-    const int64_t units = tiles * split;
+    const int64_t units = pl.full_tiles + split_tiles * split;
     const int grid = units < num_sms() ? (int)units : num_sms();
     cudaError_t e = split > 1 ? launch_pdl(gemm_fp8_prefill_kernel<true>, dim3(grid), dim3(kThreads), kSmemBytes,
                                            st, tmX, tmW, tmY, tmP, prm)
                               : launch_pdl(gemm_fp8_prefill_kernel<false>, dim3(grid), dim3(kThreads), kSmemBytes,
                                            st, tmX, tmW, tmY, tmP, prm);
     if (e != cudaSuccess || split == 1) return e;
-    const int64_t units8 = tiles * kBM * 32;
+    const int64_t units8 = split_tiles * kBM * 32;
     return launch_pdl(prefill_splitk_reduce_kernel, dim3((unsigned)((units8 + 255) / 256)), dim3(256), 0, st,
-                      (const float*)ws, M, N, prm.mtiles, split, units8, Y, ldy);
+                      (const float*)ws, M, N, prm.mtiles, split, pl.full_tiles, units8, Y, ldy);
 }
 
 // The dispatch below takes the prefill kernel for this shape (same rule).
@@ -396,7 +443,7 @@ static bool takes_prefill(int64_t M, int64_t N, int64_t K);
 size_t gemm_fp8_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     if (M <= 0) return 0;
     if (!takes_prefill(M, N, K)) return decode_workspace_bytes(M, N, K);
-    return prefill_ws_bytes(M, N, K, prefill_split(M, N, K));
+    return prefill_ws_bytes(M, N, K, prefill_plan(M, N, K));
 }
 
 // Estimated prefill-kernel time in microseconds: a fixed 3 us plus the larger of
@@ -405,12 +452,14 @@ size_t gemm_fp8_workspace_bytes(int64_t M, int64_t N, int64_t K) {
 // round trip through L2 and the reduction launch.
 static double prefill_cost_us(int64_t M, int64_t N, int64_t K) {
     const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
-    const int split = prefill_split(M, N, K);
-    const int64_t kb = (K / 128 + split - 1) / split;
-    const int64_t waves = (tiles * split + num_sms() - 1) / num_sms();
-    const double compute = (double)waves * (double)kb * 0.5;
+    const PrefillPlan pl = prefill_plan(M, N, K);
+    const int64_t kb_all = K / 128, kb = (kb_all + pl.split - 1) / pl.split, sms = num_sms();
+    // whole tiles in waves, then the split tiles' ranges (all of them when full_tiles = 0)
+    const int64_t split_units = (tiles - pl.full_tiles) * pl.split;
+    const double compute = (double)((pl.full_tiles + sms - 1) / sms) * (double)kb_all * 0.5 +
+                           (double)((split_units + sms - 1) / sms) * (double)kb * 0.5;
     const double memory = (double)(N * K + M * K + 2 * M * N) / 5.5e6;
-    const double reduce = split > 1 ? 3.0 + (double)prefill_ws_bytes(M, N, K, split) / 3e6 : 0.0;
+    const double reduce = pl.split > 1 ? 3.0 + (double)prefill_ws_bytes(M, N, K, pl) / 3e6 : 0.0;
     return 3.0 + (compute > memory ? compute : memory) + reduce;
 }
 

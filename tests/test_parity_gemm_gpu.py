@@ -53,6 +53,23 @@ def test_fp8_gemm_split_k_without_workspace_matches(cuda_lib):
     assert_fp8_gemm_close(host(Y2), ref, "no split")
 
 
+def test_fp8_gemm_prefill_tail_split_sampled(cuda_lib):
+    # 3 x 54 = 162 tiles of 128 x 256: one full wave on 152 SMs and 10 tiles
+    # after it, which are split into K ranges through the workspace; sampled
+    # rows cover every row tile and, with all columns, the split tiles too.
+    # Also run without the workspace (no split): both within tolerance.
+    M, N, K = 384, 13824, 8192
+    Wq, Ws = oracle_fp8_weight(N, K, 93)
+    Xq, Xs = oracle_fp8_act(M, K, 94)
+    rows = np.array([0, 127, 128, 200, 255, 256, 300, 383])
+    ref = oracle.fp8_gemm(Xq[rows], Xs[:, rows], Wq, Ws)
+    Y1 = fb.fp8rl_gemm_w8a8_block(dev(Xq), dev(Xs), dev(Wq), dev(Ws))
+    Y2 = fb.fp8rl_gemm_w8a8_block(dev(Xq), dev(Xs), dev(Wq), dev(Ws),
+                                  workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
+    assert_fp8_gemm_close(host(Y1)[rows], ref, "tail split")
+    assert_fp8_gemm_close(host(Y2)[rows], ref, "no split")
+
+
 def test_fp8_gemm_tiny_config(cuda_lib):
     Wq, Ws = oracle_fp8_weight(synth.TINY.N, synth.TINY.K, synth.seed_for(1, 0))
     from parity_util import act_cpu
