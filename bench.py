@@ -679,6 +679,26 @@ def profile_case(fb, case, dev, reps=3):
         Xq, Xs = fb.fp8rl_quant_act_group(synth.activation(M, s.K, synth.seed_for(2, 1), device=dev))
         for _ in range(reps):
             fb.fp8rl_gemm_w8a8_block(Xq, Xs, Wq, Ws)
+    elif case.startswith("decode7b_down_m"):
+        M = int(case[len("decode7b_down_m"):])
+        s = synth.QWEN25_7B[3]                          # down 18944 -> 3584
+        W = synth.weight_bf16_direct(s.N, s.K, synth.seed_for(2, 0), device=dev)
+        Wq, Ws = fb.fp8rl_quant_weight_block(W)
+        del W
+        Xq, Xs = fb.fp8rl_quant_act_group(synth.activation(M, s.K, synth.seed_for(2, 1), device=dev))
+        ws = torch.empty(max(16, fb.fp8rl_gemm_workspace_bytes(M, s.N, s.K)), dtype=torch.uint8, device=dev)
+        for _ in range(reps):
+            fb.fp8rl_gemm_w8a8_block(Xq, Xs, Wq, Ws, workspace=ws)
+    elif case.startswith("prefill_down_m"):
+        M = int(case[len("prefill_down_m"):])
+        s = synth.QWEN25_32B[3]                         # down 27648 -> 5120
+        W = synth.weight_bf16_direct(s.N, s.K, synth.seed_for(4, 0), device=dev)
+        Wq, Ws = fb.fp8rl_quant_weight_block(W)
+        del W
+        Xq, Xs = fb.fp8rl_quant_act_group(synth.activation(M, s.K, synth.seed_for(4, 1), device=dev))
+        ws = torch.empty(max(16, fb.fp8rl_gemm_workspace_bytes(M, s.N, s.K)), dtype=torch.uint8, device=dev)
+        for _ in range(reps):
+            fb.fp8rl_gemm_w8a8_block(Xq, Xs, Wq, Ws, workspace=ws)
     elif case.startswith("decode32b_m"):
         M = int(case[len("decode32b_m"):])
         s = synth.QWEN25_32B[2]                         # gate_up 5120 -> 55296
@@ -760,7 +780,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--profile", default=None,
-                    help="run one small case for ncu: requant | decode | decode7b_m<M> | decode32b_m<M> | prefill | int8 | int8_m32 | kv | tis")
+                    help="run one small case for ncu: requant | decode | decode7b_m<M> | decode7b_down_m<M> | decode32b_m<M> | "
+                         "prefill | prefill_down_m<M> | int8 | int8_m32 | kv | tis | moe | kl")
     args = ap.parse_args()
     world, rank, local = dist_env()
     if args.impl == "reference":

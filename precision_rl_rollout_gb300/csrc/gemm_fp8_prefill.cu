@@ -318,11 +318,24 @@ prefill_splitk_reduce_kernel(const float* __restrict__ part, int64_t M, int64_t 
     const int64_t m = (int64_t)mt * kBM + r, n = (int64_t)nt * kBN + c8 * 8;
     if (m >= M || n >= N) return;
     float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int sp = 0; sp < split; ++sp) {
-        const float4* src = reinterpret_cast<const float4*>(part + ((slot * split + sp) * kBM + r) * kBN + c8 * 8);
-        const float4 a = src[0], b = src[1];
-        s[0] += a.x; s[1] += a.y; s[2] += a.z; s[3] += a.w;
-        s[4] += b.x; s[5] += b.y; s[6] += b.z; s[7] += b.w;
+    const float* base = part + ((slot * split) * kBM + r) * kBN + c8 * 8;
+    const int64_t stride = (int64_t)kBM * kBN;         // one range's partial tile
+    for (int sp0 = 0; sp0 < split; sp0 += 4) {
+        // four ranges' loads in flight, then added in range order (deterministic)
+        float4 v[4][2];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (sp0 + j < split) {
+                const float4* src = reinterpret_cast<const float4*>(base + (sp0 + j) * stride);
+                v[j][0] = src[0];
+                v[j][1] = src[1];
+            }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (sp0 + j < split) {
+                s[0] += v[j][0].x; s[1] += v[j][0].y; s[2] += v[j][0].z; s[3] += v[j][0].w;
+                s[4] += v[j][1].x; s[5] += v[j][1].y; s[6] += v[j][1].z; s[7] += v[j][1].w;
+            }
     }
     uint4 o;
     o.x = pack_bf16x2(s[0], s[1]);

@@ -61,10 +61,15 @@ struct DecodeParams {
     const int32_t* offs;   // [E+1] first token row of each expert, device memory
     int ntiles;            // 128-row weight slabs per expert (N / 128)
     int64_t tok_bound;     // token rows per expert the grid covers (M tiles * MT)
-    // split-K without a cluster: fp32 partial tiles [slabs * M tiles * split][MT][128]
-    // for a second launch to add (nullptr: the split CTAs form a cluster)
+    // split-K exchange (kXchg*): through distributed shared memory (part ==
+    // nullptr), or through fp32 partial tiles [slabs * M tiles * split][MT][128]
+    // in the workspace, added by a second launch or, in a cluster, by the CTAs
+    // themselves after one cluster barrier
     float* part;
+    int xmode;
 };
+
+enum : int { kXchgSmem = 0, kXchgReduceLaunch = 1, kXchgClusterMem = 2 };
 
 template <int MT>
 struct DecodeCfg {
@@ -293,77 +298,92 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
         }
     }
 
-    // ---------------- split-K reduction over the cluster, then bf16 stores
+    // ---------------- split-K: the split CTAs' partials are added in rank order,
+    // then rounded to bf16 once
     tc_fence_before();
-    const bool in_cluster = p.split > 1 && p.part == nullptr;
-    // self-check: the launch shape this reduction relies on (a cluster of
-    // exactly `split` CTAs, ranked by blockIdx.x); a mismatch is recorded and
-    // the distributed-shared-memory reads are skipped
+    const bool clustered = p.split > 1 && p.xmode != kXchgReduceLaunch;
+    // self-check: the launch shape the exchange relies on (`split` CTAs per slab
+    // along x; in a cluster, ranked by blockIdx.x); a mismatch is recorded and
+    // the exchange skipped
     const bool shape_ok = gridDim.x == (unsigned)p.split &&
-                          (!in_cluster || (cluster_nctarank() == (uint32_t)p.split &&
-                                           cluster_ctarank() == (uint32_t)split_idx));
+                          (!clustered || (cluster_nctarank() == (uint32_t)p.split &&
+                                          cluster_ctarank() == (uint32_t)split_idx));
     if (!shape_ok && threadIdx.x == 0) atomicCAS(p.err, 0u, (kKernelDecode << 24) | (8u << 16) | 2u);
     const int64_t ncols = (int64_t)(p.offs ? p.ntiles : (int)gridDim.z) * 128;   // output columns
-    if (p.part != nullptr) {
-        // no cluster: this CTA's partial rows go to its workspace slot (coalesced
-        // 16-byte stores of red[m][0..127]); the reduction launch adds the slots
+    const int valid_m = rows <= 0 ? 0 : (int)(rows < MT ? rows : MT);
+    // this slab's first partial slot in the workspace (memory exchanges)
+    float* const slot0 = p.part != nullptr ? p.part + ((int64_t)z * gridDim.y + mt) * p.split * (MT * 128) : nullptr;
+    if (slot0 != nullptr) {
+        // this CTA's partial rows to its slot: coalesced 16-byte stores of red[m][0..127]
         __syncthreads();
-        const int valid_m = rows <= 0 ? 0 : (int)(rows < MT ? rows : MT);
-        float4* dst = reinterpret_cast<float4*>(
-            p.part + (((int64_t)z * gridDim.y + mt) * p.split + split_idx) * (MT * 128));
-        const float4* src = reinterpret_cast<const float4*>(smem);
-        if (shape_ok)
+        if (shape_ok) {
+            float4* dst = reinterpret_cast<float4*>(slot0 + (int64_t)split_idx * (MT * 128));
+            const float4* src = reinterpret_cast<const float4*>(smem);
             for (int i = threadIdx.x; i < valid_m * 32; i += C::kThreads) dst[i] = src[i];
-    } else {
-    if (in_cluster) cluster_sync_all(); else __syncthreads();
-    if (shape_ok) {
-        const int64_t m_tile0 = row0;
-        const int valid_m = rows <= 0 ? 0 : (int)(rows < MT ? rows : MT);
-        const int total = valid_m * 16;                   // chunks of 8 output channels
-        const int per = (total + p.split - 1) / p.split;
-        const int begin = split_idx * per, end = min(total, begin + per);
-        const uint32_t red_addr = smem_u32(smem);
-        for (int c = begin + (int)threadIdx.x; c < end; c += C::kThreads) {
-            const int m = c >> 4, n8 = c & 15;
-            const uint32_t off = (uint32_t)(m * 128 + n8 * 8) * 4u;
-            float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            if (in_cluster) {
-                // every rank's loads are in flight before the first add: one
-                // distributed-shared-memory round trip per chunk, not one per rank
-                float4 v[C::kMaxSplit][2];
-#pragma unroll
-                for (int r = 0; r < C::kMaxSplit; ++r)
-                    if (r < p.split) {
-                        const uint32_t a = map_to_rank(red_addr + off, (uint32_t)r);
-                        v[r][0] = ld_cluster_v4(a);
-                        v[r][1] = ld_cluster_v4(a + 16);
-                    }
-#pragma unroll
-                for (int r = 0; r < C::kMaxSplit; ++r)   // fixed order: deterministic
-                    if (r < p.split) {
-                        s[0] += v[r][0].x; s[1] += v[r][0].y; s[2] += v[r][0].z; s[3] += v[r][0].w;
-                        s[4] += v[r][1].x; s[5] += v[r][1].y; s[6] += v[r][1].z; s[7] += v[r][1].w;
-                    }
-            } else {
-                const float4* l = reinterpret_cast<const float4*>(smem + off);
-                const float4 v0 = l[0], v1 = l[1];
-                s[0] += v0.x; s[1] += v0.y; s[2] += v0.z; s[3] += v0.w;
-                s[4] += v1.x; s[5] += v1.y; s[6] += v1.z; s[7] += v1.w;
-            }
-            uint4 o;
-            o.x = pack_bf16x2(s[0], s[1]);
-            o.y = pack_bf16x2(s[2], s[3]);
-            o.z = pack_bf16x2(s[4], s[5]);
-            o.w = pack_bf16x2(s[6], s[7]);
-            const int64_t col = (int64_t)nt * 128 + n8 * 8;
-            if (m_tile0 + m < p.M && col + 8 <= ncols)        // self-check of the output index
-                *reinterpret_cast<uint4*>(p.Y + (m_tile0 + m) * p.ldy + col) = o;
-            else
-                atomicCAS(p.err, 0u, (kKernelDecode << 24) | (9u << 16) | 2u);
         }
     }
+    if (p.xmode != kXchgReduceLaunch) {
+        // every rank's partial is complete (and, through memory, visible to the
+        // cluster) after this barrier; each CTA then adds 1/split of the chunks
+        if (clustered) cluster_sync_all(); else __syncthreads();
+        if (shape_ok) {
+            const int total = valid_m * 16;                   // chunks of 8 output channels
+            const int per = (total + p.split - 1) / p.split;
+            const int begin = split_idx * per, end = min(total, begin + per);
+            const uint32_t red_addr = smem_u32(smem);
+            for (int c = begin + (int)threadIdx.x; c < end; c += C::kThreads) {
+                const int m = c >> 4, n8 = c & 15;
+                const uint32_t off = (uint32_t)(m * 128 + n8 * 8) * 4u;
+                float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                if (clustered) {
+                    // every rank's loads are in flight before the first add: one
+                    // round trip per chunk, not one per rank
+                    float4 v[C::kMaxSplit][2];
+                    if (p.xmode == kXchgClusterMem) {
+                        const float* src = slot0 + m * 128 + n8 * 8;
+#pragma unroll
+                        for (int r = 0; r < C::kMaxSplit; ++r)
+                            if (r < p.split) {
+                                const float4* q4 = reinterpret_cast<const float4*>(src + (int64_t)r * (MT * 128));
+                                v[r][0] = __ldcg(q4);
+                                v[r][1] = __ldcg(q4 + 1);
+                            }
+                    } else {
+#pragma unroll
+                        for (int r = 0; r < C::kMaxSplit; ++r)
+                            if (r < p.split) {
+                                const uint32_t a = map_to_rank(red_addr + off, (uint32_t)r);
+                                v[r][0] = ld_cluster_v4(a);
+                                v[r][1] = ld_cluster_v4(a + 16);
+                            }
+                    }
+#pragma unroll
+                    for (int r = 0; r < C::kMaxSplit; ++r)   // fixed order: deterministic
+                        if (r < p.split) {
+                            s[0] += v[r][0].x; s[1] += v[r][0].y; s[2] += v[r][0].z; s[3] += v[r][0].w;
+                            s[4] += v[r][1].x; s[5] += v[r][1].y; s[6] += v[r][1].z; s[7] += v[r][1].w;
+                        }
+                } else {
+                    const float4* l = reinterpret_cast<const float4*>(smem + off);
+                    const float4 v0 = l[0], v1 = l[1];
+                    s[0] += v0.x; s[1] += v0.y; s[2] += v0.z; s[3] += v0.w;
+                    s[4] += v1.x; s[5] += v1.y; s[6] += v1.z; s[7] += v1.w;
+                }
+                uint4 o;
+                o.x = pack_bf16x2(s[0], s[1]);
+                o.y = pack_bf16x2(s[2], s[3]);
+                o.z = pack_bf16x2(s[4], s[5]);
+                o.w = pack_bf16x2(s[6], s[7]);
+                const int64_t col = (int64_t)nt * 128 + n8 * 8;
+                if (row0 + m < p.M && col + 8 <= ncols)        // self-check of the output index
+                    *reinterpret_cast<uint4*>(p.Y + (row0 + m) * p.ldy + col) = o;
+                else
+                    atomicCAS(p.err, 0u, (kKernelDecode << 24) | (9u << 16) | 2u);
+            }
+        }
     }
-    if (in_cluster) cluster_sync_all(); else __syncthreads();
+    // a CTA whose shared memory its peers read stays until they are done
+    if (clustered && p.xmode == kXchgSmem) cluster_sync_all(); else __syncthreads();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, C::kTmemCols);
@@ -386,11 +406,24 @@ decode_splitk_reduce_kernel(const float* __restrict__ part, int64_t M, int mtile
     const int64_t row = mt * MT + m;
     if (row >= M) return;
     float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int sp = 0; sp < split; ++sp) {
-        const float4* src = reinterpret_cast<const float4*>(part + ((tile * split + sp) * MT + m) * 128 + c8 * 8);
-        const float4 a = src[0], b = src[1];
-        s[0] += a.x; s[1] += a.y; s[2] += a.z; s[3] += a.w;
-        s[4] += b.x; s[5] += b.y; s[6] += b.z; s[7] += b.w;
+    const float* base = part + ((tile * split) * MT + m) * 128 + c8 * 8;
+    const int64_t stride = (int64_t)MT * 128;          // one split's partial tile
+    for (int sp0 = 0; sp0 < split; sp0 += 4) {
+        // four splits' loads in flight, then added in split order (deterministic)
+        float4 v[4][2];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (sp0 + j < split) {
+                const float4* src = reinterpret_cast<const float4*>(base + (sp0 + j) * stride);
+                v[j][0] = src[0];
+                v[j][1] = src[1];
+            }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (sp0 + j < split) {
+                s[0] += v[j][0].x; s[1] += v[j][0].y; s[2] += v[j][0].z; s[3] += v[j][0].w;
+                s[4] += v[j][1].x; s[5] += v[j][1].y; s[6] += v[j][1].z; s[7] += v[j][1].w;
+            }
     }
     uint4 o;
     o.x = pack_bf16x2(s[0], s[1]);
@@ -488,25 +521,26 @@ static int64_t clusters_per_wave(int split) {
     return cache[dev][split] > 0 ? (int64_t)cache[dev][split] * DecodeCfg<MT>::kMinBlocks : 0;
 }
 
-// Split-K plan of the dense decode GEMM, from a sweep of splits 1..16 with and
-// without clusters over the Qwen2.5-7B/32B decode shapes at M = 1..128 on
+// Split-K plan of the dense decode GEMM, from a sweep of the three exchanges
+// and splits 1..16 over the Qwen2.5-7B/32B decode shapes at M = 1..128 on
 // GB300 (in the order tried):
-//  - token tiles of 32 or more, with a workspace: the split CTAs run without a
-//    cluster and add their partials through the workspace in a second launch,
-//    about one CTA per SM (1.5 for 32-token tiles).  Their exchange moves 16-64 KB
-//    per CTA, which the distributed-shared-memory reduction does slowly;
-//  - otherwise, for token tiles of up to 32, a cluster of the largest split
-//    whose clusters all run at once (per the occupancy API): more, shorter
-//    weight streams per slab, as long as a second wave of clusters is not
-//    needed;
+//  - token tiles of 64 or more, with a workspace: the split CTAs run without a
+//    cluster, about one per SM, and a second launch adds their partials;
+//  - token tiles of up to 32: a cluster of the largest split whose clusters all
+//    run at once (per the occupancy API), i.e. more, shorter weight streams per
+//    slab as long as no second wave of clusters is needed.  With a workspace
+//    the partials go through L2 and the CTAs add them after one cluster
+//    barrier (at 16-32 tokens 7-9% faster than through distributed shared
+//    memory, which needs a second barrier before any CTA may exit);
 //  - when no such split exists (long K on few slabs: the 27648-wide down
-//    projection), through the workspace again, as many CTAs per slab as one
-//    wave holds;
+//    projection), through the workspace and a second launch, as many CTAs per
+//    slab as one wave holds;
 //  - else the cost model above (without a workspace, tiles of 64 and more: it
 //    picks the best cluster split there).
 struct DecodePlan {
     int split;
-    bool global;
+    int xmode;   // kXchg*: how the split CTAs exchange their partials
+    bool uses_memory() const { return xmode != kXchgSmem; }
 };
 
 static bool split_fits(int KB, int s, int max_per) {
@@ -519,31 +553,31 @@ static DecodePlan decode_plan(int64_t tiles, int KB, bool may_use_memory) {
     using C = DecodeCfg<MT>;
     constexpr int kMaxMemSplit = 16;
     const int64_t sms = num_sms();
-    if (may_use_memory && MT >= 32) {
-        int64_t t = (MT == 32 ? 3 * sms / 2 : sms) / tiles;
+    if (may_use_memory && MT >= 64) {
+        int64_t t = sms / tiles;
         int s = (int)(t < kMaxMemSplit ? t : kMaxMemSplit);
         while (s >= 2 && !split_fits(KB, s, C::kMaxKbPerSplit)) --s;
-        if (s >= 2) return DecodePlan{s, true};
+        if (s >= 2) return DecodePlan{s, kXchgReduceLaunch};
     }
     for (int s = C::kMaxSplit; MT <= 32 && s >= 1; --s) {
         if (!split_fits(KB, s, C::kMaxKbPerSplit)) continue;
         const int64_t cpw = clusters_per_wave<MT>(s);
-        if (cpw > 0 && tiles <= cpw) return DecodePlan{s, false};
+        if (cpw > 0 && tiles <= cpw) return DecodePlan{s, s > 1 && may_use_memory ? kXchgClusterMem : kXchgSmem};
     }
     if (may_use_memory && clusters_per_wave<MT>(1) > 0) {   // occupancy known: clusters did not fit
         int64_t t = sms * C::kMinBlocks / tiles;
         int s = (int)(t < kMaxMemSplit ? t : kMaxMemSplit);
         while (s >= 2 && !split_fits(KB, s, C::kMaxKbPerSplit)) --s;
-        if (s >= 2) return DecodePlan{s, true};
+        if (s >= 2) return DecodePlan{s, kXchgReduceLaunch};
     }
-    return DecodePlan{choose_split(tiles, KB, MT, C::kMaxKbPerSplit), false};
+    return DecodePlan{choose_split(tiles, KB, MT, C::kMaxKbPerSplit), kXchgSmem};
 }
 
 template <int MT>
 static size_t decode_ws_bytes_mt(int64_t M, int64_t N, int64_t K) {
     const int64_t mtiles = (M + MT - 1) / MT, tiles = (N / 128) * mtiles;
     const DecodePlan pl = decode_plan<MT>(tiles, (int)(K / 128), true);
-    return pl.global ? (size_t)tiles * pl.split * MT * 128 * sizeof(float) : 0;
+    return pl.uses_memory() ? (size_t)tiles * pl.split * MT * 128 * sizeof(float) : 0;
 }
 
 size_t decode_workspace_bytes(int64_t M, int64_t N, int64_t K) {
@@ -570,9 +604,9 @@ static cudaError_t launch_decode_mt(const uint8_t* Xq, const float* Xs, const ui
     const int KB = (int)(K / 128);
     const int64_t mtiles = (rows_per_group + MT - 1) / MT;
     const int64_t tiles = groups * (N / 128) * mtiles;
-    DecodePlan pl = offs ? DecodePlan{choose_split(tiles, KB, MT, C::kMaxKbPerSplit), false}
+    DecodePlan pl = offs ? DecodePlan{choose_split(tiles, KB, MT, C::kMaxKbPerSplit), kXchgSmem}
                          : decode_plan<MT>(tiles, KB, true);
-    if (pl.global && (ws == nullptr || ws_bytes < (size_t)tiles * pl.split * MT * 128 * sizeof(float)))
+    if (pl.uses_memory() && (ws == nullptr || ws_bytes < (size_t)tiles * pl.split * MT * 128 * sizeof(float)))
         pl = decode_plan<MT>(tiles, KB, false);
     const int split = pl.split;
     const int per = (KB + split - 1) / split;
@@ -580,7 +614,7 @@ static cudaError_t launch_decode_mt(const uint8_t* Xq, const float* Xs, const ui
     uint32_t* err = device_error_word();
     if (!err) return cudaErrorInvalidValue;
     DecodeParams prm{err, Xs, Ws, Y, M, ldy, KB, per, split, offs, (int)(N / 128), mtiles * MT,
-                     pl.global ? static_cast<float*>(ws) : nullptr};
+                     pl.uses_memory() ? static_cast<float*>(ws) : nullptr, pl.xmode};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -600,9 +634,9 @@ static cudaError_t launch_decode_mt(const uint8_t* Xq, const float* Xs, const ui
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = pl.global ? 1 : 2;
+    cfg.numAttrs = pl.xmode == kXchgReduceLaunch ? 1 : 2;    // no cluster for the reduction launch
     e = cudaLaunchKernelEx(&cfg, gemm_fp8_decode_kernel<MT>, tmW, tmX, prm);
-    if (e != cudaSuccess || !pl.global) return e;
+    if (e != cudaSuccess || pl.xmode != kXchgReduceLaunch) return e;
     const int64_t units = tiles * MT * 16;
     return launch_pdl(decode_splitk_reduce_kernel<MT>, dim3((unsigned)((units + 255) / 256)), dim3(256), 0, st,
                       (const float*)ws, M, (int)mtiles, split, units, Y, ldy);

@@ -53,6 +53,24 @@ def test_fp8_gemm_split_k_without_workspace_matches(cuda_lib):
     assert_fp8_gemm_close(host(Y2), ref, "no split")
 
 
+@pytest.mark.parametrize("M,N,K", [(16, 4608, 3584), (9, 3584, 18944), (32, 5120, 5120), (64, 3584, 18944)])
+def test_fp8_decode_exchange_with_and_without_workspace(cuda_lib, M, N, K):
+    # decode shapes whose split CTAs exchange partials through the workspace
+    # (in a cluster after one barrier for 16-32 token tiles, through a second
+    # launch for 64) and, with no workspace, through distributed shared memory:
+    # both within tolerance of the oracle on every row
+    assert fb.fp8rl_gemm_workspace_bytes(M, N, K) > 0
+    Wq, Ws = oracle_fp8_weight(N, K, 95 + M)
+    Xq, Xs = oracle_fp8_act(M, K, 96 + M)
+    rows = sample_rows(M, 6, seed=M)
+    ref = oracle.fp8_gemm(Xq[rows], Xs[:, rows], Wq, Ws)
+    Y1 = fb.fp8rl_gemm_w8a8_block(dev(Xq), dev(Xs), dev(Wq), dev(Ws))
+    Y2 = fb.fp8rl_gemm_w8a8_block(dev(Xq), dev(Xs), dev(Wq), dev(Ws),
+                                  workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
+    assert_fp8_gemm_close(host(Y1)[rows], ref, "through memory")
+    assert_fp8_gemm_close(host(Y2)[rows], ref, "on chip")
+
+
 def test_fp8_gemm_prefill_tail_split_sampled(cuda_lib):
     # 3 x 54 = 162 tiles of 128 x 256: one full wave on 152 SMs and 10 tiles
     # after it, which are split into K ranges through the workspace; sampled
