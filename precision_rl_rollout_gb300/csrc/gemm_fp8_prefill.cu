@@ -148,6 +148,9 @@ gemm_fp8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_co
                     tma_load_2d(smem_u32(st + kABytes), &tmW, full0 + 8 * s, kb * 128, nt * kBN, pol_w);
                 }
             }
+            if (*abort)   // let copies already in flight land before the CTA can exit
+                for (uint32_t j = it > (uint32_t)kStages ? it - kStages : 0; j < it; ++j)
+                    mbar_drain(full0 + 8 * (j % kStages), (j / kStages) & 1, kWaitLimitNs);
         } else if ((warp == 1 || warp == 2) && lane == 0) {
             // ---------------- MMA issuers: warp 1 issues the K blocks that go to
             // TMEM buffer 0, warp 2 those of buffer 1, so one thread's barrier

@@ -190,7 +190,7 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
             }
             if (*abort) {   // let copies already in flight land before the CTA can exit
                 for (int j = max(0, it - C::kStages); j < it; ++j)
-                    mbar_wait_bounded(full0 + 8 * (j % C::kStages), (j / C::kStages) & 1, abort, kWaitLimitNs);
+                    mbar_drain(full0 + 8 * (j % C::kStages), (j / C::kStages) & 1, kWaitLimitNs);
             }
         }
     } else if (warp == 1) {

@@ -175,9 +175,9 @@ gemm_int8_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
                 tma_load_2d(smem_u32(st), &tmW, rfull0 + 8 * s, (kb0 + it) * 128, nt * 128, pol_w);
                 tma_load_2d(smem_u32(st + C::kRawW), &tmX, rfull0 + 8 * s, (kb0 + it) * 128, mt * MT, pol_x);
             }
-            if (*abort)
+            if (*abort)   // let copies already in flight land before the CTA can exit
                 for (int j = max(0, it - R); j < it; ++j)
-                    mbar_wait_bounded(rfull0 + 8 * (j % R), (j / R) & 1, abort, kWaitLimitNs);
+                    mbar_drain(rfull0 + 8 * (j % R), (j / R) & 1, kWaitLimitNs);
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer: 8 x (M=128, N=MT, K=16) fp16 MMAs per K block
@@ -361,11 +361,13 @@ cudaError_t launch_i8_mt(const int8_t* Xq, const float* Xs, const int8_t* Wq, co
     if (!err) return cudaErrorInvalidValue;
     Int8Params prm{err, Xs, Ws, Y, acc, M, N, ldy, KB, per, split};
     auto kern = gemm_int8_tc_kernel<MT>;
-    static bool attr_set = false;
-    if (!attr_set) {
+    static bool attr_set[64] = {};     // the attribute belongs to the device
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        attr_set[dev] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)split, (unsigned)mtiles, (unsigned)(N / 128));
@@ -394,14 +396,17 @@ cudaError_t launch_gemm_int8_tc(const int8_t* Xq, const float* Xs, const int8_t*
     return launch_i8_mt<64>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, acc, st);
 }
 
-// Every M goes through the tcgen05 kernel: measured on GB300 it runs the 32B
-// shapes at 370-445 TOPS for M = 512..4096, where the warp-level s8 MMA path
-// reaches 85-127 TOPS.
-size_t gemm_int8_workspace_bytes(int64_t, int64_t, int64_t) { return 0; }
+// Batches of 256 tokens or more with enough tiles to fill the GPU take the
+// large-batch path (fp16 copies in the workspace, 128 x 256 tiles); the rest,
+// and any call with less workspace than that path asks for, this kernel.
+size_t gemm_int8_workspace_bytes(int64_t M, int64_t N, int64_t K) { return int8_prefill_workspace_bytes(M, N, K); }
 cudaError_t launch_gemm_int8(const int8_t* Xq, const float* Xs, const int8_t* Wq,
                              const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
-                             int64_t ldy, int32_t* acc, void*, size_t, cudaStream_t st) {
+                             int64_t ldy, int32_t* acc, void* ws, size_t ws_bytes, cudaStream_t st) {
     if (M == 0) return cudaSuccess;
+    const size_t need = int8_prefill_workspace_bytes(M, N, K);
+    if (need > 0 && ws != nullptr && ws_bytes >= need)
+        return launch_gemm_int8_prefill(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, acc, ws, st);
     return launch_gemm_int8_tc(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, acc, st);
 }
 

@@ -76,6 +76,13 @@ cudaError_t launch_gemm_int8_tc(const int8_t* Xq, const float* Xs, const int8_t*
                                 cudaStream_t st);
 // INT8 GEMM.
 size_t gemm_int8_workspace_bytes(int64_t M, int64_t N, int64_t K);
+// Large-batch INT8 path: int8 -> fp16 copies in the workspace, then a 128 x 256
+// tile fp16 tcgen05 GEMM with exact int32 accumulation.
+bool int8_prefill_applies(int64_t M, int64_t N, int64_t K);
+size_t int8_prefill_workspace_bytes(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_gemm_int8_prefill(const int8_t* Xq, const float* Xs, const int8_t* Wq, const float* Ws,
+                                     int64_t M, int64_t N, int64_t K, uint16_t* Y, int64_t ldy, int32_t* acc,
+                                     void* ws, cudaStream_t st);
 cudaError_t launch_gemm_int8(const int8_t* Xq, const float* Xs, const int8_t* Wq,
                              const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
                              int64_t ldy, int32_t* acc, void* ws, size_t ws_bytes,
@@ -105,6 +112,9 @@ bool make_tmap_bf16_store(CUtensorMap* m, const void* base, uint64_t rows, uint6
 // stores of box_cols x box_rows boxes with the 128-byte swizzle (box_cols = 32).
 bool make_tmap_f32_store(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
                          uint64_t pitch_elems, uint32_t box_cols, uint32_t box_rows);
+// fp16 [rows][cols] row-major (cols % 8 == 0), loaded in boxes of box_rows x 64
+// with the 128-byte swizzle (one UMMA K-major atom of fp16).
+bool make_tmap_f16_load(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
 int num_sms();
 bool decode_supported(int64_t K);
 double decode_cost_us(int64_t M, int64_t N, int64_t K);

@@ -89,6 +89,15 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// After an abort: wait, bounded by `limit_ns` and regardless of the abort flag,
+// until the copies this thread issued on `bar` (phase `parity`) have landed, so
+// that none writes into the shared memory of a CTA that has exited.
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > limit_ns) return;
+}
+
 // ------------------------------------------------------------------ TMA
 
 // 2-D tiled TMA load into this CTA's shared memory; completion is signalled on

@@ -160,6 +160,45 @@ def test_int8_gemm_extreme_codes_exact(cuda_lib):
     assert np.array_equal(host(Y), want_y)
 
 
+def test_int8_gemm_large_batch_path_ragged(cuda_lib):
+    # 3 x 51 = 153 tiles of 128 x 256: the large-batch path (fp16 copies in the
+    # workspace).  M = 300 leaves a partial token tile, N = 12928 a last tile
+    # with one 128-column half beyond N, K = 1152 a last TMEM group of 2 of 8
+    # stages.  The same call without the workspace runs the small-batch kernel;
+    # both are bit-exact on the sampled rows.
+    M, N, K = 300, 12928, 1152
+    assert fb.int8rl_gemm_workspace_bytes(M, N, K) == (M + N) * K * 2
+    Wq, Ws = oracle_int8_weight(N, K, 97)
+    Xq, Xs = oracle_int8_act(M, K, 98)
+    rows = np.array([0, 1, 127, 128, 255, 256, 290, 299])
+    want_acc, want_y = oracle.int8_gemm(Xq[rows], Xs[rows], Wq, Ws)
+    for ws in (None, torch.empty(16, dtype=torch.uint8, device="cuda")):
+        Y, acc = fb.int8rl_gemm_w8a8(dev(Xq), dev(Xs), dev(Wq), dev(Ws), want_acc=True, workspace=ws)
+        got_acc, got_y = host(acc)[rows], host(Y)[rows]
+        assert np.array_equal(got_acc, want_acc), f"acc differs at {np.argwhere(got_acc != want_acc)[:4].tolist()}"
+        assert np.array_equal(got_y, want_y), f"Y differs at {np.argwhere(got_y != want_y)[:4].tolist()}"
+
+
+def test_int8_gemm_large_batch_extreme_codes_exact(cuda_lib):
+    # every code at +-127 over K = 8192 (16 exact TMEM groups of 512) on the
+    # large-batch path: |acc| = 127^2 K
+    M, N, K = 256, 19456, 8192
+    assert fb.int8rl_gemm_workspace_bytes(M, N, K) > 0
+    Xq = np.full((M, K), 127, np.int8)
+    Xq[1::2] = -127
+    Xq[2, ::2] = -127
+    Wq = np.full((N, K), 127, np.int8)
+    Wq[N // 2:] = -127
+    Xs = np.linspace(0.5, 3.0, M).astype(np.float32)
+    Ws = np.linspace(0.001, 2.0, N).astype(np.float32)
+    Y, acc = fb.int8rl_gemm_w8a8(dev(Xq), dev(Xs), dev(Wq), dev(Ws), want_acc=True)
+    rows = np.array([0, 1, 2, 255])
+    want_acc, want_y = oracle.int8_gemm(Xq[rows], Xs[rows], Wq, Ws)
+    assert int(want_acc[0, 0]) == 127 * 127 * K and int(want_acc[1, 0]) == -127 * 127 * K
+    assert np.array_equal(host(acc)[rows], want_acc)
+    assert np.array_equal(host(Y)[rows], want_y)
+
+
 @pytest.mark.parametrize("M", synth.INT8_M_SWEEP)
 @pytest.mark.parametrize("shape", synth.QWEN25_32B, ids=lambda s: s.name)
 def test_int8_gemm_qwen32b_sampled(cuda_lib, shape, M):
