@@ -33,7 +33,9 @@
  *                        leading dimension smaller than the row length,
  *       FP8RL_ERR_ALIGN  a tensor not 16-byte aligned, or a leading
  *                        dimension whose row pitch is not a multiple of 16 B,
- *       FP8RL_ERR_WORKSPACE  workspace smaller than the *_workspace_bytes query,
+ *       FP8RL_ERR_WORKSPACE  workspace smaller than the *_workspace_bytes query
+ *                        (where it is required; the GEMMs instead take a
+ *                        slower path, as their entries say),
  *       FP8RL_ERR_UNSUPPORTED a size above a documented limit.
  *     A launch failure reported by the runtime returns FP8RL_ERR_CUDA.  Faults
  *     during execution surface, as usual in CUDA, at the caller's next
@@ -211,8 +213,14 @@ int int8rl_quant_act_token(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
  * Bit-exact in both acc and Y.  Requires K * 127^2 < 2^31 (K <= 133143) so
  * that no accumulator can overflow; larger K returns FP8RL_ERR_UNSUPPORTED.
  * Xq [M][K] int8, Xs [M] fp32, Wq [N][K] int8, Ws [N] fp32, Y bf16 [M][ldy].
- * acc_or_null: optional int32 [M][N] copy of the accumulators.
- * workspace as for the FP8 GEMM (int8rl_gemm_workspace_bytes).
+ * acc_or_null: optional int32 [M][N] copy of the accumulators (8-byte aligned).
+ * workspace: device scratch, 16-byte aligned, of int8rl_gemm_workspace_bytes(M,
+ * N, K) bytes: (M + N) * K * 2 for batches of 256 tokens or more whose
+ * 128 x 256 output tiles fill the GPU, else 0.  It receives fp16 copies of Xq
+ * and Wq (exact), which the large-batch kernel multiplies on the fp16 tensor
+ * path; with less workspace (or NULL) the call still succeeds on the
+ * small-batch kernel (slower for those shapes).  Not zeroed, nothing kept
+ * between calls; two calls in flight at once need two workspaces.
  * ---------------------------------------------------------------------- */
 size_t int8rl_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 int int8rl_gemm_w8a8(const int8_t* Xq, const float* Xs, const int8_t* Wq, const float* Ws,
