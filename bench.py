@@ -534,10 +534,13 @@ def extras(fb, dev, reps=5):
             X = synth.activation(M, s.K, synth.seed_for(5, 1), device=dev)
             Xq, Xs = fb.int8rl_quant_act_token(X)
             Y = torch.empty(M, s.N, dtype=torch.bfloat16, device=dev)
+            iws = torch.empty(max(16, fb.int8rl_gemm_workspace_bytes(M, s.N, s.K)), dtype=torch.uint8, device=dev)
             if M <= 256:
-                ms = _time_graph([lambda c=c: fb.int8rl_gemm_w8a8(Xq, Xs, Wqs[c], Ws, Y=Y) for c in range(nc)])
+                ms = _time_graph([lambda c=c: fb.int8rl_gemm_w8a8(Xq, Xs, Wqs[c], Ws, Y=Y, workspace=iws)
+                                  for c in range(nc)])
             else:
-                ms = _time_op(lambda: fb.int8rl_gemm_w8a8(Xq, Xs, Wq, Ws, Y=Y), reps, flush)
+                ms = _time_op(lambda: fb.int8rl_gemm_w8a8(Xq, Xs, Wq, Ws, Y=Y, workspace=iws), reps, flush)
+            del iws
             i8[f"{s.name}_M{M}"] = {"gemm_us": ms * 1e3,
                                     "gemm_gbs": int8_gemm_bytes(M, s.N, s.K) / (ms * 1e-3) / 1e9,
                                     "gemm_tops": 2 * M * s.N * s.K / (ms * 1e-3) / 1e12}
