@@ -682,6 +682,26 @@ def profile_case(fb, case, dev, reps=3):
         Xq, Xs = fb.fp8rl_quant_act_group(synth.activation(M, s.K, synth.seed_for(2, 1), device=dev))
         for _ in range(reps):
             fb.fp8rl_gemm_w8a8_block(Xq, Xs, Wq, Ws)
+    elif case.startswith("decode7b_qkv_m"):
+        M = int(case[len("decode7b_qkv_m"):])
+        s = synth.QWEN25_7B[0]                          # qkv 3584 -> 4608
+        W = synth.weight_bf16_direct(s.N, s.K, synth.seed_for(2, 0), device=dev)
+        Wq, Ws = fb.fp8rl_quant_weight_block(W)
+        del W
+        Xq, Xs = fb.fp8rl_quant_act_group(synth.activation(M, s.K, synth.seed_for(2, 1), device=dev))
+        ws = torch.empty(max(16, fb.fp8rl_gemm_workspace_bytes(M, s.N, s.K)), dtype=torch.uint8, device=dev)
+        for _ in range(reps):
+            fb.fp8rl_gemm_w8a8_block(Xq, Xs, Wq, Ws, workspace=ws)
+    elif case.startswith("int8_qkv_m"):
+        M = int(case[len("int8_qkv_m"):])
+        s = synth.QWEN25_32B[0]                         # qkv 5120 -> 7168
+        W = synth.weight_bf16_direct(s.N, s.K, synth.seed_for(5, 0), device=dev)
+        Wq, Ws = fb.int8rl_quant_weight_channel(W)
+        del W
+        Xq, Xs = fb.int8rl_quant_act_token(synth.activation(M, s.K, synth.seed_for(5, 1), device=dev))
+        ws = torch.empty(max(16, fb.int8rl_gemm_workspace_bytes(M, s.N, s.K)), dtype=torch.uint8, device=dev)
+        for _ in range(reps):
+            fb.int8rl_gemm_w8a8(Xq, Xs, Wq, Ws, workspace=ws)
     elif case.startswith("decode7b_down_m"):
         M = int(case[len("decode7b_down_m"):])
         s = synth.QWEN25_7B[3]                          # down 18944 -> 3584
@@ -783,8 +803,9 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--profile", default=None,
-                    help="run one small case for ncu: requant | decode | decode7b_m<M> | decode7b_down_m<M> | decode32b_m<M> | "
-                         "prefill | prefill_down_m<M> | int8 | int8_m32 | kv | tis | moe | kl")
+                    help="run one small case for ncu: requant | decode | decode7b_m<M> | decode7b_qkv_m<M> | "
+                         "decode7b_down_m<M> | decode32b_m<M> | prefill | prefill_down_m<M> | int8 | int8_m32 | "
+                         "int8_qkv_m<M> | kv | tis | moe | kl")
     args = ap.parse_args()
     world, rank, local = dist_env()
     if args.impl == "reference":

@@ -261,30 +261,44 @@ gemm_int8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
     }
 }
 
-// int8 -> fp16, 16 codes per thread and step: v ^ 0x80 = v + 128 in the low
-// byte of the fp16 0x6400 | b = 1024 + b, so (1152 + v) - 1152 = v exactly.
+// int8 -> fp16: v ^ 0x80 = v + 128 in the low byte of the fp16 0x6400 | b =
+// 1024 + b, so (1152 + v) - 1152 = v exactly.
+__device__ __forceinline__ void i8x16_to_f16(const uint4 v, uint4* dst) {
+    const __half2 off = __floats2half2_rn(1152.f, 1152.f);
+    const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
+    uint32_t o[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        uint32_t lo = __byte_perm(w[k], 0x64646464u, 0x4140), hi = __byte_perm(w[k], 0x64646464u, 0x4342);
+        __half2 hl = __hsub2(*reinterpret_cast<__half2*>(&lo), off);
+        __half2 hh = __hsub2(*reinterpret_cast<__half2*>(&hi), off);
+        o[2 * k] = *reinterpret_cast<uint32_t*>(&hl);
+        o[2 * k + 1] = *reinterpret_cast<uint32_t*>(&hh);
+    }
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// X codes then W codes, 16 per chunk, into one fp16 array; each thread has
+// four 16-byte loads in flight per step.
 __global__ void __launch_bounds__(256)
 int8_to_f16_kernel(const int8_t* __restrict__ a, int64_t na16, const int8_t* __restrict__ b, int64_t nb16,
                    uint16_t* __restrict__ out) {
     pdl_wait_then_release();
     const int64_t total = na16 + nb16;
-    const __half2 off = __floats2half2_rn(1152.f, 1152.f);
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-        const int8_t* src = i < na16 ? a + i * 16 : b + (i - na16) * 16;
-        const uint4 v = ld_stream_v4(reinterpret_cast<const uint16_t*>(src));
-        const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
-        uint32_t o[8];
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < total; i0 += 4 * stride) {
+        uint4 v[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            uint32_t lo = __byte_perm(w[k], 0x64646464u, 0x4140), hi = __byte_perm(w[k], 0x64646464u, 0x4342);
-            __half2 hl = __hsub2(*reinterpret_cast<__half2*>(&lo), off);
-            __half2 hh = __hsub2(*reinterpret_cast<__half2*>(&hi), off);
-            o[2 * k] = *reinterpret_cast<uint32_t*>(&hl);
-            o[2 * k + 1] = *reinterpret_cast<uint32_t*>(&hh);
+        for (int u = 0; u < 4; ++u) {
+            const int64_t i = i0 + u * stride;
+            if (i < total) v[u] = ld_stream_v4(i < na16 ? a + i * 16 : b + (i - na16) * 16);
         }
-        uint4* dst = reinterpret_cast<uint4*>(out + i * 16);
-        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t i = i0 + u * stride;
+            if (i < total) i8x16_to_f16(v[u], reinterpret_cast<uint4*>(out + i * 16));
+        }
     }
 }
 
