@@ -215,11 +215,13 @@ int int8rl_quant_act_token(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
  * Xq [M][K] int8, Xs [M] fp32, Wq [N][K] int8, Ws [N] fp32, Y bf16 [M][ldy].
  * acc_or_null: optional int32 [M][N] copy of the accumulators (8-byte aligned).
  * workspace: device scratch, 16-byte aligned, of int8rl_gemm_workspace_bytes(M,
- * N, K) bytes: (M + N) * K * 2 for batches of 256 tokens or more whose
- * 128 x 256 output tiles fill the GPU, else 0.  It receives fp16 copies of Xq
- * and Wq (exact), which the large-batch kernel multiplies on the fp16 tensor
- * path; with less workspace (or NULL) the call still succeeds on the
- * small-batch kernel (slower for those shapes).  Not zeroed, nothing kept
+ * N, K) bytes: nonzero for batches of 256 tokens or more with enough 128 x 256
+ * output tiles (or tiles x K ranges) for half of the GPU.  It receives fp16
+ * copies of Xq and Wq ((M + N) * K * 2 bytes, exact), which the large-batch
+ * kernel multiplies on the fp16 tensor path, and, when its tiles are too few
+ * for the GPU, the int32 partial tiles of its K ranges (added exactly by a
+ * second launch).  With less workspace (or NULL) the call still succeeds on
+ * the small-batch kernel (slower for those shapes).  Not zeroed, nothing kept
  * between calls; two calls in flight at once need two workspaces.
  * ---------------------------------------------------------------------- */
 size_t int8rl_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);

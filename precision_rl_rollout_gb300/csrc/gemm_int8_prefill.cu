@@ -20,7 +20,10 @@
 //    alternate between groups;
 //  - the epilogue converts each group's sums to int32 (exact) and adds them in
 //    int32 registers; at the end of a tile it writes Y (bf16, TMA store) and,
-//    if asked, the int32 accumulators.
+//    if asked, the int32 accumulators;
+//  - with fewer tiles than SMs (a few hundred tokens), a work unit is a tile's
+//    K range; each unit writes its int32 partial tile to the workspace and a
+//    second launch adds them (integers: exact in any order) and writes Y.
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -66,7 +69,16 @@ struct I8pParams {
     int64_t M, N;
     int KS;            // K / 64
     int mtiles, ntiles;
+    int split, ks_per;  // K ranges per tile and stages per range (split 1: whole tiles)
+    int32_t* part;      // split > 1: int32 partial tiles [tiles * split][128][256]
 };
+
+// Work unit u: tile u / split, stages [ks_beg, ks_end) of K.
+__device__ __forceinline__ void i8p_unit(int u, const I8pParams& p, int& tile, int& ks_beg, int& ks_end) {
+    tile = u / p.split;
+    ks_beg = (u - tile * p.split) * p.ks_per;
+    ks_end = min(p.KS, ks_beg + p.ks_per);
+}
 
 __device__ __forceinline__ void record_timeout(uint32_t* err, uint32_t site, volatile int* abort) {
     atomicCAS(err, 0u, (kKernelInt8Prefill << 24) | (site << 16) | 1u);
@@ -84,8 +96,7 @@ gemm_int8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
     const uint32_t tfull0 = smem_u32(bars + 2 * kStages), tempty0 = smem_u32(bars + 2 * kStages + 2);
     const uint32_t warp = warp_id(), lane = lane_id();
-    const int tiles = p.mtiles * p.ntiles;
-    const int ngroups = (p.KS + kGroup - 1) / kGroup;
+    const int units = p.mtiles * p.ntiles * p.split;
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -116,9 +127,11 @@ gemm_int8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
             // ---------------- TMA producer
             const uint64_t pol_x = policy_evict_last(), pol_w = policy_evict_first();
             uint32_t it = 0;
-            for (int u = blockIdx.x; u < tiles && !*abort; u += gridDim.x) {
-                const int mt = u % p.mtiles, nt = u / p.mtiles;
-                for (int ks = 0; ks < p.KS; ++ks, ++it) {
+            for (int u = blockIdx.x; u < units && !*abort; u += gridDim.x) {
+                int tile, ks_beg, ks_end;
+                i8p_unit(u, p, tile, ks_beg, ks_end);
+                const int mt = tile % p.mtiles, nt = tile / p.mtiles;
+                for (int ks = ks_beg; ks < ks_end; ++ks, ++it) {
                     const int s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1;
                     if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1, abort, kWaitLimitNs)) {
@@ -137,8 +150,10 @@ gemm_int8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
         } else if (warp == 1 && lane == 0) {
             // ---------------- MMA issuer: one group of 8 stages per TMEM buffer
             uint32_t it = 0, gi = 0;
-            for (int u = blockIdx.x; u < tiles && !*abort; u += gridDim.x) {
-                for (int g = 0; g < ngroups && !*abort; ++g, ++gi) {
+            for (int u = blockIdx.x; u < units && !*abort; u += gridDim.x) {
+                int tile, ks_beg, ks_end;
+                i8p_unit(u, p, tile, ks_beg, ks_end);
+                for (int g0 = ks_beg; g0 < ks_end && !*abort; g0 += kGroup, ++gi) {
                     const uint32_t buf = gi & 1, bph = (gi >> 1) & 1;
                     if (!mbar_wait_bounded(tempty0 + 8 * buf, bph ^ 1, abort, kWaitLimitNs)) {
                         record_timeout(p.err, 3, abort);
@@ -146,8 +161,8 @@ gemm_int8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
                     }
                     tc_fence_after();
                     const uint32_t d = tmem_base + buf * kBN;
-                    const int ks_end = min(p.KS, (g + 1) * kGroup);
-                    for (int ks = g * kGroup; ks < ks_end; ++ks, ++it) {
+                    const int g_end = min(ks_end, g0 + kGroup);
+                    for (int ks = g0; ks < g_end; ++ks, ++it) {
                         const int s = it % kStages;
                         const uint32_t ph = (it / kStages) & 1;
                         if (!mbar_wait_bounded(full0 + 8 * s, ph, abort, kWaitLimitNs)) {
@@ -160,7 +175,7 @@ gemm_int8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
                         const uint64_t b = umma_desc_k128_sw128(smem_u32(st + kABytes));
 #pragma unroll
                         for (int k = 0; k < 4; ++k)      // 4 x K=16 per 64-wide atom; +32 B = +2 in the address field
-                            mma_f16(d, a + 2 * k, b + 2 * k, kIdesc, (ks > g * kGroup || k > 0) ? 1u : 0u);
+                            mma_f16(d, a + 2 * k, b + 2 * k, kIdesc, (ks > g0 || k > 0) ? 1u : 0u);
                         tc_commit(empty0 + 8 * s);
                     }
                     tc_commit(tfull0 + 8 * buf);
@@ -177,14 +192,16 @@ gemm_int8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
         const int NB = (int)(p.N / 128);
         uint32_t gi = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < tiles && ok; u += gridDim.x) {
-            const int mt = u % p.mtiles, nt = u / p.mtiles;
+        for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+            int tile, ks_beg, ks_end;
+            i8p_unit(u, p, tile, ks_beg, ks_end);
+            const int mt = tile % p.mtiles, nt = tile / p.mtiles;
             const int64_t m = (int64_t)mt * kBM + row;
             const int nb = 2 * nt + h;
             int32_t acc[128];
 #pragma unroll
             for (int j = 0; j < 128; ++j) acc[j] = 0;
-            for (int g = 0; g < ngroups; ++g, ++gi) {
+            for (int g0 = ks_beg; g0 < ks_end; g0 += kGroup, ++gi) {
                 const uint32_t buf = gi & 1, bph = (gi >> 1) & 1;
                 // the verdict is made warp-uniform: the TMEM loads below are warp-collective
                 if (!__all_sync(0xffffffffu, mbar_wait_bounded(tfull0 + 8 * buf, bph, abort, kWaitLimitNs))) {
@@ -210,6 +227,13 @@ gemm_int8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
                 for (int j = 0; j < 64; ++j) acc[64 + j] += __float2int_rn(__uint_as_float(r[j]));
             }
             if (!ok) break;
+            if (p.split > 1) {
+                // this K range's int32 partial: the thread's row, its half's 128 columns
+                int4* dst = reinterpret_cast<int4*>(p.part + ((int64_t)u * kBM + row) * kBN + h * 128);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) dst[j] = make_int4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+                continue;
+            }
             if (nb >= NB) continue;                         // N % 256 == 128: no second half
             const bool live = m < p.M;
             if (p.acc != nullptr && live) {             // 8-byte stores: acc is 8-byte aligned
@@ -221,7 +245,7 @@ gemm_int8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
             // columns as two 32 x 64 boxes, staged with the 128-byte swizzle and
             // written by TMA stores (rows beyond M are clipped by the store)
             const float xs = live ? __ldg(p.Xs + m) : 0.f;
-            const float4* ws4 = reinterpret_cast<const float4*>(p.Ws + (int64_t)nb * 128);
+            const float* wsn = p.Ws + (int64_t)nb * 128;       // 4-byte aligned: scalar loads
             uint8_t* stage = smem + kOutOffset + e * kOutBytesPerWarp;
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
@@ -230,11 +254,10 @@ gemm_int8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const int c0 = c * 64 + 8 * j;
-                    const float4 wa = __ldg(ws4 + c0 / 4), wb = __ldg(ws4 + c0 / 4 + 1);
-                    const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
                     float y[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(__fmul_rn(__int2float_rn(acc[c0 + i]), xs), w[i]);
+                    for (int i = 0; i < 8; ++i)
+                        y[i] = __fmul_rn(__fmul_rn(__int2float_rn(acc[c0 + i]), xs), __ldg(wsn + c0 + i));
                     uint4 o;
                     o.x = pack_bf16x2(y[0], y[1]);
                     o.y = pack_bf16x2(y[2], y[3]);
@@ -302,6 +325,57 @@ int8_to_f16_kernel(const int8_t* __restrict__ a, int64_t na16, const int8_t* __r
     }
 }
 
+// Split-K reduction: one thread per (tile row, 8 columns); the ranges' int32
+// partials are added (exact in any order), then Y = bf16((float(acc) * Xs[m]) *
+// Ws[n]) as in the GEMM's own epilogue, and acc if asked.
+__global__ void __launch_bounds__(256)
+i8p_reduce_kernel(const int32_t* __restrict__ part, const float* __restrict__ Xs, const float* __restrict__ Ws,
+                  int64_t M, int64_t N, int mtiles, int split, int64_t units8, uint16_t* __restrict__ Y, int64_t ldy,
+                  int32_t* __restrict__ acc) {
+    pdl_wait_then_release();
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= units8) return;
+    const int64_t tile = t >> 12;                     // 128 rows x 32 eight-column chunks per tile
+    const int r = (int)((t >> 5) & 127), c8 = (int)(t & 31);
+    const int mt = (int)(tile % mtiles), nt = (int)(tile / mtiles);
+    const int64_t m = (int64_t)mt * kBM + r, n = (int64_t)nt * kBN + c8 * 8;
+    if (m >= M || n >= N) return;
+    const int32_t* base = part + ((tile * split) * kBM + r) * kBN + c8 * 8;
+    const int64_t stride = (int64_t)kBM * kBN;         // one range's partial tile
+    int32_t sum[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int sp0 = 0; sp0 < split; sp0 += 4) {
+        int4 v[4][2];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (sp0 + j < split) {
+                const int4* src = reinterpret_cast<const int4*>(base + (sp0 + j) * stride);
+                v[j][0] = src[0];
+                v[j][1] = src[1];
+            }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (sp0 + j < split) {
+                sum[0] += v[j][0].x; sum[1] += v[j][0].y; sum[2] += v[j][0].z; sum[3] += v[j][0].w;
+                sum[4] += v[j][1].x; sum[5] += v[j][1].y; sum[6] += v[j][1].z; sum[7] += v[j][1].w;
+            }
+    }
+    if (acc != nullptr) {                              // 8-byte aligned
+        int2* d = reinterpret_cast<int2*>(acc + m * N + n);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) d[i] = make_int2(sum[2 * i], sum[2 * i + 1]);
+    }
+    const float xs = __ldg(Xs + m);
+    float y[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(__fmul_rn(__int2float_rn(sum[i]), xs), __ldg(Ws + n + i));
+    uint4 o;
+    o.x = pack_bf16x2(y[0], y[1]);
+    o.y = pack_bf16x2(y[2], y[3]);
+    o.z = pack_bf16x2(y[4], y[5]);
+    o.w = pack_bf16x2(y[6], y[7]);
+    *reinterpret_cast<uint4*>(Y + m * ldy + n) = o;
+}
+
 // The register split (setmaxnreg) assumes exactly kLaunchRegs registers per
 // thread at launch; any other build is refused.  Checked (and the shared memory
 // attribute set) once per device.
@@ -323,17 +397,42 @@ int i8p_ready(int dev) {
 
 }  // namespace
 
-// The large-batch path: 256 tokens or more, and enough 128 x 256 tiles to
-// occupy every SM (smaller shapes stay on the small-batch kernel).
-bool int8_prefill_applies(int64_t M, int64_t N, int64_t K) {
-    (void)K;
+// K ranges per tile: with fewer tiles than SMs, enough ranges that about one
+// wave of units runs, each at least two exact groups (16 stages) long and
+// aligned to a group; at most 8.
+struct I8pPlan {
+    int split, ks_per;
+};
+
+static I8pPlan i8p_plan(int64_t M, int64_t N, int64_t K) {
     const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
-    return M >= 256 && tiles >= num_sms();
+    const int KS = (int)(K / 64);
+    const int64_t sms = num_sms();
+    int64_t s = tiles >= sms ? 1 : sms / tiles;
+    if (s > KS / 16) s = KS / 16;
+    if (s > 8) s = 8;
+    if (s < 2) return I8pPlan{1, KS};
+    int per = (int)((KS + s - 1) / s);
+    per = (per + kGroup - 1) / kGroup * kGroup;
+    return I8pPlan{(KS + per - 1) / per, per};
 }
 
-// fp16 copies of X [M][K] and W [N][K], back to back.
+// The large-batch path: 256 tokens or more, with enough work units (tiles, or
+// tiles x K ranges) for at least half of the SMs.
+bool int8_prefill_applies(int64_t M, int64_t N, int64_t K) {
+    if (M < 256) return false;
+    const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
+    return tiles * i8p_plan(M, N, K).split * 2 >= num_sms();
+}
+
+// fp16 copies of X [M][K] and W [N][K], back to back, then (split K) the int32
+// partial tiles.
 size_t int8_prefill_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-    return int8_prefill_applies(M, N, K) ? (size_t)(M + N) * (size_t)K * 2 : 0;
+    if (!int8_prefill_applies(M, N, K)) return 0;
+    const I8pPlan pl = i8p_plan(M, N, K);
+    const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
+    const size_t parts = pl.split > 1 ? (size_t)tiles * pl.split * kBM * kBN * sizeof(int32_t) : 0;
+    return (size_t)(M + N) * (size_t)K * 2 + parts;
 }
 
 cudaError_t launch_gemm_int8_prefill(const int8_t* Xq, const float* Xs, const int8_t* Wq, const float* Ws,
@@ -342,8 +441,10 @@ cudaError_t launch_gemm_int8_prefill(const int8_t* Xq, const float* Xs, const in
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
     if (i8p_ready(dev) != 1) return cudaErrorInvalidDeviceFunction;
+    const I8pPlan pl = i8p_plan(M, N, K);
     uint16_t* X16 = static_cast<uint16_t*>(ws);
     uint16_t* W16 = X16 + M * K;
+    int32_t* part = pl.split > 1 ? reinterpret_cast<int32_t*>(W16 + N * K) : nullptr;   // 16-byte aligned
     CUtensorMap tmX, tmW, tmY;
     if (!make_tmap_f16_load(&tmX, X16, (uint64_t)M, (uint64_t)K, kBM)) return cudaErrorInvalidValue;
     if (!make_tmap_f16_load(&tmW, W16, (uint64_t)N, (uint64_t)K, kBN)) return cudaErrorInvalidValue;
@@ -355,10 +456,15 @@ cudaError_t launch_gemm_int8_prefill(const int8_t* Xq, const float* Xs, const in
     cudaError_t e = launch_pdl(int8_to_f16_kernel, dim3((unsigned)cvt_blocks), dim3(256), 0, st, Xq, na16, Wq, nb16,
                                X16);
     if (e != cudaSuccess) return e;
-    I8pParams prm{err, Xs, Ws, acc, M, N, (int)(K / 64), (int)((M + kBM - 1) / kBM), (int)((N + kBN - 1) / kBN)};
-    const int64_t tiles = (int64_t)prm.mtiles * prm.ntiles;
-    const int grid = tiles < num_sms() ? (int)tiles : num_sms();
-    return launch_pdl(gemm_int8_prefill_kernel, dim3(grid), dim3(kThreads), kSmemBytes, st, tmX, tmW, tmY, prm);
+    I8pParams prm{err, Xs, Ws, acc, M, N, (int)(K / 64), (int)((M + kBM - 1) / kBM), (int)((N + kBN - 1) / kBN),
+                  pl.split, pl.ks_per, part};
+    const int64_t tiles = (int64_t)prm.mtiles * prm.ntiles, units = tiles * pl.split;
+    const int grid = units < num_sms() ? (int)units : num_sms();
+    e = launch_pdl(gemm_int8_prefill_kernel, dim3(grid), dim3(kThreads), kSmemBytes, st, tmX, tmW, tmY, prm);
+    if (e != cudaSuccess || pl.split == 1) return e;
+    const int64_t units8 = tiles * kBM * 32;
+    return launch_pdl(i8p_reduce_kernel, dim3((unsigned)((units8 + 255) / 256)), dim3(256), 0, st,
+                      (const int32_t*)part, Xs, Ws, M, N, prm.mtiles, pl.split, units8, Y, ldy, acc);
 }
 
 }  // namespace fp8rl

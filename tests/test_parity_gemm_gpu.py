@@ -179,6 +179,23 @@ def test_int8_gemm_large_batch_path_ragged(cuda_lib):
         assert np.array_equal(got_y, want_y), f"Y differs at {np.argwhere(got_y != want_y)[:4].tolist()}"
 
 
+def test_int8_gemm_large_batch_split_k_ragged(cuda_lib):
+    # 3 x 11 = 33 tiles, too few for the GPU: each tile's K (4096) is split in
+    # 4 ranges of 16 stages, whose int32 partials a second launch adds; M = 300
+    # leaves a partial token tile and N = 2688 a last tile with one half beyond N
+    M, N, K = 300, 2688, 4096
+    need = fb.int8rl_gemm_workspace_bytes(M, N, K)
+    assert need > (M + N) * K * 2                      # fp16 copies + int32 partials
+    Wq, Ws = oracle_int8_weight(N, K, 99)
+    Xq, Xs = oracle_int8_act(M, K, 100)
+    rows = np.array([0, 1, 127, 128, 255, 256, 290, 299])
+    want_acc, want_y = oracle.int8_gemm(Xq[rows], Xs[rows], Wq, Ws)
+    Y, acc = fb.int8rl_gemm_w8a8(dev(Xq), dev(Xs), dev(Wq), dev(Ws), want_acc=True)
+    got_acc, got_y = host(acc)[rows], host(Y)[rows]
+    assert np.array_equal(got_acc, want_acc), f"acc differs at {np.argwhere(got_acc != want_acc)[:4].tolist()}"
+    assert np.array_equal(got_y, want_y), f"Y differs at {np.argwhere(got_y != want_y)[:4].tolist()}"
+
+
 def test_int8_gemm_large_batch_extreme_codes_exact(cuda_lib):
     # every code at +-127 over K = 8192 (16 exact TMEM groups of 512) on the
     # large-batch path: |acc| = 127^2 K
