@@ -19,10 +19,14 @@
 // Layout (swap-AB, as the FP8 decode kernel): the MMA's M side is 128 weight
 // rows, its N side a tile of MT tokens; each CTA streams one 128-row weight
 // slab.  Warp 0 issues TMA (raw int8 tiles, 128-byte swizzle), warp 1 the
-// MMAs, warps 2-9 (two groups, alternate K blocks) convert raw tiles to fp16
-// operand tiles in the UMMA K-major 128-byte-swizzle layout (a 128-wide K
-// block is two 64-wide atoms), warps 10-13 promote and hold the int32
-// accumulators.  Split-K CTAs of one slab form a
+// MMAs, warps 2-9 (two groups, alternate K blocks) convert raw tiles to fp16,
+// warps 10-13 promote and hold the int32 accumulators.  The converted weight
+// block goes to tensor memory, where the MMA reads its A operand (one weight
+// row per TMEM lane, K packed along the columns); only the small token tile
+// is written back to shared memory (UMMA K-major 128-byte-swizzle layout, two
+// 64-wide atoms per K block).  Shared memory then carries about 56 KB per
+// 16 KB weight block instead of 120 KB: with the fp16 weights in shared memory
+// its bandwidth, not HBM, set the pace.  Split-K CTAs of one slab form a
 // cluster and add their int32 partials through distributed shared memory.
 #include <cuda_fp16.h>
 
@@ -58,18 +62,20 @@ struct I8Cfg {
     static constexpr int kThreads = 448;                       // 14 warps
     static constexpr int kRawW = 128 * 128, kRawX = MT * 128;  // int8 tiles
     static constexpr int kRawStage = kRawW + kRawX;
-    // raw int8 stages fill what the fp16 stages leave of ~220 KB: the weight
-    // bytes in flight per SM keep the HBM stream going, and a third fp16 stage
-    // lets the converters run a block ahead of the MMAs (measured on the 32B
-    // shapes at M = 32..128: 8-15% faster than 7-8 raw stages and two fp16 ones)
-    static constexpr int kRawStages = MT == 16 ? 6 : MT == 32 ? 5 : 3;
-    static constexpr int kCvtW = 2 * 128 * 128, kCvtX = 2 * MT * 128;   // fp16: two 64-wide atoms
-    static constexpr int kCvtStage = kCvtW + kCvtX;
-    static constexpr int kCvtStages = 3;
+    // raw int8 stages fill what the fp16 token tiles leave of ~215 KB: the
+    // weight bytes in flight per SM keep the HBM stream going
+    static constexpr int kRawStages = MT == 16 ? 11 : MT == 32 ? 9 : 6;
+    static constexpr int kCvtStage = 2 * MT * 128;               // fp16 token tile: two 64-wide atoms
+    static constexpr int kCvtStages = 4;                         // = fp16 weight blocks in TMEM
     static constexpr int kCvtOffset = kRawStages * kRawStage;
     static constexpr int kBarOffset = kCvtOffset + kCvtStages * kCvtStage;
-    static constexpr int kSmemBytes = kBarOffset + 256 + 1024;
-    static constexpr int kTmemCols = 2 * MT < 32 ? 32 : 2 * MT;
+    static constexpr int kSmemBytes = kBarOffset + 512 + 1024;
+    // TMEM: two accumulator buffers of MT columns at 0, then the fp16 weight
+    // blocks (128 lanes x 64 columns each) from column kTmemA
+    static constexpr int kTmemA = 256;
+    static constexpr int kTmemCols = 512;
+    static_assert(2 * MT <= kTmemA && kTmemA + 64 * kCvtStages <= kTmemCols, "TMEM layout");
+    static_assert((2 * kRawStages + 2 * kCvtStages + 4) * 8 + 8 <= 512, "barrier area");
     static constexpr int kChunk = MT >= 32 ? 32 : 16;
     static_assert(MT * 128 * 4 <= kRawStages * kRawStage, "reduction buffer must fit the raw stages");
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -203,22 +209,25 @@ gemm_int8_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
                 tc_fence_after();
                 const uint8_t* st = smem + C::kCvtOffset + s * C::kCvtStage;
                 const uint32_t d = tmem_base + buf * MT;
+                const uint32_t a = tmem_base + C::kTmemA + s * 64;     // weight block s: 64 columns
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {        // K = 16 fp16 = 32 bytes per step; 4 steps per atom
-                    const uint64_t a = umma_desc_k128_sw128(smem_u32(st + (k >> 2) * (128 * 128))) + 2 * (k & 3);
-                    const uint64_t b = umma_desc_k128_sw128(smem_u32(st + C::kCvtW + (k >> 2) * (MT * 128))) + 2 * (k & 3);
-                    mma_f16(d, a, b, idesc, (first && k == 0) ? 0u : 1u);
+                for (int k = 0; k < 8; ++k) {        // K = 16 fp16 = 8 TMEM columns / 32 bytes per step
+                    const uint64_t b = umma_desc_k128_sw128(smem_u32(st + (k >> 2) * (MT * 128))) + 2 * (k & 3);
+                    mma_f16_tmem_a(d, a + 8 * k, b, idesc, (first && k == 0) ? 0u : 1u);
                 }
                 tc_commit(cempty0 + 8 * s);
                 if (last) tc_commit(tfull0 + 8 * buf);
             }
         }
     } else if (warp < 10) {
-        // ---------------- converters: raw int8 -> fp16 operand tiles.  Two
-        // groups of four warps take alternate K blocks (block it goes to fp16
-        // stage it % V), so two blocks are converted concurrently.
+        // ---------------- converters: raw int8 -> fp16.  Two groups of four
+        // warps take alternate K blocks (block it goes to TMEM weight block and
+        // token stage it % V), so two blocks are converted concurrently.  A
+        // warp may write only its own quarter of the TMEM lanes, so its thread
+        // converts weight row 32 * (warp % 4) + lane.
         const int grp = (warp - 2) >> 2;
-        const int t = ((warp - 2) & 3) * 32 + lane;  // 0..127
+        const int t = (int)(warp & 3) * 32 + lane;  // 0..127
+        const uint32_t lane_addr = tmem_base + ((uint32_t)(32 * (warp & 3)) << 16) + C::kTmemA;
         for (int it = grp; it < nkb; it += 2) {
             const int rs = it % R, cs = it % V;
             const uint32_t rph = (it / R) & 1, cph = (it / V) & 1;
@@ -229,9 +238,25 @@ gemm_int8_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
             }
             const uint8_t* raw = smem + rs * C::kRawStage;
             uint8_t* cvt = smem + C::kCvtOffset + cs * C::kCvtStage;
-            convert_row(raw, cvt, t, 128 * 128);                               // weight row t
-            if (t < MT) convert_row(raw + C::kRawW, cvt + C::kCvtW, t, MT * 128);   // token row t
+            // weight row t: 128 codes -> 64 columns of fp16 pairs in TMEM
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t r[32];
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    const int c = 4 * h + c4;        // 16-byte chunk: K codes 16c .. 16c + 15
+                    const uint4 v = *reinterpret_cast<const uint4*>(raw + t * 128 + ((c ^ (t & 7)) << 4));
+                    i8x4_to_f16x4(v.x, r[8 * c4 + 0], r[8 * c4 + 1]);
+                    i8x4_to_f16x4(v.y, r[8 * c4 + 2], r[8 * c4 + 3]);
+                    i8x4_to_f16x4(v.z, r[8 * c4 + 4], r[8 * c4 + 5]);
+                    i8x4_to_f16x4(v.w, r[8 * c4 + 6], r[8 * c4 + 7]);
+                }
+                tmem_st_32x32b_x32(lane_addr + cs * 64 + 32 * h, r);
+            }
+            if (t < MT) convert_row(raw + C::kRawW, cvt, t, MT * 128);   // token row t
+            tmem_wait_st();
             fence_proxy_async_smem();                // generic writes -> tensor-core reads
+            tc_fence_before();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(cfull0 + 8 * cs);
