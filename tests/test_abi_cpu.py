@@ -149,6 +149,27 @@ def test_gemm_validation(lib):
     assert i(A, A, A, A, 0, 128, 128, A, 128, None, None, 0, None) == 0
 
 
+def test_int8_large_batch_workspace_holds_the_fp16_copies(lib):
+    # 256+ tokens with plenty of 128 x 256 tiles: fp16 copies of X and W and
+    # nothing else (no split); a batch of 32 tokens needs none
+    M, N, K = 4096, 7168, 5120
+    assert lib.int8rl_gemm_workspace_bytes(M, N, K) == (M + N) * K * 2
+    assert lib.int8rl_gemm_workspace_bytes(32, N, K) == 0
+    # few tiles (M = 256 against N = 7168): the copies plus int32 partial tiles
+    need = lib.int8rl_gemm_workspace_bytes(256, N, K)
+    assert need > (256 + N) * K * 2
+    assert (need - (256 + N) * K * 2) % (128 * 256 * 4) == 0
+
+
+def test_fp8_gemm_workspace_is_whole_partial_tiles(lib):
+    # whatever path a shape takes, its workspace is a whole number of fp32
+    # partial tiles (decode: 128 channels x 16..128 tokens; prefill: 128 x 256)
+    for M, N, K in [(1, 4608, 3584), (16, 3584, 18944), (32, 5120, 5120), (64, 3584, 18944),
+                    (256, 5120, 27648), (300, 256, 4096)]:
+        ws = lib.fp8rl_gemm_workspace_bytes(M, N, K)
+        assert ws % (128 * 16 * 4) == 0, (M, N, K, ws)
+
+
 def test_gemm_workspace_query_is_monotone(lib):
     for f in (lib.fp8rl_gemm_workspace_bytes, lib.int8rl_gemm_workspace_bytes):
         a = f(1, 4608, 3584)
