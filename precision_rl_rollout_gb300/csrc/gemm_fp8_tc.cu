@@ -17,9 +17,10 @@
 // the Long Tail" (ASPLOS'26 blog), section 3.2 roofline and section 4.3.1):
 // swap-AB -- the MMA's M side is 128 weight rows, its N side the (padded)
 // tokens -- so each CTA streams a disjoint 128-row weight slab exactly once.
-// Split-K CTAs of one slab form a thread-block cluster and add their fp32
-// partials through distributed shared memory in a fixed order
-// (deterministic; no global workspace).
+// The split-K CTAs of one slab add their fp32 partials in a fixed order
+// (deterministic) in one of three ways: in a cluster, through distributed
+// shared memory or through the caller's workspace in L2; or, without a
+// cluster, through the workspace and a second launch (see the plan below).
 //
 // Grouped form (mixture-of-experts layers; FP8-RL, Abstract: dense and MoE
 // models): the weights of E experts are stacked as [E*N][K] and the token rows
