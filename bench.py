@@ -369,8 +369,32 @@ def _copies_for(nbytes):
     return max(2, -(-3 * L2_BYTES // max(1, nbytes)))
 
 
+def quantization_error(fb, dev):
+    """For information: the 8-bit linear layers against the unquantized bf16
+    matmul (fp32 accumulation by torch) on the Qwen2.5-7B layer set at M = 64.
+    Relative Frobenius error of Y and the largest |error| over rms(Y_ref)."""
+    res = {}
+    for i, s in enumerate(synth.QWEN25_7B):
+        W = synth.weight_bf16_direct(s.N, s.K, synth.seed_for(2, 0) + i, device=dev)
+        X = synth.activation(DECODE_M, s.K, synth.seed_for(2, 1) + i, device=dev)
+        ref = X.float() @ W.float().t()
+        Wq, Ws = fb.fp8rl_quant_weight_block(W)
+        y8 = fb.fp8rl_linear_w8a8_block(X, Wq, Ws).float()
+        Wi, Wsi = fb.int8rl_quant_weight_channel(W)
+        Xi, Xsi = fb.int8rl_quant_act_token(X)
+        yi = fb.int8rl_gemm_w8a8(Xi, Xsi, Wi, Wsi).float()
+        rms = ref.pow(2).mean().sqrt()
+        res[s.name] = {"fp8_rel_fro": float((y8 - ref).norm() / ref.norm()),
+                       "fp8_max_over_rms": float((y8 - ref).abs().max() / rms),
+                       "int8_rel_fro": float((yi - ref).norm() / ref.norm()),
+                       "int8_max_over_rms": float((yi - ref).abs().max() / rms)}
+        del W, X, ref, Wq, Ws, Wi, Wsi, Xi, Xsi
+    return res
+
+
 def extras(fb, dev, reps=5):
     out = {}
+    out["error_vs_unquantized_bf16_7b_m64"] = quantization_error(fb, dev)
     flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     flush = lambda: _flush_l2(flush_buf)  # noqa: E731
 
