@@ -554,17 +554,22 @@ static DecodePlan decode_plan(int64_t tiles, int KB, bool may_use_memory) {
     using C = DecodeCfg<MT>;
     constexpr int kMaxMemSplit = 16;
     const int64_t sms = num_sms();
+    // the largest split whose clusters all run at once (0: none)
+    int one_wave = 0;
+    for (int s = C::kMaxSplit; s >= 1 && one_wave == 0; --s)
+        if (split_fits(KB, s, C::kMaxKbPerSplit) && clusters_per_wave<MT>(s) >= tiles) one_wave = s;
+    // 64-token tiles on long K (>= 40 blocks) with a split of 6 or more: the
+    // in-cluster exchange through L2 beats the second launch (7B down at M=64:
+    // 18.1 -> 16.9 us); on short K the second launch at one CTA per SM wins
+    if (may_use_memory && MT == 64 && KB >= 40 && one_wave >= 6) return DecodePlan{one_wave, kXchgClusterMem};
     if (may_use_memory && MT >= 64) {
         int64_t t = sms / tiles;
         int s = (int)(t < kMaxMemSplit ? t : kMaxMemSplit);
         while (s >= 2 && !split_fits(KB, s, C::kMaxKbPerSplit)) --s;
         if (s >= 2) return DecodePlan{s, kXchgReduceLaunch};
     }
-    for (int s = C::kMaxSplit; MT <= 32 && s >= 1; --s) {
-        if (!split_fits(KB, s, C::kMaxKbPerSplit)) continue;
-        const int64_t cpw = clusters_per_wave<MT>(s);
-        if (cpw > 0 && tiles <= cpw) return DecodePlan{s, s > 1 && may_use_memory ? kXchgClusterMem : kXchgSmem};
-    }
+    if (MT <= 32 && one_wave > 0)
+        return DecodePlan{one_wave, one_wave > 1 && may_use_memory ? kXchgClusterMem : kXchgSmem};
     if (may_use_memory && clusters_per_wave<MT>(1) > 0) {   // occupancy known: clusters did not fit
         int64_t t = sms * C::kMinBlocks / tiles;
         int s = (int)(t < kMaxMemSplit ? t : kMaxMemSplit);
