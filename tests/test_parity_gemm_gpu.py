@@ -223,6 +223,23 @@ def test_int8_gemm_qwen32b_sampled(cuda_lib, shape, M):
                rows=sample_rows(M, 3, seed=M + shape.N))
 
 
+@pytest.mark.parametrize("M,N,K", [(1, 4608, 3584), (16, 3584, 18944), (32, 5120, 5120), (64, 3584, 3584),
+                                   (64, 3584, 18944), (256, 5120, 27648), (300, 256, 4096)])
+def test_fp8_gemm_is_deterministic(cuda_lib, M, N, K):
+    # every split-K exchange adds the partials in a fixed order: repeated calls,
+    # with the workspace reused, give the same bits (each path of the plan:
+    # cluster shared memory / cluster L2 / second launch / prefill split)
+    g = torch.Generator(device="cuda").manual_seed(M + N + K)
+    Xq = torch.randint(0, 0x7e, (M, K), dtype=torch.uint8, device="cuda", generator=g)
+    Wq = torch.randint(0, 0x7e, (N, K), dtype=torch.uint8, device="cuda", generator=g)
+    Xs = torch.rand((K // 128, M), device="cuda", generator=g)
+    Ws = torch.rand((N // 128, K // 128), device="cuda", generator=g)
+    ws = torch.empty(max(16, fb.fp8rl_gemm_workspace_bytes(M, N, K)), dtype=torch.uint8, device="cuda")
+    Y0 = fb.fp8rl_gemm_w8a8_block(Xq, Xs, Wq, Ws, workspace=ws)
+    for _ in range(3):
+        assert torch.equal(fb.fp8rl_gemm_w8a8_block(Xq, Xs, Wq, Ws, workspace=ws), Y0)
+
+
 def test_no_device_error_after_gemms(cuda_lib):
     assert fb.fp8rl_check_device_error() == 0
 
