@@ -387,7 +387,7 @@ static PrefillPlan prefill_plan(int64_t M, int64_t N, int64_t K) {
     return saved > cost ? PrefillPlan{(int)s, (int)full} : none;
 }
 
-static size_t prefill_ws_bytes(int64_t M, int64_t N, int64_t K, const PrefillPlan& pl) {
+static size_t prefill_ws_bytes(int64_t M, int64_t N, const PrefillPlan& pl) {
     if (pl.split <= 1) return 0;
     const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
     return (size_t)(tiles - pl.full_tiles) * (size_t)pl.split * kBM * kBN * sizeof(float);
@@ -421,7 +421,7 @@ cudaError_t launch_gemm_fp8_prefill(const uint8_t* Xq, const float* Xs, const ui
     PrefillPlan pl = prefill_plan(M, N, K);
     const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
     // with less workspace than the split needs, run without split-K
-    if (pl.split > 1 && (ws == nullptr || ws_bytes < prefill_ws_bytes(M, N, K, pl))) pl = PrefillPlan{1, (int)tiles};
+    if (pl.split > 1 && (ws == nullptr || ws_bytes < prefill_ws_bytes(M, N, pl))) pl = PrefillPlan{1, (int)tiles};
     const int split = pl.split;
     CUtensorMap tmX, tmW, tmY, tmP;
     if (!make_tmap_u8(&tmX, Xq, (uint64_t)M, (uint64_t)K, (uint64_t)K, kBM)) return cudaErrorInvalidValue;
@@ -459,7 +459,7 @@ static bool takes_prefill(int64_t M, int64_t N, int64_t K);
 size_t gemm_fp8_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     if (M <= 0) return 0;
     if (!takes_prefill(M, N, K)) return decode_workspace_bytes(M, N, K);
-    return prefill_ws_bytes(M, N, K, prefill_plan(M, N, K));
+    return prefill_ws_bytes(M, N, prefill_plan(M, N, K));
 }
 
 // Estimated prefill-kernel time in microseconds: a fixed 3 us plus the larger of
@@ -475,7 +475,7 @@ static double prefill_cost_us(int64_t M, int64_t N, int64_t K) {
     const double compute = (double)((pl.full_tiles + sms - 1) / sms) * (double)kb_all * 0.5 +
                            (double)((split_units + sms - 1) / sms) * (double)kb * 0.5;
     const double memory = (double)(N * K + M * K + 2 * M * N) / 5.5e6;
-    const double reduce = pl.split > 1 ? 3.0 + (double)prefill_ws_bytes(M, N, K, pl) / 3e6 : 0.0;
+    const double reduce = pl.split > 1 ? 3.0 + (double)prefill_ws_bytes(M, N, pl) / 3e6 : 0.0;
     return 3.0 + (compute > memory ? compute : memory) + reduce;
 }
 
