@@ -219,8 +219,8 @@ def time_headline(fb, args, dev, world, rank):
     sets = [LayerSet(shapes, M, synth.seed_for(2, 0) + 1000 * c, dev) for c in range(COPIES)]
     ws_bytes = max(fb.fp8rl_gemm_workspace_bytes(M, s.N, s.K) for s in shapes)
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
-    # a GEMM that uses its workspace launches the split and the reduction
-    gemm_launches = sum(2 if fb.fp8rl_gemm_workspace_bytes(M, s.N, s.K) else 1 for s in shapes)
+    # kernels per GEMM call with this workspace (a split added by a second launch counts two)
+    gemm_launches = sum(fb.fp8rl_gemm_kernel_count(M, s.N, s.K, ws_bytes) for s in shapes)
     for c in range(COPIES):                          # every copy has valid codes before step 0
         run_requant(fb, sets[c])
         run_decode(fb, sets[c], ws)                  # first calls outside capture (one-time set-up)

@@ -65,7 +65,7 @@ typedef enum {
     FP8RL_ERR_DEVICE = 8
 } fp8rl_status;
 
-#define FP8RL_ABI_VERSION 2
+#define FP8RL_ABI_VERSION 3
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* fp8rl_status_string(int status);
@@ -137,6 +137,11 @@ int fp8rl_quant_act_group(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
  * nothing between calls, but two calls in flight at once need two workspaces.
  * ---------------------------------------------------------------------- */
 size_t fp8rl_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+/* Number of kernels fp8rl_gemm_w8a8_block launches for this shape when given
+ * workspace_bytes of workspace (0: none): 1, or 2 when the K split is added by
+ * a second launch.  0 for M == 0; -FP8RL_ERR_SHAPE for an invalid shape.  For
+ * sizing CUDA graphs and counting launches; host-only, no device access. */
+int fp8rl_gemm_kernel_count(int64_t M, int64_t N, int64_t K, size_t workspace_bytes);
 int fp8rl_gemm_w8a8_block(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
                           const float* Ws, int64_t M, int64_t N, int64_t K,
                           uint16_t* Y, int64_t ldy, void* workspace,
@@ -225,6 +230,10 @@ int int8rl_quant_act_token(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
  * between calls; two calls in flight at once need two workspaces.
  * ---------------------------------------------------------------------- */
 size_t int8rl_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+/* Kernels int8rl_gemm_w8a8 launches for this shape and workspace size: 1 on the
+ * small-batch kernel; 2 or 3 on the large-batch path (conversion, GEMM, and the
+ * reduction of a K split).  0 for M == 0; -FP8RL_ERR_SHAPE for an invalid shape. */
+int int8rl_gemm_kernel_count(int64_t M, int64_t N, int64_t K, size_t workspace_bytes);
 int int8rl_gemm_w8a8(const int8_t* Xq, const float* Xs, const int8_t* Wq, const float* Ws,
                      int64_t M, int64_t N, int64_t K, uint16_t* Y, int64_t ldy,
                      int32_t* acc_or_null, void* workspace, size_t workspace_bytes,

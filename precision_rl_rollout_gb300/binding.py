@@ -30,6 +30,7 @@ EXPORTS = ("fp8rl_status_string", "fp8rl_abi_version", "fp8rl_quant_weight_block
            "fp8rl_linear_workspace_bytes", "fp8rl_linear_w8a8_block",
            "int8rl_quant_weight_channel", "int8rl_quant_act_token",
            "int8rl_gemm_workspace_bytes", "int8rl_gemm_w8a8", "fp8rl_check_device_error",
+           "fp8rl_gemm_kernel_count", "int8rl_gemm_kernel_count",
            "fp8rl_kv_workspace_bytes", "fp8rl_quant_kv_tensor", "fp8rl_quant_kv_with_scale",
            "fp8rl_quant_kv_tensor_noalloc", "fp8rl_rollout_is_workspace_bytes",
            "fp8rl_rollout_is_weights", "fp8rl_logits_kl_workspace_bytes", "fp8rl_logits_kl")
@@ -76,6 +77,10 @@ def load(path: str | None = None):
         lib.fp8rl_quant_act_group.argtypes = [P, I, I, I, P, P, S]
         lib.fp8rl_gemm_workspace_bytes.restype = Z
         lib.fp8rl_gemm_workspace_bytes.argtypes = [I, I, I]
+        lib.fp8rl_gemm_kernel_count.restype = ctypes.c_int
+        lib.fp8rl_gemm_kernel_count.argtypes = [I, I, I, Z]
+        lib.int8rl_gemm_kernel_count.restype = ctypes.c_int
+        lib.int8rl_gemm_kernel_count.argtypes = [I, I, I, Z]
         lib.fp8rl_gemm_w8a8_block.argtypes = [P, P, P, P, I, I, I, P, I, P, Z, S]
         lib.fp8rl_gemm_w8a8_block_grouped.argtypes = [P, P, P, P, P, I, I, I, I, I, P, I, S]
         lib.fp8rl_linear_workspace_bytes.restype = Z
@@ -277,6 +282,14 @@ def int8rl_quant_act_token(X, Xq=None, Xs=None, stream=None):
     _ck(lib.int8rl_quant_act_token(_p(X), M, K, ldx, _p(Xq), _p(Xs), _stream(X, stream)),
         "int8rl_quant_act_token")
     return Xq, Xs
+
+
+def fp8rl_gemm_kernel_count(M: int, N: int, K: int, workspace_bytes: int) -> int:
+    return int(load().fp8rl_gemm_kernel_count(M, N, K, workspace_bytes))
+
+
+def int8rl_gemm_kernel_count(M: int, N: int, K: int, workspace_bytes: int) -> int:
+    return int(load().int8rl_gemm_kernel_count(M, N, K, workspace_bytes))
 
 
 def int8rl_gemm_workspace_bytes(M: int, N: int, K: int) -> int:

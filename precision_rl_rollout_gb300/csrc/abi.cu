@@ -99,6 +99,11 @@ size_t fp8rl_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     return gemm_fp8_workspace_bytes(M, N, K);
 }
 
+int fp8rl_gemm_kernel_count(int64_t M, int64_t N, int64_t K, size_t workspace_bytes) {
+    if (M < 0 || N <= 0 || K <= 0 || N % kBlk || K % kBlk) return -FP8RL_ERR_SHAPE;
+    return gemm_fp8_kernel_count(M, N, K, workspace_bytes);
+}
+
 int fp8rl_gemm_w8a8_block(const uint8_t* Xq, const float* Xs, const uint8_t* Wq, const float* Ws,
                           int64_t M, int64_t N, int64_t K, uint16_t* Y, int64_t ldy,
                           void* workspace, size_t workspace_bytes, void* stream) {
@@ -169,6 +174,11 @@ int int8rl_quant_act_token(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
 
 size_t int8rl_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     return gemm_int8_workspace_bytes(M, N, K);
+}
+
+int int8rl_gemm_kernel_count(int64_t M, int64_t N, int64_t K, size_t workspace_bytes) {
+    if (M < 0 || N <= 0 || K <= 0 || N % kBlk || K % kBlk) return -FP8RL_ERR_SHAPE;
+    return gemm_int8_kernel_count(M, N, K, workspace_bytes);
 }
 
 int int8rl_gemm_w8a8(const int8_t* Xq, const float* Xs, const int8_t* Wq, const float* Ws,

@@ -490,6 +490,13 @@ static bool takes_prefill(int64_t M, int64_t N, int64_t K) {
     return M >= 64;
 }
 
+int gemm_fp8_kernel_count(int64_t M, int64_t N, int64_t K, size_t ws_bytes) {
+    if (M <= 0) return 0;
+    if (!takes_prefill(M, N, K)) return decode_supported(K) ? decode_kernel_count(M, N, K, ws_bytes) : 1;
+    const PrefillPlan pl = prefill_plan(M, N, K);
+    return pl.split > 1 && ws_bytes >= prefill_ws_bytes(M, N, pl) ? 2 : 1;
+}
+
 cudaError_t launch_gemm_fp8(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
                             const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
                             int64_t ldy, void* ws, size_t ws_bytes, cudaStream_t st) {

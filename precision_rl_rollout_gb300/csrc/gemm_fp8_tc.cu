@@ -586,6 +586,24 @@ static size_t decode_ws_bytes_mt(int64_t M, int64_t N, int64_t K) {
     return pl.uses_memory() ? (size_t)tiles * pl.split * MT * 128 * sizeof(float) : 0;
 }
 
+template <int MT>
+static int decode_kernels_mt(int64_t M, int64_t N, int64_t K, size_t ws_bytes) {
+    const int64_t mtiles = (M + MT - 1) / MT, tiles = (N / 128) * mtiles;
+    const int KB = (int)(K / 128);
+    DecodePlan pl = decode_plan<MT>(tiles, KB, true);
+    if (pl.uses_memory() && ws_bytes < (size_t)tiles * pl.split * MT * 128 * sizeof(float))
+        pl = decode_plan<MT>(tiles, KB, false);
+    return pl.xmode == kXchgReduceLaunch ? 2 : 1;
+}
+
+// Kernels the dense decode GEMM launches for this shape and workspace size.
+int decode_kernel_count(int64_t M, int64_t N, int64_t K, size_t ws_bytes) {
+    if (M <= 16) return decode_kernels_mt<16>(M, N, K, ws_bytes);
+    if (M <= 32) return decode_kernels_mt<32>(M, N, K, ws_bytes);
+    if (M <= 64) return decode_kernels_mt<64>(M, N, K, ws_bytes);
+    return decode_kernels_mt<128>(M, N, K, ws_bytes);
+}
+
 size_t decode_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     if (M <= 0 || !decode_supported(K)) return 0;
     if (M <= 16) return decode_ws_bytes_mt<16>(M, N, K);

@@ -435,6 +435,10 @@ size_t int8_prefill_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     return (size_t)(M + N) * (size_t)K * 2 + parts;
 }
 
+// Kernels of the large-batch path: the conversion, the GEMM and, with split K,
+// the reduction.
+int int8_prefill_kernel_count(int64_t M, int64_t N, int64_t K) { return i8p_plan(M, N, K).split > 1 ? 3 : 2; }
+
 cudaError_t launch_gemm_int8_prefill(const int8_t* Xq, const float* Xs, const int8_t* Wq, const float* Ws,
                                      int64_t M, int64_t N, int64_t K, uint16_t* Y, int64_t ldy, int32_t* acc,
                                      void* ws, cudaStream_t st) {

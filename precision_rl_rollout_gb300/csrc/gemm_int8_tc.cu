@@ -430,6 +430,11 @@ cudaError_t launch_gemm_int8_tc(const int8_t* Xq, const float* Xs, const int8_t*
 // large-batch path (fp16 copies in the workspace, 128 x 256 tiles); the rest,
 // and any call with less workspace than that path asks for, this kernel.
 size_t gemm_int8_workspace_bytes(int64_t M, int64_t N, int64_t K) { return int8_prefill_workspace_bytes(M, N, K); }
+int gemm_int8_kernel_count(int64_t M, int64_t N, int64_t K, size_t ws_bytes) {
+    if (M <= 0) return 0;
+    const size_t need = int8_prefill_workspace_bytes(M, N, K);
+    return need > 0 && ws_bytes >= need ? int8_prefill_kernel_count(M, N, K) : 1;
+}
 cudaError_t launch_gemm_int8(const int8_t* Xq, const float* Xs, const int8_t* Wq,
                              const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
                              int64_t ldy, int32_t* acc, void* ws, size_t ws_bytes, cudaStream_t st) {

@@ -57,6 +57,10 @@ cudaError_t launch_gemm_fp8_decode(const uint8_t* Xq, const float* Xs, const uin
                                    const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
                                    int64_t ldy, void* ws, size_t ws_bytes, cudaStream_t st);
 size_t decode_workspace_bytes(int64_t M, int64_t N, int64_t K);
+int decode_kernel_count(int64_t M, int64_t N, int64_t K, size_t ws_bytes);
+int gemm_fp8_kernel_count(int64_t M, int64_t N, int64_t K, size_t ws_bytes);
+int gemm_int8_kernel_count(int64_t M, int64_t N, int64_t K, size_t ws_bytes);
+int int8_prefill_kernel_count(int64_t M, int64_t N, int64_t K);
 // Grouped (mixture-of-experts) form of the decode kernel: experts' weights
 // stacked [E*N][K], token rows grouped by expert at offs[0..E] (device).
 cudaError_t launch_gemm_fp8_grouped(const uint8_t* Xq, const float* Xs, const uint8_t* Wq, const float* Ws,

@@ -170,6 +170,20 @@ def test_fp8_gemm_workspace_is_whole_partial_tiles(lib):
         assert ws % (128 * 16 * 4) == 0, (M, N, K, ws)
 
 
+def test_gemm_kernel_counts(lib):
+    for f in (lib.fp8rl_gemm_kernel_count, lib.int8rl_gemm_kernel_count):
+        assert f(0, 4608, 3584, 0) == 0
+        assert f(4, 100, 3584, 0) == -2                   # N % 128
+        assert f(4, 4608, 100, 0) == -2                   # K % 128
+    for M, N, K in [(1, 4608, 3584), (64, 3584, 18944), (300, 256, 4096), (8192, 5120, 27648)]:
+        # without a workspace every path launches one kernel; with the queried one, one or two
+        assert lib.fp8rl_gemm_kernel_count(M, N, K, 0) == 1
+        assert lib.fp8rl_gemm_kernel_count(M, N, K, lib.fp8rl_gemm_workspace_bytes(M, N, K)) in (1, 2)
+    assert lib.int8rl_gemm_kernel_count(32, 7168, 5120, 0) == 1
+    assert lib.int8rl_gemm_kernel_count(4096, 7168, 5120, lib.int8rl_gemm_workspace_bytes(4096, 7168, 5120)) == 2
+    assert lib.int8rl_gemm_kernel_count(4096, 7168, 5120, 0) == 1
+
+
 def test_gemm_workspace_query_is_monotone(lib):
     for f in (lib.fp8rl_gemm_workspace_bytes, lib.int8rl_gemm_workspace_bytes):
         a = f(1, 4608, 3584)
