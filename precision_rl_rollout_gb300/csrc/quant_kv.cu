@@ -13,6 +13,15 @@
 // Deterministic (no atomics, nothing to zero).  Above L2 size the tensor is
 // read twice (6.6 B of DRAM traffic per 3 algorithmic bytes); below it the
 // second read comes from L2.
+//
+// When every slice's CTA can be resident at once (tensors up to a few tens of
+// MB, e.g. one step's keys or values), one cooperative launch does all three:
+// each CTA keeps its slice in registers, writes its partial amax, waits at a
+// grid-wide barrier, reduces all the partials to the same scale, and encodes
+// its slice from registers.  One read of the tensor and no launch gaps; the
+// scale and codes are the same bits as the three-launch path's.
+#include <cooperative_groups.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -91,6 +100,66 @@ kv_quant_kernel(const uint16_t* __restrict__ X, int64_t total, int64_t cpr, int6
     }
 }
 
+__global__ void __launch_bounds__(kKvThreads)
+kv_onepass_kernel(const uint16_t* __restrict__ X, int64_t total, int64_t cpr, int64_t ld,
+                  uint32_t* __restrict__ partial, int64_t P, float* __restrict__ scale, uint8_t* __restrict__ Xq) {
+    namespace cg = cooperative_groups;
+    const int64_t base = (int64_t)blockIdx.x * kKvChunksPerCta;
+    uint4 v[kKvChunksPerThread];
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < kKvChunksPerThread; ++i) {
+        const int64_t c = base + i * kKvThreads + threadIdx.x;
+        v[i] = c < total ? ld_stream_v4(X + chunk_offset(c, cpr, ld)) : make_uint4(0, 0, 0, 0);
+        m = absmax_v4(m, v[i]);
+    }
+    __shared__ uint32_t red[kKvThreads / 32];
+    m = __reduce_max_sync(0xffffffffu, max(m & 0xFFFFu, m >> 16));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t r = red[0];
+        for (int w = 1; w < kKvThreads / 32; ++w) r = max(r, red[w]);
+        partial[blockIdx.x] = r;                          // bf16 magnitude bits of the slice's amax
+    }
+    cg::this_grid().sync();                               // every partial written and visible
+    uint32_t a = 0;
+    for (int64_t i = threadIdx.x; i < P; i += kKvThreads) a = max(a, __ldcg(partial + i));
+    a = __reduce_max_sync(0xffffffffu, a);
+    __syncthreads();                                      // red[] is reused
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
+    __syncthreads();
+    uint32_t r = red[0];
+    for (int w = 1; w < kKvThreads / 32; ++w) r = max(r, red[w]);
+    const float s = fp8_scale_from_amax(__uint_as_float(r << 16));
+    if (blockIdx.x == 0 && threadIdx.x == 0) *scale = s;
+    const BlockDivisor d = make_divisor(s);
+#pragma unroll
+    for (int i = 0; i < kKvChunksPerThread; ++i) {
+        const int64_t c = base + i * kKvThreads + threadIdx.x;
+        if (c < total)
+            *reinterpret_cast<uint2*>(Xq + c * 8) = d.fast ? quant8_e4m3_t<true>(v[i], d)
+                                                           : quant8_e4m3_t<false>(v[i], d);
+    }
+}
+
+// CTAs of the one-pass kernel that can be resident at once on the current
+// device (0 if unknown); cached per device.
+int64_t kv_onepass_capacity() {
+    static int cache[64] = {};                            // 0 unknown, -1 none, else CTAs
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cache[dev] == 0) {
+        int per_sm = 0, coop = 0;
+        const bool ok = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess && coop &&
+                        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kv_onepass_kernel, kKvThreads, 0) ==
+                            cudaSuccess && per_sm > 0;
+        cudaGetLastError();
+        cache[dev] = ok ? per_sm * num_sms() : -1;
+    }
+    return cache[dev] > 0 ? cache[dev] : 0;
+}
+
 }  // namespace
 
 int64_t kv_partials(int64_t R, int64_t C) {
@@ -112,6 +181,13 @@ cudaError_t launch_quant_kv_tensor(const uint16_t* X, int64_t R, int64_t C, int6
     const int64_t total = R * (C / 8), P = kv_partials(R, C);
     if (P > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
     cudaError_t e;
+    if (P > 0 && P <= kv_onepass_capacity()) {
+        int64_t cpr = C / 8;
+        void* args[] = {(void*)&X, (void*)&total, (void*)&cpr, (void*)&ld, (void*)&partial, (void*)&P,
+                        (void*)&scale, (void*)&Xq};
+        return cudaLaunchCooperativeKernel((const void*)kv_onepass_kernel, dim3((unsigned)P), dim3(kKvThreads),
+                                           args, 0, st);
+    }
     if (P > 0) {
         e = launch_pdl(kv_amax_partial_kernel, dim3((unsigned)P), dim3(kKvThreads), 0, st, X, total, C / 8,
                        ld, partial);
