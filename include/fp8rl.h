@@ -250,8 +250,11 @@ int int8rl_gemm_w8a8(const int8_t* Xq, const float* Xs, const int8_t* Wq, const 
  * KVq   e4m3 [R][C] contiguous, 16-byte aligned.
  * scale one fp32 in device memory (written by the call).
  * workspace: device scratch of at least fp8rl_kv_workspace_bytes(R, C) bytes
- *       (4 bytes per 16384 values); it needs no zeroing and holds nothing
- *       between calls; calls in flight at the same time need their own.
+ *       (8 bytes per 16384 values, plus 8), 8-byte aligned; it needs no zeroing and
+ *       holds nothing between calls; calls in flight at the same time need
+ *       their own.  Tensors of up to about 10 M values are done in one pass
+ *       (one cooperative launch; a bounded wait that runs out is reported by
+ *       fp8rl_check_device_error as FP8RL_ERR_TIMEOUT), larger ones in three.
  * Bit-exact.  An empty tensor (R == 0) writes scale 1.
  * ---------------------------------------------------------------------- */
 size_t fp8rl_kv_workspace_bytes(int64_t R, int64_t C);

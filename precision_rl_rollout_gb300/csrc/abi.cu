@@ -12,6 +12,7 @@ using namespace fp8rl;
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+inline bool aligned8(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; }
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? FP8RL_OK : FP8RL_ERR_CUDA; }
 
@@ -205,7 +206,7 @@ static int check_kv(const uint16_t* KV, int64_t R, int64_t C, int64_t ld, const 
 
 size_t fp8rl_kv_workspace_bytes(int64_t R, int64_t C) {
     if (R <= 0 || C <= 0) return 0;
-    return (size_t)kv_partials(R, C) * sizeof(uint32_t);
+    return (size_t)(kv_partials(R, C) + 1) * sizeof(uint64_t);   // 8-byte tagged slots + the tensor amax (one-pass path)
 }
 
 int fp8rl_quant_kv_tensor(const uint16_t* KV, int64_t R, int64_t C, int64_t ld, uint8_t* KVq,
@@ -213,7 +214,7 @@ int fp8rl_quant_kv_tensor(const uint16_t* KV, int64_t R, int64_t C, int64_t ld, 
     int rc = check_kv(KV, R, C, ld, KVq);
     if (rc) return rc;
     if (!scale) return FP8RL_ERR_NULL;
-    if (!aligned4(scale) || !aligned4(workspace)) return FP8RL_ERR_ALIGN;
+    if (!aligned4(scale) || !aligned8(workspace)) return FP8RL_ERR_ALIGN;
     const size_t need = fp8rl_kv_workspace_bytes(R, C);
     if (workspace_bytes < need || (need && !workspace)) return FP8RL_ERR_WORKSPACE;
     return cuda_status(launch_quant_kv_tensor(KV, R, C, ld, KVq, scale,

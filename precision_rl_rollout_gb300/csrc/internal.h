@@ -27,7 +27,9 @@ cudaError_t launch_quant_act_group(const uint16_t* X, int64_t M, int64_t K, int6
 cudaError_t launch_quant_int8_rows(const uint16_t* A, int64_t R, int64_t K, int64_t lda,
                                    int8_t* Q, float* S, cudaStream_t st);
 
-// FP8 KV-cache per-tensor quant (three launches; `partial` holds kv_partials(R, C) words).
+// FP8 KV-cache per-tensor quant: one cooperative launch over kv_partials(R, C) + 1
+// 8-byte slots when every slice's CTA fits at once, else three launches over
+// kv_partials(R, C) 32-bit words; `partial` is 8-byte aligned and holds the larger.
 int64_t kv_partials(int64_t R, int64_t C);
 cudaError_t launch_quant_kv_tensor(const uint16_t* X, int64_t R, int64_t C, int64_t ld, uint8_t* Xq,
                                    float* scale, uint32_t* partial, cudaStream_t st);

@@ -14,18 +14,21 @@
 // read twice (6.6 B of DRAM traffic per 3 algorithmic bytes); below it the
 // second read comes from L2.
 //
-// When every slice's CTA can be resident at once (tensors up to a few tens of
-// MB, e.g. one step's keys or values), one cooperative launch does all three:
-// each CTA keeps its slice in registers, writes its partial amax, waits at a
-// grid-wide barrier, reduces all the partials to the same scale, and encodes
-// its slice from registers.  One read of the tensor and no launch gaps; the
-// scale and codes are the same bits as the three-launch path's.
-#include <cooperative_groups.h>
-
+// When every slice's CTA can be resident at once (tensors up to ~10 M values,
+// e.g. one step's keys or values), one cooperative launch does all three: each
+// CTA keeps its slice in registers and publishes its partial amax tagged with
+// the call's sequence number; it then waits (bounded) until every slot carries
+// that tag, reduces all the partials to the same scale, and encodes its slice
+// from registers.  One read of the tensor and no launch gaps; the scale and
+// codes are the same bits as the three-launch path's.  The tags make the
+// workspace need no zeroing: a slot left by an earlier call carries an older
+// tag.
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
+#include "sm100_ptx.cuh"
 
 namespace fp8rl {
 
@@ -100,10 +103,31 @@ kv_quant_kernel(const uint16_t* __restrict__ X, int64_t total, int64_t cpr, int6
     }
 }
 
-__global__ void __launch_bounds__(kKvThreads)
+constexpr uint64_t kKvWaitLimitNs = 2000000000ull;   // 2 s: far above any legitimate wait
+constexpr uint32_t kKernelKv = 5;
+constexpr int kKvSlotsPerThread = 3;                  // one pass polls at most 768 slots
+
+// The 64-bit slot word carries both the tag and the amax, so nothing else is
+// published through it: relaxed gpu-scope accesses give all the ordering needed.
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Cooperative launch (every CTA resident) over P + 1 slots: slot[i] = tag << 32
+// | amax bits of slice i, slot[P] = tag << 32 | tensor amax bits.  Polling
+// traffic stays O(P) per round (CTA 0 reads the P slots, the rest read one
+// word), backing off between rounds so it does not crowd the loads of CTAs
+// still reading their slice.  A CTA whose wait runs out records a time-out in
+// the error word and writes nothing.
+__global__ void __launch_bounds__(kKvThreads, 4)   // four CTAs per SM: 608 slices resident at once
 kv_onepass_kernel(const uint16_t* __restrict__ X, int64_t total, int64_t cpr, int64_t ld,
-                  uint32_t* __restrict__ partial, int64_t P, float* __restrict__ scale, uint8_t* __restrict__ Xq) {
-    namespace cg = cooperative_groups;
+                  uint64_t* __restrict__ slot, int64_t P, uint32_t tag, float* __restrict__ scale,
+                  uint8_t* __restrict__ Xq, uint32_t* __restrict__ err) {
     const int64_t base = (int64_t)blockIdx.x * kKvChunksPerCta;
     uint4 v[kKvChunksPerThread];
     uint32_t m = 0;
@@ -120,17 +144,75 @@ kv_onepass_kernel(const uint16_t* __restrict__ X, int64_t total, int64_t cpr, in
     if (threadIdx.x == 0) {
         uint32_t r = red[0];
         for (int w = 1; w < kKvThreads / 32; ++w) r = max(r, red[w]);
-        partial[blockIdx.x] = r;                          // bf16 magnitude bits of the slice's amax
+        st_relaxed_u64(slot + blockIdx.x, ((uint64_t)tag << 32) | r);   // bf16 magnitude bits of the amax
     }
-    cg::this_grid().sync();                               // every partial written and visible
-    uint32_t a = 0;
-    for (int64_t i = threadIdx.x; i < P; i += kKvThreads) a = max(a, __ldcg(partial + i));
-    a = __reduce_max_sync(0xffffffffu, a);
-    __syncthreads();                                      // red[] is reused
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
+    // CTA 0 gathers every slice's amax of this call (each thread polls up to
+    // kKvSlotsPerThread slots, all loads of a round in flight together) and
+    // publishes the tensor amax in slot[P]; the other CTAs wait for that one word.
+    __shared__ uint32_t bcast[2];                          // tensor amax bits, wait ok
+    bool ok = true;
+    if (blockIdx.x == 0) {
+        uint32_t a = 0;
+        uint64_t sv[kKvSlotsPerThread];
+        uint32_t pending = 0;
+#pragma unroll
+        for (int j = 0; j < kKvSlotsPerThread; ++j) {
+            const int64_t i = threadIdx.x + (int64_t)j * kKvThreads;
+            sv[j] = 0;
+            if (i < P) {
+                sv[j] = ld_relaxed_u64(slot + i);
+                pending |= 1u << j;
+            }
+        }
+        const uint64_t t0 = sm100::globaltimer_ns();
+        for (;;) {
+#pragma unroll
+            for (int j = 0; j < kKvSlotsPerThread; ++j)
+                if (((pending >> j) & 1u) && (uint32_t)(sv[j] >> 32) == tag) {
+                    a = max(a, (uint32_t)sv[j]);
+                    pending &= ~(1u << j);
+                }
+            if (!pending) break;
+            if (sm100::globaltimer_ns() - t0 > kKvWaitLimitNs) {
+                ok = false;
+                break;
+            }
+            __nanosleep(64);
+#pragma unroll
+            for (int j = 0; j < kKvSlotsPerThread; ++j)
+                if ((pending >> j) & 1u) sv[j] = ld_relaxed_u64(slot + threadIdx.x + (int64_t)j * kKvThreads);
+        }
+        ok = __syncthreads_and(ok);
+        a = __reduce_max_sync(0xffffffffu, a);
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;   // red[] free: __syncthreads_and above
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            uint32_t r = red[0];
+            for (int w = 1; w < kKvThreads / 32; ++w) r = max(r, red[w]);
+            if (ok) st_relaxed_u64(slot + P, ((uint64_t)tag << 32) | r);
+            bcast[0] = r;
+            bcast[1] = ok;
+        }
+    } else if (threadIdx.x == 0) {
+        const uint64_t t0 = sm100::globaltimer_ns();
+        uint64_t sv = ld_relaxed_u64(slot + P);
+        while ((uint32_t)(sv >> 32) != tag) {
+            if (sm100::globaltimer_ns() - t0 > kKvWaitLimitNs) {
+                ok = false;
+                break;
+            }
+            __nanosleep(64);
+            sv = ld_relaxed_u64(slot + P);
+        }
+        bcast[0] = (uint32_t)sv;
+        bcast[1] = ok;
+    }
     __syncthreads();
-    uint32_t r = red[0];
-    for (int w = 1; w < kKvThreads / 32; ++w) r = max(r, red[w]);
+    if (!bcast[1]) {
+        if (threadIdx.x == 0) atomicCAS(err, 0u, (kKernelKv << 24) | (1u << 16) | 1u);
+        return;
+    }
+    const uint32_t r = bcast[0];
     const float s = fp8_scale_from_amax(__uint_as_float(r << 16));
     if (blockIdx.x == 0 && threadIdx.x == 0) *scale = s;
     const BlockDivisor d = make_divisor(s);
@@ -160,6 +242,23 @@ int64_t kv_onepass_capacity() {
     return cache[dev] > 0 ? cache[dev] : 0;
 }
 
+// Tag of one one-pass call: the MurmurHash3 32-bit finaliser (a bijection) of
+// a per-process call counter, so no two calls of the process share a tag within
+// 2^32 calls and words left in a reused workspace by anything else match it
+// only by chance (about 2^-32 per slot). Never 0.
+uint32_t next_tag() {
+    static std::atomic<uint32_t> seq{0};
+    for (;;) {
+        uint32_t h = seq.fetch_add(1) + 1;
+        h ^= h >> 16;
+        h *= 0x85ebca6bu;
+        h ^= h >> 13;
+        h *= 0xc2b2ae35u;
+        h ^= h >> 16;
+        if (h != 0) return h;
+    }
+}
+
 }  // namespace
 
 int64_t kv_partials(int64_t R, int64_t C) {
@@ -181,10 +280,14 @@ cudaError_t launch_quant_kv_tensor(const uint16_t* X, int64_t R, int64_t C, int6
     const int64_t total = R * (C / 8), P = kv_partials(R, C);
     if (P > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
     cudaError_t e;
-    if (P > 0 && P <= kv_onepass_capacity()) {
+    if (P > 0 && P <= kv_onepass_capacity() && P <= (int64_t)kKvSlotsPerThread * kKvThreads) {
+        const uint32_t tag = next_tag();
         int64_t cpr = C / 8;
-        void* args[] = {(void*)&X, (void*)&total, (void*)&cpr, (void*)&ld, (void*)&partial, (void*)&P,
-                        (void*)&scale, (void*)&Xq};
+        uint64_t* slots = reinterpret_cast<uint64_t*>(partial);
+        uint32_t* err = device_error_word();
+        if (!err) return cudaErrorInvalidValue;
+        void* args[] = {(void*)&X,     (void*)&total, (void*)&cpr,   (void*)&ld, (void*)&slots,
+                        (void*)&P,     (void*)&tag,   (void*)&scale, (void*)&Xq, (void*)&err};
         return cudaLaunchCooperativeKernel((const void*)kv_onepass_kernel, dim3((unsigned)P), dim3(kKvThreads),
                                            args, 0, st);
     }
@@ -210,6 +313,8 @@ cudaError_t launch_quant_kv_tensor(const uint16_t* X, int64_t R, int64_t C, int6
 
 constexpr int64_t kKvNoAllocSlots = 16384;   // partial maxima: tensors up to 16384 x 16384 values
 static __device__ __align__(256) uint32_t g_kv_noalloc_partials[kKvNoAllocSlots];
+
+static_assert((kKvSlotsPerThread * kKvThreads + 1) * 2 <= kKvNoAllocSlots, "one-pass slots fit the array");
 
 int64_t kv_noalloc_max_values() { return kKvNoAllocSlots * kKvChunksPerCta * 8; }
 

@@ -211,12 +211,13 @@ def test_product_package_never_reaches_the_oracle():
 def test_kv_quant_validation(lib):
     q = lib.fp8rl_quant_kv_tensor
     ws = lib.fp8rl_kv_workspace_bytes(64, 1024)
-    assert ws == 4 * ((64 * 1024 // 8 + 2047) // 2048)
+    assert ws == 8 * ((64 * 1024 // 8 + 2047) // 2048 + 1)
     assert q(A, 64, 1020, 1024, A, A, A, ws, None) == 2                 # C % 8
     assert q(A, 64, 1024, 1000, A, A, A, ws, None) == 2                 # ld < C
     assert q(A, 64, 1024, 1024, A, None, A, ws, None) == 1               # scale
     assert q(A, 64, 1024, 1024, A, A, A, ws - 1, None) == 4              # workspace too small
     assert q(A, 64, 1024, 1024, A + 8, A, A, ws, None) == 3              # KVq alignment
+    assert q(A, 64, 1024, 1024, A, A, A + 4, ws, None) == 3              # workspace: 8-byte slots
     w = lib.fp8rl_quant_kv_with_scale
     assert w(A, 64, 1024, 1024, None, A, None) == 1
     assert w(A, 0, 1024, 1024, A, A, None) == 0                          # empty: nothing launched
