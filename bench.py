@@ -799,6 +799,11 @@ def profile_case(fb, case, dev, reps=3):
         X = synth.activation(64 * 2048, 1024, synth.seed_for(6, 0), device=dev)
         for _ in range(reps):
             fb.fp8rl_quant_kv_tensor(X)
+    elif case == "kv8192":                            # one cooperative pass (fits the resident CTAs)
+        X = synth.activation(8192, 1024, synth.seed_for(6, 0), device=dev)
+        ws = torch.empty(fb.fp8rl_kv_workspace_bytes(8192, 1024), dtype=torch.uint8, device=dev)
+        for _ in range(reps):
+            fb.fp8rl_quant_kv_tensor(X, workspace=ws)
     elif case == "tis":
         n = 1024 * 16384
         lt = torch.randn(n, device=dev) - 2.0
