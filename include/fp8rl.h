@@ -331,7 +331,8 @@ int fp8rl_logits_kl(const uint16_t* P, int64_t ldp, const uint16_t* Q, int64_t l
  * The first call on a device looks up the array's device address (with that
  * device current) and caches it; make that first call before any stream
  * capture.  Every call shares the one array: nothing in it needs to start at
- * zero (a call writes every slot it reads before reading it), and two calls
+ * zero (the three-launch path writes every slot before reading it; the
+ * one-pass path accepts a slot only once it carries the call's tag), and two calls
  * whose kernels overlap on the GPU (different streams) race on it -- issue
  * them in one stream, or use fp8rl_quant_kv_tensor with separate workspaces.
  * Other arguments, layouts and errors as for fp8rl_quant_kv_tensor.
