@@ -185,3 +185,36 @@ def test_fp8_kv_tensor_quant_qwen32b_cache_sampled(cuda_lib):
     want_q, want_s = oracle.fp8_quant_tensor(synth.bf16_bits(X))
     assert bits_u32(host(scale))[0] == np.float32(want_s).view(np.uint32)
     assert np.array_equal(host(KVq), want_q)
+
+
+@pytest.mark.parametrize("R,where", [(9728, "last"), (9728, "first"), (9744, "last")])
+def test_fp8_kv_tensor_quant_one_pass_boundary(cuda_lib, R, where):
+    # 9728 x 1024 is 608 slices of 16384 values (every slice's CTA resident at
+    # four per SM on 152 SMs: one pass); 9744 x 1024 is 609 (three launches).
+    # The tensor amax sits in the first or last slice only.
+    C = 1024
+    X = act_cpu(R, C, 9100 + R)
+    r, c = (R - 1, C - 1) if where == "last" else (0, 0)
+    X[r, c] = -1000.0
+    ws = torch.empty(fb.fp8rl_kv_workspace_bytes(R, C), dtype=torch.uint8, device="cuda")
+    KVq, scale = fb.fp8rl_quant_kv_tensor(X.cuda(), workspace=ws)
+    want_q, want_s = oracle.fp8_quant_tensor(synth.bf16_bits(X))
+    assert bits_u32(host(scale))[0] == np.float32(want_s).view(np.uint32)
+    assert np.array_equal(host(KVq), want_q)
+    assert fb.fp8rl_check_device_error() == 0
+
+
+def test_fp8_kv_tensor_quant_reused_workspace_takes_no_stale_slot(cuda_lib):
+    # the same workspace for a tensor with a large amax, then one with a small
+    # amax: the second call's scale must come from its own slices only
+    R, C = 4096, 1024
+    ws = torch.empty(fb.fp8rl_kv_workspace_bytes(R, C), dtype=torch.uint8, device="cuda")
+    big = act_cpu(R, C, 9201)
+    big[R // 2, 7] = 3000.0
+    small = act_cpu(R, C, 9202) * 0.01
+    for X in (big, small, big, small):
+        KVq, scale = fb.fp8rl_quant_kv_tensor(X.cuda(), workspace=ws)
+        want_q, want_s = oracle.fp8_quant_tensor(synth.bf16_bits(X))
+        assert bits_u32(host(scale))[0] == np.float32(want_s).view(np.uint32)
+        assert np.array_equal(host(KVq), want_q)
+    assert fb.fp8rl_check_device_error() == 0
