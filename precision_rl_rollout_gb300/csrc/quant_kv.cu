@@ -16,13 +16,13 @@
 //
 // When every slice's CTA can be resident at once (tensors up to ~10 M values,
 // e.g. one step's keys or values), one cooperative launch does all three: each
-// CTA keeps its slice in registers and publishes its partial amax tagged with
-// the call's sequence number; it then waits (bounded) until every slot carries
-// that tag, reduces all the partials to the same scale, and encodes its slice
-// from registers.  One read of the tensor and no launch gaps; the scale and
-// codes are the same bits as the three-launch path's.  The tags make the
-// workspace need no zeroing: a slot left by an earlier call carries an older
-// tag.
+// CTA keeps its slice in registers and publishes its partial amax in an 8-byte
+// slot tagged with the call's tag; CTA 0 waits (bounded) until every slot
+// carries that tag and publishes the tensor amax in one more tagged slot, which
+// the other CTAs wait for (bounded); every CTA then encodes its slice from
+// registers.  One read of the tensor and no launch gaps; the scale and codes
+// are the same bits as the three-launch path's.  The tags make the workspace
+// need no zeroing: a slot left by an earlier call carries another tag.
 #include <atomic>
 #include <mutex>
 
