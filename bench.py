@@ -403,6 +403,34 @@ def quantization_error(fb, dev):
     return res
 
 
+def act_quant_prefill(fb, dev):
+    """A2 / A6 at their prefill sizes, where they are HBM-bound: FP8 1x128
+    groups at M=8192 and INT8 per token at M=4096, K = 5120 and 27648.  The
+    calls walk distinct input copies (> 3x L2) in one graph."""
+    hbm = load_peaks()["hbm_gbs"]
+    aq = {}
+    for K in (5120, 27648):
+        for kind, M in (("fp8_group", synth.PREFILL_M), ("int8_token", 4096)):
+            nc = _copies_for(2 * M * K)
+            Xc = [synth.activation(M, K, synth.seed_for(4, 1), device=dev)]
+            Xc += [Xc[0].clone() for _ in range(nc - 1)]
+            if kind == "fp8_group":
+                Xq = torch.empty(M, K, dtype=torch.uint8, device=dev)
+                Xs = torch.empty(K // 128, M, dtype=torch.float32, device=dev)
+                ms = _time_graph([lambda c=c: fb.fp8rl_quant_act_group(Xc[c], Xq, Xs) for c in range(nc)])
+                nbytes = act_quant_bytes(M, K)
+            else:
+                Xq = torch.empty(M, K, dtype=torch.int8, device=dev)
+                Xs = torch.empty(M, dtype=torch.float32, device=dev)
+                ms = _time_graph([lambda c=c: fb.int8rl_quant_act_token(Xc[c], Xq, Xs) for c in range(nc)])
+                nbytes = 3 * M * K + 4 * M
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            aq[f"{kind}_M{M}_K{K}"] = {"us": ms * 1e3, "gbs": gbs, "frac_of_measured_hbm": gbs / hbm,
+                                       "input_copies": nc}
+            del Xc, Xq, Xs
+    return aq
+
+
 def extras(fb, dev, reps=5):
     out = {}
     out["error_vs_unquantized_bf16_7b_m64"] = quantization_error(fb, dev)
@@ -425,6 +453,8 @@ def extras(fb, dev, reps=5):
         pre[s.name] = {"ms": ms, "tflops": 2 * synth.PREFILL_M * s.N * s.K / (ms * 1e-3) / 1e12}
         del Wq, Ws, Xq, Xs, Y
     out["prefill_fp8_gemm_m8192"] = pre
+
+    out["act_quant_prefill"] = act_quant_prefill(fb, dev)
 
     # A2 + A4: 32B decode sweep; each GEMM walks distinct weight copies (> 3x L2)
     dec = {}

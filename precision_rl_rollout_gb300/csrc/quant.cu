@@ -111,9 +111,13 @@ cudaError_t launch_quant_weight_block(const WeightDesc* d, int n, cudaStream_t s
 
 // ---------------------------------------------------------------- FP8 activations
 
-// 256 threads = 16 half-warps; half-warp h quantizes group g = blockIdx.x of
-// token m = 16*blockIdx.y + h: each of its 16 lanes holds one 16-byte chunk
-// (8 values) of the 128-value group.
+// 256 threads = 16 half-warps; half-warp h quantizes groups G*blockIdx.x ..
+// G*blockIdx.x + G-1 of token m = 16*blockIdx.y + h: each of its 16 lanes
+// holds one 16-byte chunk (8 values) of each 128-value group.  All G loads of
+// a thread are issued before the first group is reduced, so a large tensor
+// keeps enough bytes in flight to stream at HBM speed (G = 8); a small one
+// (decode) takes G = 1 for the most CTAs and the shortest per-thread chain.
+template <int G>
 __global__ void __launch_bounds__(256)
 quant_act_group_kernel(const uint16_t* __restrict__ X, int64_t M, int64_t K, int64_t ldx,
                        uint8_t* __restrict__ Xq, float* __restrict__ Xs) {
@@ -121,28 +125,42 @@ quant_act_group_kernel(const uint16_t* __restrict__ X, int64_t M, int64_t K, int
     const int t = threadIdx.x;
     const int lane16 = t & 15;
     const int64_t m = (int64_t)blockIdx.y * 16 + (t >> 4);
-    const int64_t g = blockIdx.x;
+    const int64_t KG = K / kBlk;
+    const int64_t g0 = (int64_t)blockIdx.x * G;
     const bool valid = m < M;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (valid) v = ld_stream_v4(X + m * ldx + g * kBlk + lane16 * 8);
-    uint32_t a = absmax_v4(0u, v);
-    a = max(a & 0xFFFFu, a >> 16);
+    uint4 v[G];
 #pragma unroll
-    for (int off = 8; off > 0; off >>= 1) a = max(a, __shfl_xor_sync(0xffffffffu, a, off));
-    const float s = fp8_scale_from_amax(__uint_as_float(a << 16));
-    const BlockDivisor d = make_divisor(s);
-    if (valid) {
-        uint2 q = d.fast ? quant8_e4m3_t<true>(v, d) : quant8_e4m3_t<false>(v, d);
-        *reinterpret_cast<uint2*>(Xq + m * K + g * kBlk + lane16 * 8) = q;
-        if (lane16 == 0) Xs[g * M + m] = s;
+    for (int j = 0; j < G; ++j) {
+        v[j] = make_uint4(0, 0, 0, 0);
+        if (valid && g0 + j < KG) v[j] = ld_stream_v4(X + m * ldx + (g0 + j) * kBlk + lane16 * 8);
+    }
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+        uint32_t a = absmax_v4(0u, v[j]);
+        a = max(a & 0xFFFFu, a >> 16);
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) a = max(a, __shfl_xor_sync(0xffffffffu, a, off));
+        const float s = fp8_scale_from_amax(__uint_as_float(a << 16));
+        const BlockDivisor d = make_divisor(s);
+        if (valid && g0 + j < KG) {   // g0 + j < KG is the same for the whole CTA
+            uint2 q = d.fast ? quant8_e4m3_t<true>(v[j], d) : quant8_e4m3_t<false>(v[j], d);
+            *reinterpret_cast<uint2*>(Xq + m * K + (g0 + j) * kBlk + lane16 * 8) = q;
+            if (lane16 == 0) Xs[(g0 + j) * M + m] = s;
+        }
     }
 }
 
 cudaError_t launch_quant_act_group(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
                                    uint8_t* Xq, float* Xs, cudaStream_t st) {
     if (M == 0) return cudaSuccess;
-    dim3 grid((unsigned)(K / kBlk), (unsigned)((M + 15) / 16));
-    return launch_pdl(quant_act_group_kernel, grid, dim3(256), 0, st, X, M, K, ldx, Xq, Xs);
+    const int64_t KG = K / kBlk, MB = (M + 15) / 16;
+    // eight groups per thread once one group per thread would need more than
+    // about eight full waves of CTAs (8 resident per SM)
+    if (KG * MB >= 64LL * num_sms())
+        return launch_pdl(quant_act_group_kernel<8>, dim3((unsigned)((KG + 7) / 8), (unsigned)MB), dim3(256), 0,
+                          st, X, M, K, ldx, Xq, Xs);
+    return launch_pdl(quant_act_group_kernel<1>, dim3((unsigned)KG, (unsigned)MB), dim3(256), 0, st, X, M, K,
+                      ldx, Xq, Xs);
 }
 
 // ---------------------------------------------------------------- INT8 rows

@@ -105,6 +105,17 @@ def test_fp8_act_quant_qwen32b_decode(cuda_lib, M, K):
     assert np.array_equal(host(Xq), want_q)
 
 
+@pytest.mark.parametrize("M,K", [(8191, 3456), (4096, 5120)])
+def test_fp8_act_quant_large_full(cuda_lib, M, K):
+    # large enough for eight groups per thread; 8191 x 3456 leaves a ragged
+    # last token tile (15 of 16) and a ragged last group range (27 = 3 x 8 + 3)
+    X = act_cpu(M, K, synth.seed_for(4, 1) + K)
+    Xq, Xs = fb.fp8rl_quant_act_group(X.cuda())
+    want_q, want_s = oracle.fp8_quant_act_group(synth.bf16_bits(X))
+    assert np.array_equal(bits_u32(host(Xs)), bits_u32(want_s))
+    assert np.array_equal(host(Xq), want_q)
+
+
 def test_fp8_act_quant_prefill_sampled(cuda_lib):
     M, K = synth.PREFILL_M, 27648
     X = act_cpu(M, K, synth.seed_for(4, 1))
