@@ -50,8 +50,8 @@ L2_BYTES = 129 * 2 ** 20
 # ncu-measured DRAM traffic of the dominant kernel, valid only for the source it
 # was taken on (checked by hash; null otherwise).  Filled from the committed
 # profile summary of the same workload.
-NCU_TRAFFIC = {"kernel": "quant_weight_block_kernel", "source_sha1": "41ce679f08cedbd2a78d584ca50789218d072b18",
-               "bytes_per_launch": 466135040 + 174086144,
+NCU_TRAFFIC = {"kernel": "quant_weight_block_kernel", "source_sha1": "00680aa52e9f70b087ecef736f843db992b9fb29",
+               "bytes_per_launch": 466134016 + 174421760,
                "profile": "profiles/requant_weight_block_qwen7b.md"}
 
 
