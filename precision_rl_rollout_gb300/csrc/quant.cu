@@ -165,12 +165,14 @@ cudaError_t launch_quant_act_group(const uint16_t* X, int64_t M, int64_t K, int6
 
 // ---------------------------------------------------------------- INT8 rows
 
-// One CTA of 256 threads per row; the row is held in registers between the
-// amax pass and the quantization pass: chunk c = i*256 + t for i < CPT.  CPT
+// One CTA of NT threads per row; the row is held in registers between the
+// amax pass and the quantization pass: chunk c = i*NT + t for i < CPT.  CPT
 // (chunks of 8 values per thread) is the smallest instantiation that covers
-// the row, so short rows keep few registers and many CTAs in flight.
-template <int CPT>
-__global__ void __launch_bounds__(256)
+// the row, so short rows keep few registers and many CTAs in flight.  Rows of
+// up to 8192 values take 128-thread CTAs: twice the CTAs per SM, so twice the
+// bytes in flight, and no half-empty last iteration on 5120-wide rows.
+template <int CPT, int NT>
+__global__ void __launch_bounds__(NT)
 quant_int8_rows_kernel(const uint16_t* __restrict__ A, int64_t K, int64_t lda,
                        int8_t* __restrict__ Q, float* __restrict__ S) {
     pdl_wait_then_release();
@@ -182,57 +184,64 @@ quant_int8_rows_kernel(const uint16_t* __restrict__ A, int64_t K, int64_t lda,
     uint32_t m = 0;
 #pragma unroll
     for (int i = 0; i < CPT; ++i) {
-        const int c = i * 256 + t;
+        const int c = i * NT + t;
         v[i] = make_uint4(0, 0, 0, 0);
         if (c < chunks) v[i] = ld_stream_v4(src + (int64_t)c * 8);
         m = absmax_v4(m, v[i]);
     }
     m = __reduce_max_sync(0xffffffffu, max(m & 0xFFFFu, m >> 16));
-    __shared__ uint32_t red[8];
+    __shared__ uint32_t red[NT / 32];
     if ((t & 31) == 0) red[t >> 5] = m;
     __syncthreads();
     m = red[0];
 #pragma unroll
-    for (int w = 1; w < 8; ++w) m = max(m, red[w]);
+    for (int w = 1; w < NT / 32; ++w) m = max(m, red[w]);
     const float s = int8_scale_from_amax(__uint_as_float(m << 16));
     const BlockDivisor d = make_divisor(s);
     int8_t* dst = Q + r * K;
     if (d.fast) {
 #pragma unroll
         for (int i = 0; i < CPT; ++i) {
-            const int c = i * 256 + t;
+            const int c = i * NT + t;
             if (c < chunks) *reinterpret_cast<uint2*>(dst + (int64_t)c * 8) = quant8_int8_t<true>(v[i], d);
         }
     } else {
 #pragma unroll
         for (int i = 0; i < CPT; ++i) {
-            const int c = i * 256 + t;
+            const int c = i * NT + t;
             if (c < chunks) *reinterpret_cast<uint2*>(dst + (int64_t)c * 8) = quant8_int8_t<false>(v[i], d);
         }
     }
     if (t == 0) S[r] = s;
 }
 
-template <int CPT>
+template <int CPT, int NT>
 static cudaError_t launch_int8_rows_cpt(const uint16_t* A, int64_t R, int64_t K, int64_t lda, int8_t* Q,
                                         float* S, cudaStream_t st) {
-    return launch_pdl(quant_int8_rows_kernel<CPT>, dim3((unsigned)R), dim3(256), 0, st, A, K, lda, Q, S);
+    return launch_pdl(quant_int8_rows_kernel<CPT, NT>, dim3((unsigned)R), dim3(NT), 0, st, A, K, lda, Q, S);
 }
 
 cudaError_t launch_quant_int8_rows(const uint16_t* A, int64_t R, int64_t K, int64_t lda,
                                    int8_t* Q, float* S, cudaStream_t st) {
     if (R == 0) return cudaSuccess;
     if (R > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-    const int64_t need = (K / 8 + 255) / 256;          // chunks per thread
+    const int64_t chunks = K / 8;
+    if (chunks <= 128 * 8) {                            // rows of up to 8192 values: 128 threads
+        const int64_t need = (chunks + 127) / 128;
+        if (need <= 1) return launch_int8_rows_cpt<1, 128>(A, R, K, lda, Q, S, st);
+        if (need <= 2) return launch_int8_rows_cpt<2, 128>(A, R, K, lda, Q, S, st);
+        if (need <= 3) return launch_int8_rows_cpt<3, 128>(A, R, K, lda, Q, S, st);
+        if (need <= 4) return launch_int8_rows_cpt<4, 128>(A, R, K, lda, Q, S, st);
+        if (need <= 5) return launch_int8_rows_cpt<5, 128>(A, R, K, lda, Q, S, st);
+        if (need <= 6) return launch_int8_rows_cpt<6, 128>(A, R, K, lda, Q, S, st);
+        return launch_int8_rows_cpt<8, 128>(A, R, K, lda, Q, S, st);
+    }
+    const int64_t need = (chunks + 255) / 256;          // chunks per thread
     static_assert(kInt8MaxK / (256 * 8) == 16, "largest instantiation covers kInt8MaxK");
-    if (need <= 1) return launch_int8_rows_cpt<1>(A, R, K, lda, Q, S, st);
-    if (need <= 2) return launch_int8_rows_cpt<2>(A, R, K, lda, Q, S, st);
-    if (need <= 3) return launch_int8_rows_cpt<3>(A, R, K, lda, Q, S, st);
-    if (need <= 4) return launch_int8_rows_cpt<4>(A, R, K, lda, Q, S, st);
-    if (need <= 6) return launch_int8_rows_cpt<6>(A, R, K, lda, Q, S, st);
-    if (need <= 8) return launch_int8_rows_cpt<8>(A, R, K, lda, Q, S, st);
-    if (need <= 12) return launch_int8_rows_cpt<12>(A, R, K, lda, Q, S, st);
-    return launch_int8_rows_cpt<16>(A, R, K, lda, Q, S, st);
+    if (need <= 6) return launch_int8_rows_cpt<6, 256>(A, R, K, lda, Q, S, st);
+    if (need <= 8) return launch_int8_rows_cpt<8, 256>(A, R, K, lda, Q, S, st);
+    if (need <= 12) return launch_int8_rows_cpt<12, 256>(A, R, K, lda, Q, S, st);
+    return launch_int8_rows_cpt<16, 256>(A, R, K, lda, Q, S, st);
 }
 
 }  // namespace fp8rl

@@ -126,7 +126,10 @@ def test_fp8_act_quant_prefill_sampled(cuda_lib):
     assert np.array_equal(host(Xq)[rows], want_q)
 
 
-@pytest.mark.parametrize("R,K", [(1, 128), (7, 256), (128, 5120), (33, 27648)])
+# K spans every row-kernel instance: 128-thread CTAs with 1..8 chunks of 8 per
+# thread (K <= 8192), then 256-thread CTAs with 6, 8, 12 and 16
+@pytest.mark.parametrize("R,K", [(1, 128), (7, 256), (3, 1152), (3, 2944), (3, 4096), (128, 5120),
+                                 (3, 6016), (3, 8192), (3, 8320), (3, 16384), (3, 24576), (33, 27648)])
 def test_int8_row_quant_full(cuda_lib, R, K):
     A = act_cpu(R, K, 77 + R)
     for fn in (fb.int8rl_quant_weight_channel, fb.int8rl_quant_act_token):
