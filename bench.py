@@ -50,7 +50,7 @@ L2_BYTES = 129 * 2 ** 20
 # ncu-measured DRAM traffic of the dominant kernel, valid only for the source it
 # was taken on (checked by hash; null otherwise).  Filled from the committed
 # profile summary of the same workload.
-NCU_TRAFFIC = {"kernel": "quant_weight_block_kernel", "source_sha1": "00680aa52e9f70b087ecef736f843db992b9fb29",
+NCU_TRAFFIC = {"kernel": "quant_weight_block_kernel", "source_sha1": "a13824e9a55899c7949610a0ce2a0a2e99564e3d",
                "bytes_per_launch": 466134016 + 174421760,
                "profile": "profiles/requant_weight_block_qwen7b.md"}
 
@@ -707,10 +707,20 @@ def cpu_baseline(n_steps=3, req_rows=1024, gemm_rows=16):
 
 # ------------------------------------------------------------------ main
 
-def traffic_or_null():
+def requant_source_sha1():
+    """sha1 of the requant kernel's own source: the weight section of quant.cu
+    (from its header up to the activation section), its includes and
+    common.cuh.  The other quantizers in the file do not change it."""
     csrc = os.path.join(ROOT, "precision_rl_rollout_gb300", "csrc")
-    sha = hashlib.sha1(open(os.path.join(csrc, "quant.cu"), "rb").read() +
-                       open(os.path.join(csrc, "common.cuh"), "rb").read()).hexdigest()
+    text = open(os.path.join(csrc, "quant.cu"), "rb").read()
+    head = text.index(b"// ---------------------------------------------------------------- FP8 weights")
+    tail = text.index(b"// ---------------------------------------------------------------- FP8 activations")
+    return hashlib.sha1(text[:tail] + open(os.path.join(csrc, "common.cuh"), "rb").read()
+                        if head < tail else b"").hexdigest()
+
+
+def traffic_or_null():
+    sha = requant_source_sha1()
     if NCU_TRAFFIC["source_sha1"] == sha and NCU_TRAFFIC["bytes_per_launch"]:
         return NCU_TRAFFIC["bytes_per_launch"]
     return None
