@@ -707,16 +707,19 @@ def cpu_baseline(n_steps=3, req_rows=1024, gemm_rows=16):
 
 # ------------------------------------------------------------------ main
 
-def requant_source_sha1():
-    """sha1 of the requant kernel's own source: the weight section of quant.cu
-    (from its header up to the activation section), its includes and
-    common.cuh.  The other quantizers in the file do not change it."""
+def requant_source_sha1(quant_cu=None, common_cuh=None):
+    """sha1 of the requant kernel's own source: quant.cu up to its activation
+    section (the file header, includes and the weight section) and common.cuh.
+    The other quantizers in the file do not change it.  Texts (bytes) may be
+    passed in; by default they are read from the tree."""
     csrc = os.path.join(ROOT, "precision_rl_rollout_gb300", "csrc")
-    text = open(os.path.join(csrc, "quant.cu"), "rb").read()
+    text = quant_cu if quant_cu is not None else open(os.path.join(csrc, "quant.cu"), "rb").read()
+    common = common_cuh if common_cuh is not None else open(os.path.join(csrc, "common.cuh"), "rb").read()
     head = text.index(b"// ---------------------------------------------------------------- FP8 weights")
     tail = text.index(b"// ---------------------------------------------------------------- FP8 activations")
-    return hashlib.sha1(text[:tail] + open(os.path.join(csrc, "common.cuh"), "rb").read()
-                        if head < tail else b"").hexdigest()
+    if not head < tail:
+        raise ValueError("quant.cu: the weight section must precede the activation section")
+    return hashlib.sha1(text[:tail] + common).hexdigest()
 
 
 def traffic_or_null():
