@@ -10,7 +10,7 @@ marshals numpy arrays.  bf16 tensors travel as ``uint16`` bit patterns.
 
 Functions whose result is pinned by ``tests/test_oracle_pins.py``:
 ``e4m3_encode``/``e4m3_decode`` (brute force over all 256 codes),
-``fp8_quant_act_group`` (hand-worked 2x128 example), the quantizers (round-trip
+``fp8_quant_act_group`` (hand-worked example: two worked rows and a zero row), the quantizers (round-trip
 and saturation invariants), ``int8_gemm`` (int64 library matmul) and
 ``fp8_gemm`` (exact integer special case, quantization error bound).
 """

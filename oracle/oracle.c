@@ -31,7 +31,8 @@
  *
  * Parity pins (see tests/test_oracle_pins.py): the E4M3 encoder against brute
  * force over all 256 codes; the activation quantizer against a hand-worked
- * 2x128 example; round-trip and saturation invariants; the INT8 GEMM against an
+ * example (two worked rows plus an all-zero row); round-trip and saturation
+ * invariants; the INT8 GEMM against an
  * int64 library matmul; the FP8 GEMM against an exact integer special case and
  * against an unquantized fp64 matmul within the derived quantization bound.
  */
