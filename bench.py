@@ -866,7 +866,7 @@ def profile_case(fb, case, dev, reps=3):
         X = synth.activation(64 * 2048, 1024, synth.seed_for(6, 0), device=dev)
         for _ in range(reps):
             fb.fp8rl_quant_kv_tensor(X)
-    elif case == "act_quant_prefill":                 # A2 at M=8192, K=27648: eight groups per thread
+    elif case == "act_quant_prefill":                 # A2 at M=8192, K=27648: four groups per thread
         X = synth.activation(synth.PREFILL_M, 27648, synth.seed_for(4, 1), device=dev)
         Xq = torch.empty(synth.PREFILL_M, 27648, dtype=torch.uint8, device=dev)
         Xs = torch.empty(27648 // 128, synth.PREFILL_M, dtype=torch.float32, device=dev)

@@ -115,8 +115,9 @@ cudaError_t launch_quant_weight_block(const WeightDesc* d, int n, cudaStream_t s
 // G*blockIdx.x + G-1 of token m = 16*blockIdx.y + h: each of its 16 lanes
 // holds one 16-byte chunk (8 values) of each 128-value group.  All G loads of
 // a thread are issued before the first group is reduced, so a large tensor
-// keeps enough bytes in flight to stream at HBM speed (G = 8); a small one
-// (decode) takes G = 1 for the most CTAs and the shortest per-thread chain.
+// keeps enough bytes in flight to stream at HBM speed (G = 4: 40 registers,
+// six CTAs per SM; measured faster than G = 2, 5 and 8 at every prefill size);
+// a small one (decode) takes G = 1 for the most CTAs and the shortest chain.
 template <int G>
 __global__ void __launch_bounds__(256)
 quant_act_group_kernel(const uint16_t* __restrict__ X, int64_t M, int64_t K, int64_t ldx,
@@ -154,10 +155,10 @@ cudaError_t launch_quant_act_group(const uint16_t* X, int64_t M, int64_t K, int6
                                    uint8_t* Xq, float* Xs, cudaStream_t st) {
     if (M == 0) return cudaSuccess;
     const int64_t KG = K / kBlk, MB = (M + 15) / 16;
-    // eight groups per thread once one group per thread would need more than
+    // four groups per thread once one group per thread would need more than
     // about eight full waves of CTAs (8 resident per SM)
     if (KG * MB >= 64LL * num_sms())
-        return launch_pdl(quant_act_group_kernel<8>, dim3((unsigned)((KG + 7) / 8), (unsigned)MB), dim3(256), 0,
+        return launch_pdl(quant_act_group_kernel<4>, dim3((unsigned)((KG + 3) / 4), (unsigned)MB), dim3(256), 0,
                           st, X, M, K, ldx, Xq, Xs);
     return launch_pdl(quant_act_group_kernel<1>, dim3((unsigned)KG, (unsigned)MB), dim3(256), 0, st, X, M, K,
                       ldx, Xq, Xs);

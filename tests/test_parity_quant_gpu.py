@@ -107,8 +107,8 @@ def test_fp8_act_quant_qwen32b_decode(cuda_lib, M, K):
 
 @pytest.mark.parametrize("M,K", [(8191, 3456), (4096, 5120)])
 def test_fp8_act_quant_large_full(cuda_lib, M, K):
-    # large enough for eight groups per thread; 8191 x 3456 leaves a ragged
-    # last token tile (15 of 16) and a ragged last group range (27 = 3 x 8 + 3)
+    # large enough for several groups per thread; 8191 x 3456 leaves a ragged
+    # last token tile (15 of 16) and a ragged last group range (27 = 6 x 4 + 3)
     X = act_cpu(M, K, synth.seed_for(4, 1) + K)
     Xq, Xs = fb.fp8rl_quant_act_group(X.cuda())
     want_q, want_s = oracle.fp8_quant_act_group(synth.bf16_bits(X))
