@@ -50,8 +50,8 @@ L2_BYTES = 129 * 2 ** 20
 # ncu-measured DRAM traffic of the dominant kernel, valid only for the source it
 # was taken on (checked by hash; null otherwise).  Filled from the committed
 # profile summary of the same workload.
-NCU_TRAFFIC = {"kernel": "quant_weight_block_kernel", "source_sha1": "a13824e9a55899c7949610a0ce2a0a2e99564e3d",
-               "bytes_per_launch": 466134016 + 174421760,
+NCU_TRAFFIC = {"kernel": "quant_weight_block_kernel", "source_sha1": "69912cc3432327fae840b52154efe497e2f08df4",
+               "bytes_per_launch": 466135296 + 174760960,
                "profile": "profiles/requant_weight_block_qwen7b.md"}
 
 
