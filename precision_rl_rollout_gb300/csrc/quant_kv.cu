@@ -38,8 +38,10 @@ constexpr int kKvThreads = 256;
 constexpr int kKvChunksPerThread = 8;
 constexpr int64_t kKvChunksPerCta = kKvThreads * kKvChunksPerThread;   // 2048 chunks = 16384 values
 
-// chunk c of a [R][C] tensor with row pitch ld: 8 values at row c / (C/8)
+// chunk c of a [R][C] tensor with row pitch ld: 8 values at row c / (C/8).
+// Contiguous rows (the usual cache layout) skip the 64-bit division.
 __device__ __forceinline__ int64_t chunk_offset(int64_t c, int64_t cpr, int64_t ld) {
+    if (ld == cpr * 8) return c * 8;
     const int64_t r = c / cpr;
     return r * ld + (c - r * cpr) * 8;
 }
