@@ -223,6 +223,20 @@ def test_kv_quant_validation(lib):
     assert w(A, 0, 1024, 1024, A, A, None) == 0                          # empty: nothing launched
 
 
+def test_kv_quant_noalloc_validation(lib):
+    q = lib.fp8rl_quant_kv_tensor_noalloc
+    assert q(A, 64, 1020, 1024, A, A, None) == 2                         # C % 8
+    assert q(A, 64, 1024, 1000, A, A, None) == 2                         # ld < C
+    assert q(None, 64, 1024, 1024, A, A, None) == 1                      # KV
+    assert q(A, 64, 1024, 1024, None, A, None) == 1                      # KVq
+    assert q(A, 64, 1024, 1024, A, None, None) == 1                      # scale
+    assert q(A, 64, 1024, 1024, A + 8, A, None) == 3                     # KVq alignment
+    assert q(A, 64, 1024, 1024, A, A + 2, None) == 3                     # scale alignment
+    # above the library array's 16384 x 16384 values: refused before any launch
+    assert q(A, 16384 * 16384 // 1024 + 1, 1024, 1024, A, A, None) == 6
+    assert q(A, 16385, 16384, 16384, A, A, None) == 6
+
+
 def test_rollout_is_validation(lib):
     f = lib.fp8rl_rollout_is_weights
     ws = lib.fp8rl_rollout_is_workspace_bytes(10000)
