@@ -250,11 +250,14 @@ int int8rl_gemm_w8a8(const int8_t* Xq, const float* Xs, const int8_t* Wq, const 
  * KVq   e4m3 [R][C] contiguous, 16-byte aligned.
  * scale one fp32 in device memory (written by the call).
  * workspace: device scratch of at least fp8rl_kv_workspace_bytes(R, C) bytes
- *       (8 bytes per 16384 values, plus 8), 8-byte aligned; it needs no zeroing and
- *       holds nothing between calls; calls in flight at the same time need
- *       their own.  Tensors of up to about 10 M values are done in one pass
- *       (one cooperative launch; a bounded wait that runs out is reported by
- *       fp8rl_check_device_error as FP8RL_ERR_TIMEOUT), larger ones in three.
+ *       (8 bytes per 16384 values, plus 8), 8-byte aligned; it needs no zeroing
+ *       (any content is accepted).  Its first 8 bytes carry a call counter from
+ *       one call to the next, which the device advances, so the call may be
+ *       captured in a CUDA graph and replayed.  Calls in flight at the same time
+ *       need their own workspace.  Tensors of up to about 10 M values are done
+ *       in one pass (one cooperative launch; a bounded wait that runs out is
+ *       reported by fp8rl_check_device_error as FP8RL_ERR_TIMEOUT), larger ones
+ *       in three.
  * Bit-exact.  An empty tensor (R == 0) writes scale 1.
  * ---------------------------------------------------------------------- */
 size_t fp8rl_kv_workspace_bytes(int64_t R, int64_t C);
@@ -324,15 +327,16 @@ int fp8rl_logits_kl(const uint16_t* P, int64_t ldp, const uint16_t* Q, int64_t l
  * serving loop that must not call cudaMalloc / cudaFree because they
  * synchronize the device and stall queued work.  It allocates nothing and
  * calls no allocating routine.
- * Scratch: a 64 KB array in device memory owned by the library (a file-scope
- * __device__ array), held by every GPU that loads the library until the
- * process exits.  Limit: R * C <= 268435456 (16384 x 16384) values; larger
+ * Scratch: a 64 KB (+ 8 bytes) array in device memory owned by the library (a
+ * file-scope __device__ array), held by every GPU that loads the library until
+ * the process exits.  Limit: R * C <= 268435456 (16384 x 16384) values; larger
  * tensors return FP8RL_ERR_UNSUPPORTED (use fp8rl_quant_kv_tensor instead).
  * The first call on a device looks up the array's device address (with that
  * device current) and caches it; make that first call before any stream
  * capture.  Every call shares the one array: nothing in it needs to start at
  * zero (the three-launch path writes every slot before reading it; the
- * one-pass path accepts a slot only once it carries the call's tag), and two calls
+ * one-pass path accepts a slot only once it carries the call's tag, which the
+ * device derives from the previous call's), and two calls
  * whose kernels overlap on the GPU (different streams) race on it -- issue
  * them in one stream, or use fp8rl_quant_kv_tensor with separate workspaces.
  * Other arguments, layouts and errors as for fp8rl_quant_kv_tensor.

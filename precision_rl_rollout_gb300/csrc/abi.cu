@@ -206,7 +206,7 @@ static int check_kv(const uint16_t* KV, int64_t R, int64_t C, int64_t ld, const 
 
 size_t fp8rl_kv_workspace_bytes(int64_t R, int64_t C) {
     if (R <= 0 || C <= 0) return 0;
-    return (size_t)(kv_partials(R, C) + 1) * sizeof(uint64_t);   // 8-byte tagged slots + the tensor amax (one-pass path)
+    return (size_t)(kv_partials(R, C) + 1) * sizeof(uint64_t);   // the header word + one 8-byte slot per slice
 }
 
 int fp8rl_quant_kv_tensor(const uint16_t* KV, int64_t R, int64_t C, int64_t ld, uint8_t* KVq,

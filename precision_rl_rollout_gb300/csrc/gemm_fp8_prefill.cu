@@ -298,6 +298,7 @@ gemm_fp8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_co
         if (lane == 0) bulk_wait_all();
         __syncwarp();
     }
+    __syncwarp();   // warps whose lane 0 alone ran the producer / MMA loop reconverge first
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -482,17 +483,22 @@ static double prefill_cost_us(int64_t M, int64_t N, int64_t K) {
 // Up to 256 tokens both tcgen05 kernels apply: the split-K weight-streaming
 // decode kernel wins for few, deep weight slabs, the 128x256-tile kernel once
 // there are enough tiles (or enough K to split) to fill the GPU; the cheaper
-// estimate is taken.  The warp-MMA kernel covers small-M shapes whose K exceeds
-// the decode kernel's split limit.
+// estimate is taken.  A K beyond the decode kernel's split limit (32768) goes to
+// the 128x256-tile kernel at any M.
 static bool takes_prefill(int64_t M, int64_t N, int64_t K) {
-    if (M > 256) return true;
-    if (decode_supported(K)) return prefill_cost_us(M, N, K) < decode_cost_us(M, N, K);
-    return M >= 64;
+    if (M > 256 || !decode_supported(K)) return true;
+    return prefill_cost_us(M, N, K) < decode_cost_us(M, N, K);
+}
+
+// The decode kernel runs a shape when the dispatch picks it and its split fits
+// the workspace given (see decode_fits); otherwise the 128x256-tile kernel does.
+static bool runs_decode(int64_t M, int64_t N, int64_t K, size_t ws_bytes) {
+    return !takes_prefill(M, N, K) && decode_fits(M, N, K, ws_bytes);
 }
 
 int gemm_fp8_kernel_count(int64_t M, int64_t N, int64_t K, size_t ws_bytes) {
     if (M <= 0) return 0;
-    if (!takes_prefill(M, N, K)) return decode_supported(K) ? decode_kernel_count(M, N, K, ws_bytes) : 1;
+    if (runs_decode(M, N, K, ws_bytes)) return decode_kernel_count(M, N, K, ws_bytes);
     const PrefillPlan pl = prefill_plan(M, N, K);
     return pl.split > 1 && ws_bytes >= prefill_ws_bytes(M, N, pl) ? 2 : 1;
 }
@@ -500,10 +506,8 @@ int gemm_fp8_kernel_count(int64_t M, int64_t N, int64_t K, size_t ws_bytes) {
 cudaError_t launch_gemm_fp8(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
                             const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
                             int64_t ldy, void* ws, size_t ws_bytes, cudaStream_t st) {
-    if (!takes_prefill(M, N, K)) {
-        if (decode_supported(K)) return launch_gemm_fp8_decode(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, ws, ws_bytes, st);
-        return launch_gemm_fp8_mma_sync(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, st);
-    }
+    if (runs_decode(M, N, K, ws_bytes))
+        return launch_gemm_fp8_decode(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, ws, ws_bytes, st);
     return launch_gemm_fp8_prefill(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, ws, ws_bytes, st);
 }
 

@@ -300,7 +300,10 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
     }
 
     // ---------------- split-K: the split CTAs' partials are added in rank order,
-    // then rounded to bf16 once
+    // then rounded to bf16 once.  Warps 0 and 1 ran their producer / MMA loop on
+    // lane 0 alone: the warp is reconverged before the .aligned barriers below,
+    // which every lane of a warp must execute together.
+    __syncwarp();
     tc_fence_before();
     const bool clustered = p.split > 1 && p.xmode != kXchgReduceLaunch;
     // self-check: the launch shape the exchange relies on (`split` CTAs per slab
@@ -384,6 +387,7 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
         }
     }
     // a CTA whose shared memory its peers read stays until they are done
+    __syncwarp();
     if (clustered && p.xmode == kXchgSmem) cluster_sync_all(); else __syncthreads();
     if (warp == 1) {
         tc_fence_after();
@@ -465,6 +469,15 @@ static int choose_split(int64_t tiles, int KB, int MT, int max_kb_per_split, dou
     }
     if (cost_out) *cost_out = best_cost;
     return best;
+}
+
+// Split for the exchange through distributed shared memory, which is used
+// only for token tiles of up to 32 (partial tiles of at most 16 KB per CTA);
+// wider tiles without a workspace run unsplit.
+template <int MT>
+static int smem_exchange_split(int64_t tiles, int KB) {
+    if (MT > 32) return 1;
+    return choose_split(tiles, KB, MT, DecodeCfg<MT>::kMaxKbPerSplit);
 }
 
 static int token_tile(int64_t M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128; }
@@ -576,7 +589,7 @@ static DecodePlan decode_plan(int64_t tiles, int KB, bool may_use_memory) {
         while (s >= 2 && !split_fits(KB, s, C::kMaxKbPerSplit)) --s;
         if (s >= 2) return DecodePlan{s, kXchgReduceLaunch};
     }
-    return DecodePlan{choose_split(tiles, KB, MT, C::kMaxKbPerSplit), kXchgSmem};
+    return DecodePlan{smem_exchange_split<MT>(tiles, KB), kXchgSmem};
 }
 
 template <int MT>
@@ -594,6 +607,28 @@ static int decode_kernels_mt(int64_t M, int64_t N, int64_t K, size_t ws_bytes) {
     if (pl.uses_memory() && ws_bytes < (size_t)tiles * pl.split * MT * 128 * sizeof(float))
         pl = decode_plan<MT>(tiles, KB, false);
     return pl.xmode == kXchgReduceLaunch ? 2 : 1;
+}
+
+template <int MT>
+static bool decode_fits_mt(int64_t M, int64_t N, int64_t K, size_t ws_bytes) {
+    const int64_t mtiles = (M + MT - 1) / MT, tiles = (N / 128) * mtiles;
+    const int KB = (int)(K / 128);
+    DecodePlan pl = decode_plan<MT>(tiles, KB, true);
+    if (pl.uses_memory() && ws_bytes < (size_t)tiles * pl.split * MT * 128 * sizeof(float))
+        pl = decode_plan<MT>(tiles, KB, false);
+    return (KB + pl.split - 1) / pl.split <= DecodeCfg<MT>::kMaxKbPerSplit;
+}
+
+// Whether the dense decode kernel can run this shape with `ws_bytes` of
+// workspace: without a workspace, token tiles of 64 and more run unsplit (the
+// exchange through distributed shared memory is kept to tiles of up to 32), so
+// a K beyond one CTA's 32 blocks then goes to the 128 x 256 tile kernel.
+bool decode_fits(int64_t M, int64_t N, int64_t K, size_t ws_bytes) {
+    if (M <= 0 || !decode_supported(K)) return false;
+    if (M <= 16) return decode_fits_mt<16>(M, N, K, ws_bytes);
+    if (M <= 32) return decode_fits_mt<32>(M, N, K, ws_bytes);
+    if (M <= 64) return decode_fits_mt<64>(M, N, K, ws_bytes);
+    return decode_fits_mt<128>(M, N, K, ws_bytes);
 }
 
 // Kernels the dense decode GEMM launches for this shape and workspace size.
@@ -628,7 +663,7 @@ static cudaError_t launch_decode_mt(const uint8_t* Xq, const float* Xs, const ui
     const int KB = (int)(K / 128);
     const int64_t mtiles = (rows_per_group + MT - 1) / MT;
     const int64_t tiles = groups * (N / 128) * mtiles;
-    DecodePlan pl = offs ? DecodePlan{choose_split(tiles, KB, MT, C::kMaxKbPerSplit), kXchgSmem}
+    DecodePlan pl = offs ? DecodePlan{smem_exchange_split<MT>(tiles, KB), kXchgSmem}
                          : decode_plan<MT>(tiles, KB, true);
     if (pl.uses_memory() && (ws == nullptr || ws_bytes < (size_t)tiles * pl.split * MT * 128 * sizeof(float)))
         pl = decode_plan<MT>(tiles, KB, false);

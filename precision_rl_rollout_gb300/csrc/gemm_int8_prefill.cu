@@ -276,6 +276,7 @@ gemm_int8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
         if (lane == 0) bulk_wait_all();
         __syncwarp();
     }
+    __syncwarp();   // warps whose lane 0 alone ran the producer / MMA loop reconverge first
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {

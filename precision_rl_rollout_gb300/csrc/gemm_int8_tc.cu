@@ -301,6 +301,9 @@ gemm_int8_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
     }
 
     // ---------------- split-K reduction over the cluster (int32: exact), epilogue stores
+    // (warps 0 and 1 ran their loops on lane 0 alone: reconverged before the
+    // .aligned barriers, which every lane of a warp must execute together)
+    __syncwarp();
     tc_fence_before();
     if (p.split > 1) cluster_sync_all(); else __syncthreads();
     {
@@ -350,6 +353,7 @@ gemm_int8_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
             }
         }
     }
+    __syncwarp();
     if (p.split > 1) cluster_sync_all(); else __syncthreads();
     if (warp == 1) {
         tc_fence_after();

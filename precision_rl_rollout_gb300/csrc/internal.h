@@ -27,9 +27,10 @@ cudaError_t launch_quant_act_group(const uint16_t* X, int64_t M, int64_t K, int6
 cudaError_t launch_quant_int8_rows(const uint16_t* A, int64_t R, int64_t K, int64_t lda,
                                    int8_t* Q, float* S, cudaStream_t st);
 
-// FP8 KV-cache per-tensor quant: one cooperative launch over kv_partials(R, C) + 1
-// 8-byte slots when every slice's CTA fits at once, else three launches over
-// kv_partials(R, C) 32-bit words; `partial` is 8-byte aligned and holds the larger.
+// FP8 KV-cache per-tensor quant: one cooperative launch over a header word and
+// kv_partials(R, C) 8-byte slots when every slice's CTA fits at once, else three
+// launches over kv_partials(R, C) 32-bit words placed after the header;
+// `partial` is 8-byte aligned and holds (kv_partials(R, C) + 1) * 8 bytes.
 int64_t kv_partials(int64_t R, int64_t C);
 cudaError_t launch_quant_kv_tensor(const uint16_t* X, int64_t R, int64_t C, int64_t ld, uint8_t* Xq,
                                    float* scale, uint32_t* partial, cudaStream_t st);
@@ -68,9 +69,6 @@ int int8_prefill_kernel_count(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_gemm_fp8_grouped(const uint8_t* Xq, const float* Xs, const uint8_t* Wq, const float* Ws,
                                     const int32_t* offs, int64_t E, int64_t T, int64_t N, int64_t K,
                                     int64_t max_rows, uint16_t* Y, int64_t ldy, cudaStream_t st);
-cudaError_t launch_gemm_fp8_mma_sync(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
-                                     const float* Ws, int64_t M, int64_t N, int64_t K,
-                                     uint16_t* Y, int64_t ldy, cudaStream_t st);
 size_t gemm_fp8_workspace_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_gemm_fp8(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
                             const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
@@ -123,6 +121,7 @@ bool make_tmap_f32_store(CUtensorMap* m, const void* base, uint64_t rows, uint64
 bool make_tmap_f16_load(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
 int num_sms();
 bool decode_supported(int64_t K);
+bool decode_fits(int64_t M, int64_t N, int64_t K, size_t ws_bytes);
 double decode_cost_us(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_gemm_fp8_prefill(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
                                     const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,

@@ -18,12 +18,22 @@
 // e.g. one step's keys or values), one cooperative launch does all three: each
 // CTA keeps its slice in registers and publishes its partial amax in an 8-byte
 // slot tagged with the call's tag; CTA 0 waits (bounded) until every slot
-// carries that tag and publishes the tensor amax in one more tagged slot, which
+// carries that tag and publishes the tensor amax in the header word, which
 // the other CTAs wait for (bounded); every CTA then encodes its slice from
 // registers.  One read of the tensor and no launch gaps; the scale and codes
-// are the same bits as the three-launch path's.  The tags make the workspace
-// need no zeroing: a slot left by an earlier call carries another tag.
-#include <atomic>
+// are the same bits as the three-launch path's.
+//
+// The call's tag is derived on the device from the tag the previous call left
+// in the header word (next tag = previous + 1, top bit set), so a CUDA graph
+// that replays one launch still gives every replay a new tag, and a slot left
+// by an earlier call never carries the current one.  The workspace needs no
+// zeroing: the three-launch path's partials (bf16 magnitude bits, below
+// 0x8000) never have the top bit of a tag, and anything else a reused
+// workspace holds matches a tag only by chance.
+//
+// Workspace layout (64-bit words): word 0 is the one-pass header, words
+// 1 .. P the one-pass slots; the three-launch path keeps its 32-bit partials
+// from byte 8 on, so it never overwrites the header.
 #include <mutex>
 
 #include "common.cuh"
@@ -108,28 +118,40 @@ kv_quant_kernel(const uint16_t* __restrict__ X, int64_t total, int64_t cpr, int6
 constexpr uint64_t kKvWaitLimitNs = 2000000000ull;   // 2 s: far above any legitimate wait
 constexpr uint32_t kKernelKv = 5;
 constexpr int kKvSlotsPerThread = 3;                  // one pass polls at most 768 slots
+constexpr uint32_t kKvAborted = 0xFFFFFFFFu;          // header amax of a call whose gather ran out
 
-// The 64-bit slot word carries both the tag and the amax, so nothing else is
-// published through it: relaxed gpu-scope accesses give all the ordering needed.
-__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
-    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+// The tag of the call after the one whose tag is `prev`: top bit always set,
+// the low 31 bits counting up.
+__device__ __forceinline__ uint32_t kv_next_tag(uint32_t prev) {
+    return ((prev + 1u) & 0x7FFFFFFFu) | 0x80000000u;
 }
-__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+
+__device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
     uint64_t v;
-    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
 
-// Cooperative launch (every CTA resident) over P + 1 slots: slot[i] = tag << 32
-// | amax bits of slice i, slot[P] = tag << 32 | tensor amax bits.  Polling
-// traffic stays O(P) per round (CTA 0 reads the P slots, the rest read one
-// word), backing off between rounds so it does not crowd the loads of CTAs
-// still reading their slice.  A CTA whose wait runs out records a time-out in
-// the error word and writes nothing.
+// Cooperative launch (every CTA resident) over the header word and P slots:
+// slot[1 + i] = tag << 32 | amax bits of slice i; the header, slot[0], ends as
+// tag << 32 | tensor amax bits.  Every CTA reads the header before it
+// publishes its slot, and CTA 0 overwrites the header only after it has seen
+// every slot of this call (release / acquire order), so all CTAs derive the
+// same tag.  Polling traffic stays O(P) per round (CTA 0 reads the P slots, the
+// rest read one word), backing off between rounds so it does not crowd the
+// loads of CTAs still reading their slice.  A CTA whose wait runs out records
+// a time-out in the error word and writes no codes; if CTA 0's gather runs out
+// it still advances the header (with an abort marker), so the next call's tag
+// differs from this one's.
 __global__ void __launch_bounds__(kKvThreads, 4)   // four CTAs per SM: 608 slices resident at once
 kv_onepass_kernel(const uint16_t* __restrict__ X, int64_t total, int64_t cpr, int64_t ld,
-                  uint64_t* __restrict__ slot, int64_t P, uint32_t tag, float* __restrict__ scale,
+                  uint64_t* __restrict__ slot, int64_t P, float* __restrict__ scale,
                   uint8_t* __restrict__ Xq, uint32_t* __restrict__ err) {
+    __shared__ uint32_t s_tag;
+    if (threadIdx.x == 0) s_tag = kv_next_tag((uint32_t)(ld_acquire_u64(slot) >> 32));
     const int64_t base = (int64_t)blockIdx.x * kKvChunksPerCta;
     uint4 v[kKvChunksPerThread];
     uint32_t m = 0;
@@ -143,14 +165,15 @@ kv_onepass_kernel(const uint16_t* __restrict__ X, int64_t total, int64_t cpr, in
     m = __reduce_max_sync(0xffffffffu, max(m & 0xFFFFu, m >> 16));
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
     __syncthreads();
+    const uint32_t tag = s_tag;
     if (threadIdx.x == 0) {
         uint32_t r = red[0];
         for (int w = 1; w < kKvThreads / 32; ++w) r = max(r, red[w]);
-        st_relaxed_u64(slot + blockIdx.x, ((uint64_t)tag << 32) | r);   // bf16 magnitude bits of the amax
+        st_release_u64(slot + 1 + blockIdx.x, ((uint64_t)tag << 32) | r);   // bf16 magnitude bits of the amax
     }
     // CTA 0 gathers every slice's amax of this call (each thread polls up to
     // kKvSlotsPerThread slots, all loads of a round in flight together) and
-    // publishes the tensor amax in slot[P]; the other CTAs wait for that one word.
+    // publishes the tensor amax in the header; the other CTAs wait for that word.
     __shared__ uint32_t bcast[2];                          // tensor amax bits, wait ok
     bool ok = true;
     if (blockIdx.x == 0) {
@@ -162,7 +185,7 @@ kv_onepass_kernel(const uint16_t* __restrict__ X, int64_t total, int64_t cpr, in
             const int64_t i = threadIdx.x + (int64_t)j * kKvThreads;
             sv[j] = 0;
             if (i < P) {
-                sv[j] = ld_relaxed_u64(slot + i);
+                sv[j] = ld_acquire_u64(slot + 1 + i);
                 pending |= 1u << j;
             }
         }
@@ -182,7 +205,7 @@ kv_onepass_kernel(const uint16_t* __restrict__ X, int64_t total, int64_t cpr, in
             __nanosleep(64);
 #pragma unroll
             for (int j = 0; j < kKvSlotsPerThread; ++j)
-                if ((pending >> j) & 1u) sv[j] = ld_relaxed_u64(slot + threadIdx.x + (int64_t)j * kKvThreads);
+                if ((pending >> j) & 1u) sv[j] = ld_acquire_u64(slot + 1 + threadIdx.x + (int64_t)j * kKvThreads);
         }
         ok = __syncthreads_and(ok);
         a = __reduce_max_sync(0xffffffffu, a);
@@ -191,21 +214,22 @@ kv_onepass_kernel(const uint16_t* __restrict__ X, int64_t total, int64_t cpr, in
         if (threadIdx.x == 0) {
             uint32_t r = red[0];
             for (int w = 1; w < kKvThreads / 32; ++w) r = max(r, red[w]);
-            if (ok) st_relaxed_u64(slot + P, ((uint64_t)tag << 32) | r);
+            st_release_u64(slot, ((uint64_t)tag << 32) | (ok ? r : kKvAborted));
             bcast[0] = r;
             bcast[1] = ok;
         }
     } else if (threadIdx.x == 0) {
         const uint64_t t0 = sm100::globaltimer_ns();
-        uint64_t sv = ld_relaxed_u64(slot + P);
+        uint64_t sv = ld_acquire_u64(slot);
         while ((uint32_t)(sv >> 32) != tag) {
             if (sm100::globaltimer_ns() - t0 > kKvWaitLimitNs) {
                 ok = false;
                 break;
             }
             __nanosleep(64);
-            sv = ld_relaxed_u64(slot + P);
+            sv = ld_acquire_u64(slot);
         }
+        if ((uint32_t)sv == kKvAborted) ok = false;      // CTA 0's gather ran out (it recorded that)
         bcast[0] = (uint32_t)sv;
         bcast[1] = ok;
     }
@@ -244,23 +268,6 @@ int64_t kv_onepass_capacity() {
     return cache[dev] > 0 ? cache[dev] : 0;
 }
 
-// Tag of one one-pass call: the MurmurHash3 32-bit finaliser (a bijection) of
-// a per-process call counter, so no two calls of the process share a tag within
-// 2^32 calls and words left in a reused workspace by anything else match it
-// only by chance (about 2^-32 per slot). Never 0.
-uint32_t next_tag() {
-    static std::atomic<uint32_t> seq{0};
-    for (;;) {
-        uint32_t h = seq.fetch_add(1) + 1;
-        h ^= h >> 16;
-        h *= 0x85ebca6bu;
-        h ^= h >> 13;
-        h *= 0xc2b2ae35u;
-        h ^= h >> 16;
-        if (h != 0) return h;
-    }
-}
-
 }  // namespace
 
 int64_t kv_partials(int64_t R, int64_t C) {
@@ -283,22 +290,22 @@ cudaError_t launch_quant_kv_tensor(const uint16_t* X, int64_t R, int64_t C, int6
     if (P > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
     cudaError_t e;
     if (P > 0 && P <= kv_onepass_capacity() && P <= (int64_t)kKvSlotsPerThread * kKvThreads) {
-        const uint32_t tag = next_tag();
         int64_t cpr = C / 8;
         uint64_t* slots = reinterpret_cast<uint64_t*>(partial);
         uint32_t* err = device_error_word();
         if (!err) return cudaErrorInvalidValue;
-        void* args[] = {(void*)&X,     (void*)&total, (void*)&cpr,   (void*)&ld, (void*)&slots,
-                        (void*)&P,     (void*)&tag,   (void*)&scale, (void*)&Xq, (void*)&err};
+        void* args[] = {(void*)&X,     (void*)&total, (void*)&cpr, (void*)&ld, (void*)&slots,
+                        (void*)&P,     (void*)&scale, (void*)&Xq,  (void*)&err};
         return cudaLaunchCooperativeKernel((const void*)kv_onepass_kernel, dim3((unsigned)P), dim3(kKvThreads),
                                            args, 0, st);
     }
+    uint32_t* part = P > 0 ? partial + 2 : partial;       // past the one-pass header word
     if (P > 0) {
         e = launch_pdl(kv_amax_partial_kernel, dim3((unsigned)P), dim3(kKvThreads), 0, st, X, total, C / 8,
-                       ld, partial);
+                       ld, part);
         if (e != cudaSuccess) return e;
     }
-    e = launch_pdl(kv_scale_kernel, dim3(1), dim3(1024), 0, st, (const uint32_t*)partial, P, scale);
+    e = launch_pdl(kv_scale_kernel, dim3(1), dim3(1024), 0, st, (const uint32_t*)part, P, scale);
     if (e != cudaSuccess) return e;
     return launch_quant_kv_with_scale(X, R, C, ld, scale, Xq, st);
 }
@@ -311,12 +318,14 @@ cudaError_t launch_quant_kv_tensor(const uint16_t* X, int64_t R, int64_t C, int6
 // must not call cudaMalloc / cudaFree because those calls synchronize the
 // device and would stall the work already queued.  For them the partial maxima
 // live in this file-scope device array instead of a caller workspace.  Every
-// GPU that loads the library holds the array (64 KB) until the process exits.
+// GPU that loads the library holds the array (64 KB + 8 B) until the process exits.
 
 constexpr int64_t kKvNoAllocSlots = 16384;   // partial maxima: tensors up to 16384 x 16384 values
-static __device__ __align__(256) uint32_t g_kv_noalloc_partials[kKvNoAllocSlots];
+// 32-bit words: the 8-byte one-pass header, then one word per partial (the
+// three-launch path) or two per slot (the one-pass path)
+static __device__ __align__(256) uint32_t g_kv_noalloc_partials[2 + kKvNoAllocSlots];
 
-static_assert((kKvSlotsPerThread * kKvThreads + 1) * 2 <= kKvNoAllocSlots, "one-pass slots fit the array");
+static_assert((kKvSlotsPerThread * kKvThreads + 1) * 2 <= 2 + kKvNoAllocSlots, "one-pass slots fit the array");
 
 int64_t kv_noalloc_max_values() { return kKvNoAllocSlots * kKvChunksPerCta * 8; }
 

@@ -53,12 +53,12 @@ def test_fp8_gemm_split_k_without_workspace_matches(cuda_lib):
     assert_fp8_gemm_close(host(Y2), ref, "no split")
 
 
-@pytest.mark.parametrize("M,N,K", [(16, 4608, 3584), (9, 3584, 18944), (32, 5120, 5120), (64, 3584, 18944)])
+@pytest.mark.parametrize("M,N,K", [(16, 4608, 3584), (9, 3584, 18944), (32, 5120, 5120)])
 def test_fp8_decode_exchange_with_and_without_workspace(cuda_lib, M, N, K):
     # decode shapes whose split CTAs exchange partials through the workspace
-    # (in a cluster after one barrier for 16-32 token tiles, through a second
-    # launch for 64) and, with no workspace, through distributed shared memory:
-    # both within tolerance of the oracle on every row
+    # (in a cluster after one barrier for 16-32 token tiles) and, with no
+    # workspace, through distributed shared memory (kept to token tiles of up
+    # to 32): both within tolerance of the oracle on the sampled rows
     assert fb.fp8rl_gemm_workspace_bytes(M, N, K) > 0
     Wq, Ws = oracle_fp8_weight(N, K, 95 + M)
     Xq, Xs = oracle_fp8_act(M, K, 96 + M)
@@ -69,6 +69,39 @@ def test_fp8_decode_exchange_with_and_without_workspace(cuda_lib, M, N, K):
                                   workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
     assert_fp8_gemm_close(host(Y1)[rows], ref, "through memory")
     assert_fp8_gemm_close(host(Y2)[rows], ref, "on chip")
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 1024, 8192), (100, 768, 6144)])
+def test_fp8_wide_token_tile_without_workspace(cuda_lib, M, N, K):
+    # 64- and 128-token tiles with a K longer than one CTA's 32 blocks: with the
+    # workspace the split CTAs exchange through memory; without it the call
+    # goes to the 128 x 256 tile kernel (no exchange through distributed shared
+    # memory for these tiles); both within tolerance on every row
+    Wq, Ws = oracle_fp8_weight(N, K, 81 + M)
+    Xq, Xs = oracle_fp8_act(M, K, 82 + M)
+    ref = oracle.fp8_gemm(Xq, Xs, Wq, Ws)
+    Y1 = fb.fp8rl_gemm_w8a8_block(dev(Xq), dev(Xs), dev(Wq), dev(Ws))
+    Y2 = fb.fp8rl_gemm_w8a8_block(dev(Xq), dev(Xs), dev(Wq), dev(Ws),
+                                  workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
+    assert_fp8_gemm_close(host(Y1), ref, "with workspace")
+    assert_fp8_gemm_close(host(Y2), ref, "without workspace")
+
+
+@pytest.mark.parametrize("M", [1, 8, 40])
+def test_fp8_gemm_k_beyond_decode_limit(cuda_lib, M):
+    # K = 33024 (258 blocks) is beyond the decode kernel's 8 x 32 blocks: every
+    # M goes to the 128 x 256 tile kernel (split into K ranges through the
+    # workspace, or whole without it); both within tolerance on every row
+    N, K = 256, 33024
+    Wq, Ws = oracle_fp8_weight(N, K, 83)
+    Xq, Xs = oracle_fp8_act(M, K, 84 + M)
+    ref = oracle.fp8_gemm(Xq, Xs, Wq, Ws)
+    assert fb.fp8rl_gemm_workspace_bytes(M, N, K) > 0
+    Y1 = fb.fp8rl_gemm_w8a8_block(dev(Xq), dev(Xs), dev(Wq), dev(Ws))
+    Y2 = fb.fp8rl_gemm_w8a8_block(dev(Xq), dev(Xs), dev(Wq), dev(Ws),
+                                  workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
+    assert_fp8_gemm_close(host(Y1), ref, f"split K, M={M}")
+    assert_fp8_gemm_close(host(Y2), ref, f"whole K, M={M}")
 
 
 def test_fp8_gemm_prefill_tail_split_sampled(cuda_lib):

@@ -232,3 +232,51 @@ def test_fp8_kv_tensor_quant_reused_workspace_takes_no_stale_slot(cuda_lib):
         assert bits_u32(host(scale))[0] == np.float32(want_s).view(np.uint32)
         assert np.array_equal(host(KVq), want_q)
     assert fb.fp8rl_check_device_error() == 0
+
+
+@pytest.mark.parametrize("R", [4096, 16384])
+def test_fp8_kv_tensor_quant_graph_replays_recalibrate(cuda_lib, R):
+    # one call captured in a CUDA graph (4096 x 1024: the one-pass kernel;
+    # 16384 x 1024: three launches), replayed after new data is copied into its
+    # input: every replay recalibrates the scale from that data (the one-pass
+    # call's tag advances on the device, so a replay never accepts a slot left
+    # by the one before), checked against the oracle each time
+    C = 1024
+    X = torch.empty(R, C, dtype=torch.bfloat16, device="cuda")
+    KVq = torch.empty(R, C, dtype=torch.uint8, device="cuda")
+    scale = torch.empty(1, dtype=torch.float32, device="cuda")
+    ws = torch.empty(fb.fp8rl_kv_workspace_bytes(R, C), dtype=torch.uint8, device="cuda")
+    inputs = []
+    for i, (gain, r, c, v) in enumerate([(1.0, 7, 3, 900.0), (0.01, R - 1, C - 1, -0.5),
+                                         (1.0, R // 2, 100, 2500.0), (0.001, 0, 0, 0.0)]):
+        h = act_cpu(R, C, 9300 + i) * gain
+        h[r, c] = v
+        inputs.append(h)
+    X.copy_(inputs[0])
+    fb.fp8rl_quant_kv_tensor(X, KVq, scale, workspace=ws)          # warm-up outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fb.fp8rl_quant_kv_tensor(X, KVq, scale, workspace=ws)
+    for h in inputs + inputs[::-1]:
+        X.copy_(h)
+        g.replay()
+        torch.cuda.synchronize()
+        want_q, want_s = oracle.fp8_quant_tensor(synth.bf16_bits(h))
+        assert bits_u32(host(scale))[0] == np.float32(want_s).view(np.uint32)
+        assert np.array_equal(host(KVq), want_q)
+    assert fb.fp8rl_check_device_error() == 0
+
+
+def test_fp8_kv_tensor_quant_workspace_reused_across_paths(cuda_lib):
+    # one workspace for a three-launch call (its partials follow the header
+    # word), then one-pass calls, then three-launch again: each bit-exact
+    C = 1024
+    ws = torch.empty(fb.fp8rl_kv_workspace_bytes(16384, C), dtype=torch.uint8, device="cuda")
+    for R, seed in [(16384, 9401), (4096, 9402), (2048, 9403), (16384, 9404), (4096, 9405)]:
+        X = act_cpu(R, C, seed)
+        KVq, scale = fb.fp8rl_quant_kv_tensor(X.cuda(), workspace=ws)
+        want_q, want_s = oracle.fp8_quant_tensor(synth.bf16_bits(X))
+        assert bits_u32(host(scale))[0] == np.float32(want_s).view(np.uint32)
+        assert np.array_equal(host(KVq), want_q)
+    assert fb.fp8rl_check_device_error() == 0

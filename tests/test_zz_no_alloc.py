@@ -14,6 +14,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from precision_rl_rollout_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -69,3 +70,52 @@ def test_noalloc_kv_quant_rejects_tensors_above_its_limit(cuda_lib):
     assert rc == 6  # FP8RL_ERR_UNSUPPORTED
     rc = lib.fp8rl_quant_kv_tensor_noalloc(A, 16384, 16384 + 8, 16384 + 8, A, A, None)
     assert rc == 6
+
+
+def _check_error_word(lib):
+    word = ctypes.c_uint32(0)
+    rc = lib.fp8rl_check_device_error(ctypes.byref(word))
+    assert rc == 0 and word.value == 0, f"device error word {word.value:#x} (status {rc})"
+
+
+def test_noalloc_kv_quant_three_launch_then_one_pass_matches_oracle(cuda_lib):
+    lib = cuda_lib
+    # 16384 x 1024 is 1024 slices: too many for one pass, so its partials go
+    # through the shared array in three launches; the one-pass calls after it
+    # find those partials in the same array and must not mistake them for their
+    # own slots.  Every output is compared with the oracle, bit for bit.
+    for R, C, seed in [(16384, 1024, 11), (3000, 1024, 12), (16384, 1024, 13), (8229, 1024, 14)]:
+        X = synth.activation(R, C, synth.seed_for(6, seed), device="cuda")
+        KVq = torch.empty(R, C, dtype=torch.uint8, device="cuda")
+        scale = torch.empty(1, dtype=torch.float32, device="cuda")
+        assert _call_noalloc(lib, X, KVq, scale) == 0
+        torch.cuda.synchronize()
+        want_q, want_s = oracle.fp8_quant_tensor(synth.bf16_bits(X.cpu()))
+        assert scale.cpu().view(torch.int32).item() == int(np.float32(want_s).view(np.int32))
+        assert np.array_equal(KVq.cpu().numpy(), want_q)
+    _check_error_word(lib)
+
+
+def test_noalloc_kv_quant_at_its_size_limit(cuda_lib):
+    lib = cuda_lib
+    # 16384 x 16384 values, the documented maximum (16384 partials filling the
+    # array): equal to the workspace entry point bit for bit, its scale equal
+    # to fl32(amax / 448) of the whole tensor, and sampled rows equal to the
+    # oracle's codes under that scale
+    R = C = 16384
+    X = synth.activation(R, C, synth.seed_for(6, 15), device="cuda")
+    X[R - 1, C - 1] = -777.0                       # the amax in the last slice
+    KVq = torch.empty(R, C, dtype=torch.uint8, device="cuda")
+    scale = torch.empty(1, dtype=torch.float32, device="cuda")
+    assert _call_noalloc(lib, X, KVq, scale) == 0
+    ref_q, ref_s = _call_workspace(lib, X)
+    torch.cuda.synchronize()
+    assert torch.equal(scale.view(torch.int32), ref_s.view(torch.int32))
+    assert torch.equal(KVq, ref_q)
+    amax = np.float32(abs(X.float()).max().item())
+    assert scale.cpu().numpy()[0] == np.float32(amax / np.float32(448.0))
+    rows = np.array([0, 1, 8191, R - 2, R - 1])
+    want = oracle.fp8_quant_with_scale(synth.bf16_bits(X[rows].cpu()), float(scale.cpu().numpy()[0]))
+    assert np.array_equal(KVq[rows].cpu().numpy(), want)
+    del X, KVq, ref_q
+    _check_error_word(lib)
