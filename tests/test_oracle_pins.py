@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 import torch
 
+import golden_pins
 import oracle
 from precision_rl_rollout_gb300 import synth
 
@@ -173,6 +174,23 @@ def test_act_quant_hand_worked_example():
         assert np.array_equal(Xq[r], want_codes), f"row {r}: {Xq[r][:12]}"
         want_scale = np.array([int(d["scale"][0], 16)], np.uint32).view(np.float32)[0]
         assert Xs[0, r].view(np.uint32) == want_scale.view(np.uint32), f"row {r} scale"
+
+
+def test_weight_block_quant_hand_worked_example():
+    # 2 x 2 blocks: an inexact scale (amax 4: 3c124925) with a tie at -336, an exact
+    # non-power-of-two scale (amax 49: 7/64) whose quotients all land on E4M3
+    # midpoints, a block of zeros and negative zeros, and a fourth block whose
+    # scale (1/896) shares the first one's mantissa; each amax away from row 0 and
+    # column 0 of its block (tests/golden/e4m3_weight_block_256x256.txt)
+    golden_pins.check_weight_block_golden(oracle.fp8_quant_weight_block)
+
+
+def test_int8_row_quant_hand_worked_example():
+    # an inexact scale with amax 19/32 (3b993265, derived bit by bit) whose x/s
+    # lands exactly on 63.5, an exact scale (1/32) with ties at 64.5, 80.5, 66.5,
+    # 0.5, 1.5, 2.5 (to even), a zero row, and amax 9/32 (3b112245) whose x = amax/2
+    # falls just below 63.5 (tests/golden/int8_rows_4x128.txt)
+    golden_pins.check_int8_rows_golden(oracle.int8_quant_rows)
 
 
 # ------------------------------------------------------------------ quantizer invariants
