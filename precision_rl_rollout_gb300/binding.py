@@ -181,6 +181,30 @@ def fp8rl_quant_weight_block_grouped(items, stream=None):
         "fp8rl_quant_weight_block_grouped")
 
 
+class GroupedRequant:
+    """A fixed set of (W, Wq, Ws) for repeated fp8rl_quant_weight_block_grouped
+    calls (one per RL step): the descriptor array is marshalled once, so a call
+    costs one C-ABI call on the host."""
+
+    def __init__(self, items):
+        if not items or len(items) > 256:
+            raise ValueError("1 to 256 tensors per grouped requant")
+        self.lib = load()
+        self.items = list(items)                      # keeps the tensors alive
+        self.arr = (FP8RL_WDESC * len(self.items))()
+        for i, (W, Wq, Ws) in enumerate(self.items):
+            ldw = _rowmajor(W, "W")
+            N, K = W.shape
+            _need(Wq, (N, K), torch.uint8, W.device, "Wq")
+            _need(Ws, (N // 128, K // 128), torch.float32, W.device, "Ws")
+            self.arr[i] = FP8RL_WDESC(W.data_ptr(), Wq.data_ptr(), Ws.data_ptr(), N, K, ldw)
+
+    def __call__(self, stream=None):
+        _ck(self.lib.fp8rl_quant_weight_block_grouped(self.arr, len(self.items),
+                                                      _stream(self.items[0][0], stream)),
+            "fp8rl_quant_weight_block_grouped")
+
+
 def fp8rl_quant_act_group(X, Xq=None, Xs=None, stream=None):
     """X bf16 [M,K] -> (Xq uint8 [M,K], Xs fp32 [K/128, M])."""
     lib = load()
