@@ -474,7 +474,9 @@ def time_e2e(fb, args, dev, model, chunk_layers=8):
 
 def decode_sweep_32b(fb, dev, reps=10):
     """A2 + A4 on the Qwen2.5-32B shapes at M in {1, 8, 32, 128, 256}: each GEMM
-    walks distinct weight copies (> 3x L2) back to back in one CUDA graph."""
+    walks distinct weight copies (> 3x L2) back to back in one CUDA graph.  No
+    kernel in the graph writes weights, so the GEMMs pass
+    FP8RL_GEMM_WEIGHTS_STABLE."""
     dec = {}
     for s in synth.QWEN25_32B:
         W = synth.weight_bf16_direct(s.N, s.K, synth.seed_for(3, 0), device=dev)
@@ -488,7 +490,8 @@ def decode_sweep_32b(fb, dev, reps=10):
             Xq, Xs = fb.fp8rl_quant_act_group(X)
             Y = torch.empty(M, s.N, dtype=torch.bfloat16, device=dev)
             gws = torch.empty(max(16, fb.fp8rl_gemm_workspace_bytes(M, s.N, s.K)), dtype=torch.uint8, device=dev)
-            ms = _time_graph([lambda c=c: fb.fp8rl_gemm_w8a8_block(Xq, Xs, Wqs[c], Wss[c], Y=Y, workspace=gws)
+            ms = _time_graph([lambda c=c: fb.fp8rl_gemm_w8a8_block(Xq, Xs, Wqs[c], Wss[c], Y=Y, workspace=gws,
+                                                                   weights_stable=True)
                               for c in range(nc)], reps)
             aq = _time_graph([lambda: fb.fp8rl_quant_act_group(X, Xq, Xs)] * 16, reps)
             dec[f"{s.name}_M{M}"] = {"shape": s.name, "M": M, "N": s.N, "K": s.K,
@@ -659,9 +662,10 @@ def time_step_7b(fb, dev, steps=200):
         for i in range(len(shapes)):
             fb.fp8rl_quant_act_group(ls.X[i], ls.Xq[i], ls.Xs[i])
 
-    def gemm(ls):
+    def gemm(ls):                      # its codes were written two steps earlier: stable
         for i in range(len(shapes)):
-            fb.fp8rl_gemm_w8a8_block(ls.Xq[i], ls.Xs[i], ls.Wq[i], ls.Ws[i], Y=ls.Y[i], workspace=ws)
+            fb.fp8rl_gemm_w8a8_block(ls.Xq[i], ls.Xs[i], ls.Wq[i], ls.Ws[i], Y=ls.Y[i], workspace=ws,
+                                     weights_stable=True)
 
     g_step = [capture_graph(lambda r=r: (run_requant(fb, sets[r]), aq(sets[(r + COPIES // 2) % COPIES]),
                                          gemm(sets[(r + COPIES // 2) % COPIES])))

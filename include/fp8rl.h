@@ -147,6 +147,27 @@ int fp8rl_gemm_w8a8_block(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
                           uint16_t* Y, int64_t ldy, void* workspace,
                           size_t workspace_bytes, void* stream);
 
+/* fp8rl_gemm_w8a8_block with flags (same arithmetic, arguments and errors;
+ * fp8rl_gemm_w8a8_block is this call with flags = 0).
+ * FP8RL_GEMM_WEIGHTS_STABLE: the caller guarantees that the kernel issued
+ *     immediately before this call on the same stream did not write Wq (the
+ *     usual case in a decode loop: the weights were requantized earlier in the
+ *     step, and the call before this one produced the activations).  Every
+ *     kernel of this library is launched only after the one before it has
+ *     passed its own wait for its predecessor, so anything issued earlier than
+ *     the immediately preceding kernel has completed by then.  Small weight
+ *     matrices (at most 48 MB) then start streaming into the GEMM before its
+ *     wait for that preceding kernel, overlapping its tail.  With a Wq written
+ *     by the immediately preceding kernel the result is undefined.
+ * Unknown flag bits: FP8RL_ERR_UNSUPPORTED.
+ * fp8rl_linear_w8a8_block applies this internally (its GEMM always follows its
+ * own activation quantizer). */
+#define FP8RL_GEMM_WEIGHTS_STABLE 1u
+int fp8rl_gemm_w8a8_block_ex(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
+                             const float* Ws, int64_t M, int64_t N, int64_t K,
+                             uint16_t* Y, int64_t ldy, void* workspace,
+                             size_t workspace_bytes, unsigned flags, void* stream);
+
 /* ------------------------------------------------------------------------
  * Grouped block-scaled FP8 GEMM for mixture-of-experts layers (FP8-RL,
  * Abstract: the FP8 rollout stack serves dense and MoE models).  The T token

@@ -26,7 +26,8 @@ STATUS = {0: "FP8RL_OK", 1: "FP8RL_ERR_NULL", 2: "FP8RL_ERR_SHAPE", 3: "FP8RL_ER
 # Every symbol the header declares (the CPU test checks the library exports them).
 EXPORTS = ("fp8rl_status_string", "fp8rl_abi_version", "fp8rl_quant_weight_block",
            "fp8rl_quant_weight_block_grouped", "fp8rl_quant_act_group",
-           "fp8rl_gemm_workspace_bytes", "fp8rl_gemm_w8a8_block", "fp8rl_gemm_w8a8_block_grouped",
+           "fp8rl_gemm_workspace_bytes", "fp8rl_gemm_w8a8_block", "fp8rl_gemm_w8a8_block_ex",
+           "fp8rl_gemm_w8a8_block_grouped",
            "fp8rl_linear_workspace_bytes", "fp8rl_linear_w8a8_block",
            "int8rl_quant_weight_channel", "int8rl_quant_act_token",
            "int8rl_gemm_workspace_bytes", "int8rl_gemm_w8a8", "fp8rl_check_device_error",
@@ -82,6 +83,7 @@ def load(path: str | None = None):
         lib.int8rl_gemm_kernel_count.restype = ctypes.c_int
         lib.int8rl_gemm_kernel_count.argtypes = [I, I, I, Z]
         lib.fp8rl_gemm_w8a8_block.argtypes = [P, P, P, P, I, I, I, P, I, P, Z, S]
+        lib.fp8rl_gemm_w8a8_block_ex.argtypes = [P, P, P, P, I, I, I, P, I, P, Z, ctypes.c_uint, S]
         lib.fp8rl_gemm_w8a8_block_grouped.argtypes = [P, P, P, P, P, I, I, I, I, I, P, I, S]
         lib.fp8rl_linear_workspace_bytes.restype = Z
         lib.fp8rl_linear_workspace_bytes.argtypes = [I, I, I]
@@ -221,8 +223,12 @@ def fp8rl_gemm_workspace_bytes(M: int, N: int, K: int) -> int:
     return int(load().fp8rl_gemm_workspace_bytes(M, N, K))
 
 
-def fp8rl_gemm_w8a8_block(Xq, Xs, Wq, Ws, Y=None, workspace=None, stream=None):
-    """-> Y bf16 [M,N]."""
+FP8RL_GEMM_WEIGHTS_STABLE = 1
+
+
+def fp8rl_gemm_w8a8_block(Xq, Xs, Wq, Ws, Y=None, workspace=None, stream=None, weights_stable=False):
+    """-> Y bf16 [M,N].  weights_stable=True passes FP8RL_GEMM_WEIGHTS_STABLE
+    (the kernel issued right before this call on the stream did not write Wq)."""
     lib = load()
     M, K = Xq.shape
     N = Wq.shape[0]
@@ -232,9 +238,14 @@ def fp8rl_gemm_w8a8_block(Xq, Xs, Wq, Ws, Y=None, workspace=None, stream=None):
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=Wq.device)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _ck(lib.fp8rl_gemm_w8a8_block(_p(Xq), _p(Xs), _p(Wq), _p(Ws), M, N, K, _p(Y), ldy,
-                                  _p(workspace), wbytes, _stream(Wq, stream)),
-        "fp8rl_gemm_w8a8_block")
+    if weights_stable:
+        _ck(lib.fp8rl_gemm_w8a8_block_ex(_p(Xq), _p(Xs), _p(Wq), _p(Ws), M, N, K, _p(Y), ldy,
+                                         _p(workspace), wbytes, FP8RL_GEMM_WEIGHTS_STABLE, _stream(Wq, stream)),
+            "fp8rl_gemm_w8a8_block_ex")
+    else:
+        _ck(lib.fp8rl_gemm_w8a8_block(_p(Xq), _p(Xs), _p(Wq), _p(Ws), M, N, K, _p(Y), ldy,
+                                      _p(workspace), wbytes, _stream(Wq, stream)),
+            "fp8rl_gemm_w8a8_block")
     return Y
 
 

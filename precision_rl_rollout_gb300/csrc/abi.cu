@@ -105,17 +105,25 @@ int fp8rl_gemm_kernel_count(int64_t M, int64_t N, int64_t K, size_t workspace_by
     return gemm_fp8_kernel_count(M, N, K, workspace_bytes);
 }
 
-int fp8rl_gemm_w8a8_block(const uint8_t* Xq, const float* Xs, const uint8_t* Wq, const float* Ws,
-                          int64_t M, int64_t N, int64_t K, uint16_t* Y, int64_t ldy,
-                          void* workspace, size_t workspace_bytes, void* stream) {
+int fp8rl_gemm_w8a8_block_ex(const uint8_t* Xq, const float* Xs, const uint8_t* Wq, const float* Ws,
+                             int64_t M, int64_t N, int64_t K, uint16_t* Y, int64_t ldy,
+                             void* workspace, size_t workspace_bytes, unsigned flags, void* stream) {
     int rc = check_gemm_common(Xq, Xs, Wq, Ws, M, N, K, Y, ldy);
     if (rc) return rc;
+    if (flags & ~(unsigned)FP8RL_GEMM_WEIGHTS_STABLE) return FP8RL_ERR_UNSUPPORTED;
     if (M > 65535LL * 32) return FP8RL_ERR_UNSUPPORTED;
     if (!aligned16(workspace)) return FP8RL_ERR_ALIGN;
     if (M == 0) return FP8RL_OK;
     // less workspace than the query only gives up split-K (see the header)
     return cuda_status(launch_gemm_fp8(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, workspace,
-                                       workspace ? workspace_bytes : 0, as_stream(stream)));
+                                       workspace ? workspace_bytes : 0,
+                                       (flags & FP8RL_GEMM_WEIGHTS_STABLE) != 0, as_stream(stream)));
+}
+
+int fp8rl_gemm_w8a8_block(const uint8_t* Xq, const float* Xs, const uint8_t* Wq, const float* Ws,
+                          int64_t M, int64_t N, int64_t K, uint16_t* Y, int64_t ldy,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+    return fp8rl_gemm_w8a8_block_ex(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, workspace, workspace_bytes, 0u, stream);
 }
 
 int fp8rl_gemm_w8a8_block_grouped(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,

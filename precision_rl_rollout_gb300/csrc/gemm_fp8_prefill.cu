@@ -505,9 +505,9 @@ int gemm_fp8_kernel_count(int64_t M, int64_t N, int64_t K, size_t ws_bytes) {
 
 cudaError_t launch_gemm_fp8(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
                             const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
-                            int64_t ldy, void* ws, size_t ws_bytes, cudaStream_t st) {
+                            int64_t ldy, void* ws, size_t ws_bytes, bool weights_stable, cudaStream_t st) {
     if (runs_decode(M, N, K, ws_bytes))
-        return launch_gemm_fp8_decode(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, ws, ws_bytes, st);
+        return launch_gemm_fp8_decode(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, ws, ws_bytes, weights_stable, st);
     return launch_gemm_fp8_prefill(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, ws, ws_bytes, st);
 }
 

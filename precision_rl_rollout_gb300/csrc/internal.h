@@ -56,9 +56,12 @@ cudaError_t launch_logits_kl(const uint16_t* P, int64_t ldp, const uint16_t* Q, 
                              int64_t V, float* kl, void* ws, cudaStream_t st);
 
 // FP8 block-scaled GEMM: dispatch by M (tcgen05 decode kernel for M <= 256).
+// weights_stable: the kernel immediately preceding the call in the stream did
+// not write Wq, so small weights may start streaming before the dependency wait.
 cudaError_t launch_gemm_fp8_decode(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
                                    const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
-                                   int64_t ldy, void* ws, size_t ws_bytes, cudaStream_t st);
+                                   int64_t ldy, void* ws, size_t ws_bytes, bool weights_stable,
+                                   cudaStream_t st);
 size_t decode_workspace_bytes(int64_t M, int64_t N, int64_t K);
 int decode_kernel_count(int64_t M, int64_t N, int64_t K, size_t ws_bytes);
 int gemm_fp8_kernel_count(int64_t M, int64_t N, int64_t K, size_t ws_bytes);
@@ -72,7 +75,7 @@ cudaError_t launch_gemm_fp8_grouped(const uint8_t* Xq, const float* Xs, const ui
 size_t gemm_fp8_workspace_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_gemm_fp8(const uint8_t* Xq, const float* Xs, const uint8_t* Wq,
                             const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
-                            int64_t ldy, void* ws, size_t ws_bytes, cudaStream_t st);
+                            int64_t ldy, void* ws, size_t ws_bytes, bool weights_stable, cudaStream_t st);
 
 // INT8 GEMM: exact integer arithmetic on the fp16 tensor path (tcgen05).
 cudaError_t launch_gemm_int8_tc(const int8_t* Xq, const float* Xs, const int8_t* Wq, const float* Ws,

@@ -129,6 +129,11 @@ __device__ __forceinline__ uint32_t kv_next_tag(uint32_t prev) {
 __device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
     asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
 __device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
     uint64_t v;
     asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
@@ -150,17 +155,20 @@ __global__ void __launch_bounds__(kKvThreads, 4)   // four CTAs per SM: 608 slic
 kv_onepass_kernel(const uint16_t* __restrict__ X, int64_t total, int64_t cpr, int64_t ld,
                   uint64_t* __restrict__ slot, int64_t P, float* __restrict__ scale,
                   uint8_t* __restrict__ Xq, uint32_t* __restrict__ err) {
-    __shared__ uint32_t s_tag;
-    if (threadIdx.x == 0) s_tag = kv_next_tag((uint32_t)(ld_acquire_u64(slot) >> 32));
     const int64_t base = (int64_t)blockIdx.x * kKvChunksPerCta;
     uint4 v[kKvChunksPerThread];
-    uint32_t m = 0;
 #pragma unroll
     for (int i = 0; i < kKvChunksPerThread; ++i) {
         const int64_t c = base + i * kKvThreads + threadIdx.x;
         v[i] = c < total ? ld_stream_v4(X + chunk_offset(c, cpr, ld)) : make_uint4(0, 0, 0, 0);
-        m = absmax_v4(m, v[i]);
     }
+    // the header is read after the slice's loads are in flight; a relaxed load
+    // suffices, as the release store of this CTA's slot below orders it first
+    __shared__ uint32_t s_tag;
+    if (threadIdx.x == 0) s_tag = kv_next_tag((uint32_t)(ld_relaxed_u64(slot) >> 32));
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < kKvChunksPerThread; ++i) m = absmax_v4(m, v[i]);
     __shared__ uint32_t red[kKvThreads / 32];
     m = __reduce_max_sync(0xffffffffu, max(m & 0xFFFFu, m >> 16));
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;

@@ -143,6 +143,11 @@ def test_gemm_validation(lib):
     assert g(A + 4, A, A, A, 4, 128, 128, A, 128, None, ws, None) == 3
     assert g(A, A, A, A, 4, 128, 128, A, 132, None, ws, None) == 3   # row pitch 264 B
     assert g(A, A, A, A, 0, 128, 128, A, 128, None, ws, None) == 0   # empty batch
+    e = lib.fp8rl_gemm_w8a8_block_ex
+    assert e(A, A, A, A, 4, 100, 128, A, 100, None, ws, 1, None) == 2   # same validation
+    assert e(A, A, A, A, 0, 128, 128, A, 128, None, ws, 1, None) == 0   # empty batch, known flag
+    assert e(A, A, A, A, 0, 128, 128, A, 128, None, ws, 2, None) == 6   # unknown flag bit
+    assert e(A, A, A, A, 0, 128, 128, A, 128, None, ws, 0x80000000, None) == 6
     i = lib.int8rl_gemm_w8a8
     assert i(A, A, A, A, 4, 128, 140032, A, 128, None, None, 0, None) == 6  # K * 127^2 >= 2^31
     assert i(A, A, A, A, 4, 128, 128, A, 128, A + 4, None, 0, None) == 3    # acc alignment

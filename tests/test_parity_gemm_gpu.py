@@ -155,10 +155,24 @@ def test_fp8_gemm_qwen32b_decode_sweep_sampled(cuda_lib, shape, M):
               rows=sample_rows(M, 3, seed=M), what=f"32B {shape.name} M={M}")
 
 
+def _rows_in_distinct_tiles(M, n, seed, tile=128):
+    """n rows, each in its own `tile`-row tile: the first and last tiles and n-2
+    seeded ones between them, one seeded row inside each."""
+    rng = np.random.default_rng(seed)
+    tiles = (M + tile - 1) // tile
+    pick = np.concatenate([[0, tiles - 1], rng.choice(np.arange(1, tiles - 1), size=n - 2, replace=False)])
+    rows = [min(M - 1, t * tile + int(rng.integers(tile))) for t in sorted(pick)]
+    return np.array(rows)
+
+
 @pytest.mark.parametrize("shape", synth.QWEN25_32B, ids=lambda s: s.name)
 def test_fp8_gemm_qwen32b_prefill_sampled(cuda_lib, shape):
+    # M = 8192 (64 token tiles of the persistent 128 x 256 schedule): 16 rows,
+    # each in a different token tile, against every output column
+    rows = _rows_in_distinct_tiles(synth.PREFILL_M, 16, seed=shape.K + shape.N)
+    assert len(set(r // 128 for r in rows)) == 16
     _fp8_case(synth.PREFILL_M, shape.N, shape.K, synth.seed_for(4, 0), synth.seed_for(4, 1),
-              rows=sample_rows(synth.PREFILL_M, 3, seed=shape.K), what=f"prefill {shape.name}")
+              rows=rows, what=f"prefill {shape.name}")
 
 
 def _int8_case(M, N, K, seed_w, seed_x, rows=None):
@@ -271,6 +285,26 @@ def test_fp8_gemm_is_deterministic(cuda_lib, M, N, K):
     Y0 = fb.fp8rl_gemm_w8a8_block(Xq, Xs, Wq, Ws, workspace=ws)
     for _ in range(3):
         assert torch.equal(fb.fp8rl_gemm_w8a8_block(Xq, Xs, Wq, Ws, workspace=ws), Y0)
+
+
+@pytest.mark.parametrize("M", [1, 8, 32, 64, 200])
+@pytest.mark.parametrize("shape", [synth.QWEN25_7B[0], synth.QWEN25_7B[1], synth.QWEN25_32B[0],
+                                   synth.QWEN25_32B[1], synth.QWEN25_7B[3]], ids=lambda s: s.name + str(s.K))
+def test_fp8_gemm_weights_stable_flag_back_to_back(cuda_lib, shape, M):
+    # FP8RL_GEMM_WEIGHTS_STABLE: weight tiles are loaded before the dependency
+    # wait (shapes of at most 48 MB); a chain of calls on different weights
+    # and inputs, each right after the previous GEMM, every output checked
+    seeds = [(61, 62), (63, 64), (65, 66)]
+    cases = [(oracle_fp8_weight(shape.N, shape.K, sw), oracle_fp8_act(M, shape.K, sx)) for sw, sx in seeds]
+    dev_cases = [(dev(wq), dev(ws), dev(xq), dev(xs)) for (wq, ws), (xq, xs) in cases]
+    Ys = [torch.empty(M, shape.N, dtype=torch.bfloat16, device="cuda") for _ in seeds]
+    torch.cuda.synchronize()
+    for (wq, ws, xq, xs), Y in zip(dev_cases, Ys):
+        fb.fp8rl_gemm_w8a8_block(xq, xs, wq, ws, Y=Y, weights_stable=True)
+    rows = sample_rows(M, 4, seed=M + shape.N)
+    for ((wq, ws), (xq, xs)), Y in zip(cases, Ys):
+        ref = oracle.fp8_gemm(xq[rows], xs[:, rows], wq, ws)
+        assert_fp8_gemm_close(host(Y)[rows], ref, f"stable weights {shape.name} M={M}")
 
 
 def test_no_device_error_after_gemms(cuda_lib):

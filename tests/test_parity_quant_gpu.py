@@ -75,6 +75,37 @@ def test_grouped_requant_matches_oracle_across_launches(cuda_lib):
         _cmp_weight_block(cpu[i], items[i][1], items[i][2], f"grouped[{i}]")
 
 
+def test_grouped_requant_qwen32b_full_model_sampled(cuda_lib):
+    # the full-model requant as timed: 64 layers x 4 Qwen2.5-32B weights (256
+    # tensors, 31.2 G values, 62.4 GB) after a policy update, in one grouped
+    # launch; sampled blocks of the first, a middle and the last layer of
+    # every shape -- corner blocks and seeded interior ones -- against the oracle
+    items = []
+    for layer in range(synth.QWEN25_32B_LAYERS):
+        for i, s in enumerate(synth.QWEN25_32B):
+            seed = synth.seed_for(4, 0) + 1000 * layer + i
+            W = synth.weight_bf16_direct(s.N, s.K, seed, device="cuda")
+            synth.policy_update_(W, seed + 500)
+            items.append((W, torch.empty(s.N, s.K, dtype=torch.uint8, device="cuda"),
+                          torch.empty(s.N // 128, s.K // 128, dtype=torch.float32, device="cuda")))
+    fb.GroupedRequant(items)()
+    torch.cuda.synchronize()
+    nshapes = len(synth.QWEN25_32B)
+    for layer in (0, 37, synth.QWEN25_32B_LAYERS - 1):
+        for i, s in enumerate(synth.QWEN25_32B):
+            W, Wq, Ws = items[layer * nshapes + i]
+            Ws_h = host(Ws)
+            for nb, kb in sample_blocks(s.N // 128, s.K // 128, 12, seed=layer * 10 + i):
+                blk = W[nb * 128:(nb + 1) * 128, kb * 128:(kb + 1) * 128].contiguous().cpu()
+                q, sc = oracle.fp8_quant_weight_block(synth.bf16_bits(blk))
+                got = host(Wq[nb * 128:(nb + 1) * 128, kb * 128:(kb + 1) * 128])
+                assert bits_u32(Ws_h[nb, kb:kb + 1])[0] == bits_u32(sc)[0, 0], (layer, s.name, nb, kb)
+                assert np.array_equal(got, q), (layer, s.name, nb, kb)
+    del items
+    torch.cuda.empty_cache()
+    assert fb.fp8rl_check_device_error() == 0
+
+
 @pytest.mark.parametrize("M,K", [(1, 128), (5, 256), (16, 256), (17, 384), (33, 3584),
                                  (64, 3584), (257, 640)])
 def test_fp8_act_quant_full(cuda_lib, M, K):
