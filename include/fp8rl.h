@@ -200,8 +200,11 @@ int fp8rl_gemm_w8a8_block_grouped(const uint8_t* Xq, const float* Xs, const uint
  * quantized on the fly, token by token).  The result is
  *   Y = fp8rl_gemm_w8a8_block(Xq, Xs, Wq, Ws)  with  (Xq, Xs) = fp8rl_quant_act_group(X):
  * the same codes and scales (bit-exact) and Y within the GEMM's tolerance.
- * Two kernels run back to back on `stream`; the GEMM is scheduled while the
- * quantizer runs and prefetches its first weight blocks meanwhile.
+ * Two kernels run back to back on `stream`: the quantizer, then the GEMM,
+ * which is scheduled while the quantizer runs and starts streaming its weights
+ * meanwhile (the quantizer writes no weights, so the GEMM loads the weight
+ * tiles of its first pipeline stages before its dependency wait, as with
+ * FP8RL_GEMM_WEIGHTS_STABLE).  fp8rl_linear_kernel_count gives the count.
  * X   bf16 [M][ldx], ldx >= K, ldx % 8 == 0, 16-byte aligned.
  * Wq, Ws, Y, ldy as for fp8rl_gemm_w8a8_block.
  * Xq_or_null, Xs_or_null: both NULL, or both given ([M][K] e4m3 contiguous,
@@ -214,6 +217,11 @@ int fp8rl_gemm_w8a8_block_grouped(const uint8_t* Xq, const float* Xs, const uint
  * Limit: M <= 1048560 (FP8RL_ERR_UNSUPPORTED above).
  * ---------------------------------------------------------------------- */
 size_t fp8rl_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
+/* Kernels fp8rl_linear_w8a8_block launches for this shape with workspace_bytes
+ * of workspace (want_codes != 0 when Xq/Xs are to be returned): the quantizer
+ * plus the GEMM's kernel count.  0 for M == 0; -FP8RL_ERR_SHAPE for an invalid
+ * shape.  Host-only, no device access. */
+int fp8rl_linear_kernel_count(int64_t M, int64_t N, int64_t K, size_t workspace_bytes, int want_codes);
 int fp8rl_linear_w8a8_block(const uint16_t* X, int64_t ldx, const uint8_t* Wq, const float* Ws,
                             int64_t M, int64_t N, int64_t K, uint16_t* Y, int64_t ldy,
                             uint8_t* Xq_or_null, float* Xs_or_null, void* workspace,

@@ -28,7 +28,7 @@ EXPORTS = ("fp8rl_status_string", "fp8rl_abi_version", "fp8rl_quant_weight_block
            "fp8rl_quant_weight_block_grouped", "fp8rl_quant_act_group",
            "fp8rl_gemm_workspace_bytes", "fp8rl_gemm_w8a8_block", "fp8rl_gemm_w8a8_block_ex",
            "fp8rl_gemm_w8a8_block_grouped",
-           "fp8rl_linear_workspace_bytes", "fp8rl_linear_w8a8_block",
+           "fp8rl_linear_workspace_bytes", "fp8rl_linear_kernel_count", "fp8rl_linear_w8a8_block",
            "int8rl_quant_weight_channel", "int8rl_quant_act_token",
            "int8rl_gemm_workspace_bytes", "int8rl_gemm_w8a8", "fp8rl_check_device_error",
            "fp8rl_gemm_kernel_count", "int8rl_gemm_kernel_count",
@@ -88,6 +88,8 @@ def load(path: str | None = None):
         lib.fp8rl_linear_workspace_bytes.restype = Z
         lib.fp8rl_linear_workspace_bytes.argtypes = [I, I, I]
         lib.fp8rl_linear_w8a8_block.argtypes = [P, I, P, P, I, I, I, P, I, P, P, P, Z, S]
+        lib.fp8rl_linear_kernel_count.restype = ctypes.c_int
+        lib.fp8rl_linear_kernel_count.argtypes = [I, I, I, Z, ctypes.c_int]
         lib.int8rl_quant_weight_channel.argtypes = [P, I, I, I, P, P, S]
         lib.int8rl_quant_act_token.argtypes = [P, I, I, I, P, P, S]
         lib.int8rl_gemm_workspace_bytes.restype = Z
@@ -321,6 +323,10 @@ def int8rl_quant_act_token(X, Xq=None, Xs=None, stream=None):
 
 def fp8rl_gemm_kernel_count(M: int, N: int, K: int, workspace_bytes: int) -> int:
     return int(load().fp8rl_gemm_kernel_count(M, N, K, workspace_bytes))
+
+
+def fp8rl_linear_kernel_count(M: int, N: int, K: int, workspace_bytes: int, want_codes: bool = False) -> int:
+    return int(load().fp8rl_linear_kernel_count(M, N, K, workspace_bytes, 1 if want_codes else 0))
 
 
 def int8rl_gemm_kernel_count(M: int, N: int, K: int, workspace_bytes: int) -> int:

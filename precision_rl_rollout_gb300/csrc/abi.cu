@@ -147,6 +147,15 @@ size_t fp8rl_linear_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     return linear_workspace_bytes(M, N, K);
 }
 
+int fp8rl_linear_kernel_count(int64_t M, int64_t N, int64_t K, size_t workspace_bytes, int want_codes) {
+    (void)want_codes;                                   // the same kernels either way
+    if (M < 0 || N <= 0 || K <= 0 || N % kBlk || K % kBlk) return -FP8RL_ERR_SHAPE;
+    if (M == 0) return 0;
+    const size_t g = gemm_fp8_workspace_bytes(M, N, K);
+    const size_t gws = (g && workspace_bytes >= linear_workspace_bytes(M, N, K)) ? g : 0;
+    return 1 + gemm_fp8_kernel_count(M, N, K, gws);
+}
+
 int fp8rl_linear_w8a8_block(const uint16_t* X, int64_t ldx, const uint8_t* Wq, const float* Ws,
                             int64_t M, int64_t N, int64_t K, uint16_t* Y, int64_t ldy,
                             uint8_t* Xq_or_null, float* Xs_or_null, void* workspace,

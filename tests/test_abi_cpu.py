@@ -189,6 +189,20 @@ def test_gemm_kernel_counts(lib):
     assert lib.int8rl_gemm_kernel_count(4096, 7168, 5120, 0) == 1
 
 
+def test_linear_kernel_counts(lib):
+    f = lib.fp8rl_linear_kernel_count
+    assert f(0, 4608, 3584, 0, 0) == 0
+    assert f(4, 100, 3584, 0, 0) == -2
+    for M, N, K in [(1, 4608, 3584), (16, 3584, 18944), (32, 5120, 5120), (64, 3584, 18944), (300, 256, 4096)]:
+        ws = lib.fp8rl_linear_workspace_bytes(M, N, K)
+        gws = lib.fp8rl_gemm_workspace_bytes(M, N, K)
+        # the quantizer plus the GEMM's kernels, with or without the codes back
+        for want in (0, 1):
+            assert f(M, N, K, ws, want) == 1 + lib.fp8rl_gemm_kernel_count(M, N, K, gws)
+        # without the workspace the GEMM gives up its memory split
+        assert f(M, N, K, 0, 0) == 1 + lib.fp8rl_gemm_kernel_count(M, N, K, 0)
+
+
 def test_gemm_workspace_query_is_monotone(lib):
     for f in (lib.fp8rl_gemm_workspace_bytes, lib.int8rl_gemm_workspace_bytes):
         a = f(1, 4608, 3584)
