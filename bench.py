@@ -65,12 +65,15 @@ PREFILL_M = synth.PREFILL_M
 #  - prefill: the four M = 8192 GEMMs of the 32B layer, summed;
 #  - decode: one launch of the worst decode-sweep shape.
 NCU_TRAFFIC = {"kernel": "quant_weight_block_kernel", "source_sha1": "69912cc3432327fae840b52154efe497e2f08df4",
-               "bytes_per_value": (466135296 + 174760960) / sum(s.elems for s in synth.QWEN25_7B),
-               "profile": "profiles/requant_weight_block_qwen7b.md"}
-NCU_TRAFFIC_PREFILL = {"kernel": "gemm_fp8_prefill_kernel", "source_sha1": None, "bytes_per_step": None,
-                       "profile": None}
-NCU_TRAFFIC_DECODE = {"kernel": "gemm_fp8_decode_kernel", "source_sha1": None, "case": None,
-                      "bytes_per_launch": None, "profile": None}
+               "bytes_per_value": (1950448000 + 918897664) / (2 * sum(s.elems for s in synth.QWEN25_32B)),
+               "profile": "profiles/requant_weight_block_qwen32b_2layers.md"}
+NCU_TRAFFIC_PREFILL = {"kernel": "gemm_fp8_prefill_kernel", "source_sha1": "be4c0715a2a500d77f21e912c6e6d27cc4966fce",
+                       "bytes_per_step": (114916000 + 90111232) + (92420000 + 57136640) + (1569437000 + 882317824)
+                       + (3264048000 + 83973632),
+                       "profile": "profiles/prefill_gemm_qwen32b_m8192_four_shapes.md"}
+NCU_TRAFFIC_DECODE = {"kernel": "FP8 GEMM at a decode size", "source_sha1": "ce5f356c98b581a1d4b387caccdd6ce5962e51b8",
+                      "case": "o_proj_M256", "bytes_per_launch": 27609344 + 15736064,
+                      "profile": "profiles/decode_gemm_qwen32b_o_proj_m256.md"}
 
 
 # ------------------------------------------------------------------ algorithmic bytes
@@ -536,7 +539,8 @@ def prefill_source_sha1():
 
 
 def decode_source_sha1():
-    return _file_sha1("gemm_fp8_tc.cu", "sm100_ptx.cuh", "common.cuh")
+    """Both GEMM kernels: the dispatch may give a decode size to either."""
+    return _file_sha1("gemm_fp8_tc.cu", "gemm_fp8_prefill.cu", "sm100_ptx.cuh", "common.cuh")
 
 
 def traffic_or_null(values=None):
@@ -599,8 +603,10 @@ def roofline_entries(head, dec, peaks):
     gbs = w["bytes"] / (w["us"] * 1e-6) / 1e9
     worst_shape = min(w["shapes"], key=w["shapes"].get)
     ent.append({"part": "decode GEMM (A4)", "bound": "hbm",
-                "kernel": f"gemm_fp8_decode_kernel (+ split-K reduction where planned), Qwen2.5-32B shapes at "
-                          f"M={worst_m}, the sweep M with the lowest aggregate fraction",
+                "kernel": f"the FP8 GEMM kernels the dispatch picks at decode sizes (gemm_fp8_decode_kernel, or "
+                          f"gemm_fp8_prefill_kernel where its cost model is lower; each with its split-K "
+                          f"reduction launch where planned), Qwen2.5-32B shapes at M={worst_m}, the sweep M with "
+                          f"the lowest aggregate fraction",
                 "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                 "traffic": decode_traffic_or_null(f"{worst_shape}_M{worst_m}"),
                 "algorithmic_bytes": w["bytes"], "per_shape_frac": w["shapes"],
