@@ -67,9 +67,9 @@ PREFILL_M = synth.PREFILL_M
 NCU_TRAFFIC = {"kernel": "quant_weight_block_kernel", "source_sha1": "69912cc3432327fae840b52154efe497e2f08df4",
                "bytes_per_value": (1950448000 + 918897664) / (2 * sum(s.elems for s in synth.QWEN25_32B)),
                "profile": "profiles/requant_weight_block_qwen32b_2layers.md"}
-NCU_TRAFFIC_PREFILL = {"kernel": "gemm_fp8_prefill_kernel", "source_sha1": "be4c0715a2a500d77f21e912c6e6d27cc4966fce",
-                       "bytes_per_step": (114916000 + 90111232) + (92420000 + 57136640) + (1569437000 + 882317824)
-                       + (3264048000 + 83973632),
+NCU_TRAFFIC_PREFILL = {"kernel": "gemm_fp8_prefill_kernel", "source_sha1": "51a938b4bdca35303f75f82d3edfa7aa725d6c33",
+                       "bytes_per_step": (108063488 + 89519104) + (87500288 + 53253632) + (1324224256 + 878707712)
+                       + (2229088000 + 78596096),
                        "profile": "profiles/prefill_gemm_qwen32b_m8192_four_shapes.md"}
 NCU_TRAFFIC_DECODE = {"kernel": "FP8 GEMM at a decode size", "source_sha1": "ce5f356c98b581a1d4b387caccdd6ce5962e51b8",
                       "case": "o_proj_M256", "bytes_per_launch": 27609344 + 15736064,

@@ -61,9 +61,25 @@ struct PrefillParams {
     int64_t M, ldy;
     int KB, NB;        // K/128, N/128
     int mtiles, ntiles;
+    int group_m;        // token tiles per group of the tile order (see tile_coords)
     int split, kb_per;  // K ranges per split tile and K blocks per range (split 1: no workspace)
     int full_tiles;     // tiles [0, full_tiles) are not split (all of them when split == 1)
 };
+
+// Tile order: groups of group_m token tiles; within a group the weight-column
+// tile advances slowest and the token tile fastest.  With group_m = mtiles this
+// is the token-tile-fastest order over the whole output (every weight tile is
+// read by all token tiles while it is in L2); a smaller group keeps the
+// activations of the group in L2 while the weight columns stream past, for
+// activations larger than L2.
+__host__ __device__ __forceinline__ void tile_coords(int64_t tile, int mtiles, int ntiles, int group_m, int& mt,
+                                                     int& nt) {
+    const int64_t per_group = (int64_t)group_m * ntiles;
+    const int64_t g = tile / per_group, r = tile - g * per_group;
+    const int rows = min(group_m, mtiles - (int)g * group_m);      // token tiles in this group
+    nt = (int)(r / rows);
+    mt = (int)(g * group_m + r % rows);
+}
 
 // Work unit u: tile, K range [kb_beg, kb_end), and the range's index (-1: the
 // whole tile, written as bf16).  Units [0, full_tiles) are whole tiles; each
@@ -134,7 +150,8 @@ gemm_fp8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_co
             uint32_t it = 0;
             for (int u = blockIdx.x; u < total_units && !*abort; u += gridDim.x) {
                 const PrefillUnit un = prefill_unit<kSplit>(u, p);
-                const int mt = un.tile % p.mtiles, nt = un.tile / p.mtiles;
+                int mt, nt;
+                tile_coords(un.tile, p.mtiles, p.ntiles, p.group_m, mt, nt);
                 for (int kb = un.kb_beg; kb < un.kb_end; ++kb, ++it) {
                     const int s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1;
@@ -197,7 +214,8 @@ gemm_fp8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_co
         for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
             const PrefillUnit un = prefill_unit<kSplit>(u, p);
             const int tile = un.tile, sp = un.sp;
-            const int mt = tile % p.mtiles, nt = tile / p.mtiles;
+            int mt, nt;
+            tile_coords(tile, p.mtiles, p.ntiles, p.group_m, mt, nt);
             const int kb_beg = un.kb_beg, kb_end = un.kb_end;
             const int64_t m = (int64_t)mt * kBM + row;
             const int nb = 2 * nt + h;
@@ -310,15 +328,17 @@ gemm_fp8_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_co
 // Split-K reduction: one thread per (tile row, 8 output columns); the splits
 // are added in order in fp32, then rounded to bf16 once.
 __global__ void __launch_bounds__(256)
-prefill_splitk_reduce_kernel(const float* __restrict__ part, int64_t M, int64_t N, int mtiles, int split,
-                             int tile0, int64_t units8, uint16_t* __restrict__ Y, int64_t ldy) {
+prefill_splitk_reduce_kernel(const float* __restrict__ part, int64_t M, int64_t N, int mtiles, int ntiles,
+                             int group_m, int split, int tile0, int64_t units8, uint16_t* __restrict__ Y,
+                             int64_t ldy) {
     pdl_wait_then_release();
     const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= units8) return;
     const int64_t slot = t >> 12;                     // 128 rows x 32 eight-column chunks per tile
     const int64_t tile = tile0 + slot;                // split tiles start at tile0
     const int r = (int)((t >> 5) & 127), c8 = (int)(t & 31);
-    const int mt = (int)(tile % mtiles), nt = (int)(tile / mtiles);
+    int mt, nt;
+    tile_coords(tile, mtiles, ntiles, group_m, mt, nt);
     const int64_t m = (int64_t)mt * kBM + r, n = (int64_t)nt * kBN + c8 * 8;
     if (m >= M || n >= N) return;
     float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -350,6 +370,15 @@ prefill_splitk_reduce_kernel(const float* __restrict__ part, int64_t M, int64_t 
 }
 
 }  // namespace
+
+// Token tiles per group of the tile order: all of them (token-tile fastest over
+// the whole output) while the activations fit comfortably in L2, else 16, so
+// that 16 token tiles' activations stay in L2 while the weight tiles stream
+// past (the 27648-wide down projection at M = 8192: 226 MB of activations).
+static int prefill_group_m(int64_t M, int64_t K, int mtiles) {
+    constexpr int64_t kActInL2 = 48ll << 20;
+    return M * K <= kActInL2 ? mtiles : (mtiles < 16 ? mtiles : 16);
+}
 
 // Which tiles are split into K ranges, and into how many (split 1: none).
 //  - Fewer tiles than about one wave: every tile, so that about one wave of
@@ -431,9 +460,10 @@ cudaError_t launch_gemm_fp8_prefill(const uint8_t* Xq, const float* Xs, const ui
     uint32_t* err = device_error_word();
     if (!err) return cudaErrorInvalidValue;
     const int KB = (int)(K / 128);
+    const int mtiles = (int)((M + kBM - 1) / kBM);
     PrefillParams prm{err, Xs, Ws, Y, M, ldy, KB, (int)(N / 128),
-                      (int)((M + kBM - 1) / kBM), (int)((N + kBN - 1) / kBN), split, (KB + split - 1) / split,
-                      pl.full_tiles};
+                      mtiles, (int)((N + kBN - 1) / kBN), prefill_group_m(M, K, mtiles), split,
+                      (KB + split - 1) / split, pl.full_tiles};
     const int64_t split_tiles = tiles - pl.full_tiles;
     if (split > 1) {
         if (!make_tmap_f32_store(&tmP, ws, (uint64_t)(split_tiles * split * kBM), (uint64_t)kBN, (uint64_t)kBN, 32,
@@ -451,7 +481,8 @@ cudaError_t launch_gemm_fp8_prefill(const uint8_t* Xq, const float* Xs, const ui
     if (e != cudaSuccess || split == 1) return e;
     const int64_t units8 = split_tiles * kBM * 32;
     return launch_pdl(prefill_splitk_reduce_kernel, dim3((unsigned)((units8 + 255) / 256)), dim3(256), 0, st,
-                      (const float*)ws, M, N, prm.mtiles, split, pl.full_tiles, units8, Y, ldy);
+                      (const float*)ws, M, N, prm.mtiles, prm.ntiles, prm.group_m, split, pl.full_tiles, units8, Y,
+                      ldy);
 }
 
 // The dispatch below takes the prefill kernel for this shape (same rule).

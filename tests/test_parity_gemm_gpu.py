@@ -121,6 +121,21 @@ def test_fp8_gemm_prefill_tail_split_sampled(cuda_lib):
     assert_fp8_gemm_close(host(Y2)[rows], ref, "no split")
 
 
+@pytest.mark.parametrize("N", [768, 13824])
+def test_fp8_gemm_prefill_grouped_tile_order(cuda_lib, N):
+    # activations above 48 MB (2560 x 20480): the 128 x 256 tile kernel walks
+    # groups of 16 token tiles (here 16 + a last group of 4); N = 768 splits
+    # every tile in K (reduced by a second launch), N = 13824 splits none.
+    # One sampled row in every token tile, all columns.
+    M, K = 2560, 20480
+    Wq, Ws = oracle_fp8_weight(N, K, 77)
+    Xq, Xs = oracle_fp8_act(M, K, 78)
+    rows = _rows_in_distinct_tiles(M, 20, seed=N)
+    ref = oracle.fp8_gemm(Xq[rows], Xs[:, rows], Wq, Ws)
+    Y = fb.fp8rl_gemm_w8a8_block(dev(Xq), dev(Xs), dev(Wq), dev(Ws))
+    assert_fp8_gemm_close(host(Y)[rows], ref, f"grouped order N={N}")
+
+
 def test_fp8_gemm_tiny_config(cuda_lib):
     Wq, Ws = oracle_fp8_weight(synth.TINY.N, synth.TINY.K, synth.seed_for(1, 0))
     from parity_util import act_cpu
