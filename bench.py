@@ -71,8 +71,8 @@ NCU_TRAFFIC_PREFILL = {"kernel": "gemm_fp8_prefill_kernel", "source_sha1": "51a9
                        "bytes_per_step": (108063488 + 89519104) + (87500288 + 53253632) + (1324224256 + 878707712)
                        + (2229088000 + 78596096),
                        "profile": "profiles/prefill_gemm_qwen32b_m8192_four_shapes.md"}
-NCU_TRAFFIC_DECODE = {"kernel": "FP8 GEMM at a decode size", "source_sha1": "ce5f356c98b581a1d4b387caccdd6ce5962e51b8",
-                      "case": "o_proj_M256", "bytes_per_launch": 27609344 + 15736064,
+NCU_TRAFFIC_DECODE = {"kernel": "FP8 GEMM at a decode size", "source_sha1": "9415829969a1433108c3fb528fade227e06a2e75",
+                      "case": "o_proj_M256", "bytes_per_launch": 27614208 + 15736064,
                       "profile": "profiles/decode_gemm_qwen32b_o_proj_m256.md"}
 
 
