@@ -388,9 +388,24 @@ def time_headline(fb, args, dev, world, rank, model):
     req_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     aq_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     gemm_ms = [statistics.mean(e[2 + i].elapsed_time(e[3 + i]) for e in evs) for i in range(ns)]
+    step_ms = [e[0].elapsed_time(e[2 + ns]) for e in evs]
     assert fb.fp8rl_check_device_error() == 0
     return {"total_ms": total_ms, "req_ms": req_ms, "aq_ms": aq_ms, "gemm_ms": gemm_ms,
-            "clocks": clk.summary(), "launches_per_step": launches}
+            "step_ms_pct": step_percentiles(step_ms), "clocks": clk.summary(), "launches_per_step": launches}
+
+
+def step_percentiles(ms):
+    """p10 / median / p90 of per-step times (linear interpolation between order statistics)."""
+    xs = sorted(ms)
+    if not xs:
+        return None
+
+    def q(f):
+        pos = f * (len(xs) - 1)
+        lo = int(pos)
+        hi = min(lo + 1, len(xs) - 1)
+        return xs[lo] + (xs[hi] - xs[lo]) * (pos - lo)
+    return {"p10": q(0.1), "p50": q(0.5), "p90": q(0.9), "n": len(xs)}
 
 
 def time_e2e(fb, args, dev, model, chunk_layers=8):
@@ -1319,6 +1334,7 @@ def main():
             "breakdown": {"requant_ms": head["req_ms"], "act_quant_ms": head["aq_ms"],
                           "act_quant_gbs": parts["act_quant_bytes"] / (head["aq_ms"] * 1e-3) / 1e9,
                           "gemm_ms": dict(zip([s.name for s in synth.QWEN25_32B], head["gemm_ms"])),
+                          "step_ms_p10_p50_p90": head["step_ms_pct"],
                           "step_bytes": sb, "step_parts": parts,
                           "method": "CUDA events between the parts of every timed step, on the launching stream"},
             "decode_sweep_32b": dec,

@@ -249,18 +249,22 @@ int int8rl_quant_act_token(const uint16_t* X, int64_t M, int64_t K, int64_t ldx,
  * Xq [M][K] int8, Xs [M] fp32, Wq [N][K] int8, Ws [N] fp32, Y bf16 [M][ldy].
  * acc_or_null: optional int32 [M][N] copy of the accumulators (8-byte aligned).
  * workspace: device scratch, 16-byte aligned, of int8rl_gemm_workspace_bytes(M,
- * N, K) bytes: nonzero for batches of 256 tokens or more with enough 128 x 256
- * output tiles (or tiles x K ranges) for half of the GPU.  It receives fp16
- * copies of Xq and Wq ((M + N) * K * 2 bytes, exact), which the large-batch
- * kernel multiplies on the fp16 tensor path, and, when its tiles are too few
- * for the GPU, the int32 partial tiles of its K ranges (added exactly by a
- * second launch).  With less workspace (or NULL) the call still succeeds on
- * the small-batch kernel (slower for those shapes).  Not zeroed, nothing kept
- * between calls; two calls in flight at once need two workspaces.
+ * N, K) bytes; zero where the small-batch kernel runs (always for up to 64
+ * tokens), which needs none.
+ *   - 65 to 256 tokens, and up to 512 on layers of at least 2^27 weights: an
+ *     fp16 copy of Xq (M * K * 2 bytes, rounded up to 16, exact), loaded in
+ *     256-token tiles, and, when those tiles are too few for the GPU, the int32
+ *     partial tiles of the K ranges (added exactly by a second launch).
+ *   - Larger batches with enough 128 x 256 output tiles (or tiles x K ranges)
+ *     for half of the GPU: fp16 copies of Xq and Wq ((M + N) * K * 2 bytes),
+ *     and the int32 partial tiles of a K split.
+ * With less workspace (or NULL) the call still succeeds on the small-batch
+ * kernel (slower for those shapes).  Not zeroed, nothing kept between calls;
+ * two calls in flight at once need two workspaces.
  * ---------------------------------------------------------------------- */
 size_t int8rl_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 /* Kernels int8rl_gemm_w8a8 launches for this shape and workspace size: 1 on the
- * small-batch kernel; 2 or 3 on the large-batch path (conversion, GEMM, and the
+ * small-batch kernel; 2 or 3 on the other two paths (conversion, GEMM, and the
  * reduction of a K split).  0 for M == 0; -FP8RL_ERR_SHAPE for an invalid shape. */
 int int8rl_gemm_kernel_count(int64_t M, int64_t N, int64_t K, size_t workspace_bytes);
 int int8rl_gemm_w8a8(const int8_t* Xq, const float* Xs, const int8_t* Wq, const float* Ws,

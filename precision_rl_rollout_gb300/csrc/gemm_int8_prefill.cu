@@ -440,6 +440,15 @@ size_t int8_prefill_workspace_bytes(int64_t M, int64_t N, int64_t K) {
 // the reduction.
 int int8_prefill_kernel_count(int64_t M, int64_t N, int64_t K) { return i8p_plan(M, N, K).split > 1 ? 3 : 2; }
 
+// fp16 copy of n int8 codes (n % 16 == 0; both pointers 16-byte aligned).
+cudaError_t launch_int8_to_f16(const int8_t* src, int64_t n, uint16_t* dst, cudaStream_t st) {
+    const int64_t n16 = n / 16;
+    if (n16 == 0) return cudaSuccess;
+    const int64_t blocks = std::min<int64_t>((n16 + 255) / 256, (int64_t)num_sms() * 8);
+    return launch_pdl(int8_to_f16_kernel, dim3((unsigned)blocks), dim3(256), 0, st, src, n16,
+                      static_cast<const int8_t*>(nullptr), (int64_t)0, dst);
+}
+
 cudaError_t launch_gemm_int8_prefill(const int8_t* Xq, const float* Xs, const int8_t* Wq, const float* Ws,
                                      int64_t M, int64_t N, int64_t K, uint16_t* Y, int64_t ldy, int32_t* acc,
                                      void* ws, cudaStream_t st) {

@@ -430,22 +430,36 @@ cudaError_t launch_gemm_int8_tc(const int8_t* Xq, const float* Xs, const int8_t*
     return launch_i8_mt<64>(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, acc, st);
 }
 
-// Batches of 256 tokens or more with enough tiles to fill the GPU take the
-// large-batch path (fp16 copies in the workspace, 128 x 256 tiles); the rest,
-// and any call with less workspace than that path asks for, this kernel.
-size_t gemm_int8_workspace_bytes(int64_t M, int64_t N, int64_t K) { return int8_prefill_workspace_bytes(M, N, K); }
+// Dispatch (32B shapes measured at M = 64 .. 4096, graphs over weight copies):
+//  - up to 64 tokens: this kernel (64-token tiles at most, weights in TMEM);
+//  - 65 .. 256 tokens, and up to 512 on layers of at least 2^27 weights: the
+//    256-token kernel (an fp16 copy of X and, for a K split, int32 partials in
+//    the workspace);
+//  - larger batches with enough tiles: fp16 copies of X and W and the
+//    128 x 256 tile kernel;
+//  - anything else, or too little workspace for the chosen path: this kernel.
+static bool int8_t256_applies(int64_t M, int64_t N, int64_t K) {
+    return M > 64 && (M <= 256 || (M <= 512 && N * K >= (int64_t(1) << 27)));
+}
+size_t gemm_int8_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    if (int8_t256_applies(M, N, K)) return int8_t256_workspace_bytes(M, N, K);
+    return int8_prefill_workspace_bytes(M, N, K);
+}
 int gemm_int8_kernel_count(int64_t M, int64_t N, int64_t K, size_t ws_bytes) {
     if (M <= 0) return 0;
-    const size_t need = int8_prefill_workspace_bytes(M, N, K);
-    return need > 0 && ws_bytes >= need ? int8_prefill_kernel_count(M, N, K) : 1;
+    const size_t need = gemm_int8_workspace_bytes(M, N, K);
+    if (need == 0 || ws_bytes < need) return 1;
+    return int8_t256_applies(M, N, K) ? int8_t256_kernel_count(M, N, K) : int8_prefill_kernel_count(M, N, K);
 }
 cudaError_t launch_gemm_int8(const int8_t* Xq, const float* Xs, const int8_t* Wq,
                              const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
                              int64_t ldy, int32_t* acc, void* ws, size_t ws_bytes, cudaStream_t st) {
     if (M == 0) return cudaSuccess;
-    const size_t need = int8_prefill_workspace_bytes(M, N, K);
-    if (need > 0 && ws != nullptr && ws_bytes >= need)
+    const size_t need = gemm_int8_workspace_bytes(M, N, K);
+    if (need > 0 && ws != nullptr && ws_bytes >= need) {
+        if (int8_t256_applies(M, N, K)) return launch_gemm_int8_t256(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, acc, ws, st);
         return launch_gemm_int8_prefill(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, acc, ws, st);
+    }
     return launch_gemm_int8_tc(Xq, Xs, Wq, Ws, M, N, K, Y, ldy, acc, st);
 }
 

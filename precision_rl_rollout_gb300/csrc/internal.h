@@ -90,6 +90,15 @@ size_t int8_prefill_workspace_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_gemm_int8_prefill(const int8_t* Xq, const float* Xs, const int8_t* Wq, const float* Ws,
                                      int64_t M, int64_t N, int64_t K, uint16_t* Y, int64_t ldy, int32_t* acc,
                                      void* ws, cudaStream_t st);
+// fp16 copy of n int8 codes (exact), n % 16 == 0.
+cudaError_t launch_int8_to_f16(const int8_t* src, int64_t n, uint16_t* dst, cudaStream_t st);
+// Mid-size batches: weight blocks in TMEM, 256-token tiles of an fp16 copy of X
+// (in the workspace, with the int32 partials of a K split).
+size_t int8_t256_workspace_bytes(int64_t M, int64_t N, int64_t K);
+int int8_t256_kernel_count(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_gemm_int8_t256(const int8_t* Xq, const float* Xs, const int8_t* Wq, const float* Ws,
+                                  int64_t M, int64_t N, int64_t K, uint16_t* Y, int64_t ldy, int32_t* acc,
+                                  void* ws, cudaStream_t st);
 cudaError_t launch_gemm_int8(const int8_t* Xq, const float* Xs, const int8_t* Wq,
                              const float* Ws, int64_t M, int64_t N, int64_t K, uint16_t* Y,
                              int64_t ldy, int32_t* acc, void* ws, size_t ws_bytes,

@@ -154,16 +154,30 @@ def test_gemm_validation(lib):
     assert i(A, A, A, A, 0, 128, 128, A, 128, None, None, 0, None) == 0
 
 
-def test_int8_large_batch_workspace_holds_the_fp16_copies(lib):
-    # 256+ tokens with plenty of 128 x 256 tiles: fp16 copies of X and W and
+def test_int8_workspace_by_path(lib):
+    # 4096 tokens with plenty of 128 x 256 tiles: fp16 copies of X and W and
     # nothing else (no split); a batch of 32 tokens needs none
     M, N, K = 4096, 7168, 5120
     assert lib.int8rl_gemm_workspace_bytes(M, N, K) == (M + N) * K * 2
     assert lib.int8rl_gemm_workspace_bytes(32, N, K) == 0
-    # few tiles (M = 256 against N = 7168): the copies plus int32 partial tiles
-    need = lib.int8rl_gemm_workspace_bytes(256, N, K)
-    assert need > (256 + N) * K * 2
-    assert (need - (256 + N) * K * 2) % (128 * 256 * 4) == 0
+    assert lib.int8rl_gemm_workspace_bytes(64, N, K) == 0
+    # 65 .. 256 tokens (and up to 512 on layers of 2^27 weights or more): the
+    # 256-token kernel's fp16 copy of X, plus whole int32 partial tiles (256
+    # tokens x 128 weight rows) of the K ranges when it splits K
+    for M, N, K in [(65, 7168, 5120), (256, 7168, 5120), (256, 5120, 27648), (300, 55296, 5120),
+                    (512, 5120, 27648)]:
+        need = lib.int8rl_gemm_workspace_bytes(M, N, K)
+        x16 = -(-(M * K * 2) // 16) * 16
+        assert need >= x16 and (need - x16) % (256 * 128 * 4) == 0, (M, N, K, need)
+        tiles = -(-M // 256) * (N // 128)
+        assert (need - x16) // (256 * 128 * 4) in [s * tiles for s in (0, 2, 3, 4, 5, 6, 7, 8)]
+    # 300 tokens on a layer below 2^27 weights: the large-batch path, with the
+    # copies alone when its tiles fill the GPU, plus int32 partial tiles of
+    # 128 x 256 when they are few (N = 2688: 33 tiles)
+    assert lib.int8rl_gemm_workspace_bytes(300, 7168, 5120) == (300 + 7168) * 5120 * 2
+    need = lib.int8rl_gemm_workspace_bytes(300, 2688, 4096)
+    assert need > (300 + 2688) * 4096 * 2
+    assert (need - (300 + 2688) * 4096 * 2) % (128 * 256 * 4) == 0
 
 
 def test_fp8_gemm_workspace_is_whole_partial_tiles(lib):
@@ -187,6 +201,12 @@ def test_gemm_kernel_counts(lib):
     assert lib.int8rl_gemm_kernel_count(32, 7168, 5120, 0) == 1
     assert lib.int8rl_gemm_kernel_count(4096, 7168, 5120, lib.int8rl_gemm_workspace_bytes(4096, 7168, 5120)) == 2
     assert lib.int8rl_gemm_kernel_count(4096, 7168, 5120, 0) == 1
+    # the 256-token path: X conversion and GEMM, plus the reduction of a K split
+    for M, N, K in [(128, 7168, 5120), (256, 55296, 5120), (256, 5120, 27648)]:
+        ws = lib.int8rl_gemm_workspace_bytes(M, N, K)
+        split = (ws - M * K * 2) // (256 * 128 * 4 * (N // 128))
+        assert lib.int8rl_gemm_kernel_count(M, N, K, ws) == (3 if split > 1 else 2)
+        assert lib.int8rl_gemm_kernel_count(M, N, K, ws - 16) == 1     # too little: small-batch kernel
 
 
 def test_linear_kernel_counts(lib):

@@ -85,3 +85,11 @@ def test_clock_summary():
 def test_clock_csv_is_not_written_into_the_repository():
     c = bench.ClockSampler(0, 0)
     assert not os.path.abspath(c.path).startswith(ROOT + os.sep)
+
+
+def test_step_percentiles():
+    p = bench.step_percentiles([5.0, 1.0, 3.0, 2.0, 4.0])
+    assert p == {"p10": 1.4, "p50": 3.0, "p90": 4.6, "n": 5}
+    assert bench.step_percentiles([]) is None
+    one = bench.step_percentiles([7.0])
+    assert one["p10"] == one["p50"] == one["p90"] == 7.0

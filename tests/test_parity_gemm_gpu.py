@@ -278,6 +278,69 @@ def test_int8_gemm_large_batch_extreme_codes_exact(cuda_lib):
     assert np.array_equal(host(Y)[rows], want_y)
 
 
+@pytest.mark.parametrize("M,N,K", [(65, 384, 640), (129, 256, 1152), (200, 384, 2048), (256, 128, 128),
+                                   (256, 1280, 3840)])
+def test_int8_gemm_256_token_path(cuda_lib, M, N, K):
+    # 65 .. 256 tokens: weight blocks in TMEM against 256-token tiles of an fp16
+    # copy of X (in the workspace).  Few weight slabs split K: the int32
+    # partials of the ranges go to the workspace and a second launch adds them.
+    # K = 128 is one exact group of one block; K = 1152 ends on a group of one.
+    need = fb.int8rl_gemm_workspace_bytes(M, N, K)
+    assert need >= M * K * 2
+    assert fb.int8rl_gemm_kernel_count(M, N, K, need) in (2, 3)
+    _int8_case(M, N, K, 500 + N + K, 600 + M + K)
+
+
+def test_int8_gemm_256_token_path_splits_and_ragged_second_tile(cuda_lib):
+    # 300 tokens on a layer of 2^27 weights: two 256-token tiles, the second
+    # with 44 live rows; checked on rows of both tiles.  Seeded random codes
+    # and scales (the quantizer is not under test here).
+    M, N, K = 300, 16384, 8192
+    assert N * K >= 1 << 27 and fb.int8rl_gemm_workspace_bytes(M, N, K) >= M * K * 2
+    rng = np.random.default_rng(77)
+    Wq = rng.integers(-127, 128, size=(N, K), dtype=np.int8)
+    Xq = rng.integers(-127, 128, size=(M, K), dtype=np.int8)
+    Ws = (rng.random(N) * 1e-3 + 1e-5).astype(np.float32)
+    Xs = (rng.random(M) * 1e-2 + 1e-4).astype(np.float32)
+    Y, acc = fb.int8rl_gemm_w8a8(dev(Xq), dev(Xs), dev(Wq), dev(Ws), want_acc=True)
+    rows = np.array([0, 1, 130, 255, 256, 280, 299])
+    want_acc, want_y = oracle.int8_gemm(Xq[rows], Xs[rows], Wq, Ws)
+    assert np.array_equal(host(acc)[rows], want_acc), "acc differs"
+    assert np.array_equal(host(Y)[rows], want_y), "Y differs"
+
+
+def test_int8_gemm_256_token_path_extreme_codes_exact(cuda_lib):
+    # every code at +-127 over K = 8192 on the 256-token path with a K split
+    # (two weight slabs): each exact TMEM group of two K blocks reaches
+    # 256 * 127^2, the top of its range, and |acc| = 127^2 K
+    M, N, K = 200, 256, 8192
+    ws = fb.int8rl_gemm_workspace_bytes(M, N, K)
+    assert fb.int8rl_gemm_kernel_count(M, N, K, ws) == 3            # conversion, GEMM, split reduction
+    Xq = np.full((M, K), 127, np.int8)
+    Xq[1::2] = -127
+    Xq[2, ::2] = -127
+    Wq = np.full((N, K), 127, np.int8)
+    Wq[N // 2:] = -127
+    Xs = np.linspace(0.5, 3.0, M).astype(np.float32)
+    Ws = np.linspace(0.001, 2.0, N).astype(np.float32)
+    Y, acc = fb.int8rl_gemm_w8a8(dev(Xq), dev(Xs), dev(Wq), dev(Ws), want_acc=True)
+    want_acc, want_y = oracle.int8_gemm(Xq, Xs, Wq, Ws)
+    assert int(want_acc[0, 0]) == 127 * 127 * K and int(want_acc[1, 0]) == -127 * 127 * K
+    assert np.array_equal(host(acc), want_acc)
+    assert np.array_equal(host(Y), want_y)
+
+
+def test_int8_gemm_256_token_shape_without_workspace(cuda_lib):
+    # the same batch with too little workspace runs the small-batch kernel: also exact
+    M, N, K = 200, 384, 2048
+    Wq, Ws = oracle_int8_weight(N, K, 81)
+    Xq, Xs = oracle_int8_act(M, K, 82)
+    want_acc, want_y = oracle.int8_gemm(Xq, Xs, Wq, Ws)
+    Y, acc = fb.int8rl_gemm_w8a8(dev(Xq), dev(Xs), dev(Wq), dev(Ws), want_acc=True,
+                                 workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
+    assert np.array_equal(host(acc), want_acc) and np.array_equal(host(Y), want_y)
+
+
 @pytest.mark.parametrize("M", synth.INT8_M_SWEEP)
 @pytest.mark.parametrize("shape", synth.QWEN25_32B, ids=lambda s: s.name)
 def test_int8_gemm_qwen32b_sampled(cuda_lib, shape, M):
