@@ -1193,6 +1193,15 @@ def profile_case(fb, case, dev, reps=3):
         Q = (R.float() + 0.02 * torch.randn(DECODE_M, V, device=dev, generator=g)).to(torch.bfloat16)
         for _ in range(reps):
             fb.fp8rl_logits_kl(R, Q)
+    elif case == "int8_gate_up_m256":                 # A7 on the 256-token kernel
+        s = synth.QWEN25_32B[2]                          # gate_up 5120 -> 55296
+        W = synth.weight_bf16_direct(s.N, s.K, synth.seed_for(5, 0), device=dev)
+        Wq, Ws = fb.int8rl_quant_weight_channel(W)
+        del W
+        Xq, Xs = fb.int8rl_quant_act_token(synth.activation(256, s.K, synth.seed_for(5, 1), device=dev))
+        ws = torch.empty(max(16, fb.int8rl_gemm_workspace_bytes(256, s.N, s.K)), dtype=torch.uint8, device=dev)
+        for _ in range(reps):
+            fb.int8rl_gemm_w8a8(Xq, Xs, Wq, Ws, workspace=ws)
     elif case == "int8_m32":
         s = synth.QWEN25_32B[2]                          # gate_up 5120 -> 55296
         W = synth.weight_bf16_direct(s.N, s.K, synth.seed_for(5, 0), device=dev)
@@ -1294,7 +1303,7 @@ def main():
                     help="run one small case for ncu: requant | requant32b_layers<n> | prefill32b | "
                          "decode32b_<shape>_m<M> | decode | decode7b_m<M> | decode7b_qkv_m<M> | "
                          "decode7b_down_m<M> | decode32b_m<M> | prefill | prefill_down_m<M> | int8 | int8_m32 | "
-                         "int8_qkv_m<M> | kv | kv8192 | tis | moe | kl | act_quant_prefill")
+                         "int8_qkv_m<M> | int8_gate_up_m256 | kv | kv8192 | tis | moe | kl | act_quant_prefill")
     args = ap.parse_args()
     world, rank, local = dist_env()
     if args.impl == "reference":

@@ -11,9 +11,8 @@
 //   2. kv_scale_kernel: one CTA reduces the partials and writes the scale;
 //   3. kv_quant_kernel: every CTA reads the scale and encodes its slice.
 // Deterministic (no atomics, nothing to zero).  Above L2 size the tensor is
-// read twice, less the part of it still in L2 when the encode pass starts
-// (that pass walks the slices backwards); below L2 size the second read comes
-// from L2.
+// read twice (6.6 B of DRAM traffic per 3 algorithmic bytes); below it the
+// second read comes from L2.
 //
 // When every slice's CTA can be resident at once (tensors up to ~10 M values,
 // e.g. one step's keys or values), one cooperative launch does all three: each
@@ -95,15 +94,12 @@ kv_scale_kernel(const uint32_t* __restrict__ partial, int64_t P, float* __restri
     }
 }
 
-// The slices go in reverse order: after the amax pass the L2 holds the
-// tensor's last slices, so the first CTAs scheduled here read those from L2.
-// The codes are stored evict-first so that they do not push the rest out.
 __global__ void __launch_bounds__(kKvThreads)
 kv_quant_kernel(const uint16_t* __restrict__ X, int64_t total, int64_t cpr, int64_t ld,
                 const float* __restrict__ scale, uint8_t* __restrict__ Xq) {
     pdl_wait_then_release();
     const BlockDivisor d = make_divisor(*scale);
-    const int64_t base = (int64_t)(gridDim.x - 1 - blockIdx.x) * kKvChunksPerCta;
+    const int64_t base = (int64_t)blockIdx.x * kKvChunksPerCta;
     uint4 v[kKvChunksPerThread];
 #pragma unroll
     for (int i = 0; i < kKvChunksPerThread; ++i) {
@@ -114,8 +110,8 @@ kv_quant_kernel(const uint16_t* __restrict__ X, int64_t total, int64_t cpr, int6
     for (int i = 0; i < kKvChunksPerThread; ++i) {
         const int64_t c = base + i * kKvThreads + threadIdx.x;
         if (c < total)
-            __stcs(reinterpret_cast<uint2*>(Xq + c * 8),
-                   d.fast ? quant8_e4m3_t<true>(v[i], d) : quant8_e4m3_t<false>(v[i], d));
+            *reinterpret_cast<uint2*>(Xq + c * 8) = d.fast ? quant8_e4m3_t<true>(v[i], d)
+                                                           : quant8_e4m3_t<false>(v[i], d);
     }
 }
 
