@@ -9,18 +9,19 @@
 //     offset-binary identity fp16(0x6400 | (v ^ 0x80)) = 1152 + v followed by
 //     one packed fp16 subtraction of 1152 (exact: the result needs <= 8 bits);
 //   * each product is an integer below 2^14, exact in the fp32 accumulator;
-//   * a TMEM accumulator collects at most 4 K blocks (512 products per output,
-//     |sum| <= 512 * 127^2 < 2^23) so every partial sum is an integer well
+//   * a TMEM accumulator collects at most 2 K blocks (256 products per output,
+//     |sum| <= 256 * 127^2 < 2^22) so every partial sum is an integer well
 //     inside fp32's 24-bit significand and no rounding can occur; it is then
-//     converted to int32 (exact) and added in int32 registers.
+//     moved to 32-bit integer registers exactly (see the epilogue).
 // The bit-exact parity tests against the int64 CPU reference include the
 // extreme case of every code at +-127.
 //
 // Layout (swap-AB, as the FP8 decode kernel): the MMA's M side is 128 weight
 // rows, its N side a tile of MT tokens; each CTA streams one 128-row weight
-// slab.  Warp 0 issues TMA (raw int8 tiles, 128-byte swizzle), warp 1 the
-// MMAs, warps 2-9 (two groups, alternate K blocks) convert raw tiles to fp16,
-// warps 10-13 promote and hold the int32 accumulators.  The converted weight
+// slab.  Warp 0 issues TMA (raw int8 tiles, 128-byte swizzle), warps 1 and 14
+// the MMAs of alternate K blocks (each into its own accumulators), warps 2-9
+// (two groups, alternate K blocks) convert raw tiles to fp16, warps 10-13
+// promote and hold the integer accumulators.  The converted weight
 // block goes to tensor memory, where the MMA reads its A operand (one weight
 // row per TMEM lane, K packed along the columns); only the small token tile
 // is written back to shared memory (UMMA K-major 128-byte-swizzle layout, two
@@ -42,7 +43,7 @@ namespace {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint32_t kKernelInt8 = 3;
-constexpr int kGroupKb = 4;   // K blocks accumulated in TMEM before promotion (exactness bound)
+constexpr int kGroupKb = 4;   // K blocks per promotion group, two per MMA issuer (exactness bound)
 
 struct Int8Params {
     uint32_t* err;
@@ -59,14 +60,13 @@ struct Int8Params {
 template <int MT>
 struct I8Cfg {
     static_assert(MT == 16 || MT == 32 || MT == 64, "token tile");
-    static constexpr int kThreads = 448;                       // 14 warps
+    static constexpr int kThreads = 480;                       // 15 warps
     static constexpr int kRawW = 128 * 128, kRawX = MT * 128;  // int8 tiles
     static constexpr int kRawStage = kRawW + kRawX;
-    // TMEM: two accumulator buffers of MT columns at 0, then as many fp16
-    // weight blocks (128 lanes x 64 columns each) as the rest holds, from
-    // column kTmemA: the converters must not wait for the MMA to release a
-    // block (measured: four blocks in flight held the pace at ~0.55 us/block)
-    static constexpr int kTmemA = 2 * MT < 64 ? 64 : 2 * MT;
+    // TMEM: four accumulator buffers of MT columns at 0 (two MMA issuers x two
+    // alternating groups), then as many fp16 weight blocks (128 lanes x 64
+    // columns each) as the rest holds, from column kTmemA
+    static constexpr int kTmemA = 4 * MT < 64 ? 64 : 4 * MT;
     static constexpr int kTmemCols = 512;
     static constexpr int kCvtStages = (kTmemCols - kTmemA) / 64;   // fp16 weight blocks = token stages
     static constexpr int kCvtStage = 2 * MT * 128;                 // fp16 token tile: two 64-wide atoms
@@ -76,8 +76,9 @@ struct I8Cfg {
     static constexpr int kCvtOffset = kRawStages * kRawStage;
     static constexpr int kBarOffset = kCvtOffset + kCvtStages * kCvtStage;
     static constexpr int kSmemBytes = kBarOffset + 512 + 1024;
-    static_assert(2 * MT <= kTmemA && kTmemA + 64 * kCvtStages <= kTmemCols, "TMEM layout");
-    static_assert((2 * kRawStages + 2 * kCvtStages + 4) * 8 + 8 <= 512, "barrier area");
+    static_assert(4 * MT <= kTmemA && kTmemA + 64 * kCvtStages <= kTmemCols, "TMEM layout");
+    static_assert(kCvtStages >= kGroupKb, "a group's blocks must fit in TMEM at once");
+    static_assert((2 * kRawStages + 2 * kCvtStages + 6) * 8 + 8 <= 512, "barrier area");
     static constexpr int kChunk = MT >= 32 ? 32 : 16;
     static_assert(MT * 128 * 4 <= kRawStages * kRawStage, "reduction buffer must fit the raw stages");
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -125,13 +126,13 @@ gemm_int8_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
-    // raw_full[R], raw_empty[R], cvt_full[V], cvt_empty[V], tfull[2], tempty[2]
+    // raw_full[R], raw_empty[R], cvt_full[V], cvt_empty[V], tfull[4] (issuer x buffer), tempty[2]
     constexpr int R = C::kRawStages, V = C::kCvtStages;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * R + 2 * V + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * R + 2 * V + 6);
     volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const uint32_t rfull0 = smem_u32(bars), rempty0 = smem_u32(bars + R);
     const uint32_t cfull0 = smem_u32(bars + 2 * R), cempty0 = smem_u32(bars + 2 * R + V);
-    const uint32_t tfull0 = smem_u32(bars + 2 * R + 2 * V), tempty0 = smem_u32(bars + 2 * R + 2 * V + 2);
+    const uint32_t tfull0 = smem_u32(bars + 2 * R + 2 * V), tempty0 = smem_u32(bars + 2 * R + 2 * V + 4);
 
     const uint32_t warp = warp_id(), lane = lane_id();
     const int split_idx = blockIdx.x;
@@ -149,10 +150,8 @@ gemm_int8_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
             mbar_init(cfull0 + 8 * s, 4);
             mbar_init(cempty0 + 8 * s, 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(tfull0 + 8 * b, 1);
-            mbar_init(tempty0 + 8 * b, 4);           // the four epilogue warps
-        }
+        for (int b = 0; b < 4; ++b) mbar_init(tfull0 + 8 * b, 1);
+        for (int b = 0; b < 2; ++b) mbar_init(tempty0 + 8 * b, 4);   // the four epilogue warps
         *abort = 0;
         fence_mbar_init();
         prefetch_tmap(&tmW);
@@ -187,17 +186,23 @@ gemm_int8_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
                 for (int j = max(0, it - R); j < it; ++j)
                     mbar_drain(rfull0 + 8 * (j % R), (j / R) & 1, kWaitLimitNs);
         }
-    } else if (warp == 1) {
-        // ---------------- MMA issuer: 8 x (M=128, N=MT, K=16) fp16 MMAs per K block
+    } else if (warp == 1 || warp == 14) {
+        // ---------------- MMA issuers: 8 x (M=128, N=MT, K=16) fp16 MMAs per K
+        // block.  Two threads take alternate blocks, each into its own pair of
+        // accumulator buffers: a thread's barrier wait returns only after its
+        // own MMAs in flight have completed, so with one issuer every block
+        // drained the tensor pipe, while the other thread's MMAs keep it busy.
+        // Group g (blocks 4g .. 4g+3) gives each issuer two blocks.
         if (lane == 0) {
             constexpr uint32_t idesc = (1u << 4) | ((uint32_t)(MT >> 3) << 17) | ((128u >> 4) << 24);  // f16 x f16 -> f32
-            for (int it = 0; it < nkb; ++it) {
+            const int me = warp == 1 ? 0 : 1;
+            for (int it = me; it < nkb; it += 2) {
                 const int s = it % V;
                 const uint32_t ph = (it / V) & 1;
                 const int g = it / kGroupKb;
                 const uint32_t buf = g & 1, bph = (g >> 1) & 1;
-                const bool first = (it % kGroupKb) == 0;
-                const bool last = (it % kGroupKb) == kGroupKb - 1 || it == nkb - 1;
+                const bool first = it - g * kGroupKb < 2;                       // my first block of the group
+                const bool last = it + 2 >= min(nkb, (g + 1) * kGroupKb);       // my last block of the group
                 if (!mbar_wait_bounded(cfull0 + 8 * s, ph, abort, kWaitLimitNs)) {
                     record_timeout(p.err, 2, abort);
                     break;
@@ -208,7 +213,7 @@ gemm_int8_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
                 }
                 tc_fence_after();
                 const uint8_t* st = smem + C::kCvtOffset + s * C::kCvtStage;
-                const uint32_t d = tmem_base + buf * MT;
+                const uint32_t d = tmem_base + (2 * me + buf) * MT;
                 const uint32_t a = tmem_base + C::kTmemA + s * 64;     // weight block s: 64 columns
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {        // K = 16 fp16 = 8 TMEM columns / 32 bytes per step
@@ -216,7 +221,7 @@ gemm_int8_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
                     mma_f16_tmem_a(d, a + 8 * k, b, idesc, (first && k == 0) ? 0u : 1u);
                 }
                 tc_commit(cempty0 + 8 * s);
-                if (last) tc_commit(tfull0 + 8 * buf);
+                if (last) tc_commit(tfull0 + 8 * (2 * me + buf));
             }
         }
     } else if (warp < 10) {
@@ -267,28 +272,41 @@ gemm_int8_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
             }
         }
     } else {
-        // ---------------- epilogue: exact promotion into int32 registers
+        // ---------------- epilogue: exact promotion into integer registers.  Per
+        // group, each issuer's accumulator holds at most two blocks' products
+        // (256 per output, |sum| <= 256 * 127^2 < 2^22), so v + 1.5 * 2^23 is
+        // exact and its bits are 0x4B400000 + v: one add and one integer add per
+        // value; the offsets come off at the end (32-bit wrap-around).
         const int q = warp & 3;
         const int n_local = 32 * q + lane;
-        int32_t acc[MT];
+        uint32_t acc[MT];
 #pragma unroll
         for (int j = 0; j < MT; ++j) acc[j] = 0;
+        uint32_t reads = 0;
         for (int g = 0; g < ngroups; ++g) {
             const uint32_t buf = g & 1, bph = (g >> 1) & 1;
-            if (!mbar_wait_bounded(tfull0 + 8 * buf, bph, abort, kWaitLimitNs)) {
+            const int nblk = min(nkb - g * kGroupKb, kGroupKb);
+            const int nacc = nblk >= 2 ? 2 : 1;       // issuer 1 has no block in a one-block group
+            bool got = true;
+            for (int i = 0; i < nacc; ++i) got = got && mbar_wait_bounded(tfull0 + 8 * (2 * i + buf), bph, abort, kWaitLimitNs);
+            if (!got) {
                 record_timeout(p.err, 5, abort);
                 break;
             }
             tc_fence_after();
-            const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + buf * MT;
+            for (int i = 0; i < nacc; ++i) {
+                const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (2 * i + buf) * MT;
 #pragma unroll
-            for (int ch = 0; ch < MT / C::kChunk; ++ch) {
-                uint32_t r[C::kChunk];
-                if constexpr (C::kChunk == 32) tmem_ld_32x32b_x32(taddr + ch * 32, r);
-                else tmem_ld_32x32b_x16(taddr + ch * 16, r);
-                tmem_wait_ld();
+                for (int ch = 0; ch < MT / C::kChunk; ++ch) {
+                    uint32_t r[C::kChunk];
+                    if constexpr (C::kChunk == 32) tmem_ld_32x32b_x32(taddr + ch * 32, r);
+                    else tmem_ld_32x32b_x16(taddr + ch * 16, r);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < C::kChunk; ++j) acc[ch * C::kChunk + j] += __float2int_rn(__uint_as_float(r[j]));
+                    for (int j = 0; j < C::kChunk; ++j)
+                        acc[ch * C::kChunk + j] += __float_as_uint(__fadd_rn(__uint_as_float(r[j]), 12582912.0f));
+                }
+                ++reads;
             }
             tc_fence_before();
             __syncwarp();
@@ -296,8 +314,9 @@ gemm_int8_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
         }
         // every MMA has completed: the raw stages hold the transposed partial tile
         int32_t* red = reinterpret_cast<int32_t*>(smem);
+        const uint32_t bias = reads * 0x4B400000u;
 #pragma unroll
-        for (int j = 0; j < MT; ++j) red[j * 128 + n_local] = acc[j];
+        for (int j = 0; j < MT; ++j) red[j * 128 + n_local] = (int32_t)(acc[j] - bias);
     }
 
     // ---------------- split-K reduction over the cluster (int32: exact), epilogue stores
