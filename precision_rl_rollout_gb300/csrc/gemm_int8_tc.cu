@@ -55,6 +55,8 @@ struct Int8Params {
     int KB;
     int kb_per_split;
     int split;
+    int mtiles;        // token tiles
+    int items;         // split == 1: (token tile, slab) work items, taken by CTAs in turn
 };
 
 template <int MT>
@@ -74,13 +76,13 @@ struct I8Cfg {
     // SM keep the HBM stream going
     static constexpr int kRawStages = MT == 16 ? 10 : MT == 32 ? 8 : 5;
     static constexpr int kCvtOffset = kRawStages * kRawStage;
-    static constexpr int kBarOffset = kCvtOffset + kCvtStages * kCvtStage;
+    static constexpr int kRedOffset = kCvtOffset + kCvtStages * kCvtStage;   // int32 tile red[MT][128]
+    static constexpr int kBarOffset = kRedOffset + MT * 128 * 4;
     static constexpr int kSmemBytes = kBarOffset + 512 + 1024;
     static_assert(4 * MT <= kTmemA && kTmemA + 64 * kCvtStages <= kTmemCols, "TMEM layout");
     static_assert(kCvtStages >= kGroupKb, "a group's blocks must fit in TMEM at once");
     static_assert((2 * kRawStages + 2 * kCvtStages + 6) * 8 + 8 <= 512, "barrier area");
     static constexpr int kChunk = MT >= 32 ? 32 : 16;
-    static_assert(MT * 128 * 4 <= kRawStages * kRawStage, "reduction buffer must fit the raw stages");
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
@@ -118,6 +120,47 @@ __device__ __forceinline__ void convert_chunk(const uint8_t* raw, uint8_t* cvt, 
     *reinterpret_cast<uint4*>(dst + (((j + 1) ^ sw) << 4)) = o1;
 }
 
+// One verdict for the threads of a named barrier: true if any of them passes true.
+__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n.reg .pred p, q;\n"
+        "setp.ne.u32 p, %1, 0;\n"
+        "bar.red.or.pred q, %2, %3, p;\n"
+        "selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+// Y[m][n0 .. n0+7] = bf16((float(acc) * Xs[m]) * Ws[n]) and the accumulators if asked.
+__device__ __forceinline__ void store_out8(const Int8Params& p, int64_t mg, int64_t n0, const int32_t (&s)[8]) {
+    const float xs = p.Xs[mg];
+    float y[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) y[e] = __fmul_rn(__fmul_rn(__int2float_rn(s[e]), xs), p.Ws[n0 + e]);
+    uint4 o;
+    o.x = pack_bf16x2(y[0], y[1]);
+    o.y = pack_bf16x2(y[2], y[3]);
+    o.z = pack_bf16x2(y[4], y[5]);
+    o.w = pack_bf16x2(y[6], y[7]);
+    *reinterpret_cast<uint4*>(p.Y + mg * p.ldy + n0) = o;
+    if (p.acc) {                                 // 8-byte stores: the ABI guarantees 8-byte alignment
+        int2* a2 = reinterpret_cast<int2*>(p.acc + mg * p.N + n0);
+        a2[0] = make_int2(s[0], s[1]);
+        a2[1] = make_int2(s[2], s[3]);
+        a2[2] = make_int2(s[4], s[5]);
+        a2[3] = make_int2(s[6], s[7]);
+    }
+}
+
+// Two modes.  Split K (p.split > 1): CTA (split rank, token tile, slab) in a
+// cluster of the split CTAs, which add their int32 tiles through distributed
+// shared memory.  No split: a persistent grid; CTA c takes the work items
+// (token tile, slab) c, c + gridDim.x, ... with every pipeline counter running
+// on across items, so the next item's loads and MMAs overlap this item's
+// promotion and stores (done by the epilogue warps alone).
 template <int MT>
 __global__ void __launch_bounds__(I8Cfg<MT>::kThreads, 1)
 gemm_int8_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
@@ -133,13 +176,18 @@ gemm_int8_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
     const uint32_t rfull0 = smem_u32(bars), rempty0 = smem_u32(bars + R);
     const uint32_t cfull0 = smem_u32(bars + 2 * R), cempty0 = smem_u32(bars + 2 * R + V);
     const uint32_t tfull0 = smem_u32(bars + 2 * R + 2 * V), tempty0 = smem_u32(bars + 2 * R + 2 * V + 4);
+    int32_t* red = reinterpret_cast<int32_t*>(smem + C::kRedOffset);
 
     const uint32_t warp = warp_id(), lane = lane_id();
-    const int split_idx = blockIdx.x;
-    const int mt = blockIdx.y, nt = blockIdx.z;
+    const bool persist = p.split == 1;
+    const int split_idx = persist ? 0 : (int)blockIdx.x;
+    const int w_begin = persist ? (int)blockIdx.x : 0, w_end = persist ? p.items : 1;
+    const int w_step = persist ? (int)gridDim.x : 1;
     const int kb0 = split_idx * p.kb_per_split;
     const int nkb = min(p.KB, kb0 + p.kb_per_split) - kb0;
     const int ngroups = (nkb + kGroupKb - 1) / kGroupKb;
+#define ITEM_MT(w) (persist ? (w) % p.mtiles : (int)blockIdx.y)
+#define ITEM_NT(w) (persist ? (w) / p.mtiles : (int)blockIdx.z)
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < R; ++s) {
@@ -169,21 +217,26 @@ gemm_int8_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
         // ---------------- TMA producer: raw int8 tiles
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
-            int it = 0;
-            for (; it < nkb; ++it) {
-                const int s = it % R;
-                const uint32_t ph = (it / R) & 1;
-                if (!mbar_wait_bounded(rempty0 + 8 * s, ph ^ 1, abort, kWaitLimitNs)) {
-                    record_timeout(p.err, 1, abort);
-                    break;
+            int b = 0;                                   // blocks issued, over all items
+            bool ok = true;
+            for (int w = w_begin; ok && w < w_end; w += w_step) {
+                const int mt = ITEM_MT(w), nt = ITEM_NT(w);
+                for (int it = 0; it < nkb; ++it, ++b) {
+                    const int s = b % R;
+                    const uint32_t ph = (b / R) & 1;
+                    if (!mbar_wait_bounded(rempty0 + 8 * s, ph ^ 1, abort, kWaitLimitNs)) {
+                        record_timeout(p.err, 1, abort);
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = smem + s * C::kRawStage;
+                    mbar_arrive_expect_tx(rfull0 + 8 * s, C::kRawStage);
+                    tma_load_2d(smem_u32(st), &tmW, rfull0 + 8 * s, (kb0 + it) * 128, nt * 128, pol_w);
+                    tma_load_2d(smem_u32(st + C::kRawW), &tmX, rfull0 + 8 * s, (kb0 + it) * 128, mt * MT, pol_x);
                 }
-                uint8_t* st = smem + s * C::kRawStage;
-                mbar_arrive_expect_tx(rfull0 + 8 * s, C::kRawStage);
-                tma_load_2d(smem_u32(st), &tmW, rfull0 + 8 * s, (kb0 + it) * 128, nt * 128, pol_w);
-                tma_load_2d(smem_u32(st + C::kRawW), &tmX, rfull0 + 8 * s, (kb0 + it) * 128, mt * MT, pol_x);
             }
             if (*abort)   // let copies already in flight land before the CTA can exit
-                for (int j = max(0, it - R); j < it; ++j)
+                for (int j = max(0, b - R); j < b; ++j)
                     mbar_drain(rfull0 + 8 * (j % R), (j / R) & 1, kWaitLimitNs);
         }
     } else if (warp == 1 || warp == 14) {
@@ -192,53 +245,76 @@ gemm_int8_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
         // accumulator buffers: a thread's barrier wait returns only after its
         // own MMAs in flight have completed, so with one issuer every block
         // drained the tensor pipe, while the other thread's MMAs keep it busy.
-        // Group g (blocks 4g .. 4g+3) gives each issuer two blocks.
+        // Group g (blocks 4g .. 4g+3 of an item) gives each issuer two blocks.
         if (lane == 0) {
             constexpr uint32_t idesc = (1u << 4) | ((uint32_t)(MT >> 3) << 17) | ((128u >> 4) << 24);  // f16 x f16 -> f32
             const int me = warp == 1 ? 0 : 1;
-            for (int it = me; it < nkb; it += 2) {
-                const int s = it % V;
-                const uint32_t ph = (it / V) & 1;
-                const int g = it / kGroupKb;
-                const uint32_t buf = g & 1, bph = (g >> 1) & 1;
-                const bool first = it - g * kGroupKb < 2;                       // my first block of the group
-                const bool last = it + 2 >= min(nkb, (g + 1) * kGroupKb);       // my last block of the group
-                if (!mbar_wait_bounded(cfull0 + 8 * s, ph, abort, kWaitLimitNs)) {
-                    record_timeout(p.err, 2, abort);
-                    break;
-                }
-                if (first && !mbar_wait_bounded(tempty0 + 8 * buf, bph ^ 1, abort, kWaitLimitNs)) {
-                    record_timeout(p.err, 3, abort);
-                    break;
-                }
-                tc_fence_after();
-                const uint8_t* st = smem + C::kCvtOffset + s * C::kCvtStage;
-                const uint32_t d = tmem_base + (2 * me + buf) * MT;
-                const uint32_t a = tmem_base + C::kTmemA + s * 64;     // weight block s: 64 columns
+            int b0 = 0, G0 = 0;                          // blocks and groups of earlier items
+            bool ok = true;
+            for (int w = w_begin; ok && w < w_end; w += w_step) {
+                for (int g = 0; ok && g < ngroups; ++g) {
+                    const int G = G0 + g;
+                    const uint32_t buf = G & 1, bph = (G >> 1) & 1;
+                    const int g_beg = g * kGroupKb, g_end = min(nkb, g_beg + kGroupKb);
+                    if (g_beg + me >= g_end) {
+                        // issuer 1 in a one-block group: no MMAs, but its barrier
+                        // phases stay in step with the epilogue's
+                        if (!mbar_wait_bounded(tempty0 + 8 * buf, bph ^ 1, abort, kWaitLimitNs)) {
+                            record_timeout(p.err, 3, abort);
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive(tfull0 + 8 * (2 * me + buf));
+                        continue;
+                    }
+                    for (int it = g_beg + me; it < g_end; it += 2) {
+                        const bool first = it == g_beg + me, last = it + 2 >= g_end;
+                        const int bb = b0 + it, s = bb % V;
+                        const uint32_t ph = (bb / V) & 1;
+                        if (!mbar_wait_bounded(cfull0 + 8 * s, ph, abort, kWaitLimitNs)) {
+                            record_timeout(p.err, 2, abort);
+                            ok = false;
+                            break;
+                        }
+                        if (first && !mbar_wait_bounded(tempty0 + 8 * buf, bph ^ 1, abort, kWaitLimitNs)) {
+                            record_timeout(p.err, 3, abort);
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint8_t* st = smem + C::kCvtOffset + s * C::kCvtStage;
+                        const uint32_t d = tmem_base + (2 * me + buf) * MT;
+                        const uint32_t a = tmem_base + C::kTmemA + s * 64;     // weight block s: 64 columns
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {        // K = 16 fp16 = 8 TMEM columns / 32 bytes per step
-                    const uint64_t b = umma_desc_k128_sw128(smem_u32(st + (k >> 2) * (MT * 128))) + 2 * (k & 3);
-                    mma_f16_tmem_a(d, a + 8 * k, b, idesc, (first && k == 0) ? 0u : 1u);
+                        for (int k = 0; k < 8; ++k) {    // K = 16 fp16 = 8 TMEM columns / 32 bytes per step
+                            const uint64_t bd = umma_desc_k128_sw128(smem_u32(st + (k >> 2) * (MT * 128))) + 2 * (k & 3);
+                            mma_f16_tmem_a(d, a + 8 * k, bd, idesc, (first && k == 0) ? 0u : 1u);
+                        }
+                        tc_commit(cempty0 + 8 * s);
+                        if (last) tc_commit(tfull0 + 8 * (2 * me + buf));
+                    }
                 }
-                tc_commit(cempty0 + 8 * s);
-                if (last) tc_commit(tfull0 + 8 * (2 * me + buf));
+                b0 += nkb;
+                G0 += ngroups;
             }
         }
     } else if (warp < 10) {
         // ---------------- converters: raw int8 -> fp16.  Two groups of four
-        // warps take alternate K blocks (block it goes to TMEM weight block and
-        // token stage it % V), so two blocks are converted concurrently.  A
-        // warp may write only its own quarter of the TMEM lanes, so its thread
+        // warps take alternate blocks (block b goes to TMEM weight block and
+        // token stage b % V), so two blocks are converted concurrently.  A warp
+        // may write only its own quarter of the TMEM lanes, so its thread
         // converts weight row 32 * (warp % 4) + lane.
         const int grp = (warp - 2) >> 2;
         const int t = (int)(warp & 3) * 32 + lane;  // 0..127
         const uint32_t lane_addr = tmem_base + ((uint32_t)(32 * (warp & 3)) << 16) + C::kTmemA;
-        for (int it = grp; it < nkb; it += 2) {
-            const int rs = it % R, cs = it % V;
-            const uint32_t rph = (it / R) & 1, cph = (it / V) & 1;
-            if (!mbar_wait_bounded(rfull0 + 8 * rs, rph, abort, kWaitLimitNs) ||
-                !mbar_wait_bounded(cempty0 + 8 * cs, cph ^ 1, abort, kWaitLimitNs)) {
-                record_timeout(p.err, 4, abort);
+        const int nblocks = nkb * ((w_end - w_begin + w_step - 1) / w_step);
+        for (int b = grp; b < nblocks; b += 2) {
+            const int rs = b % R, cs = b % V;
+            const uint32_t rph = (b / R) & 1, cph = (b / V) & 1;
+            const bool got = mbar_wait_bounded(rfull0 + 8 * rs, rph, abort, kWaitLimitNs) &&
+                             mbar_wait_bounded(cempty0 + 8 * cs, cph ^ 1, abort, kWaitLimitNs);
+            if (!__all_sync(0xffffffffu, got)) {
+                if (lane == 0) record_timeout(p.err, 4, abort);
                 break;
             }
             const uint8_t* raw = smem + rs * C::kRawStage;
@@ -276,104 +352,111 @@ gemm_int8_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_consta
         // group, each issuer's accumulator holds at most two blocks' products
         // (256 per output, |sum| <= 256 * 127^2 < 2^22), so v + 1.5 * 2^23 is
         // exact and its bits are 0x4B400000 + v: one add and one integer add per
-        // value; the offsets come off at the end (32-bit wrap-around).
+        // value; the offsets come off at the end of the item (32-bit wrap-around).
         const int q = warp & 3;
         const int n_local = 32 * q + lane;
-        uint32_t acc[MT];
+        const int et = (int)threadIdx.x - 320;      // 0..127 over the four epilogue warps
+        int G0 = 0;
+        for (int w = w_begin; w < w_end; w += w_step) {
+            const int mt = ITEM_MT(w), nt = ITEM_NT(w);
+            uint32_t acc[MT];
 #pragma unroll
-        for (int j = 0; j < MT; ++j) acc[j] = 0;
-        uint32_t reads = 0;
-        for (int g = 0; g < ngroups; ++g) {
-            const uint32_t buf = g & 1, bph = (g >> 1) & 1;
-            const int nblk = min(nkb - g * kGroupKb, kGroupKb);
-            const int nacc = nblk >= 2 ? 2 : 1;       // issuer 1 has no block in a one-block group
-            bool got = true;
-            for (int i = 0; i < nacc; ++i) got = got && mbar_wait_bounded(tfull0 + 8 * (2 * i + buf), bph, abort, kWaitLimitNs);
-            if (!got) {
-                record_timeout(p.err, 5, abort);
-                break;
-            }
-            tc_fence_after();
-            for (int i = 0; i < nacc; ++i) {
-                const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (2 * i + buf) * MT;
-#pragma unroll
-                for (int ch = 0; ch < MT / C::kChunk; ++ch) {
-                    uint32_t r[C::kChunk];
-                    if constexpr (C::kChunk == 32) tmem_ld_32x32b_x32(taddr + ch * 32, r);
-                    else tmem_ld_32x32b_x16(taddr + ch * 16, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < C::kChunk; ++j)
-                        acc[ch * C::kChunk + j] += __float_as_uint(__fadd_rn(__uint_as_float(r[j]), 12582912.0f));
+            for (int j = 0; j < MT; ++j) acc[j] = 0;
+            uint32_t reads = 0;
+            bool ok = true;
+            for (int g = 0; g < ngroups; ++g) {
+                const int G = G0 + g;
+                const uint32_t buf = G & 1, bph = (G >> 1) & 1;
+                const int nblk = min(nkb - g * kGroupKb, kGroupKb);
+                // both issuers arrive once per group (issuer 1 without MMAs in a one-block group)
+                const bool got = mbar_wait_bounded(tfull0 + 8 * buf, bph, abort, kWaitLimitNs) &&
+                                 mbar_wait_bounded(tfull0 + 8 * (2 + buf), bph, abort, kWaitLimitNs);
+                if (!__all_sync(0xffffffffu, got)) {
+                    if (lane == 0) record_timeout(p.err, 5, abort);
+                    ok = false;
+                    break;
                 }
-                ++reads;
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
-        }
-        // every MMA has completed: the raw stages hold the transposed partial tile
-        int32_t* red = reinterpret_cast<int32_t*>(smem);
-        const uint32_t bias = reads * 0x4B400000u;
+                tc_fence_after();
+                const int nacc = nblk >= 2 ? 2 : 1;
+                for (int i = 0; i < nacc; ++i) {
+                    const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (2 * i + buf) * MT;
 #pragma unroll
-        for (int j = 0; j < MT; ++j) red[j * 128 + n_local] = (int32_t)(acc[j] - bias);
+                    for (int ch = 0; ch < MT / C::kChunk; ++ch) {
+                        uint32_t r[C::kChunk];
+                        if constexpr (C::kChunk == 32) tmem_ld_32x32b_x32(taddr + ch * 32, r);
+                        else tmem_ld_32x32b_x16(taddr + ch * 16, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < C::kChunk; ++j)
+                            acc[ch * C::kChunk + j] += __float_as_uint(__fadd_rn(__uint_as_float(r[j]), 12582912.0f));
+                    }
+                    ++reads;
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
+            }
+            G0 += ngroups;
+            if (ok) {
+                const uint32_t bias = reads * 0x4B400000u;
+#pragma unroll
+                for (int j = 0; j < MT; ++j) red[j * 128 + n_local] = (int32_t)(acc[j] - bias);
+            }
+            if (!persist) break;                         // split K: the whole CTA adds and stores below
+            // persistent: the four epilogue warps store this item's tile while
+            // the other warps go on with the next item
+            named_bar_sync(1, 128);
+            if (ok && !*abort) {
+                const int64_t m_tile0 = (int64_t)mt * MT;
+                const int valid_m = (int)(p.M - m_tile0 < MT ? p.M - m_tile0 : MT);
+                for (int c = et; c < valid_m * 16; c += 128) {
+                    const int m = c >> 4, n8 = c & 15;
+                    const int4 u0 = *reinterpret_cast<const int4*>(red + m * 128 + n8 * 8);
+                    const int4 u1 = *reinterpret_cast<const int4*>(red + m * 128 + n8 * 8 + 4);
+                    const int32_t v[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+                    store_out8(p, m_tile0 + m, (int64_t)nt * 128 + n8 * 8, v);
+                }
+            }
+            // red is free again, and every epilogue thread takes the same decision
+            if (bar_red_or(1, 128, !ok || *abort)) break;
+        }
     }
+#undef ITEM_MT
+#undef ITEM_NT
 
-    // ---------------- split-K reduction over the cluster (int32: exact), epilogue stores
-    // (warps 0 and 1 ran their loops on lane 0 alone: reconverged before the
+    // ---------------- split K: reduction over the cluster (int32: exact) and stores
+    // (warps 0, 1 and 14 ran their loops on lane 0 alone: reconverged before the
     // .aligned barriers, which every lane of a warp must execute together)
     __syncwarp();
     tc_fence_before();
-    if (p.split > 1) cluster_sync_all(); else __syncthreads();
-    {
+    if (!persist) {
+        cluster_sync_all();
+        const int mt = blockIdx.y, nt = blockIdx.z;
         const int64_t m_tile0 = (int64_t)mt * MT;
         const int valid_m = (int)(p.M - m_tile0 < MT ? p.M - m_tile0 : MT);
         const int total = valid_m * 16;
         const int per = (total + p.split - 1) / p.split;
         const int begin = split_idx * per, end = min(total, begin + per);
-        const uint32_t red_addr = smem_u32(smem);
-        for (int c = begin + (int)threadIdx.x; c < end; c += C::kThreads) {
+        const uint32_t red_addr = smem_u32(red);
+        for (int c = begin + (int)threadIdx.x; c < end && !*abort; c += C::kThreads) {
             const int m = c >> 4, n8 = c & 15;
             const uint32_t off = (uint32_t)(m * 128 + n8 * 8) * 4u;
-            int32_t s[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            int32_t sum[8] = {0, 0, 0, 0, 0, 0, 0, 0};
             for (int rk = 0; rk < p.split; ++rk) {
-                float4 v0, v1;
-                if (p.split > 1) {
-                    const uint32_t a = map_to_rank(red_addr + off, (uint32_t)rk);
-                    v0 = ld_cluster_v4(a);
-                    v1 = ld_cluster_v4(a + 16);
-                } else {
-                    const float4* l = reinterpret_cast<const float4*>(smem + off);
-                    v0 = l[0];
-                    v1 = l[1];
-                }
-                s[0] += __float_as_int(v0.x); s[1] += __float_as_int(v0.y);
-                s[2] += __float_as_int(v0.z); s[3] += __float_as_int(v0.w);
-                s[4] += __float_as_int(v1.x); s[5] += __float_as_int(v1.y);
-                s[6] += __float_as_int(v1.z); s[7] += __float_as_int(v1.w);
+                const uint32_t a = map_to_rank(red_addr + off, (uint32_t)rk);
+                const float4 v0 = ld_cluster_v4(a), v1 = ld_cluster_v4(a + 16);
+                sum[0] += __float_as_int(v0.x); sum[1] += __float_as_int(v0.y);
+                sum[2] += __float_as_int(v0.z); sum[3] += __float_as_int(v0.w);
+                sum[4] += __float_as_int(v1.x); sum[5] += __float_as_int(v1.y);
+                sum[6] += __float_as_int(v1.z); sum[7] += __float_as_int(v1.w);
             }
-            const int64_t mg = m_tile0 + m, n0 = (int64_t)nt * 128 + n8 * 8;
-            const float xs = p.Xs[mg];
-            float y[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) y[e] = __fmul_rn(__fmul_rn(__int2float_rn(s[e]), xs), p.Ws[n0 + e]);
-            uint4 o;
-            o.x = pack_bf16x2(y[0], y[1]);
-            o.y = pack_bf16x2(y[2], y[3]);
-            o.z = pack_bf16x2(y[4], y[5]);
-            o.w = pack_bf16x2(y[6], y[7]);
-            *reinterpret_cast<uint4*>(p.Y + mg * p.ldy + n0) = o;
-            if (p.acc) {                             // 8-byte stores: the ABI guarantees 8-byte alignment
-                int2* a2 = reinterpret_cast<int2*>(p.acc + mg * p.N + n0);
-                a2[0] = make_int2(s[0], s[1]);
-                a2[1] = make_int2(s[2], s[3]);
-                a2[2] = make_int2(s[4], s[5]);
-                a2[3] = make_int2(s[6], s[7]);
-            }
+            store_out8(p, m_tile0 + m, (int64_t)nt * 128 + n8 * 8, sum);
         }
+        __syncwarp();
+        cluster_sync_all();
+    } else {
+        __syncthreads();
     }
-    __syncwarp();
-    if (p.split > 1) cluster_sync_all(); else __syncthreads();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, C::kTmemCols);
@@ -412,7 +495,9 @@ cudaError_t launch_i8_mt(const int8_t* Xq, const float* Xs, const int8_t* Wq, co
     const int per = (KB + split - 1) / split;
     uint32_t* err = device_error_word();
     if (!err) return cudaErrorInvalidValue;
-    Int8Params prm{err, Xs, Ws, Y, acc, M, N, ldy, KB, per, split};
+    const int64_t items = mtiles * (N / 128);
+    if (items > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    Int8Params prm{err, Xs, Ws, Y, acc, M, N, ldy, KB, per, split, (int)mtiles, (int)items};
     auto kern = gemm_int8_tc_kernel<MT>;
     static bool attr_set[64] = {};     // the attribute belongs to the device
     int dev = 0;
@@ -423,7 +508,9 @@ cudaError_t launch_i8_mt(const int8_t* Xq, const float* Xs, const int8_t* Wq, co
         attr_set[dev] = true;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)split, (unsigned)mtiles, (unsigned)(N / 128));
+    // no split: a persistent grid of at most one CTA per SM over the work items
+    cfg.gridDim = split > 1 ? dim3((unsigned)split, (unsigned)mtiles, (unsigned)(N / 128))
+                            : dim3((unsigned)(items < num_sms() ? items : num_sms()));
     cfg.blockDim = dim3(C::kThreads);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = st;
