@@ -291,6 +291,24 @@ def test_int8_gemm_256_token_path(cuda_lib, M, N, K):
     _int8_case(M, N, K, 500 + N + K, 600 + M + K)
 
 
+@pytest.mark.parametrize("K", [640, 1152])
+def test_int8_small_batch_persistent_many_items(cuda_lib, K):
+    # the small-batch kernel without a workspace: 200 tokens are four 64-token
+    # tiles, 19456 rows 152 slabs, so 608 work items over a persistent grid of
+    # one CTA per SM (four each, token tile fastest).  K = 640 is 5 blocks: a
+    # last promotion group of one block, where the second MMA issuer has no
+    # block and only keeps its barrier phases in step, item after item.
+    M, N = 200, 19456
+    Wq, Ws = oracle_int8_weight(N, K, 71 + K)
+    Xq, Xs = oracle_int8_act(M, K, 72 + K)
+    Y, acc = fb.int8rl_gemm_w8a8(dev(Xq), dev(Xs), dev(Wq), dev(Ws), want_acc=True,
+                                 workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
+    rows = np.array([0, 63, 64, 127, 130, 191, 192, 199])
+    want_acc, want_y = oracle.int8_gemm(Xq[rows], Xs[rows], Wq, Ws)
+    assert np.array_equal(host(acc)[rows], want_acc), f"acc differs at {np.argwhere(host(acc)[rows] != want_acc)[:4].tolist()}"
+    assert np.array_equal(host(Y)[rows], want_y), f"Y differs at {np.argwhere(host(Y)[rows] != want_y)[:4].tolist()}"
+
+
 def test_int8_gemm_256_token_path_splits_and_ragged_second_tile(cuda_lib):
     # 300 tokens on a layer of 2^27 weights: two 256-token tiles, the second
     # with 44 live rows; checked on rows of both tiles.  Seeded random codes
