@@ -1172,8 +1172,9 @@ def profile_case(fb, case, dev, reps=3):
         Xq, Xs = fb.fp8rl_quant_act_group(synth.activation(M, s.K, synth.seed_for(3, 1), device=dev))
         for _ in range(reps):
             fb.fp8rl_gemm_w8a8_block(Xq, Xs, Wq, Ws)
-    elif case == "moe":
-        E, N, K = 128, 1536, 2048                         # MoE gate_up, top-8 of 64 tokens
+    elif case in ("moe", "moe_down"):
+        E = 128                                          # top-8 of 64 tokens
+        N, K = (1536, 2048) if case == "moe" else (2048, 768)   # gate_up / down
         rng = torch.Generator().manual_seed(synth.seed_for(8, 0))
         picks = torch.stack([torch.randperm(E, generator=rng)[:8] for _ in range(DECODE_M)])
         counts = torch.bincount(picks.flatten(), minlength=E)
@@ -1303,7 +1304,7 @@ def main():
                     help="run one small case for ncu: requant | requant32b_layers<n> | prefill32b | "
                          "decode32b_<shape>_m<M> | decode | decode7b_m<M> | decode7b_qkv_m<M> | "
                          "decode7b_down_m<M> | decode32b_m<M> | prefill | prefill_down_m<M> | int8 | int8_m32 | "
-                         "int8_qkv_m<M> | int8_gate_up_m256 | kv | kv8192 | tis | moe | kl | act_quant_prefill")
+                         "int8_qkv_m<M> | int8_gate_up_m256 | kv | kv8192 | tis | moe | moe_down | kl | act_quant_prefill")
     args = ap.parse_args()
     world, rank, local = dist_env()
     if args.impl == "reference":

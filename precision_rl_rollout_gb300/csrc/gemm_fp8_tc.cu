@@ -462,6 +462,251 @@ decode_splitk_reduce_kernel(const float* __restrict__ part, int64_t M, int mtile
     *reinterpret_cast<uint4*>(Y + row * ldy + z * 128 + c8 * 8) = o;
 }
 
+// ------------------------------------------------------------------ persistent decode kernel
+//
+// For shapes with several waves of (weight slab, token tile) items and K not
+// split (the grouped form's experts: thousands of short items).  One CTA per
+// SM slot takes items w = blockIdx.x, w + gridDim.x, ...; item w is token tile
+// w % mtiles of weight slab w / mtiles.  The TMA ring and the TMEM buffers run
+// on from one item to the next, so each CTA pays its set-up once and the
+// weight blocks of the next item stream while the epilogue finishes the
+// current one; the epilogue writes Y straight from its registers.  The roles
+// and the per-block promotion are those of the kernel above.
+struct PersistParams {
+    uint32_t* err;
+    const float* Xs;       // [KB][M]
+    const float* Ws;       // [slabs][KB]
+    uint16_t* Y;           // [M][ldy]
+    int64_t M, ldy;
+    int KB;                // K / 128 (at most kMaxKbPerSplit)
+    int items, mtiles;     // items = mtiles x weight slabs
+    const int32_t* offs;   // grouped form: [E+1] first token row of each expert (nullptr: dense)
+    int ntiles;            // 128-row slabs per expert (grouped) or per matrix (dense)
+    int64_t tok_bound;     // grouped form: token rows per expert the items cover
+};
+
+// Token rows of item (mt, z): row0 .. row0 + rows - 1 (rows <= 0: none).  The
+// same for every thread that asks (offs is not written while the kernel runs).
+template <int MT>
+__device__ __forceinline__ void persist_item_rows(const PersistParams& p, int mt, int z, int64_t& row0,
+                                                  int64_t& rows) {
+    row0 = (int64_t)mt * MT;
+    rows = p.M - row0;
+    if (p.offs) {
+        const int e = z / p.ntiles;
+        int64_t b = p.offs[e], en = p.offs[e + 1];
+        b = b < 0 ? 0 : (b > p.M ? p.M : b);
+        en = en < b ? b : (en > p.M ? p.M : en);
+        row0 = b + (int64_t)mt * MT;
+        rows = en - row0;
+    }
+}
+
+template <int MT>
+__global__ void __launch_bounds__(DecodeCfg<MT>::kThreads, DecodeCfg<MT>::kMinBlocks)
+gemm_fp8_decode_persistent_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                                  const __grid_constant__ PersistParams p) {
+    using C = DecodeCfg<MT>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* cscale = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 2 * C::kTmemBufs);
+    volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + C::kStages);
+    const uint32_t tfull0 = smem_u32(bars + 2 * C::kStages);
+    const uint32_t tempty0 = smem_u32(bars + 2 * C::kStages + C::kTmemBufs);
+    const uint32_t warp = warp_id(), lane = lane_id();
+    const int KB = p.KB;
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int b = 0; b < C::kTmemBufs; ++b) {
+            mbar_init(tfull0 + 8 * b, 1);
+            mbar_init(tempty0 + 8 * b, C::kEpiWarps);
+        }
+        *abort = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmW);
+        prefetch_tmap(&tmX);
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    // nothing in global memory is read before the previous kernel has completed
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    if (warp == 0) {
+        // ---------------- TMA producer: one pipeline counter over all items
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+            uint32_t it = 0;
+            bool ok = true;
+            for (int w = blockIdx.x; ok && w < p.items; w += gridDim.x) {
+                const int mt = w % p.mtiles, z = w / p.mtiles;
+                int64_t row0, rows;
+                persist_item_rows<MT>(p, mt, z, row0, rows);
+                if (rows <= 0) continue;
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int s = it % C::kStages;
+                    const uint32_t ph = (it / C::kStages) & 1;
+                    if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1, abort, kWaitLimitNs)) {
+                        record_timeout(p.err, kKernelDecode, 11, abort);
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = smem + s * C::kStageBytes;
+                    mbar_arrive_expect_tx(full0 + 8 * s, C::kStageBytes);
+                    tma_load_2d(smem_u32(st), &tmW, full0 + 8 * s, kb * 128, z * 128, pol_w);
+                    tma_load_2d(smem_u32(st + 16384), &tmX, full0 + 8 * s, kb * 128, (int32_t)row0, pol_x);
+                }
+            }
+            if (*abort) {   // let copies already in flight land before the CTA can exit
+                for (uint32_t j = it > (uint32_t)C::kStages ? it - C::kStages : 0; j < it; ++j)
+                    mbar_drain(full0 + 8 * (j % C::kStages), (j / C::kStages) & 1, kWaitLimitNs);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer (one thread), the same counter
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_e4m3_f32(128, MT);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int w = blockIdx.x; ok && w < p.items; w += gridDim.x) {
+                const int mt = w % p.mtiles, z = w / p.mtiles;
+                int64_t row0, rows;
+                persist_item_rows<MT>(p, mt, z, row0, rows);
+                if (rows <= 0) continue;
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int s = it % C::kStages;
+                    const uint32_t ph = (it / C::kStages) & 1;
+                    const int buf = it % C::kTmemBufs;
+                    const uint32_t bph = (it / C::kTmemBufs) & 1;
+                    if (!mbar_wait_bounded(full0 + 8 * s, ph, abort, kWaitLimitNs)) {
+                        record_timeout(p.err, kKernelDecode, 12, abort);
+                        ok = false;
+                        break;
+                    }
+                    if (!mbar_wait_bounded(tempty0 + 8 * buf, bph ^ 1, abort, kWaitLimitNs)) {
+                        record_timeout(p.err, kKernelDecode, 13, abort);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint8_t* st = smem + s * C::kStageBytes;
+                    const uint64_t a = umma_desc_k128_sw128(smem_u32(st));
+                    const uint64_t b = umma_desc_k128_sw128(smem_u32(st + 16384));
+                    const uint32_t d = tmem_base + buf * MT;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) mma_f8f6f4(d, a + 2 * k, b + 2 * k, idesc, k > 0 ? 1u : 0u);
+                    tc_commit(empty0 + 8 * s);
+                    tc_commit(tfull0 + 8 * buf);
+                }
+            }
+        }
+    } else {
+        // ---------------- epilogue: per-block promotion, then Y from registers
+        constexpr int kEpiThreads = C::kEpiWarps * 32;
+        const int e = warp - 2;
+        const int q = warp & 3;                          // TMEM lane quadrant of this warp
+        const int colbase = (e >> 2) * C::kCols;         // token columns of this thread
+        const int n_local = 32 * q + lane;               // weight row within the slab
+        const int et = e * 32 + lane;
+        uint32_t it = 0;
+        for (int w = blockIdx.x; w < p.items; w += gridDim.x) {
+            const int mt = w % p.mtiles, z = w / p.mtiles;
+            const int nt = p.offs ? z % p.ntiles : z;
+            int64_t row0, rows;
+            persist_item_rows<MT>(p, mt, z, row0, rows);
+            if (rows <= 0) continue;
+            if (p.offs && et == 0 && mt == 0 && nt == 0) {
+                const int ex = z / p.ntiles;
+                if ((int64_t)p.offs[ex + 1] - p.offs[ex] > p.tok_bound)
+                    atomicCAS(p.err, 0u, (kKernelDecode << 24) | (7u << 16) | 2u);   // tokens beyond the bound
+            }
+            // every epilogue thread is done with the previous item's scales, and
+            // all of them take the same decision on going on
+            if (bar_red_or(1, kEpiThreads, *abort != 0)) break;
+            {
+                // c[kb][j] = Ws[z][kb] * Xs[kb][row0 + j] (0 beyond the item's rows)
+                const float* __restrict__ ws = p.Ws + (int64_t)z * KB;
+                const float* __restrict__ xs = p.Xs + row0;
+                const int total = KB * MT;
+                for (int base = et; base < total; base += 8 * kEpiThreads) {
+                    float v[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int idx = base + u * kEpiThreads;
+                        const int kb = idx / MT, j = idx - kb * MT;
+                        v[u] = (idx < total && j < rows) ? __ldg(ws + kb) * __ldg(xs + (int64_t)kb * p.M + j) : 0.f;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        if (base + u * kEpiThreads < total) cscale[base + u * kEpiThreads] = v[u];
+                }
+            }
+            named_bar_sync(1, kEpiThreads);
+            uint64_t acc[C::kCols / 2];
+#pragma unroll
+            for (int j = 0; j < C::kCols / 2; ++j) acc[j] = 0ull;
+            bool ok = true;
+            for (int kb = 0; kb < KB; ++kb, ++it) {
+                const int buf = it % C::kTmemBufs;
+                const uint32_t bph = (it / C::kTmemBufs) & 1;
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(tfull0 + 8 * buf, bph, abort, kWaitLimitNs))) {
+                    if (lane == 0) record_timeout(p.err, kKernelDecode, 14, abort);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + buf * MT + colbase;
+                static_assert(C::kCols == C::kGroup, "one load group per block");
+                uint32_t r[C::kGroup];
+#pragma unroll
+                for (int ch = 0; ch < C::kGroup / C::kChunk; ++ch) {
+                    uint32_t(&rc)[C::kChunk] = *reinterpret_cast<uint32_t(*)[C::kChunk]>(r + ch * C::kChunk);
+                    const uint32_t a = taddr + ch * C::kChunk;
+                    if constexpr (C::kChunk == 32) tmem_ld_32x32b_x32(a, rc);
+                    else tmem_ld_32x32b_x16(a, rc);
+                }
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
+                const uint64_t* cs2 = reinterpret_cast<const uint64_t*>(cscale + kb * MT + colbase);
+#pragma unroll
+                for (int j = 0; j < C::kGroup / 2; ++j)
+                    fma_f32x2(acc[j], f32x2_pack(r[2 * j], r[2 * j + 1]), cs2[j]);
+            }
+            if (!ok) continue;   // the abort flag is set: the next item's barrier ends the loop
+            // Y[row0 + colbase + j][nt * 128 + n_local]: per token column, a warp
+            // writes 32 consecutive channels (64 bytes)
+            const int valid = rows < MT ? (int)rows : MT;
+            uint16_t* yp = p.Y + (row0 + colbase) * p.ldy + (int64_t)nt * 128 + n_local;
+#pragma unroll
+            for (int j = 0; j < C::kCols / 2; ++j) {
+                const float2 v = f32x2_unpack(acc[j]);
+                const uint32_t pk = pack_bf16x2(v.x, v.y);
+                if (colbase + 2 * j < valid) yp[(int64_t)(2 * j) * p.ldy] = (uint16_t)(pk & 0xffffu);
+                if (colbase + 2 * j + 1 < valid) yp[(int64_t)(2 * j + 1) * p.ldy] = (uint16_t)(pk >> 16);
+            }
+        }
+    }
+    __syncwarp();   // warps 0 and 1 ran their loops on lane 0 alone
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
 // Split-K factor for `tiles` weight slabs of KB blocks and a token tile of MT.
 // Cost model fitted to a sweep of cluster splits 1..8 over the Qwen2.5-7B/32B
 // decode shapes at M = 1..256 on GB300.  It underrates larger splits on short
@@ -522,6 +767,18 @@ static cudaError_t set_decode_smem(int dev) {
     if (!attr_set[dev]) {
         cudaError_t e = cudaFuncSetAttribute(gemm_fp8_decode_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              DecodeCfg<MT>::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    return cudaSuccess;
+}
+
+template <int MT>
+static cudaError_t set_persist_smem(int dev) {
+    static bool attr_set[64] = {};     // the attribute belongs to the device
+    if (!attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_fp8_decode_persistent_kernel<MT>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, DecodeCfg<MT>::kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
@@ -702,13 +959,22 @@ static cudaError_t launch_decode_mt(const uint8_t* Xq, const float* Xs, const ui
     if (per > C::kMaxKbPerSplit) return cudaErrorInvalidValue;
     uint32_t* err = device_error_word();
     if (!err) return cudaErrorInvalidValue;
-    const int early_w = (weights_stable && offs == nullptr && N * K <= kEarlyWeightMaxBytes) ? 1 : 0;
-    DecodeParams prm{err, Xs, Ws, Y, M, ldy, KB, per, split, offs, (int)(N / 128), mtiles * MT,
-                     pl.uses_memory() ? static_cast<float*>(ws) : nullptr, pl.xmode, early_w};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    // grouped form, K not split, more items than CTAs fit at once: persistent CTAs
+    const int64_t slots = (int64_t)num_sms() * C::kMinBlocks;
+    if (offs != nullptr && split == 1 && tiles > slots && tiles < (1ll << 31)) {
+        e = set_persist_smem<MT>(dev);
+        if (e != cudaSuccess) return e;
+        PersistParams pp{err, Xs, Ws, Y, M, ldy, KB, (int)tiles, (int)mtiles, offs, (int)(N / 128), mtiles * MT};
+        return launch_pdl(gemm_fp8_decode_persistent_kernel<MT>, dim3((unsigned)slots), dim3(C::kThreads),
+                          C::kSmemBytes, st, tmW, tmX, pp);
+    }
+    const int early_w = (weights_stable && offs == nullptr && N * K <= kEarlyWeightMaxBytes) ? 1 : 0;
+    DecodeParams prm{err, Xs, Ws, Y, M, ldy, KB, per, split, offs, (int)(N / 128), mtiles * MT,
+                     pl.uses_memory() ? static_cast<float*>(ws) : nullptr, pl.xmode, early_w};
     e = set_decode_smem<MT>(dev);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};

@@ -120,20 +120,6 @@ __device__ __forceinline__ void convert_chunk(const uint8_t* raw, uint8_t* cvt, 
     *reinterpret_cast<uint4*>(dst + (((j + 1) ^ sw) << 4)) = o1;
 }
 
-// One verdict for the threads of a named barrier: true if any of them passes true.
-__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t count, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n.reg .pred p, q;\n"
-        "setp.ne.u32 p, %1, 0;\n"
-        "bar.red.or.pred q, %2, %3, p;\n"
-        "selp.u32 %0, 1, 0, q;\n}\n"
-        : "=r"(r)
-        : "r"((uint32_t)pred), "r"(id), "r"(count)
-        : "memory");
-    return r != 0;
-}
-
 // Y[m][n0 .. n0+7] = bf16((float(acc) * Xs[m]) * Ws[n]) and the accumulators if asked.
 __device__ __forceinline__ void store_out8(const Int8Params& p, int64_t mg, int64_t n0, const int32_t (&s)[8]) {
     const float xs = p.Xs[mg];

@@ -91,3 +91,45 @@ def test_grouped_rows_beyond_the_bound_are_reported_not_written(cuda_lib):
     assert_fp8_gemm_close(Yh[done], ref[done], "covered rows")
     assert np.all(oracle.bf16_to_f32(Yh[16:40]) == 5.0), "rows beyond the bound were written"
     assert fb.fp8rl_check_device_error() == 0, "the device word is cleared by the check"
+
+
+def test_grouped_persistent_many_items_skewed_routing(cuda_lib):
+    # 64 experts x 16 weight slabs = 1024 (expert, slab) items, more than the
+    # GPU holds at once, K = 768 not split: persistent CTAs take the items in
+    # turn.  Skewed routing leaves some experts empty (items skipped by every
+    # role) and gives others up to a few dozen tokens (one 32- or 64-row tile)
+    rng = np.random.default_rng(71)
+    counts = rng.multinomial(256, rng.dirichlet(np.ones(64) * 0.3))
+    assert (counts == 0).any() and counts.max() > 16
+    _grouped_case(counts, 2048, 768, seed=73, bound=int(counts.max()),
+                  what=f"persistent, routing {counts.tolist()}")
+
+
+def test_grouped_persistent_two_token_tiles(cuda_lib):
+    # bound 150 -> 128-row token tiles, two per expert: 8 experts x 10 slabs x
+    # 2 tiles = 160 items over one CTA per SM; item w is token tile w % 2 of
+    # slab w / 2, and the second tile of an expert with <= 128 tokens is empty
+    counts = np.array([150, 0, 3, 129, 1, 0, 40, 77])
+    _grouped_case(counts, 1280, 512, seed=79, bound=150, what="persistent, two token tiles")
+
+
+def test_grouped_persistent_rows_beyond_the_bound(cuda_lib):
+    # 40 experts x 8 slabs = 320 items (persistent); expert 0 has 40 tokens
+    # but the caller promised at most 4: rows 16..39 keep their sentinel and
+    # the device reports the broken bound
+    counts = np.array([40] + [1] * 39)
+    N, K = 1024, 256
+    Wq, Ws = _experts(40, N, K, 81)
+    Xq, Xs, offsets = _routed_tokens(counts, K, 82)
+    T = int(counts.sum())
+    Y = torch.full((T, N), 5.0, dtype=torch.bfloat16, device="cuda")
+    fb.fp8rl_gemm_w8a8_block_grouped(dev(Xq), dev(Xs), dev(Wq), dev(Ws), dev(offsets),
+                                     max_tokens_per_expert=4, Y=Y)
+    word = fb.fp8rl_check_device_error()
+    assert word != 0 and (word & 0xFFFF) == 2, hex(word)
+    ref = oracle.fp8_gemm_grouped(Xq, Xs, Wq, Ws, offsets)
+    Yh = host(Y)
+    done = np.r_[0:16, 40:T]
+    assert_fp8_gemm_close(Yh[done], ref[done], "covered rows")
+    assert np.all(oracle.bf16_to_f32(Yh[16:40]) == 5.0), "rows beyond the bound were written"
+    assert fb.fp8rl_check_device_error() == 0
