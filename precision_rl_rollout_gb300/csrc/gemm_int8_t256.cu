@@ -15,21 +15,27 @@
 // launch and loaded by TMA (128-byte swizzle, two 64-wide K atoms per block):
 // each weight block costs 8 MMAs of N = 256, for all 256 tokens.
 //
-// TMEM: one 256-column fp32 accumulator (token = column, weight row = lane)
-// and four 64-column fp16 weight blocks.  The accumulator collects one exact
-// group of 2 K blocks (256 products, |sum| <= 256 * 127^2 < 2^22: every
-// partial sum is an integer held exactly in fp32); the epilogue warps then
-// move it into integer registers and release it, while the MMAs wait.  That
-// move is kept short: for an integer v with |v| < 2^22, v + 1.5 * 2^23 is
-// exact and its bits are 0x4B400000 + v, so one add and one integer add per
-// value replace the quarter-rate float -> int conversion; the offsets are
-// taken off once at the end (32-bit wrap-around arithmetic).
+// TMEM: two 128-column fp32 half accumulators, tokens 0..127 (half 0) and
+// 128..255 (half 1) (token = column, weight row = lane), and four 64-column
+// fp16 weight blocks.  A half collects one exact group of at most 2 K blocks
+// (256 products, |sum| <= 256 * 127^2 < 2^22: every partial sum is an integer
+// held exactly in fp32); its epilogue warps then move it into integer
+// registers and release it.  The halves' groups are staggered by one block
+// (half 0: blocks {0,1}, {2,3}, ...; half 1: {0}, {1,2}, {3,4}, ...), and each
+// half has its own MMA issuer, so while one half is being moved the MMAs of
+// the other keep the tensor pipe busy (an issuer's barrier waits drain only
+// its own MMAs in flight).  The move is kept short: for an integer v with
+// |v| < 2^22, v + 1.5 * 2^23 is exact and its bits are 0x4B400000 + v, so one
+// add and one integer add per value replace the quarter-rate float -> int
+// conversion; the offsets are taken off once at the end (32-bit wrap-around
+// arithmetic).
 //
 // Warps (512 threads): 0 = TMA of the weight blocks, 2 = TMA of the token
-// tiles, 1 = MMA issuer, 4..7 = converters, 8..15 = epilogue (two warps per
-// TMEM lane quadrant, 128 tokens each).  The int32 tile is transposed through
-// shared memory for coalesced stores of Y (or of an int32 partial tile when
-// the K range is split; a second launch adds the partials, exact in any order).
+// tiles, 1 and 3 = MMA issuers of halves 0 and 1, 4..7 = converters, 8..15 =
+// epilogue (warps 8..11 half 0, 12..15 half 1, one per TMEM lane quadrant).
+// The int32 tile is transposed through shared memory for coalesced stores of
+// Y (or of an int32 partial tile when the K range is split; a second launch
+// adds the partials, exact in any order).
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -54,7 +60,7 @@ constexpr int kThreads = 512;
 constexpr int kXOffset = kWStages * kRawW;
 constexpr int kBarOffset = kXOffset + kXStages * kXStage;
 constexpr int kSmemBytes = kBarOffset + 256 + 1024;
-constexpr int kTmemCols = 512;                     // accumulator 0..255, weight slots from 256
+constexpr int kTmemCols = 512;                     // half accumulators 0..127, 128..255; weight slots from 256
 constexpr int kLaunchRegs = 128, kLowRegs = 72, kEpiRegs = 184;
 static_assert(kXOffset % 1024 == 0 && kXAtom % 1024 == 0, "swizzled tiles start on 1024-byte atoms");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -64,12 +70,22 @@ static_assert(256 * kLowRegs + 256 * kEpiRegs <= kThreads * kLaunchRegs,
 static_assert(kGroupKb * 128 * 127 * 127 < (1 << 22), "group sums must stay exact, and within the magic-add range");
 constexpr float kMagic = 12582912.0f;              // 1.5 * 2^23
 constexpr uint32_t kMagicBits = 0x4B400000u;
-static_assert((2 * kWStages + 2 * kSlots + 2 * kXStages + 2) * 8 + 8 <= 256, "barrier area");
+static_assert((2 * kWStages + 2 * kSlots + 2 * kXStages + 4) * 8 + 8 <= 256, "barrier area");
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint32_t kKernelInt8T256 = 6;
 
-// kind::f16: A = B = fp16, D = fp32, K-major, M = 128 (weight rows), N = 256 (tokens).
-constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kTok >> 3) << 17) | ((128u >> 4) << 24);
+// kind::f16: A = B = fp16, D = fp32, K-major, M = 128 (weight rows), N = 128 (one half's tokens).
+constexpr uint32_t kIdesc = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+constexpr int kHalfRows = 128 * 128;               // bytes of 128 token rows in one swizzled K atom
+
+// Exact groups of half h: half 0 ends a group after every odd block, half 1
+// after block 0 and every even block; both end one after the last block.
+__device__ __forceinline__ bool group_first(int h, int it) { return h == 0 ? (it & 1) == 0 : (it == 0 || (it & 1)); }
+__device__ __forceinline__ bool group_last(int h, int it, int nkb) {
+    return it == nkb - 1 || (h == 0 ? (it & 1) == 1 : (it & 1) == 0);
+}
+__device__ __forceinline__ int group_index(int h, int it) { return h == 0 ? it >> 1 : (it + 1) >> 1; }
+__device__ __forceinline__ int group_count(int h, int nkb) { return h == 0 ? (nkb + 1) >> 1 : (nkb >> 1) + 1; }
 
 struct T256Params {
     uint32_t* err;
@@ -112,13 +128,13 @@ gemm_int8_t256_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOffset);
-    // wfull[4] wempty[4] sfull[4] sempty[4] xfull[2] xempty[2] afull aempty
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kWStages + 2 * kSlots + 2 * kXStages + 2);
+    // wfull[4] wempty[4] sfull[4] sempty[4] xfull[2] xempty[2] afull[2] aempty[2]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kWStages + 2 * kSlots + 2 * kXStages + 4);
     volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const uint32_t wfull0 = smem_u32(bars), wempty0 = wfull0 + 8 * kWStages;
     const uint32_t sfull0 = wempty0 + 8 * kWStages, sempty0 = sfull0 + 8 * kSlots;
     const uint32_t xfull0 = sempty0 + 8 * kSlots, xempty0 = xfull0 + 8 * kXStages;
-    const uint32_t afull = xempty0 + 8 * kXStages, aempty = afull + 8;
+    const uint32_t afull0 = xempty0 + 8 * kXStages, aempty0 = afull0 + 16;   // per half
     const uint32_t warp = warp_id(), lane = lane_id();
     const int sp = blockIdx.x, mt = blockIdx.y, nt = blockIdx.z;     // K range, token tile, weight slab
     const int kb0 = sp * p.kb_per;
@@ -131,14 +147,16 @@ gemm_int8_t256_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
         }
         for (int s = 0; s < kSlots; ++s) {
             mbar_init(sfull0 + 8 * s, 4);
-            mbar_init(sempty0 + 8 * s, 1);
+            mbar_init(sempty0 + 8 * s, 2);           // the MMAs of both halves
         }
         for (int s = 0; s < kXStages; ++s) {
             mbar_init(xfull0 + 8 * s, 1);
-            mbar_init(xempty0 + 8 * s, 1);
+            mbar_init(xempty0 + 8 * s, 2);
         }
-        mbar_init(afull, 1);
-        mbar_init(aempty, 8);                        // the eight epilogue warps
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(afull0 + 8 * h, 1);
+            mbar_init(aempty0 + 8 * h, 4);           // the half's four epilogue warps
+        }
         *abort = 0;
         fence_mbar_init();
         prefetch_tmap(&tmW);
@@ -188,13 +206,16 @@ gemm_int8_t256_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
             if (*abort)
                 for (int j = max(0, it - kXStages); j < it; ++j)
                     mbar_drain(xfull0 + 8 * (j % kXStages), (j / kXStages) & 1, kWaitLimitNs);
-        } else if (warp == 1 && lane == 0) {
-            // ---------------- MMA issuer: 8 x (M=128, N=256, K=16) per K block
+        } else if ((warp == 1 || warp == 3) && lane == 0) {
+            // ---------------- MMA issuers, one per half: 8 x (M=128, N=128, K=16)
+            // per K block into columns 128 h .. 128 h + 127
+            const int h = warp == 1 ? 0 : 1;
+            const uint32_t d = tmem_base + 128 * h;
             for (int it = 0; it < nkb; ++it) {
                 const int s = it % kSlots, xs = it % kXStages;
-                const bool first = (it % kGroupKb) == 0;
-                const bool last = (it % kGroupKb) == kGroupKb - 1 || it == nkb - 1;
-                if (first && !mbar_wait_bounded(aempty, ((it / kGroupKb) & 1) ^ 1, abort, kWaitLimitNs)) {
+                const bool first = group_first(h, it);
+                if (first &&
+                    !mbar_wait_bounded(aempty0 + 8 * h, (group_index(h, it) & 1) ^ 1, abort, kWaitLimitNs)) {
                     record_timeout(p.err, 3, abort);
                     break;
                 }
@@ -205,15 +226,15 @@ gemm_int8_t256_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
                 }
                 tc_fence_after();
                 const uint32_t a = tmem_base + 256 + s * 64;       // weight block: 64 columns
-                const uint32_t xst = smem_u32(smem + kXOffset + xs * kXStage);
+                const uint32_t xst = smem_u32(smem + kXOffset + xs * kXStage) + h * kHalfRows;
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {    // K = 16 fp16 = 8 TMEM columns / 32 bytes per step
                     const uint64_t b = umma_desc_k128_sw128(xst + (k >> 2) * kXAtom) + 2 * (k & 3);
-                    mma_f16_tmem_a(tmem_base, a + 8 * k, b, kIdesc, (first && k == 0) ? 0u : 1u);
+                    mma_f16_tmem_a(d, a + 8 * k, b, kIdesc, (first && k == 0) ? 0u : 1u);
                 }
                 tc_commit(sempty0 + 8 * s);
                 tc_commit(xempty0 + 8 * xs);
-                if (last) tc_commit(afull);
+                if (group_last(h, it, nkb)) tc_commit(afull0 + 8 * h);
             }
         } else if (warp >= 4) {
             // ---------------- converters: weight row 32 * (warp % 4) + lane of each
@@ -257,16 +278,16 @@ gemm_int8_t256_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
     } else {
         regs_inc<kEpiRegs>();
         // ---------------- epilogue: exact int32 accumulation; weight row = lane,
-        // tokens 128 h .. 128 h + 127
+        // tokens 128 h .. 128 h + 127 (half h)
         const int q = (int)(warp & 3), h = ((int)warp - 8) >> 2;
         const int n_local = 32 * q + (int)lane;
-        const int ngroups = (nkb + kGroupKb - 1) / kGroupKb;
+        const int ngroups = group_count(h, nkb);
         uint32_t acc[128];                            // sum of (0x4B400000 + group sum) over the groups
 #pragma unroll
         for (int j = 0; j < 128; ++j) acc[j] = 0;
         bool ok = true;
         for (int g = 0; g < ngroups; ++g) {
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(afull, g & 1, abort, kWaitLimitNs))) {
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(afull0 + 8 * h, g & 1, abort, kWaitLimitNs))) {
                 if (lane == 0) record_timeout(p.err, 6, abort);
                 ok = false;
                 break;
@@ -283,18 +304,19 @@ gemm_int8_t256_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(aempty);
+            if (lane == 0) mbar_arrive(aempty0 + 8 * h);
         }
-        // The last group's commit means every MMA of this CTA has completed (and
-        // with them every TMA copy and converter read): the stage buffers are
-        // free, and the tile goes there as red[token][weight row].
+        // Once both halves' last groups have been read, every MMA of this CTA
+        // has completed (and with them every TMA copy and converter read): the
+        // stage buffers are free, and the tile goes there as red[token][weight row].
+        named_bar_sync(1, 256);                      // the eight epilogue warps
         int32_t* red = reinterpret_cast<int32_t*>(smem);
         if (ok) {
             const uint32_t bias = (uint32_t)ngroups * kMagicBits;
 #pragma unroll
             for (int j = 0; j < 128; ++j) red[(h * 128 + j) * 128 + n_local] = (int32_t)(acc[j] - bias);
         }
-        named_bar_sync(1, 256);                      // the eight epilogue warps
+        named_bar_sync(1, 256);
         if (!*abort) {
             // thread -> (token, 8 weight rows), 16-byte accesses
             const int et = (int)threadIdx.x - 256;
