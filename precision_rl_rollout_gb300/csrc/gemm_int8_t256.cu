@@ -28,7 +28,9 @@
 // |v| < 2^22, v + 1.5 * 2^23 is exact and its bits are 0x4B400000 + v, so one
 // add and one integer add per value replace the quarter-rate float -> int
 // conversion; the offsets are taken off once at the end (32-bit wrap-around
-// arithmetic).
+// arithmetic).  With at most 128 tokens (one-half form) the token tiles are
+// 128 rows, and the two issuers take alternate K blocks into the two
+// accumulators, both for tokens 0..127; their int32 tiles are added at the end.
 //
 // Warps (512 threads): 0 = TMA of the weight blocks, 2 = TMA of the token
 // tiles, 1 and 3 = MMA issuers of halves 0 and 1, 4..7 = converters, 8..15 =
@@ -87,6 +89,16 @@ __device__ __forceinline__ bool group_last(int h, int it, int nkb) {
 __device__ __forceinline__ int group_index(int h, int it) { return h == 0 ? it >> 1 : (it + 1) >> 1; }
 __device__ __forceinline__ int group_count(int h, int nkb) { return h == 0 ? (nkb + 1) >> 1 : (nkb >> 1) + 1; }
 
+// One-half form (at most 128 tokens): issuer h takes the blocks it = h, h + 2,
+// ... into its own accumulator (columns 128 h ..), all for tokens 0..127; its
+// own blocks pair up into exact groups, so the two accumulators' drains
+// alternate with the other issuer's MMAs.  The two int32 tiles are added at
+// the end.
+__device__ __forceinline__ bool oh_first(int it) { return ((it >> 1) & 1) == 0; }
+__device__ __forceinline__ bool oh_last(int it, int nkb) { return ((it >> 1) & 1) == 1 || it + 2 >= nkb; }
+__device__ __forceinline__ int oh_group(int it) { return it >> 2; }
+__device__ __forceinline__ int oh_count(int h, int nkb) { return (((nkb - h + 1) >> 1) + 1) >> 1; }
+
 struct T256Params {
     uint32_t* err;
     const float* Xs;    // [M]
@@ -97,6 +109,7 @@ struct T256Params {
     int64_t M, N, ldy;
     int KB;             // K / 128
     int kb_per, split;  // K blocks per range, ranges
+    int one_half;       // at most 128 tokens: 128-row token tiles, the issuers take alternate blocks
 };
 
 __device__ __forceinline__ void record_timeout(uint32_t* err, uint32_t site, volatile int* abort) {
@@ -145,13 +158,14 @@ gemm_int8_t256_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
             mbar_init(wfull0 + 8 * s, 1);
             mbar_init(wempty0 + 8 * s, 4);           // the four converter warps
         }
+        const uint32_t halves = p.one_half ? 1 : 2;
         for (int s = 0; s < kSlots; ++s) {
             mbar_init(sfull0 + 8 * s, 4);
-            mbar_init(sempty0 + 8 * s, 2);           // the MMAs of both halves
+            mbar_init(sempty0 + 8 * s, halves);      // the MMAs of each live half
         }
         for (int s = 0; s < kXStages; ++s) {
             mbar_init(xfull0 + 8 * s, 1);
-            mbar_init(xempty0 + 8 * s, 2);
+            mbar_init(xempty0 + 8 * s, halves);
         }
         for (int h = 0; h < 2; ++h) {
             mbar_init(afull0 + 8 * h, 1);
@@ -189,8 +203,10 @@ gemm_int8_t256_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
                 for (int j = max(0, it - kWStages); j < it; ++j)
                     mbar_drain(wfull0 + 8 * (j % kWStages), (j / kWStages) & 1, kWaitLimitNs);
         } else if (warp == 2 && lane == 0) {
-            // ---------------- TMA: fp16 token tiles (two 64-wide K atoms per block)
+            // ---------------- TMA: fp16 token tiles (two 64-wide K atoms per block;
+            // 128 rows of each atom in the one-half form)
             const uint64_t pol = policy_evict_last();
+            const uint32_t bytes = p.one_half ? kXStage / 2 : kXStage;
             int it = 0;
             for (; it < nkb; ++it) {
                 const int s = it % kXStages;
@@ -199,7 +215,7 @@ gemm_int8_t256_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
                     break;
                 }
                 uint8_t* st = smem + kXOffset + s * kXStage;
-                mbar_arrive_expect_tx(xfull0 + 8 * s, kXStage);
+                mbar_arrive_expect_tx(xfull0 + 8 * s, bytes);
                 tma_load_2d(smem_u32(st), &tmX, xfull0 + 8 * s, (kb0 + it) * 128, mt * kTok, pol);
                 tma_load_2d(smem_u32(st + kXAtom), &tmX, xfull0 + 8 * s, (kb0 + it) * 128 + 64, mt * kTok, pol);
             }
@@ -208,14 +224,16 @@ gemm_int8_t256_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
                     mbar_drain(xfull0 + 8 * (j % kXStages), (j / kXStages) & 1, kWaitLimitNs);
         } else if ((warp == 1 || warp == 3) && lane == 0) {
             // ---------------- MMA issuers, one per half: 8 x (M=128, N=128, K=16)
-            // per K block into columns 128 h .. 128 h + 127
+            // per K block into columns 128 h .. 128 h + 127 (one-half form: the
+            // issuers' alternate blocks, both for tokens 0..127)
             const int h = warp == 1 ? 0 : 1;
+            const bool oh = p.one_half != 0;
             const uint32_t d = tmem_base + 128 * h;
-            for (int it = 0; it < nkb; ++it) {
+            for (int it = oh ? h : 0; it < nkb; it += oh ? 2 : 1) {
                 const int s = it % kSlots, xs = it % kXStages;
-                const bool first = group_first(h, it);
-                if (first &&
-                    !mbar_wait_bounded(aempty0 + 8 * h, (group_index(h, it) & 1) ^ 1, abort, kWaitLimitNs)) {
+                const bool first = oh ? oh_first(it) : group_first(h, it);
+                const int gi = oh ? oh_group(it) : group_index(h, it);
+                if (first && !mbar_wait_bounded(aempty0 + 8 * h, (gi & 1) ^ 1, abort, kWaitLimitNs)) {
                     record_timeout(p.err, 3, abort);
                     break;
                 }
@@ -226,7 +244,7 @@ gemm_int8_t256_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
                 }
                 tc_fence_after();
                 const uint32_t a = tmem_base + 256 + s * 64;       // weight block: 64 columns
-                const uint32_t xst = smem_u32(smem + kXOffset + xs * kXStage) + h * kHalfRows;
+                const uint32_t xst = smem_u32(smem + kXOffset + xs * kXStage) + (oh ? 0 : h * kHalfRows);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {    // K = 16 fp16 = 8 TMEM columns / 32 bytes per step
                     const uint64_t b = umma_desc_k128_sw128(xst + (k >> 2) * kXAtom) + 2 * (k & 3);
@@ -234,7 +252,7 @@ gemm_int8_t256_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
                 }
                 tc_commit(sempty0 + 8 * s);
                 tc_commit(xempty0 + 8 * xs);
-                if (group_last(h, it, nkb)) tc_commit(afull0 + 8 * h);
+                if (oh ? oh_last(it, nkb) : group_last(h, it, nkb)) tc_commit(afull0 + 8 * h);
             }
         } else if (warp >= 4) {
             // ---------------- converters: weight row 32 * (warp % 4) + lane of each
@@ -281,7 +299,7 @@ gemm_int8_t256_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
         // tokens 128 h .. 128 h + 127 (half h)
         const int q = (int)(warp & 3), h = ((int)warp - 8) >> 2;
         const int n_local = 32 * q + (int)lane;
-        const int ngroups = group_count(h, nkb);
+        const int ngroups = p.one_half ? oh_count(h, nkb) : group_count(h, nkb);
         uint32_t acc[128];                            // sum of (0x4B400000 + group sum) over the groups
 #pragma unroll
         for (int j = 0; j < 128; ++j) acc[j] = 0;
@@ -311,10 +329,23 @@ gemm_int8_t256_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
         // stage buffers are free, and the tile goes there as red[token][weight row].
         named_bar_sync(1, 256);                      // the eight epilogue warps
         int32_t* red = reinterpret_cast<int32_t*>(smem);
-        if (ok) {
-            const uint32_t bias = (uint32_t)ngroups * kMagicBits;
+        const uint32_t bias = (uint32_t)ngroups * kMagicBits;
+        if (!p.one_half) {
+            if (ok) {
 #pragma unroll
-            for (int j = 0; j < 128; ++j) red[(h * 128 + j) * 128 + n_local] = (int32_t)(acc[j] - bias);
+                for (int j = 0; j < 128; ++j) red[(h * 128 + j) * 128 + n_local] = (int32_t)(acc[j] - bias);
+            }
+        } else {
+            // both accumulators hold tokens 0..127: half 1's tile, then half 0 adds its own
+            if (ok && h == 1) {
+#pragma unroll
+                for (int j = 0; j < 128; ++j) red[j * 128 + n_local] = (int32_t)(acc[j] - bias);
+            }
+            named_bar_sync(1, 256);
+            if (ok && h == 0) {
+#pragma unroll
+                for (int j = 0; j < 128; ++j) red[j * 128 + n_local] += (int32_t)(acc[j] - bias);
+            }
         }
         named_bar_sync(1, 256);
         if (!*abort) {
@@ -421,15 +452,24 @@ int t256_ready(int dev) {
 }
 
 // K ranges: one CTA per (range, token tile, weight slab), at most one CTA per
-// SM.  Choose the split that minimises the busiest SM's K blocks (rounds of
-// CTAs times blocks per range) plus the partials' round trip, in K-block units.
+// SM.  Estimated time in microseconds, fitted to sweeps of splits 1..8 over
+// the Qwen2.5-32B shapes at M = 96, 128 and 256 on GB300 (within 11% of all 96
+// points; it picks the fastest split for each of the twelve shape and size
+// pairs):
+//   5.2 + rounds * (3.9 + t_block * K blocks per range)
+//       + (split: 1.9 + 0.055 * partial tiles * tokens per tile / 256)
+// with t_block = 0.9 for two token halves and 0.54 for the one-half form
+// (rounds of CTAs over the SMs; each split CTA writes an int32 partial of its
+// tile's live tokens, which the reduction launch reads back).
 struct T256Plan {
     int split, kb_per;
 };
 
 T256Plan t256_plan(int64_t M, int64_t N, int64_t K) {
     const int KB = (int)(K / 128);
-    const int64_t ctas1 = ((M + kTok - 1) / kTok) * (N / 128);
+    const int64_t mtiles = (M + kTok - 1) / kTok;
+    const int64_t ctas1 = mtiles * (N / 128);
+    const double rows = (double)M / (double)mtiles;     // live tokens per tile, on average
     const int64_t sms = num_sms();
     T256Plan best{1, KB};
     double best_cost = 1e30;
@@ -437,7 +477,8 @@ T256Plan t256_plan(int64_t M, int64_t N, int64_t K) {
         const int per = (KB + s - 1) / s;
         if ((int64_t)(s - 1) * per >= KB) continue;
         const int64_t rounds = (ctas1 * s + sms - 1) / sms;
-        const double cost = (double)rounds * (per + 2) + (s > 1 ? 4.0 : 0.0);
+        double cost = 5.2 + (double)rounds * (3.9 + (M <= 128 ? 0.54 : 0.9) * per);
+        if (s > 1) cost += 1.9 + 0.055 * (double)(ctas1 * s) * rows / kTok;
         if (cost < best_cost - 1e-9) {
             best_cost = cost;
             best = T256Plan{s, per};
@@ -471,13 +512,15 @@ cudaError_t launch_gemm_int8_t256(const int8_t* Xq, const float* Xs, const int8_
                                  : nullptr;
     CUtensorMap tmW, tmX;
     if (!make_tmap_u8(&tmW, Wq, (uint64_t)N, (uint64_t)K, (uint64_t)K, 128)) return cudaErrorInvalidValue;
-    if (!make_tmap_f16_load(&tmX, X16, (uint64_t)M, (uint64_t)K, kTok)) return cudaErrorInvalidValue;
+    const int one_half = M <= 128 ? 1 : 0;             // one token tile with at most 128 live rows
+    if (!make_tmap_f16_load(&tmX, X16, (uint64_t)M, (uint64_t)K, one_half ? kTok / 2 : kTok))
+        return cudaErrorInvalidValue;
     uint32_t* err = device_error_word();
     if (!err) return cudaErrorInvalidValue;
     cudaError_t e = launch_int8_to_f16(Xq, M * K, X16, st);
     if (e != cudaSuccess) return e;
     const int mtiles = (int)((M + kTok - 1) / kTok);
-    T256Params prm{err, Xs, Ws, Y, acc, part, M, N, ldy, (int)(K / 128), pl.kb_per, pl.split};
+    T256Params prm{err, Xs, Ws, Y, acc, part, M, N, ldy, (int)(K / 128), pl.kb_per, pl.split, one_half};
     e = launch_pdl(gemm_int8_t256_kernel, dim3((unsigned)pl.split, (unsigned)mtiles, (unsigned)(N / 128)),
                    dim3(kThreads), kSmemBytes, st, tmW, tmX, prm);
     if (e != cudaSuccess || pl.split == 1) return e;

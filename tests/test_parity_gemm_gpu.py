@@ -279,12 +279,15 @@ def test_int8_gemm_large_batch_extreme_codes_exact(cuda_lib):
 
 
 @pytest.mark.parametrize("M,N,K", [(65, 384, 640), (129, 256, 1152), (200, 384, 2048), (256, 128, 128),
-                                   (256, 1280, 3840)])
+                                   (256, 1280, 3840), (128, 128, 128), (100, 512, 256), (96, 256, 1152),
+                                   (128, 768, 4096)])
 def test_int8_gemm_256_token_path(cuda_lib, M, N, K):
     # 65 .. 256 tokens: weight blocks in TMEM against 256-token tiles of an fp16
     # copy of X (in the workspace).  Few weight slabs split K: the int32
     # partials of the ranges go to the workspace and a second launch adds them.
     # K = 128 is one exact group of one block; K = 1152 ends on a group of one.
+    # Up to 128 tokens the two MMA threads take alternate blocks for the same
+    # 128 tokens (M = 128, K = 128: the second has none; K = 256: one each).
     need = fb.int8rl_gemm_workspace_bytes(M, N, K)
     assert need >= M * K * 2
     assert fb.int8rl_gemm_kernel_count(M, N, K, need) in (2, 3)
@@ -327,11 +330,13 @@ def test_int8_gemm_256_token_path_splits_and_ragged_second_tile(cuda_lib):
     assert np.array_equal(host(Y)[rows], want_y), "Y differs"
 
 
-def test_int8_gemm_256_token_path_extreme_codes_exact(cuda_lib):
+@pytest.mark.parametrize("M", [200, 128])
+def test_int8_gemm_256_token_path_extreme_codes_exact(cuda_lib, M):
     # every code at +-127 over K = 8192 on the 256-token path with a K split
     # (two weight slabs): each exact TMEM group of two K blocks reaches
-    # 256 * 127^2, the top of its range, and |acc| = 127^2 K
-    M, N, K = 200, 256, 8192
+    # 256 * 127^2, the top of its range, and |acc| = 127^2 K (M = 128: the
+    # one-half form, whose two accumulators are added at the end)
+    N, K = 256, 8192
     ws = fb.int8rl_gemm_workspace_bytes(M, N, K)
     assert fb.int8rl_gemm_kernel_count(M, N, K, ws) == 3            # conversion, GEMM, split reduction
     Xq = np.full((M, K), 127, np.int8)
