@@ -67,12 +67,12 @@ PREFILL_M = synth.PREFILL_M
 NCU_TRAFFIC = {"kernel": "quant_weight_block_kernel", "source_sha1": "69912cc3432327fae840b52154efe497e2f08df4",
                "bytes_per_value": (1950448000 + 918897664) / (2 * sum(s.elems for s in synth.QWEN25_32B)),
                "profile": "profiles/requant_weight_block_qwen32b_2layers.md"}
-NCU_TRAFFIC_PREFILL = {"kernel": "gemm_fp8_prefill_kernel", "source_sha1": "51a938b4bdca35303f75f82d3edfa7aa725d6c33",
-                       "bytes_per_step": (108063488 + 89519104) + (87500288 + 53253632) + (1324224256 + 878707712)
-                       + (2229088000 + 78596096),
+NCU_TRAFFIC_PREFILL = {"kernel": "gemm_fp8_prefill_kernel", "source_sha1": "1a1fff07d63cc4d0f6e7a516f57a4970cd1f63d5",
+                       "bytes_per_step": (106420992 + 89201408) + (87272960 + 53447424) + (1500265728 + 880049664)
+                       + (1955701760 + 78481664),
                        "profile": "profiles/prefill_gemm_qwen32b_m8192_four_shapes.md"}
-NCU_TRAFFIC_DECODE = {"kernel": "FP8 GEMM at a decode size", "source_sha1": "9415829969a1433108c3fb528fade227e06a2e75",
-                      "case": "o_proj_M256", "bytes_per_launch": 27614208 + 15736064,
+NCU_TRAFFIC_DECODE = {"kernel": "FP8 GEMM at a decode size", "source_sha1": "06834084e05f354dc9b0651d0abb367a7352b82b",
+                      "case": "o_proj_M256", "bytes_per_launch": 27614208 + 15736576,
                       "profile": "profiles/decode_gemm_qwen32b_o_proj_m256.md"}
 
 
