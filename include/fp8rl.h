@@ -322,7 +322,10 @@ int fp8rl_quant_kv_with_scale(const uint16_t* KV, int64_t R, int64_t C, int64_t 
  * from the rollout policy).  The sums are reduced in a fixed order
  * (deterministic run to run).
  * workspace: at least fp8rl_rollout_is_workspace_bytes(n) bytes, 8-byte
- * aligned (32 bytes per 4096 tokens).
+ * aligned (8 bytes plus 32 bytes per 4096 tokens).  It needs no zeroing; the
+ * call leaves a tag in its first word that the next call on the same
+ * workspace builds on, so two calls sharing one workspace must not run
+ * concurrently (on different streams).
  * ---------------------------------------------------------------------- */
 #define FP8RL_IS_TRUNCATE 0
 #define FP8RL_IS_MASK 1

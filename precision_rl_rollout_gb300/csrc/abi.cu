@@ -249,7 +249,7 @@ int fp8rl_quant_kv_with_scale(const uint16_t* KV, int64_t R, int64_t C, int64_t 
 
 size_t fp8rl_rollout_is_workspace_bytes(int64_t n) {
     if (n <= 0) return 0;
-    return (size_t)rollout_is_max_partials(n) * rollout_is_partial_bytes();
+    return 8 + (size_t)rollout_is_max_partials(n) * rollout_is_partial_bytes();   // header word + records
 }
 
 int fp8rl_rollout_is_weights(const float* logp_train, const float* logp_rollout, const uint8_t* mask,

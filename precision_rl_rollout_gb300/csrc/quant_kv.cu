@@ -39,6 +39,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "sm100_ptx.cuh"
+#include "tagged_slots.cuh"
 
 namespace fp8rl {
 
@@ -120,32 +121,15 @@ constexpr uint32_t kKernelKv = 5;
 constexpr int kKvSlotsPerThread = 3;                  // one pass polls at most 768 slots
 constexpr uint32_t kKvAborted = 0xFFFFFFFFu;          // header amax of a call whose gather ran out
 
-// The tag of the call after the one whose tag is `prev`: top bit always set,
-// the low 31 bits counting up.
-__device__ __forceinline__ uint32_t kv_next_tag(uint32_t prev) {
-    return ((prev + 1u) & 0x7FFFFFFFu) | 0x80000000u;
-}
-
-__device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
-    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
-    uint64_t v;
-    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
-    uint64_t v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-
 // Cooperative launch (every CTA resident) over the header word and P slots:
 // slot[1 + i] = tag << 32 | amax bits of slice i; the header, slot[0], ends as
 // tag << 32 | tensor amax bits.  Every CTA reads the header before it
 // publishes its slot, and CTA 0 overwrites the header only after it has seen
-// every slot of this call (release / acquire order), so all CTAs derive the
-// same tag.  Polling traffic stays O(P) per round (CTA 0 reads the P slots, the
+// every slot of this call, so all CTAs derive the same tag (release stores,
+// relaxed polling and a fence before the header write: each slot word carries
+// its own tag and value, and relaxed loads stay in flight together where
+// acquire loads would complete one after another).  Polling traffic stays
+// O(P) per round (CTA 0 reads the P slots, the
 // rest read one word), backing off between rounds so it does not crowd the
 // loads of CTAs still reading their slice.  A CTA whose wait runs out records
 // a time-out in the error word and writes no codes; if CTA 0's gather runs out
@@ -165,7 +149,7 @@ kv_onepass_kernel(const uint16_t* __restrict__ X, int64_t total, int64_t cpr, in
     // the header is read after the slice's loads are in flight; a relaxed load
     // suffices, as the release store of this CTA's slot below orders it first
     __shared__ uint32_t s_tag;
-    if (threadIdx.x == 0) s_tag = kv_next_tag((uint32_t)(ld_relaxed_u64(slot) >> 32));
+    if (threadIdx.x == 0) s_tag = next_call_tag((uint32_t)(ld_relaxed_u64(slot) >> 32));
     uint32_t m = 0;
 #pragma unroll
     for (int i = 0; i < kKvChunksPerThread; ++i) m = absmax_v4(m, v[i]);
@@ -193,7 +177,7 @@ kv_onepass_kernel(const uint16_t* __restrict__ X, int64_t total, int64_t cpr, in
             const int64_t i = threadIdx.x + (int64_t)j * kKvThreads;
             sv[j] = 0;
             if (i < P) {
-                sv[j] = ld_acquire_u64(slot + 1 + i);
+                sv[j] = ld_relaxed_u64(slot + 1 + i);
                 pending |= 1u << j;
             }
         }
@@ -213,7 +197,7 @@ kv_onepass_kernel(const uint16_t* __restrict__ X, int64_t total, int64_t cpr, in
             __nanosleep(64);
 #pragma unroll
             for (int j = 0; j < kKvSlotsPerThread; ++j)
-                if ((pending >> j) & 1u) sv[j] = ld_acquire_u64(slot + 1 + threadIdx.x + (int64_t)j * kKvThreads);
+                if ((pending >> j) & 1u) sv[j] = ld_relaxed_u64(slot + 1 + threadIdx.x + (int64_t)j * kKvThreads);
         }
         ok = __syncthreads_and(ok);
         a = __reduce_max_sync(0xffffffffu, a);
@@ -222,20 +206,21 @@ kv_onepass_kernel(const uint16_t* __restrict__ X, int64_t total, int64_t cpr, in
         if (threadIdx.x == 0) {
             uint32_t r = red[0];
             for (int w = 1; w < kKvThreads / 32; ++w) r = max(r, red[w]);
+            __threadfence();       // the slots seen above happen before the header write
             st_release_u64(slot, ((uint64_t)tag << 32) | (ok ? r : kKvAborted));
             bcast[0] = r;
             bcast[1] = ok;
         }
     } else if (threadIdx.x == 0) {
         const uint64_t t0 = sm100::globaltimer_ns();
-        uint64_t sv = ld_acquire_u64(slot);
+        uint64_t sv = ld_relaxed_u64(slot);
         while ((uint32_t)(sv >> 32) != tag) {
             if (sm100::globaltimer_ns() - t0 > kKvWaitLimitNs) {
                 ok = false;
                 break;
             }
             __nanosleep(64);
-            sv = ld_acquire_u64(slot);
+            sv = ld_relaxed_u64(slot);
         }
         if ((uint32_t)sv == kKvAborted) ok = false;      // CTA 0's gather ran out (it recorded that)
         bcast[0] = (uint32_t)sv;

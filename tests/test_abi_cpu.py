@@ -279,7 +279,7 @@ def test_kv_quant_noalloc_validation(lib):
 def test_rollout_is_validation(lib):
     f = lib.fp8rl_rollout_is_weights
     ws = lib.fp8rl_rollout_is_workspace_bytes(10000)
-    assert ws == 3 * 32
+    assert ws == 8 + 3 * 32                  # header word + one 32-byte record per 4096 tokens
     assert f(A, A, None, 10000, ctypes.c_float(0.5), 2, A, A, A, ws, None) == 2      # bad mode
     assert f(A, A, None, 10000, ctypes.c_float(0.5), 0, A, None, A, ws, None) == 1   # stats NULL
     assert f(A, A, None, 10000, ctypes.c_float(0.5), 0, A, A + 4, A, ws, None) == 3  # stats alignment
