@@ -27,7 +27,8 @@
 // are grouped by expert, expert e owning rows offsets[e] .. offsets[e+1]-1.
 // Grid z runs over (expert, 128-row slab); each CTA reads its expert's token
 // range after the dependency wait (the router may have just written it), and
-// a CTA whose token tile is empty streams nothing.
+// a CTA whose token tile is empty streams nothing.  With more such items than
+// CTAs fit at once, the persistent kernel below takes them in turn instead.
 #include <algorithm>
 
 #include "common.cuh"

@@ -81,7 +81,7 @@ constexpr uint32_t kIdesc = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24
 constexpr int kHalfRows = 128 * 128;               // bytes of 128 token rows in one swizzled K atom
 
 // Exact groups of half h: half 0 ends a group after every odd block, half 1
-// after block 0 and every even block; both end one after the last block.
+// after block 0 and every even block; both also end a group at the last block.
 __device__ __forceinline__ bool group_first(int h, int it) { return h == 0 ? (it & 1) == 0 : (it == 0 || (it & 1)); }
 __device__ __forceinline__ bool group_last(int h, int it, int nkb) {
     return it == nkb - 1 || (h == 0 ? (it & 1) == 1 : (it & 1) == 0);
@@ -158,10 +158,11 @@ gemm_int8_t256_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
             mbar_init(wfull0 + 8 * s, 1);
             mbar_init(wempty0 + 8 * s, 4);           // the four converter warps
         }
+        // a block is read by both issuers' MMAs, or in the one-half form by one
         const uint32_t halves = p.one_half ? 1 : 2;
         for (int s = 0; s < kSlots; ++s) {
             mbar_init(sfull0 + 8 * s, 4);
-            mbar_init(sempty0 + 8 * s, halves);      // the MMAs of each live half
+            mbar_init(sempty0 + 8 * s, halves);
         }
         for (int s = 0; s < kXStages; ++s) {
             mbar_init(xfull0 + 8 * s, 1);

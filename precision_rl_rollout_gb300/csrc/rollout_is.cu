@@ -13,10 +13,11 @@
 // Every CTA of a persistent grid writes the weights of its token range and
 // one partial record (valid, clipped, sum w, sum d; fp32 sums inside the CTA);
 // the records are added in a fixed order, the counts exactly and the sums in
-// compensated fp32 (deterministic statistics for a given GPU).  One cooperative launch (the grid, at most four CTAs per SM,
-// is resident at once) does both: each CTA publishes its record as four tagged
-// words (see tagged_slots.cuh) and CTA 0, after its own range, gathers them
-// (bounded wait) and writes the statistics.
+// compensated fp32 (deterministic statistics for a given GPU).  One
+// cooperative launch (the grid, at most four CTAs per SM, is resident at once)
+// does both: each CTA publishes its record as four tagged words (see
+// tagged_slots.cuh) and CTA 0, after its own range, gathers them (bounded
+// wait) and writes the statistics.
 #include "common.cuh"
 #include "internal.h"
 #include "sm100_ptx.cuh"
