@@ -901,7 +901,9 @@ def extras(fb, dev, reps=5):
         del W, Wc
         nc = _copies_for(s.N * s.K)
         Wqs = [Wq] + [Wq.clone() for _ in range(nc - 1)]
-        for M in synth.INT8_M_SWEEP:
+        # the INT8 sweep's sizes, and 128 tokens between them (the 256-token
+        # kernel's one-half form)
+        for M in sorted(set(synth.INT8_M_SWEEP) | {128}):
             X = synth.activation(M, s.K, synth.seed_for(5, 1), device=dev)
             Xq, Xs = fb.int8rl_quant_act_token(X)
             Y = torch.empty(M, s.N, dtype=torch.bfloat16, device=dev)
