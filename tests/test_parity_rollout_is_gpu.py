@@ -88,3 +88,22 @@ def test_rollout_is_shared_workspace_across_calls_and_graph_replays(cuda_lib):
         assert got[0] == want_st[0] and got[1] == want_st[1], (r, got, want_st)
         assert np.all(np.abs(host(w).astype(np.float64) - want_w) <= 4 * 2.0 ** -23 * np.abs(want_w))
     assert fb.fp8rl_check_device_error() == 0
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_rollout_is_unaligned_inputs_take_the_scalar_path(cuda_lib, mode):
+    # log-prob views that start one element into their buffers (4-byte but not
+    # 16-byte aligned) and a mask that starts one byte in: the kernel's scalar
+    # path, with the same one-launch statistics; over several CTAs' ranges
+    n = 3 * 4096 * 7 + 13
+    lt, lr, mask = _inputs(n + 1, 900 + mode)
+    lt_d, lr_d, mask_d = lt.cuda()[1:], lr.cuda()[1:], mask.cuda()[1:]
+    assert lt_d.data_ptr() % 16 != 0 and mask_d.data_ptr() % 4 != 0
+    log_clip = float(np.float32(math.log(2.0)))
+    w, stats = fb.fp8rl_rollout_is_weights(lt_d, lr_d, mask_d, log_clip, mode)
+    want_w, want_st = oracle.rollout_is(lt.numpy()[1:], lr.numpy()[1:], mask.numpy()[1:], log_clip, mode)
+    got_w, got_st = host(w).astype(np.float64), host(stats)
+    assert got_st[0] == want_st[0] and got_st[1] == want_st[1]
+    assert np.all(np.abs(got_w - want_w) <= 4 * 2.0 ** -23 * np.abs(want_w))
+    assert abs(got_st[2] - want_st[2]) <= 1e-6 * max(1.0, float(np.sum(np.abs(want_w))))
+    assert fb.fp8rl_check_device_error() == 0
