@@ -107,6 +107,96 @@ struct DecodeCfg {
     static_assert(MT * 128 * 4 <= kStages * kStageBytes, "reduction buffer must fit the stage area");
 };
 
+// ---- pieces shared by the decode kernels (the per-slab kernel and the
+// persistent kernel below run the same roles on the same shared-memory layout)
+
+// One thread: the stage barriers full/empty, the TMEM buffer barriers
+// tfull/tempty (one arrival per epilogue warp) and the abort flag.
+template <int MT>
+__device__ __forceinline__ void decode_init_barriers(uint32_t full0, uint32_t empty0, uint32_t tfull0,
+                                                     uint32_t tempty0, volatile int* abort) {
+    using C = DecodeCfg<MT>;
+    for (int s = 0; s < C::kStages; ++s) {
+        mbar_init(full0 + 8 * s, 1);
+        mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int b = 0; b < C::kTmemBufs; ++b) {
+        mbar_init(tfull0 + 8 * b, 1);
+        mbar_init(tempty0 + 8 * b, C::kEpiWarps);
+    }
+    *abort = 0;
+    fence_mbar_init();
+}
+
+// MMA thread: one 128-wide K block of the stage at `st` (weight tile, then the
+// token tile 16 KB on) into TMEM columns d .. d + MT - 1, as 4 MMAs of K = 32;
+// the stage and the buffer are then handed on (released / filled) when the
+// MMAs complete.
+template <int MT>
+__device__ __forceinline__ void decode_mma_block(const uint8_t* st, uint32_t d, uint32_t empty_bar,
+                                                 uint32_t tfull_bar) {
+    constexpr uint32_t idesc = idesc_e4m3_f32(128, MT);
+    tc_fence_after();
+    const uint64_t a = umma_desc_k128_sw128(smem_u32(st));
+    const uint64_t b = umma_desc_k128_sw128(smem_u32(st + 16384));
+#pragma unroll
+    for (int k = 0; k < 4; ++k)     // +32 B along K = +2 in the descriptors' address field
+        mma_f8f6f4(d, a + 2 * k, b + 2 * k, idesc, k > 0 ? 1u : 0u);
+    tc_commit(empty_bar);
+    tc_commit(tfull_bar);
+}
+
+// Epilogue threads (thread et of kThreadsFill): the per-block scale products
+// c[b][j] = ws[b] * xs[b * M + j] for b < nblk, j < MT (0 for j >= rows).  The
+// loads are issued in batches of 8 so that their latencies overlap.
+template <int MT, int kThreadsFill>
+__device__ __forceinline__ void decode_fill_scales(float* cscale, const float* __restrict__ ws,
+                                                   const float* __restrict__ xs, int64_t M, int nblk,
+                                                   int64_t rows, int et) {
+    const int total = nblk * MT;
+    for (int base = et; base < total; base += 8 * kThreadsFill) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int idx = base + u * kThreadsFill;
+            const int b = idx / MT, j = idx - b * MT;
+            v[u] = (idx < total && j < rows) ? __ldg(ws + b) * __ldg(xs + (int64_t)b * M + j) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (base + u * kThreadsFill < total) cscale[base + u * kThreadsFill] = v[u];
+    }
+}
+
+// Epilogue warp, after the buffer's tfull wait: this thread's kCols columns of
+// one K block (TMEM address taddr) into registers, all in flight under one
+// wait; the buffer is released as soon as they are there, before the
+// promotion, so the next MMAs into it need not wait for the FMAs.  Then
+// acc += block * c (c: this thread's scale products of the block).
+template <int MT>
+__device__ __forceinline__ void decode_promote_block(uint64_t (&acc)[DecodeCfg<MT>::kCols / 2], uint32_t taddr,
+                                                     const float* cs, uint32_t tempty_bar, uint32_t lane) {
+    using C = DecodeCfg<MT>;
+    static_assert(C::kCols == C::kGroup, "one load group per block");
+    tc_fence_after();
+    uint32_t r[C::kGroup];
+#pragma unroll
+    for (int ch = 0; ch < C::kGroup / C::kChunk; ++ch) {
+        uint32_t(&rc)[C::kChunk] = *reinterpret_cast<uint32_t(*)[C::kChunk]>(r + ch * C::kChunk);
+        const uint32_t a = taddr + ch * C::kChunk;
+        if constexpr (C::kChunk == 32) tmem_ld_32x32b_x32(a, rc);
+        else tmem_ld_32x32b_x16(a, rc);
+    }
+    tmem_wait_ld();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(tempty_bar);
+    const uint64_t* cs2 = reinterpret_cast<const uint64_t*>(cs);
+#pragma unroll
+    for (int j = 0; j < C::kGroup / 2; ++j)
+        fma_f32x2(acc[j], f32x2_pack(r[2 * j], r[2 * j + 1]), cs2[j]);
+}
+
 template <int MT>
 __global__ void __launch_bounds__(DecodeCfg<MT>::kThreads, DecodeCfg<MT>::kMinBlocks)
 gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
@@ -132,16 +222,7 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
     const int nkb = min(p.KB, kb0 + p.kb_per_split) - kb0;   // >= 1 by construction
 
     if (warp == 0 && lane == 0) {
-        for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, 1);
-        }
-        for (int b = 0; b < C::kTmemBufs; ++b) {
-            mbar_init(tfull0 + 8 * b, 1);
-            mbar_init(tempty0 + 8 * b, C::kEpiWarps);
-        }
-        *abort = 0;
-        fence_mbar_init();
+        decode_init_barriers<MT>(full0, empty0, tfull0, tempty0, abort);
         prefetch_tmap(&tmW);
         prefetch_tmap(&tmX);
         // The first weight blocks of this slab start moving into L2 while the
@@ -222,7 +303,6 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
     } else if (warp == 1) {
         // ---------------- MMA issuer (one thread)
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_e4m3_f32(128, MT);
             for (int it = 0; it < nrun; ++it) {
                 const int s = it % C::kStages;
                 const uint32_t ph = (it / C::kStages) & 1;
@@ -236,16 +316,8 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
                     record_timeout(p.err, kKernelDecode, 3, abort);
                     break;
                 }
-                tc_fence_after();
-                const uint8_t* st = smem + s * C::kStageBytes;
-                const uint64_t a = umma_desc_k128_sw128(smem_u32(st));
-                const uint64_t b = umma_desc_k128_sw128(smem_u32(st + 16384));
-                const uint32_t d = tmem_base + buf * MT;
-#pragma unroll
-                for (int k = 0; k < 4; ++k)     // 4 x K=32 per 128-wide block; +32 B = +2 in the address field
-                    mma_f8f6f4(d, a + 2 * k, b + 2 * k, idesc, k > 0 ? 1u : 0u);
-                tc_commit(empty0 + 8 * s);
-                tc_commit(tfull0 + 8 * buf);
+                decode_mma_block<MT>(smem + s * C::kStageBytes, tmem_base + buf * MT, empty0 + 8 * s,
+                                     tfull0 + 8 * buf);
             }
         }
     } else {
@@ -255,27 +327,9 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
         const int colbase = (e >> 2) * C::kCols;         // token columns of this thread
         const int n_local = 32 * q + lane;               // weight row within the slab
         const int et = e * 32 + lane;
-        // c[it][j] = Ws[z][kb0+it] * Xs[kb0+it][row0 + j] (0 beyond the tile's
-        // rows); the loads are issued in batches of 8 so their latencies overlap
-        {
-            const float* __restrict__ ws = p.Ws + (int64_t)z * p.KB + kb0;
-            const float* __restrict__ xs = p.Xs + (int64_t)kb0 * p.M + row0;
-            const int total = nrun * MT;
-            const int64_t mrem = rows;
-            constexpr int kStride = C::kEpiWarps * 32;
-            for (int base = et; base < total; base += 8 * kStride) {
-                float v[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int idx = base + u * kStride;
-                    const int it = idx / MT, j = idx - it * MT;
-                    v[u] = (idx < total && j < mrem) ? __ldg(ws + it) * __ldg(xs + (int64_t)it * p.M + j) : 0.f;
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    if (base + u * kStride < total) cscale[base + u * kStride] = v[u];
-            }
-        }
+        // c[it][j] = Ws[z][kb0+it] * Xs[kb0+it][row0 + j]
+        decode_fill_scales<MT, C::kEpiWarps * 32>(cscale, p.Ws + (int64_t)z * p.KB + kb0,
+                                                  p.Xs + (int64_t)kb0 * p.M + row0, p.M, nrun, rows, et);
         named_bar_sync(1, C::kEpiWarps * 32);
 
         uint64_t acc[C::kCols / 2];              // fp32 accumulators as packed pairs
@@ -289,29 +343,8 @@ gemm_fp8_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
                 if (lane == 0) record_timeout(p.err, kKernelDecode, 4, abort);
                 break;
             }
-            tc_fence_after();
-            const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + buf * MT + colbase;
-            const float* cs = cscale + it * MT + colbase;
-            // all of this thread's columns (<= 64) in flight under one wait; the
-            // buffer is released as soon as they are in registers, before the
-            // promotion, so the next MMAs into it need not wait for the FMAs
-            static_assert(C::kCols == C::kGroup, "one load group per block");
-            uint32_t r[C::kGroup];
-#pragma unroll
-            for (int ch = 0; ch < C::kGroup / C::kChunk; ++ch) {
-                uint32_t(&rc)[C::kChunk] = *reinterpret_cast<uint32_t(*)[C::kChunk]>(r + ch * C::kChunk);
-                const uint32_t a = taddr + ch * C::kChunk;
-                if constexpr (C::kChunk == 32) tmem_ld_32x32b_x32(a, rc);
-                else tmem_ld_32x32b_x16(a, rc);
-            }
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
-            const uint64_t* cs2 = reinterpret_cast<const uint64_t*>(cs);
-#pragma unroll
-            for (int j = 0; j < C::kGroup / 2; ++j)
-                fma_f32x2(acc[j], f32x2_pack(r[2 * j], r[2 * j + 1]), cs2[j]);
+            decode_promote_block<MT>(acc, tmem_base + ((uint32_t)(32 * q) << 16) + buf * MT + colbase,
+                                     cscale + it * MT + colbase, tempty0 + 8 * buf, lane);
         }
         // every MMA of this CTA has completed: the stage area is free for the
         // transposed partial tile red[m][n_local]
@@ -472,7 +505,7 @@ decode_splitk_reduce_kernel(const float* __restrict__ part, int64_t M, int mtile
 // on from one item to the next, so each CTA pays its set-up once and the
 // weight blocks of the next item stream while the epilogue finishes the
 // current one; the epilogue writes Y straight from its registers.  The roles
-// and the per-block promotion are those of the kernel above.
+// and the per-block promotion are the shared pieces above.
 struct PersistParams {
     uint32_t* err;
     const float* Xs;       // [KB][M]
@@ -521,16 +554,7 @@ gemm_fp8_decode_persistent_kernel(const __grid_constant__ CUtensorMap tmW, const
     const int KB = p.KB;
 
     if (warp == 0 && lane == 0) {
-        for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, 1);
-        }
-        for (int b = 0; b < C::kTmemBufs; ++b) {
-            mbar_init(tfull0 + 8 * b, 1);
-            mbar_init(tempty0 + 8 * b, C::kEpiWarps);
-        }
-        *abort = 0;
-        fence_mbar_init();
+        decode_init_barriers<MT>(full0, empty0, tfull0, tempty0, abort);
         prefetch_tmap(&tmW);
         prefetch_tmap(&tmX);
     }
@@ -576,7 +600,6 @@ gemm_fp8_decode_persistent_kernel(const __grid_constant__ CUtensorMap tmW, const
     } else if (warp == 1) {
         // ---------------- MMA issuer (one thread), the same counter
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_e4m3_f32(128, MT);
             uint32_t it = 0;
             bool ok = true;
             for (int w = blockIdx.x; ok && w < p.items; w += gridDim.x) {
@@ -599,15 +622,8 @@ gemm_fp8_decode_persistent_kernel(const __grid_constant__ CUtensorMap tmW, const
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
-                    const uint8_t* st = smem + s * C::kStageBytes;
-                    const uint64_t a = umma_desc_k128_sw128(smem_u32(st));
-                    const uint64_t b = umma_desc_k128_sw128(smem_u32(st + 16384));
-                    const uint32_t d = tmem_base + buf * MT;
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) mma_f8f6f4(d, a + 2 * k, b + 2 * k, idesc, k > 0 ? 1u : 0u);
-                    tc_commit(empty0 + 8 * s);
-                    tc_commit(tfull0 + 8 * buf);
+                    decode_mma_block<MT>(smem + s * C::kStageBytes, tmem_base + buf * MT, empty0 + 8 * s,
+                                         tfull0 + 8 * buf);
                 }
             }
         }
@@ -634,24 +650,8 @@ gemm_fp8_decode_persistent_kernel(const __grid_constant__ CUtensorMap tmW, const
             // every epilogue thread is done with the previous item's scales, and
             // all of them take the same decision on going on
             if (bar_red_or(1, kEpiThreads, *abort != 0)) break;
-            {
-                // c[kb][j] = Ws[z][kb] * Xs[kb][row0 + j] (0 beyond the item's rows)
-                const float* __restrict__ ws = p.Ws + (int64_t)z * KB;
-                const float* __restrict__ xs = p.Xs + row0;
-                const int total = KB * MT;
-                for (int base = et; base < total; base += 8 * kEpiThreads) {
-                    float v[8];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int idx = base + u * kEpiThreads;
-                        const int kb = idx / MT, j = idx - kb * MT;
-                        v[u] = (idx < total && j < rows) ? __ldg(ws + kb) * __ldg(xs + (int64_t)kb * p.M + j) : 0.f;
-                    }
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        if (base + u * kEpiThreads < total) cscale[base + u * kEpiThreads] = v[u];
-                }
-            }
+            // c[kb][j] = Ws[z][kb] * Xs[kb][row0 + j]
+            decode_fill_scales<MT, kEpiThreads>(cscale, p.Ws + (int64_t)z * KB, p.Xs + row0, p.M, KB, rows, et);
             named_bar_sync(1, kEpiThreads);
             uint64_t acc[C::kCols / 2];
 #pragma unroll
@@ -665,25 +665,8 @@ gemm_fp8_decode_persistent_kernel(const __grid_constant__ CUtensorMap tmW, const
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + buf * MT + colbase;
-                static_assert(C::kCols == C::kGroup, "one load group per block");
-                uint32_t r[C::kGroup];
-#pragma unroll
-                for (int ch = 0; ch < C::kGroup / C::kChunk; ++ch) {
-                    uint32_t(&rc)[C::kChunk] = *reinterpret_cast<uint32_t(*)[C::kChunk]>(r + ch * C::kChunk);
-                    const uint32_t a = taddr + ch * C::kChunk;
-                    if constexpr (C::kChunk == 32) tmem_ld_32x32b_x32(a, rc);
-                    else tmem_ld_32x32b_x16(a, rc);
-                }
-                tmem_wait_ld();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
-                const uint64_t* cs2 = reinterpret_cast<const uint64_t*>(cscale + kb * MT + colbase);
-#pragma unroll
-                for (int j = 0; j < C::kGroup / 2; ++j)
-                    fma_f32x2(acc[j], f32x2_pack(r[2 * j], r[2 * j + 1]), cs2[j]);
+                decode_promote_block<MT>(acc, tmem_base + ((uint32_t)(32 * q) << 16) + buf * MT + colbase,
+                                         cscale + kb * MT + colbase, tempty0 + 8 * buf, lane);
             }
             if (!ok) continue;   // the abort flag is set: the next item's barrier ends the loop
             // Y[row0 + colbase + j][nt * 128 + n_local]: per token column, a warp
