@@ -805,12 +805,14 @@ static int64_t clusters_per_wave(int split) {
 // GB300 (in the order tried):
 //  - token tiles of 64 or more, with a workspace: the split CTAs run without a
 //    cluster, about one per SM, and a second launch adds their partials;
-//  - token tiles of up to 32: a cluster of the largest split whose clusters all
-//    run at once (per the occupancy API), i.e. more, shorter weight streams per
-//    slab as long as no second wave of clusters is needed.  With a workspace
-//    the partials go through L2 and the CTAs add them after one cluster
-//    barrier (at 16-32 tokens 7-9% faster than through distributed shared
-//    memory, which needs a second barrier before any CTA may exit);
+//  - token tiles of up to 32: a cluster split whose clusters all run at once
+//    (per the occupancy API).  Without a workspace the largest such split, i.e.
+//    more, shorter weight streams per slab as long as no second wave of
+//    clusters is needed, exchanging through distributed shared memory.  With
+//    a workspace the partials go through L2 and the CTAs add them after one
+//    cluster barrier (at 16-32 tokens 7-9% faster than through distributed
+//    shared memory, which needs a second barrier before any CTA may exit), and
+//    the split is l2_exchange_split's;
 //  - when no such split exists (long K on few slabs: the 27648-wide down
 //    projection), through the workspace and a second launch, as many CTAs per
 //    slab as one wave holds;
@@ -825,6 +827,34 @@ struct DecodePlan {
 static bool split_fits(int KB, int s, int max_per) {
     const int per = (KB + s - 1) / s;
     return per <= max_per && (s - 1) * per < KB;   // no empty split
+}
+
+// Split of a token tile of up to 32 whose exchange goes through L2, among the
+// splits whose clusters all run at once (one_wave: the largest of them).  In a
+// sweep of every such split over 12 shapes (N, K from 1536 to 10240) at M = 1,
+// 8 and 32 on GB300, the fastest was, in this order:
+//  - the largest split that leaves at most one CTA per SM, if it keeps at least
+//    90% of the SMs busy with weight streams of at most 8 K blocks (128 KB) per
+//    CTA: a CTA alone on its SM streams faster than two sharing one;
+//  - else the smallest split whose CTAs cover every SM with streams of at most
+//    8 blocks: a larger split adds ranks to the exchange, not bandwidth;
+//  - else the largest one-wave split.
+// Against the largest one-wave split alone this took, e.g., Qwen2.5-7B qkv at
+// M = 8 from 6.5 to 5.8 us and Qwen2.5-32B o_proj at M = 1 from 8.2 to 7.7 us.
+template <int MT>
+static int l2_exchange_split(int64_t tiles, int KB, int one_wave) {
+    constexpr int kMaxKbPerCta = 8;
+    const int64_t sms = num_sms();
+    auto usable = [&](int s) {
+        return split_fits(KB, s, DecodeCfg<MT>::kMaxKbPerSplit) && clusters_per_wave<MT>(s) >= tiles;
+    };
+    int alone = 0;   // largest split with at most one CTA per SM
+    for (int s = 1; s <= one_wave; ++s)
+        if (tiles * s <= sms && usable(s)) alone = s;
+    if (alone > 0 && tiles * alone * 10 >= sms * 9 && (KB + alone - 1) / alone <= kMaxKbPerCta) return alone;
+    for (int s = 1; s <= one_wave; ++s)
+        if (tiles * s >= sms && (KB + s - 1) / s <= kMaxKbPerCta && usable(s)) return s;
+    return one_wave;
 }
 
 template <int MT>
@@ -846,8 +876,11 @@ static DecodePlan decode_plan(int64_t tiles, int KB, bool may_use_memory) {
         while (s >= 2 && !split_fits(KB, s, C::kMaxKbPerSplit)) --s;
         if (s >= 2) return DecodePlan{s, kXchgReduceLaunch};
     }
-    if (MT <= 32 && one_wave > 0)
-        return DecodePlan{one_wave, one_wave > 1 && may_use_memory ? kXchgClusterMem : kXchgSmem};
+    if (MT <= 32 && one_wave > 0) {
+        if (!may_use_memory || one_wave == 1) return DecodePlan{one_wave, kXchgSmem};
+        const int s = l2_exchange_split<MT>(tiles, KB, one_wave);
+        return DecodePlan{s, s > 1 ? kXchgClusterMem : kXchgSmem};
+    }
     if (may_use_memory && clusters_per_wave<MT>(1) > 0) {   // occupancy known: clusters did not fit
         int64_t t = sms * C::kMinBlocks / tiles;
         int s = (int)(t < kMaxMemSplit ? t : kMaxMemSplit);
