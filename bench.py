@@ -71,8 +71,8 @@ NCU_TRAFFIC_PREFILL = {"kernel": "gemm_fp8_prefill_kernel", "source_sha1": "1a1f
                        "bytes_per_step": (106420992 + 89201408) + (87272960 + 53447424) + (1500265728 + 880049664)
                        + (1955701760 + 78481664),
                        "profile": "profiles/prefill_gemm_qwen32b_m8192_four_shapes.md"}
-NCU_TRAFFIC_DECODE = {"kernel": "FP8 GEMM at a decode size", "source_sha1": "374aa93c4f732d4eeedf9d505a38a607323dd546",
-                      "case": "o_proj_M256", "bytes_per_launch": 27613952 + 15736320,
+NCU_TRAFFIC_DECODE = {"kernel": "FP8 GEMM at a decode size", "source_sha1": "3739b283c2aefa71d0c2550760163876721d6c48",
+                      "case": "o_proj_M256", "bytes_per_launch": 27614464 + 15736064,
                       "profile": "profiles/decode_gemm_qwen32b_o_proj_m256.md"}
 
 
