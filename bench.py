@@ -857,7 +857,7 @@ def extras(fb, dev, reps=5):
 
     # FP8 KV-cache quant with a per-tensor scale recalibrated each step (32B: 8 kv heads x 128)
     kv = {}
-    for tokens in (8192, 64 * 2048):
+    for tokens in (8192, 32768, 64 * 2048):
         X = synth.activation(tokens, 1024, synth.seed_for(6, 0), device=dev)
         Xq = torch.empty(tokens, 1024, dtype=torch.uint8, device=dev)
         sc = torch.empty(1, dtype=torch.float32, device=dev)

@@ -289,8 +289,12 @@ int int8rl_gemm_w8a8(const int8_t* Xq, const float* Xs, const int8_t* Wq, const 
  *       captured in a CUDA graph and replayed.  Calls in flight at the same time
  *       need their own workspace.  Tensors of up to about 10 M values are done
  *       in one pass (one cooperative launch; a bounded wait that runs out is
- *       reported by fp8rl_check_device_error as FP8RL_ERR_TIMEOUT), larger ones
- *       in three.
+ *       reported by fp8rl_check_device_error as FP8RL_ERR_TIMEOUT).  Larger
+ *       ones with contiguous rows (ld == C) take one cooperative launch of one
+ *       CTA per SM that keeps up to 448 KB of each SM's range on chip between
+ *       the amax and the encode (read once up to ~34 M values on GB300, the
+ *       rest read again above that; time-outs reported the same way); larger
+ *       ones with a row pitch take three launches.
  * Bit-exact.  An empty tensor (R == 0) writes scale 1.
  * ---------------------------------------------------------------------- */
 size_t fp8rl_kv_workspace_bytes(int64_t R, int64_t C);
@@ -371,8 +375,8 @@ int fp8rl_logits_kl(const uint16_t* P, int64_t ldp, const uint16_t* Q, int64_t l
  * device current) and caches it; make that first call before any stream
  * capture.  Every call shares the one array: nothing in it needs to start at
  * zero (the three-launch path writes every slot before reading it; the
- * one-pass path accepts a slot only once it carries the call's tag, which the
- * device derives from the previous call's), and two calls
+ * cooperative paths accept a slot only once it carries the call's tag, which
+ * the device derives from the previous call's), and two calls
  * whose kernels overlap on the GPU (different streams) race on it -- issue
  * them in one stream, or use fp8rl_quant_kv_tensor with separate workspaces.
  * Other arguments, layouts and errors as for fp8rl_quant_kv_tensor.

@@ -235,14 +235,70 @@ def test_fp8_kv_tensor_quant_qwen32b_cache_sampled(cuda_lib):
 @pytest.mark.parametrize("R,where", [(9728, "last"), (9728, "first"), (9744, "last")])
 def test_fp8_kv_tensor_quant_one_pass_boundary(cuda_lib, R, where):
     # 9728 x 1024 is 608 slices of 16384 values (every slice's CTA resident at
-    # four per SM on 152 SMs: one pass); 9744 x 1024 is 609 (three launches).
-    # The tensor amax sits in the first or last slice only.
+    # four per SM on 152 SMs: one pass); 9744 x 1024 is 609 (one CTA per SM
+    # over ranges kept partly on chip).  The tensor amax sits in the first or
+    # last slice only.
     C = 1024
     X = act_cpu(R, C, 9100 + R)
     r, c = (R - 1, C - 1) if where == "last" else (0, 0)
     X[r, c] = -1000.0
     ws = torch.empty(fb.fp8rl_kv_workspace_bytes(R, C), dtype=torch.uint8, device="cuda")
     KVq, scale = fb.fp8rl_quant_kv_tensor(X.cuda(), workspace=ws)
+    want_q, want_s = oracle.fp8_quant_tensor(synth.bf16_bits(X))
+    assert bits_u32(host(scale))[0] == np.float32(want_s).view(np.uint32)
+    assert np.array_equal(host(KVq), want_q)
+    assert fb.fp8rl_check_device_error() == 0
+
+
+KV_BATCH_CHUNKS = 8 * 512     # 16-byte chunks per batch of the resident kernel (8 rounds of 512 threads)
+
+
+def _kv_resident_range(R, C):
+    """Chunks per CTA of the resident kernel on this GPU (one CTA per SM)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    total = R * (C // 8)
+    per = -(-total // sms)
+    return -(-per // KV_BATCH_CHUNKS) * KV_BATCH_CHUNKS
+
+
+@pytest.mark.parametrize("R,C,where", [(9744, 1024, "last"), (20011, 1032, "first"), (20011, 1032, "last"),
+                                       (32768, 1024, "smem"), (60000, 1024, "tmem"), (60000, 1024, "reread"),
+                                       (60000, 1024, "last")])
+def test_fp8_kv_tensor_quant_resident_path(cuda_lib, R, C, where):
+    # Contiguous tensors above the one-pass size: one CTA per SM over a range of
+    # chunks whose first 7 batches stay on chip (4 in tensor memory, then 3 in
+    # shared memory) between the amax and the encode; later batches are read
+    # again.  On 152 SMs: 9744 x 1024 has 3 batches per CTA, 20011 x 1032 5
+    # (the last ranges ragged or empty), 32768 x 1024 7 (all on chip, read
+    # once), 60000 x 1024 13 (6 read again).  The tensor amax sits in the first
+    # or last value, or in a batch held in shared memory, in tensor memory or
+    # read again.
+    X = act_cpu(R, C, 9500 + R + C)
+    per = _kv_resident_range(R, C)
+    chunk = {"first": 0, "last": R * (C // 8) - 1,
+             "tmem": per + 2 * KV_BATCH_CHUNKS + 77,
+             "smem": 2 * per + 6 * KV_BATCH_CHUNKS + 300,
+             "reread": 3 * per + 9 * KV_BATCH_CHUNKS + 5}[where]
+    chunk = min(chunk, R * (C // 8) - 1)
+    e = chunk * 8 + 5
+    X[e // C, e % C] = -1000.0
+    ws = torch.empty(fb.fp8rl_kv_workspace_bytes(R, C), dtype=torch.uint8, device="cuda")
+    KVq, scale = fb.fp8rl_quant_kv_tensor(X.cuda(), workspace=ws)
+    want_q, want_s = oracle.fp8_quant_tensor(synth.bf16_bits(X))
+    assert bits_u32(host(scale))[0] == np.float32(want_s).view(np.uint32)
+    assert np.array_equal(host(KVq), want_q)
+    assert fb.fp8rl_check_device_error() == 0
+
+
+@pytest.mark.parametrize("R,C,ld", [(9744, 1024, 1032), (20011, 1032, 1040)])
+def test_fp8_kv_tensor_quant_strided_above_one_pass(cuda_lib, R, C, ld):
+    # rows with a pitch, above the one-pass size: the three-launch path
+    X = act_cpu(R, C, 9600 + R)
+    X[R - 1, C - 1] = 2000.0
+    wide = torch.zeros(R, ld, dtype=torch.bfloat16)
+    wide[:, :C] = X
+    ws = torch.empty(fb.fp8rl_kv_workspace_bytes(R, C), dtype=torch.uint8, device="cuda")
+    KVq, scale = fb.fp8rl_quant_kv_tensor(wide.cuda()[:, :C], workspace=ws)
     want_q, want_s = oracle.fp8_quant_tensor(synth.bf16_bits(X))
     assert bits_u32(host(scale))[0] == np.float32(want_s).view(np.uint32)
     assert np.array_equal(host(KVq), want_q)
@@ -268,7 +324,7 @@ def test_fp8_kv_tensor_quant_reused_workspace_takes_no_stale_slot(cuda_lib):
 @pytest.mark.parametrize("R", [4096, 16384])
 def test_fp8_kv_tensor_quant_graph_replays_recalibrate(cuda_lib, R):
     # one call captured in a CUDA graph (4096 x 1024: the one-pass kernel;
-    # 16384 x 1024: three launches), replayed after new data is copied into its
+    # 16384 x 1024: one CTA per SM, partly on chip), replayed after new data is copied into its
     # input: every replay recalibrates the scale from that data (the one-pass
     # call's tag advances on the device, so a replay never accepts a slot left
     # by the one before), checked against the oracle each time
@@ -300,13 +356,17 @@ def test_fp8_kv_tensor_quant_graph_replays_recalibrate(cuda_lib, R):
 
 
 def test_fp8_kv_tensor_quant_workspace_reused_across_paths(cuda_lib):
-    # one workspace for a three-launch call (its partials follow the header
-    # word), then one-pass calls, then three-launch again: each bit-exact
+    # one workspace for a three-launch call (rows with a pitch; its partials
+    # follow the header word), one-pass calls and calls of one CTA per SM (the
+    # last two share the header word's tags): each bit-exact
     C = 1024
     ws = torch.empty(fb.fp8rl_kv_workspace_bytes(16384, C), dtype=torch.uint8, device="cuda")
-    for R, seed in [(16384, 9401), (4096, 9402), (2048, 9403), (16384, 9404), (4096, 9405)]:
+    for R, seed, ld in [(16384, 9401, 1040), (4096, 9402, C), (16384, 9406, C), (2048, 9403, C),
+                        (16384, 9404, 1040), (16384, 9407, C), (4096, 9405, C)]:
         X = act_cpu(R, C, seed)
-        KVq, scale = fb.fp8rl_quant_kv_tensor(X.cuda(), workspace=ws)
+        wide = torch.zeros(R, ld, dtype=torch.bfloat16)
+        wide[:, :C] = X
+        KVq, scale = fb.fp8rl_quant_kv_tensor(wide.cuda()[:, :C], workspace=ws)
         want_q, want_s = oracle.fp8_quant_tensor(synth.bf16_bits(X))
         assert bits_u32(host(scale))[0] == np.float32(want_s).view(np.uint32)
         assert np.array_equal(host(KVq), want_q)

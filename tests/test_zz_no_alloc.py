@@ -78,14 +78,17 @@ def _check_error_word(lib):
     assert rc == 0 and word.value == 0, f"device error word {word.value:#x} (status {rc})"
 
 
-def test_noalloc_kv_quant_three_launch_then_one_pass_matches_oracle(cuda_lib):
+def test_noalloc_kv_quant_paths_in_turn_match_oracle(cuda_lib):
     lib = cuda_lib
-    # 16384 x 1024 is 1024 slices: too many for one pass, so its partials go
-    # through the shared array in three launches; the one-pass calls after it
-    # find those partials in the same array and must not mistake them for their
-    # own slots.  Every output is compared with the oracle, bit for bit.
-    for R, C, seed in [(16384, 1024, 11), (3000, 1024, 12), (16384, 1024, 13), (8229, 1024, 14)]:
-        X = synth.activation(R, C, synth.seed_for(6, seed), device="cuda")
+    # 16384 x 1024 is 1024 slices: too many for one pass.  With a row pitch its
+    # partials go through the shared array in three launches; contiguous, one
+    # CTA per SM publishes tagged slots there.  The calls after each find the
+    # earlier call's words in the same array and must not mistake them for
+    # their own slots.  Every output is compared with the oracle, bit for bit.
+    for R, C, ld, seed in [(16384, 1024, 1032, 11), (3000, 1024, 1024, 12), (16384, 1024, 1024, 13),
+                           (16384, 1024, 1032, 16), (8229, 1024, 1024, 14), (16384, 1024, 1024, 17)]:
+        wide = synth.activation(R, ld, synth.seed_for(6, seed), device="cuda")
+        X = wide[:, :C]
         KVq = torch.empty(R, C, dtype=torch.uint8, device="cuda")
         scale = torch.empty(1, dtype=torch.float32, device="cuda")
         assert _call_noalloc(lib, X, KVq, scale) == 0
