@@ -85,15 +85,41 @@ __device__ __forceinline__ float div_by_scale(float x, const BlockDivisor& d) {
     }
 }
 
+// The two bf16 values of one 32-bit word (low half first) divided by the block
+// scale exactly as div_by_scale<true> divides each, both at once: mul.rn.f32x2
+// and fma.rn.f32x2 round each lane as the scalar instructions do, so the
+// quotients are the same bits (the residual is formed as RN(|x| + q0 * (-s)),
+// which equals RN(|x| - q0 * s)).  Three packed instructions instead of six.
+__device__ __forceinline__ float2 div2_by_scale_fast(uint32_t w, const BlockDivisor& d) {
+    const uint32_t lo = w << 16, hi = w & 0xFFFF0000u;      // the two values as fp32 bits
+    uint64_t a, y2, ns2, q0, r, q;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "r"(lo & 0x7FFFFFFFu), "r"(hi & 0x7FFFFFFFu));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(y2) : "f"(d.y));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(ns2) : "f"(-d.s));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q0) : "l"(a), "l"(y2));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(q0), "l"(ns2), "l"(a));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q) : "l"(r), "l"(y2), "l"(q0));
+    uint32_t qlo, qhi;
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(qlo), "=r"(qhi) : "l"(q));
+    return make_float2(__uint_as_float(qlo | (lo & 0x80000000u)), __uint_as_float(qhi | (hi & 0x80000000u)));
+}
+
 // Eight bf16 (one 16-byte chunk) divided by the block scale and encoded to
 // eight E4M3FN codes, packed little-endian into 8 bytes.
 template <bool kFast>
 __device__ __forceinline__ uint2 quant8_e4m3_t(uint4 v, const BlockDivisor& d) {
     uint2 o;
-    o.x = e4m3x2(div_by_scale<kFast>(bf16_lo(v.x), d), div_by_scale<kFast>(bf16_hi(v.x), d)) |
-          (e4m3x2(div_by_scale<kFast>(bf16_lo(v.y), d), div_by_scale<kFast>(bf16_hi(v.y), d)) << 16);
-    o.y = e4m3x2(div_by_scale<kFast>(bf16_lo(v.z), d), div_by_scale<kFast>(bf16_hi(v.z), d)) |
-          (e4m3x2(div_by_scale<kFast>(bf16_lo(v.w), d), div_by_scale<kFast>(bf16_hi(v.w), d)) << 16);
+    if constexpr (kFast) {
+        const float2 a = div2_by_scale_fast(v.x, d), b = div2_by_scale_fast(v.y, d);
+        const float2 c = div2_by_scale_fast(v.z, d), e = div2_by_scale_fast(v.w, d);
+        o.x = e4m3x2(a.x, a.y) | (e4m3x2(b.x, b.y) << 16);
+        o.y = e4m3x2(c.x, c.y) | (e4m3x2(e.x, e.y) << 16);
+    } else {
+        o.x = e4m3x2(div_by_scale<false>(bf16_lo(v.x), d), div_by_scale<false>(bf16_hi(v.x), d)) |
+              (e4m3x2(div_by_scale<false>(bf16_lo(v.y), d), div_by_scale<false>(bf16_hi(v.y), d)) << 16);
+        o.y = e4m3x2(div_by_scale<false>(bf16_lo(v.z), d), div_by_scale<false>(bf16_hi(v.z), d)) |
+              (e4m3x2(div_by_scale<false>(bf16_lo(v.w), d), div_by_scale<false>(bf16_hi(v.w), d)) << 16);
+    }
     return o;
 }
 
@@ -104,20 +130,32 @@ __device__ __forceinline__ float int8_scale_from_amax(float amax) {
     return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 127.0f);
 }
 
+// One quotient -> int8 code: clamp(rint(q), -127, 127).
+__device__ __forceinline__ uint32_t int8_code(float q) {
+    int c = __float2int_rn(q);
+    c = min(127, max(-127, c));
+    return (uint32_t)(c & 0xFF);
+}
 // One bf16 -> int8 code: clamp(rint(x / s), -127, 127).
 template <bool kFast>
 __device__ __forceinline__ uint32_t q_int8(float x, const BlockDivisor& d) {
-    int q = __float2int_rn(div_by_scale<kFast>(x, d));
-    q = min(127, max(-127, q));
-    return (uint32_t)(q & 0xFF);
+    return int8_code(div_by_scale<kFast>(x, d));
+}
+// A word's two bf16 -> two int8 codes (low value in the low byte).
+template <bool kFast>
+__device__ __forceinline__ uint32_t q_int8x2(uint32_t w, const BlockDivisor& d) {
+    if constexpr (kFast) {
+        const float2 q = div2_by_scale_fast(w, d);
+        return int8_code(q.x) | (int8_code(q.y) << 8);
+    } else {
+        return q_int8<false>(bf16_lo(w), d) | (q_int8<false>(bf16_hi(w), d) << 8);
+    }
 }
 template <bool kFast>
 __device__ __forceinline__ uint2 quant8_int8_t(uint4 v, const BlockDivisor& d) {
     uint2 o;
-    o.x = q_int8<kFast>(bf16_lo(v.x), d) | (q_int8<kFast>(bf16_hi(v.x), d) << 8) |
-          (q_int8<kFast>(bf16_lo(v.y), d) << 16) | (q_int8<kFast>(bf16_hi(v.y), d) << 24);
-    o.y = q_int8<kFast>(bf16_lo(v.z), d) | (q_int8<kFast>(bf16_hi(v.z), d) << 8) |
-          (q_int8<kFast>(bf16_lo(v.w), d) << 16) | (q_int8<kFast>(bf16_hi(v.w), d) << 24);
+    o.x = q_int8x2<kFast>(v.x, d) | (q_int8x2<kFast>(v.y, d) << 16);
+    o.y = q_int8x2<kFast>(v.z, d) | (q_int8x2<kFast>(v.w, d) << 16);
     return o;
 }
 

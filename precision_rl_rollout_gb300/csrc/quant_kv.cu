@@ -260,16 +260,17 @@ kv_onepass_kernel(const uint16_t* __restrict__ X, int64_t total, int64_t cpr, in
 }
 
 // Tensors too large for one slice per CTA (contiguous rows, 16-byte aligned):
-// one cooperative launch of one 512-thread CTA per SM, each over a contiguous
-// range of `per` chunks, taken in batches of kResBatch rounds (a round is one
-// 16-byte chunk per thread, 8 KB).  While the range is read for its amax (the
-// next batch's loads in flight while one is reduced and stored), its first
-// kResResident batches stay on chip -- kResTmemBatches in tensor memory (32
-// columns of each warp's lane quadrant per batch), then kResSmemBatches in
-// shared memory, 448 KB per CTA -- so after the grid maximum only the rest of
-// the range is read again.  Tensors up to the on-chip total (152 x 448 KB of
-// bf16 on GB300, ~34 M values) are read once; larger ones save that much of
-// the second read.
+// one cooperative launch of one 512-thread CTA per SM.  The tensor is cut into
+// batches of kResBatch rounds (a round is one 16-byte chunk per thread, so a
+// batch is 64 KB), dealt to the CTAs in turn -- CTA b takes batches b, b + G,
+// b + 2G, ... -- which spreads every SM's share over the whole tensor.  While
+// its batches are read for the amax (the next batch's loads in flight while
+// one is reduced and stored), a CTA keeps its first kResResident on chip --
+// kResTmemBatches in tensor memory (32 columns of each warp's lane quadrant per
+// batch), then kResSmemBatches in shared memory, 448 KB per CTA -- so after
+// the grid maximum only the rest is read again.  Tensors up to the on-chip
+// total (152 x 448 KB of bf16 on GB300, ~34 M values) are read once; larger
+// ones save that much of the second read.
 constexpr int kResThreads = 512;
 constexpr int kResBatch = 8;                            // rounds per batch: loads in flight per thread
 constexpr int kResTmemBatches = 4;                      // 4 x 32 columns per warp: all 512 TMEM columns
@@ -311,8 +312,8 @@ __device__ __forceinline__ void keep_batch(int b, const uint4 (&v)[kResBatch], u
 }
 
 __global__ void __launch_bounds__(kResThreads, 1)
-kv_resident_kernel(const uint16_t* __restrict__ X, int64_t total, int64_t per, uint64_t* __restrict__ slot,
-                   int64_t P, float* __restrict__ scale, uint8_t* __restrict__ Xq, uint32_t* __restrict__ err) {
+kv_resident_kernel(const uint16_t* __restrict__ X, int64_t total, uint64_t* __restrict__ slot, int64_t P,
+                   float* __restrict__ scale, uint8_t* __restrict__ Xq, uint32_t* __restrict__ err) {
     extern __shared__ uint4 sres[];                    // [kResSmemBatches][kResBatch][kResThreads]
     __shared__ uint32_t tmem_slot, s_tag;
     __shared__ uint32_t red[kResThreads / 32];
@@ -324,20 +325,23 @@ kv_resident_kernel(const uint16_t* __restrict__ X, int64_t total, int64_t per, u
     sm100::tc_fence_after();
     // this warp's TMEM: its lane quadrant, 128 columns from (warp / 4) * 128
     const uint32_t tw = tmem_slot + ((32u * (warp & 3)) << 16) + (warp >> 2) * (kResTmemBatches * 32);
-    const int64_t c0 = (int64_t)blockIdx.x * per + threadIdx.x;   // this thread's chunk of batch 0, round 0
-    const int nb = (int)(per / kResChunksPerBatch);
+    const int64_t G = gridDim.x;
+    const int64_t tb = (total + kResChunksPerBatch - 1) / kResChunksPerBatch;   // batches in the tensor
+    const int nb = (int)((tb - blockIdx.x + G - 1) / G);                      // this CTA's: b + j G < tb
+    const int64_t c0 = (int64_t)blockIdx.x * kResChunksPerBatch + threadIdx.x;   // its first chunk
+    const int64_t cstride = G * kResChunksPerBatch;                           // chunks between its batches
 
     // pass 1: the range's amax, its first batches kept on chip; two batches
     // alternate in registers so that one is always being loaded
     uint32_t m = 0;
     {
         uint4 va[kResBatch], vb[kResBatch];
-        load_batch(va, X, c0, total);
+        if (nb > 0) load_batch(va, X, c0, total);
         for (int b = 0; b < nb; b += 2) {
-            if (b + 1 < nb) load_batch(vb, X, c0 + (b + 1) * kResChunksPerBatch, total);
+            if (b + 1 < nb) load_batch(vb, X, c0 + (b + 1) * cstride, total);
             keep_batch(b, va, m, tw, sres);
             if (b + 1 >= nb) break;
-            if (b + 2 < nb) load_batch(va, X, c0 + (b + 2) * kResChunksPerBatch, total);
+            if (b + 2 < nb) load_batch(va, X, c0 + (b + 2) * cstride, total);
             keep_batch(b + 1, vb, m, tw, sres);
         }
     }
@@ -351,26 +355,26 @@ kv_resident_kernel(const uint16_t* __restrict__ X, int64_t total, int64_t per, u
         // pass 2: the resident batches are encoded while the first batch read
         // again is in flight
         uint4 nxt[kResBatch];
-        if (nb > kResResident) load_batch(nxt, X, c0 + kResResident * kResChunksPerBatch, total);
+        if (nb > kResResident) load_batch(nxt, X, c0 + kResResident * cstride, total);
         for (int b = 0; b < kResTmemBatches && b < nb; ++b) {
             uint4 v[kResBatch];
             sm100::tmem_ld_32x32b_x32(tw + b * 32, *reinterpret_cast<uint32_t(*)[32]>(v));
             sm100::tmem_wait_ld();
-            encode_batch(v, c0 + b * kResChunksPerBatch, total, d, Xq);
+            encode_batch(v, c0 + b * cstride, total, d, Xq);
         }
         for (int b = kResTmemBatches; b < kResResident && b < nb; ++b) {
             uint4 v[kResBatch];
             const uint4* src = sres + (int64_t)(b - kResTmemBatches) * kResBatch * kResThreads + threadIdx.x;
 #pragma unroll
             for (int i = 0; i < kResBatch; ++i) v[i] = src[i * kResThreads];
-            encode_batch(v, c0 + b * kResChunksPerBatch, total, d, Xq);
+            encode_batch(v, c0 + b * cstride, total, d, Xq);
         }
         for (int b = kResResident; b < nb; ++b) {
             uint4 v[kResBatch];
 #pragma unroll
             for (int i = 0; i < kResBatch; ++i) v[i] = nxt[i];
-            if (b + 1 < nb) load_batch(nxt, X, c0 + (b + 1) * kResChunksPerBatch, total);
-            encode_batch(v, c0 + b * kResChunksPerBatch, total, d, Xq);
+            if (b + 1 < nb) load_batch(nxt, X, c0 + (b + 1) * cstride, total);
+            encode_batch(v, c0 + b * cstride, total, d, Xq);
         }
     }
     sm100::tc_fence_before();
@@ -455,12 +459,10 @@ cudaError_t launch_quant_kv_tensor(const uint16_t* X, int64_t R, int64_t C, int6
     // one-pass capacity, at least 4 slices per SM)
     const int64_t G = kv_resident_ctas();
     if (P > 0 && G > 0 && G <= P && ld == C && (reinterpret_cast<uintptr_t>(X) & 15) == 0) {
-        const int64_t per = ((total + G - 1) / G + kResChunksPerBatch - 1) / kResChunksPerBatch * kResChunksPerBatch;
         uint32_t* err = device_error_word();
         if (!err) return cudaErrorInvalidValue;
         int64_t Pr = G;
-        void* args[] = {(void*)&X, (void*)&total, (void*)&per, (void*)&slots, (void*)&Pr,
-                        (void*)&scale, (void*)&Xq, (void*)&err};
+        void* args[] = {(void*)&X, (void*)&total, (void*)&slots, (void*)&Pr, (void*)&scale, (void*)&Xq, (void*)&err};
         return cudaLaunchCooperativeKernel((const void*)kv_resident_kernel, dim3((unsigned)G), dim3(kResThreads),
                                            args, kResSmemBytes, st);
     }

@@ -250,36 +250,30 @@ def test_fp8_kv_tensor_quant_one_pass_boundary(cuda_lib, R, where):
     assert fb.fp8rl_check_device_error() == 0
 
 
-KV_BATCH_CHUNKS = 8 * 512     # 16-byte chunks per batch of the resident kernel (8 rounds of 512 threads)
-
-
-def _kv_resident_range(R, C):
-    """Chunks per CTA of the resident kernel on this GPU (one CTA per SM)."""
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    total = R * (C // 8)
-    per = -(-total // sms)
-    return -(-per // KV_BATCH_CHUNKS) * KV_BATCH_CHUNKS
+KV_BATCH_CHUNKS = 4 * 1024    # 16-byte chunks per batch of the resident kernel (4 rounds of 1024 threads)
 
 
 @pytest.mark.parametrize("R,C,where", [(9744, 1024, "last"), (20011, 1032, "first"), (20011, 1032, "last"),
                                        (32768, 1024, "smem"), (60000, 1024, "tmem"), (60000, 1024, "reread"),
                                        (60000, 1024, "last")])
 def test_fp8_kv_tensor_quant_resident_path(cuda_lib, R, C, where):
-    # Contiguous tensors above the one-pass size: one CTA per SM over a range of
-    # chunks whose first 7 batches stay on chip (4 in tensor memory, then 3 in
-    # shared memory) between the amax and the encode; later batches are read
-    # again.  On 152 SMs: 9744 x 1024 has 3 batches per CTA, 20011 x 1032 5
-    # (the last ranges ragged or empty), 32768 x 1024 7 (all on chip, read
-    # once), 60000 x 1024 13 (6 read again).  The tensor amax sits in the first
-    # or last value, or in a batch held in shared memory, in tensor memory or
-    # read again.
+    # Contiguous tensors above the one-pass size: one CTA per SM; the tensor's
+    # batches of 4096 chunks are dealt to the CTAs in turn (CTA b takes batches
+    # b, b + G, ...), and each CTA's first 7 stay on chip (4 in tensor memory,
+    # then 3 in shared memory) between the amax and the encode; later ones are
+    # read again.  On 152 SMs: 9744 x 1024 gives 2-3 batches per CTA, 20011 x
+    # 1032 4-5 (ragged last batch), 32768 x 1024 6-7 (all on chip, read once),
+    # 60000 x 1024 12-13 (5-6 read again).  The tensor amax sits in the first or
+    # last value, or in a batch held in tensor memory, in shared memory or read
+    # again.
     X = act_cpu(R, C, 9500 + R + C)
-    per = _kv_resident_range(R, C)
-    chunk = {"first": 0, "last": R * (C // 8) - 1,
-             "tmem": per + 2 * KV_BATCH_CHUNKS + 77,
-             "smem": 2 * per + 6 * KV_BATCH_CHUNKS + 300,
-             "reread": 3 * per + 9 * KV_BATCH_CHUNKS + 5}[where]
-    chunk = min(chunk, R * (C // 8) - 1)
+    G = torch.cuda.get_device_properties(0).multi_processor_count
+    batch = {"first": 0, "last": None,
+             "tmem": 1 * G + 5,            # CTA 5's second batch
+             "smem": 5 * G + 7,            # CTA 7's sixth
+             "reread": 9 * G + 3}[where]   # CTA 3's tenth
+    total = R * (C // 8)
+    chunk = total - 1 if batch is None else min(batch * KV_BATCH_CHUNKS + 1234, total - 1)
     e = chunk * 8 + 5
     X[e // C, e % C] = -1000.0
     ws = torch.empty(fb.fp8rl_kv_workspace_bytes(R, C), dtype=torch.uint8, device="cuda")
