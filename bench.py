@@ -64,14 +64,14 @@ PREFILL_M = synth.PREFILL_M
 #    scaled to the 64-layer launch by the values processed;
 #  - prefill: the four M = 8192 GEMMs of the 32B layer, summed;
 #  - decode: one launch of the worst decode-sweep shape.
-NCU_TRAFFIC = {"kernel": "quant_weight_block_kernel", "source_sha1": "69912cc3432327fae840b52154efe497e2f08df4",
-               "bytes_per_value": (1950448000 + 918897664) / (2 * sum(s.elems for s in synth.QWEN25_32B)),
+NCU_TRAFFIC = {"kernel": "quant_weight_block_kernel", "source_sha1": "14ed2e9e98c2a88ac5aaac25907debfb6bbd1bf2",
+               "bytes_per_value": (1950416128 + 918452736) / (2 * sum(s.elems for s in synth.QWEN25_32B)),
                "profile": "profiles/requant_weight_block_qwen32b_2layers.md"}
-NCU_TRAFFIC_PREFILL = {"kernel": "gemm_fp8_prefill_kernel", "source_sha1": "1a1fff07d63cc4d0f6e7a516f57a4970cd1f63d5",
-                       "bytes_per_step": (106420992 + 89201408) + (87272960 + 53447424) + (1500265728 + 880049664)
-                       + (1955701760 + 78481664),
+NCU_TRAFFIC_PREFILL = {"kernel": "gemm_fp8_prefill_kernel", "source_sha1": "a0a012e74cd88f9bda36e610f17a2232643fb487",
+                       "bytes_per_step": (107077888 + 89341184) + (88692736 + 53771520) + (1350391296 + 879037440)
+                       + (2134614528 + 78475776),
                        "profile": "profiles/prefill_gemm_qwen32b_m8192_four_shapes.md"}
-NCU_TRAFFIC_DECODE = {"kernel": "FP8 GEMM at a decode size", "source_sha1": "3739b283c2aefa71d0c2550760163876721d6c48",
+NCU_TRAFFIC_DECODE = {"kernel": "FP8 GEMM at a decode size", "source_sha1": "64951b493d759d438dbc562c473ae58db6ea70ff",
                       "case": "o_proj_M256", "bytes_per_launch": 27614464 + 15736064,
                       "profile": "profiles/decode_gemm_qwen32b_o_proj_m256.md"}
 
