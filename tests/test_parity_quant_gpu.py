@@ -284,6 +284,40 @@ def test_fp8_kv_tensor_quant_resident_path(cuda_lib, R, C, where):
     assert fb.fp8rl_check_device_error() == 0
 
 
+@pytest.mark.parametrize("kind", ["zeros", "tiny", "ties"])
+def test_fp8_kv_tensor_quant_resident_path_special_values(cuda_lib, kind):
+    # The resident path (40000 x 1024: 8-9 batches per CTA on 152 SMs, so
+    # batches held in tensor memory, in shared memory and read again) on
+    # special tensors: all zero with half the rows -0.0 (scale 1, codes 0x00
+    # and 0x80); every value below 1e-37, bf16 subnormals among them (scale
+    # below 2^-90: the encode takes the IEEE division); amax exactly 448
+    # (scale 1) with rows of E4M3 ties and subnormal codes spread over the
+    # tensor.
+    R, C = 40000, 1024
+    if kind == "zeros":
+        X = torch.zeros(R, C, dtype=torch.bfloat16)
+        X[1::2] = -0.0
+    elif kind == "tiny":
+        X = (act_cpu(R, C, 9700).float() * 1e-38).to(torch.bfloat16)
+    else:
+        X = act_cpu(R, C, 9701).float().clamp(-400.0, 400.0)
+        ties = torch.tensor([448.0, 17.0, -18.0, 2.0 ** -9, 2.0 ** -10, 3 * 2.0 ** -10, 1.5, -0.4375,
+                             -2.0 ** -7, 2.0 ** -8 * 1.0625, 240.0, 232.0])
+        for r in (0, R // 7, R // 3, R // 2, R - 1):
+            X[r] = ties.repeat(C // ties.numel() + 1)[:C]
+        X = X.to(torch.bfloat16)
+    ws = torch.empty(fb.fp8rl_kv_workspace_bytes(R, C), dtype=torch.uint8, device="cuda")
+    KVq, scale = fb.fp8rl_quant_kv_tensor(X.cuda(), workspace=ws)
+    want_q, want_s = oracle.fp8_quant_tensor(synth.bf16_bits(X))
+    if kind != "tiny":
+        assert float(want_s) == 1.0
+    else:
+        assert float(want_s) < 2.0 ** -90
+    assert bits_u32(host(scale))[0] == np.float32(want_s).view(np.uint32)
+    assert np.array_equal(host(KVq), want_q)
+    assert fb.fp8rl_check_device_error() == 0
+
+
 @pytest.mark.parametrize("R,C,ld", [(9744, 1024, 1032), (20011, 1032, 1040)])
 def test_fp8_kv_tensor_quant_strided_above_one_pass(cuda_lib, R, C, ld):
     # rows with a pitch, above the one-pass size: the three-launch path
