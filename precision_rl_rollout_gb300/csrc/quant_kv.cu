@@ -143,9 +143,9 @@ __device__ __forceinline__ uint32_t cta_max_u32(uint32_t v, uint32_t* red) {
 // header, slot[0], ends as tag << 32 | the grid maximum.  Every CTA reads the
 // header before it publishes its slot, and CTA 0 overwrites the header only
 // after it has seen every slot of this call, so all CTAs derive the same tag
-// (release stores, relaxed polling and a fence before the header write: each
-// slot word carries its own tag and value, and relaxed loads stay in flight
-// together where acquire loads would complete one after another).  Polling
+// (release stores and relaxed polling: each slot word carries its own tag and
+// value, and relaxed loads stay in flight together where acquire loads would
+// complete one after another).  Polling
 // traffic stays O(P) per round (CTA 0 reads the P slots, the rest read one
 // word), backing off between rounds so it does not crowd the loads of CTAs
 // still reading their part.  v_cta: this CTA's maximum (the same in every
@@ -187,7 +187,7 @@ __device__ bool kv_grid_max(uint64_t* __restrict__ slot, int64_t P, uint32_t tag
                 ok = false;
                 break;
             }
-            __nanosleep(64);
+            __nanosleep(16);
 #pragma unroll
             for (int j = 0; j < kSlotsPerThread; ++j)
                 if ((pending >> j) & 1u) sv[j] = ld_relaxed_u64(slot + 1 + threadIdx.x + (int64_t)j * kThreads);
@@ -195,7 +195,8 @@ __device__ bool kv_grid_max(uint64_t* __restrict__ slot, int64_t P, uint32_t tag
         ok = __syncthreads_and(ok);
         a = cta_max_u32<kThreads>(a, red);
         if (threadIdx.x == 0) {
-            __threadfence();       // the slots seen above happen before the header write
+            // a release store: the slots this CTA saw (through the barriers
+            // above) are ordered before it; readers take only this word
             st_release_u64(slot, ((uint64_t)tag << 32) | (ok ? a : kKvAborted));
             bcast[0] = a;
             bcast[1] = ok;
@@ -208,7 +209,7 @@ __device__ bool kv_grid_max(uint64_t* __restrict__ slot, int64_t P, uint32_t tag
                 ok = false;
                 break;
             }
-            __nanosleep(64);
+            __nanosleep(16);
             sv = ld_relaxed_u64(slot);
         }
         if ((uint32_t)sv == kKvAborted) ok = false;      // CTA 0's gather ran out (it recorded that)

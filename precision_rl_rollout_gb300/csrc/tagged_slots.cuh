@@ -7,8 +7,9 @@
 // gathering CTA waits until every slot word it needs carries that tag, then
 // writes the header with the new tag.  Each word carries its own tag and
 // payload, so the polling uses relaxed loads (which stay in flight together;
-// acquire loads complete one after another), and a fence before the header
-// write orders the slots seen before it.  A CUDA graph that replays one launch
+// acquire loads complete one after another), and the header is written with a
+// release store, which orders the slots seen before it (a kernel that writes
+// other results for the readers of the header fences those first).  A CUDA graph that replays one launch
 // still gives each replay a new tag, and the workspace needs no zeroing: a
 // word left by an earlier call carries an older tag.
 #pragma once
