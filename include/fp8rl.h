@@ -351,7 +351,7 @@ int fp8rl_rollout_is_weights(const float* logp_train, const float* logp_rollout,
  * |P - Q| < 32 elementwise (keeps every fp32 term finite).  Accuracy: |kl - kl_exact| <= 1e-4 kl_exact + 1e-7
  * (fp32 elementwise terms, fp64 combination; see mismatch_kl.cu).
  * Deterministic.  workspace: at least fp8rl_logits_kl_workspace_bytes(M, V)
- * bytes, 16-byte aligned, no zeroing needed (32 bytes per 8192 logits).
+ * bytes, 16-byte aligned, no zeroing needed (32 bytes per 4096 logits).
  * Limit: M <= 65535 (FP8RL_ERR_UNSUPPORTED).
  * ---------------------------------------------------------------------- */
 size_t fp8rl_logits_kl_workspace_bytes(int64_t M, int64_t V);

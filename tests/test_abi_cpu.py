@@ -120,7 +120,7 @@ def test_logits_kl_validation(lib):
     f = lib.fp8rl_logits_kl
     ws = lib.fp8rl_logits_kl_workspace_bytes(4, 1000)
     assert ws == 4 * 1 * 32
-    assert lib.fp8rl_logits_kl_workspace_bytes(2, 8193) == 2 * 2 * 32
+    assert lib.fp8rl_logits_kl_workspace_bytes(2, 8193) == 2 * 3 * 32       # 32 bytes per 4096 logits
     #      P  ldp  Q  ldq  M  V     kl ws bytes
     assert f(A, 1000, A, 1000, 4, 0, A, A, ws, None) == 2         # V < 1
     assert f(A, 996, A, 1000, 4, 1000, A, A, ws, None) == 2       # ldp < V
