@@ -803,8 +803,11 @@ static int64_t clusters_per_wave(int split) {
 // Split-K plan of the dense decode GEMM, from a sweep of the three exchanges
 // and splits 1..16 over the Qwen2.5-7B/32B decode shapes at M = 1..128 on
 // GB300 (in the order tried):
-//  - token tiles of 64 or more, with a workspace: the split CTAs run without a
-//    cluster, about one per SM, and a second launch adds their partials;
+//  - token tiles of 64, with a workspace: the largest split whose clusters all
+//    run at once, exchanging through L2 (below);
+//  - token tiles of 128 (or 64 without such a split), with a workspace: the
+//    split CTAs run without a cluster, about one per SM, and a second launch
+//    adds their partials;
 //  - token tiles of up to 32: a cluster split whose clusters all run at once
 //    (per the occupancy API).  Without a workspace the largest such split, i.e.
 //    more, shorter weight streams per slab as long as no second wave of
@@ -866,10 +869,12 @@ static DecodePlan decode_plan(int64_t tiles, int KB, bool may_use_memory) {
     int one_wave = 0;
     for (int s = C::kMaxSplit; s >= 1 && one_wave == 0; --s)
         if (split_fits(KB, s, C::kMaxKbPerSplit) && clusters_per_wave<MT>(s) >= tiles) one_wave = s;
-    // 64-token tiles on long K (>= 40 blocks) with a split of 6 or more: the
-    // in-cluster exchange through L2 beats the second launch (7B down at M=64:
-    // 18.1 -> 16.9 us); on short K the second launch at one CTA per SM wins
-    if (may_use_memory && MT == 64 && KB >= 40 && one_wave >= 6) return DecodePlan{one_wave, kXchgClusterMem};
+    // 64-token tiles: the largest one-wave cluster split, exchanging through
+    // L2.  Against the second launch at one CTA per SM, over 12 shapes (N, K
+    // from 1536 to 10240) at M = 64: 127.1 -> 120.0 us in all, e.g. an 8192 x
+    // 8192 GEMM 20.6 -> 16.4 us, Qwen2.5-32B qkv 13.7 -> 13.0 us, 7B down
+    // 18.1 -> 16.9 us; the worst case, 7B qkv, 8.4 -> 8.8 us
+    if (may_use_memory && MT == 64 && one_wave >= 2) return DecodePlan{one_wave, kXchgClusterMem};
     if (may_use_memory && MT >= 64) {
         int64_t t = sms / tiles;
         int s = (int)(t < kMaxMemSplit ? t : kMaxMemSplit);
