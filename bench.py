@@ -71,8 +71,8 @@ NCU_TRAFFIC_PREFILL = {"kernel": "gemm_fp8_prefill_kernel", "source_sha1": "a0a0
                        "bytes_per_step": (107077888 + 89341184) + (88692736 + 53771520) + (1350391296 + 879037440)
                        + (2134614528 + 78475776),
                        "profile": "profiles/prefill_gemm_qwen32b_m8192_four_shapes.md"}
-NCU_TRAFFIC_DECODE = {"kernel": "FP8 GEMM at a decode size", "source_sha1": "64951b493d759d438dbc562c473ae58db6ea70ff",
-                      "case": "o_proj_M256", "bytes_per_launch": 27614464 + 15736064,
+NCU_TRAFFIC_DECODE = {"kernel": "FP8 GEMM at a decode size", "source_sha1": "45b109e770ec644a2e355791db05740407eaebce",
+                      "case": "o_proj_M256", "bytes_per_launch": 27614208 + 15736832,
                       "profile": "profiles/decode_gemm_qwen32b_o_proj_m256.md"}
 
 
